@@ -1,0 +1,231 @@
+"""CPU FP64 oracle for the dense GEMM hot path -- TEST INFRASTRUCTURE.
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library never loads it and
+the two share no code: the oracle is plain C (``oracle.c``) built with gcc,
+loaded here with ctypes.
+
+Definition followed (see the header of ``oracle.c`` for the passages):
+``C[b,i,j] = alpha * sum_k A[b,i,k] * opB[b,k,j] + beta * C0[b,i,j]`` in IEEE
+double, with exact widening of float32 / bfloat16 inputs, and one
+round-to-nearest-even to bfloat16 afterwards where the output is BF16
+("Operator & Runtime", sections 5.4.2-5.4.3: round once after the full K
+accumulation).
+
+Every function is pinned by tests/test_oracle_pins.py against values fixed by
+the pages or by mathematics (hand products, identities, closed forms,
+numpy's float64 matmul on integer data, IEEE rounding cases).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+
+F32, BF16, F64 = 0, 1, 2
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into a shared library (gcc, no CUDA)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        # -O2 without -ffast-math: IEEE double arithmetic, no reassociation.
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
+               "-ffp-contract=off", "-pthread", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        i64, dbl, vp, ci = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p, ctypes.c_int
+        gemm_args = [i64, i64, i64, i64, dbl,
+                     vp, ci, i64, i64,
+                     vp, ci, i64, i64, ci,
+                     dbl, vp, ci, i64, i64,
+                     vp, i64, i64, ci]
+        lib.oracle_gemm.argtypes = gemm_args
+        lib.oracle_gemm.restype = ci
+        lib.oracle_gemm_absden.argtypes = gemm_args
+        lib.oracle_gemm_absden.restype = ci
+        lib.oracle_gemm_entries.argtypes = [i64, i64, i64, dbl,
+                                            vp, ci, i64, i64,
+                                            vp, ci, i64, i64, ci,
+                                            dbl, vp, ci, i64, i64,
+                                            i64, vp, vp, vp, vp, vp]
+        lib.oracle_gemm_entries.restype = ci
+        lib.oracle_round_bf16.argtypes = [vp, vp, i64]
+        lib.oracle_round_bf16.restype = None
+        lib.oracle_bf16_to_double.argtypes = [vp, vp, i64]
+        lib.oracle_bf16_to_double.restype = None
+        lib.oracle_ulp_bf16_array.argtypes = [vp, vp, i64]
+        lib.oracle_ulp_bf16_array.restype = None
+        lib.oracle_ulp_bf16.argtypes = [dbl]
+        lib.oracle_ulp_bf16.restype = dbl
+        lib.oracle_gemm_flops.argtypes = [i64, i64, i64, i64]
+        lib.oracle_gemm_flops.restype = dbl
+        _lib = lib
+        return lib
+
+
+def _typed(arr: np.ndarray):
+    """(contiguous array, type code) for a float32 / bf16-bits (uint16) / float64 array."""
+    arr = np.ascontiguousarray(arr)
+    if arr.dtype == np.float32:
+        return arr, F32
+    if arr.dtype == np.uint16:
+        return arr, BF16
+    if arr.dtype == np.float64:
+        return arr, F64
+    raise TypeError(f"oracle inputs are float32, float64 or uint16 (bf16 bits), got {arr.dtype}")
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p) if a is not None else None
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def gemm(M, N, K, alpha, A, lda, B, ldb, beta=0.0, C0=None, ldc=None, *, op_b=0,
+         batch=1, strideA=0, strideB=0, strideC=0, nthreads=None, absden=False):
+    """Full result (batch, M, N) in float64 (and the error scale D if absden).
+
+    ``A``, ``B``, ``C0`` are flat (or any-shape, contiguous) arrays indexed with
+    the given leading dimensions and batch strides, exactly as the GPU sees them.
+    ``alpha`` and ``beta`` should be the float32 values passed to the GPU.
+    """
+    lib = _load()
+    A, at = _typed(A)
+    B, bt = _typed(B)
+    if C0 is not None:
+        C0, ct = _typed(C0)
+    else:
+        ct = F64
+    if ldc is None:
+        ldc = N
+    nthreads = nthreads or default_threads()
+    out = np.empty((batch, M, N), dtype=np.float64)
+    rc = lib.oracle_gemm(batch, M, N, K, float(alpha), _ptr(A), at, lda, strideA,
+                         _ptr(B), bt, ldb, strideB, op_b, float(beta), _ptr(C0), ct, ldc,
+                         strideC, _ptr(out), N, M * N, nthreads)
+    if rc != 0:
+        raise RuntimeError(f"oracle_gemm failed ({rc})")
+    if not absden:
+        return out
+    den = np.empty((batch, M, N), dtype=np.float64)
+    rc = lib.oracle_gemm_absden(batch, M, N, K, float(alpha), _ptr(A), at, lda, strideA,
+                                _ptr(B), bt, ldb, strideB, op_b, float(beta), _ptr(C0), ct,
+                                ldc, strideC, _ptr(den), N, M * N, nthreads)
+    if rc != 0:
+        raise RuntimeError(f"oracle_gemm_absden failed ({rc})")
+    return out, den
+
+
+def gemm_entries(M, N, K, alpha, A, lda, B, ldb, beta, C0, ldc, rows, cols, *, op_b=0,
+                 bidx=None, strideA=0, strideB=0, strideC=0):
+    """Selected outputs (values, error scales) computed one dot product each."""
+    lib = _load()
+    A, at = _typed(A)
+    B, bt = _typed(B)
+    if C0 is not None:
+        C0, ct = _typed(C0)
+    else:
+        ct = F64
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    n = rows.size
+    if bidx is not None:
+        bidx = np.ascontiguousarray(bidx, dtype=np.int64)
+    out = np.empty(n, dtype=np.float64)
+    den = np.empty(n, dtype=np.float64)
+    rc = lib.oracle_gemm_entries(M, N, K, float(alpha), _ptr(A), at, lda, strideA,
+                                 _ptr(B), bt, ldb, strideB, op_b, float(beta), _ptr(C0), ct,
+                                 ldc if ldc is not None else N, strideC, n, _ptr(bidx),
+                                 _ptr(rows), _ptr(cols), _ptr(out), _ptr(den))
+    if rc != 0:
+        raise RuntimeError(f"oracle_gemm_entries failed ({rc})")
+    return out, den
+
+
+def round_bf16(x) -> np.ndarray:
+    """Round-to-nearest-even of float64 values to bfloat16 bit patterns (uint16)."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(x.shape, dtype=np.uint16)
+    lib.oracle_round_bf16(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def bf16_to_f64(bits) -> np.ndarray:
+    """Exact widening of bfloat16 bit patterns to float64."""
+    lib = _load()
+    bits = np.ascontiguousarray(bits, dtype=np.uint16)
+    out = np.empty(bits.shape, dtype=np.float64)
+    lib.oracle_bf16_to_double(_ptr(bits), _ptr(out), bits.size)
+    return out
+
+
+def ulp_bf16(x) -> np.ndarray:
+    """Spacing of bfloat16 values at |x|."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(x.shape, dtype=np.float64)
+    lib.oracle_ulp_bf16_array(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def flops(batch, M, N, K) -> float:
+    return _load().oracle_gemm_flops(batch, M, N, K)
+
+
+# ---------------------------------------------------------------------------
+# Acceptance bounds (the tolerance stated for this path):
+#   FP32 output: |C - C_ref| <= 1e-5 * D
+#   BF16 output: |C - C_ref| <= 2e-4 * D + ulp_bf16(|C_ref|)
+# with D = sum_k |alpha a b| + |beta c0| (the error scale from gemm(absden=True)).
+# Where D == 0 the result must equal C_ref exactly.
+# ---------------------------------------------------------------------------
+FP32_REL = 1e-5
+BF16_REL = 2e-4
+
+
+def check_f32(C, ref, den):
+    """(ok, worst normalised error) for FP32 output."""
+    C = np.asarray(C, dtype=np.float64)
+    err = np.abs(C - ref)
+    bound = FP32_REL * den
+    ok = bool(np.all((err <= bound) | ((den == 0) & (err == 0))) and np.all(np.isfinite(C)))
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = np.where(den > 0, err / np.where(den > 0, den, 1.0), np.where(err == 0, 0.0, np.inf))
+    return ok, float(ratio.max()) if ratio.size else 0.0
+
+
+def check_bf16(C_bits, ref, den):
+    """(ok, worst error / bound) for BF16 output given as uint16 bit patterns."""
+    C = bf16_to_f64(C_bits)
+    err = np.abs(C - ref)
+    bound = BF16_REL * den + ulp_bf16(np.abs(ref))
+    ok = bool(np.all(err <= bound) and np.all(np.isfinite(C)))
+    ratio = err / bound
+    return ok, float(ratio.max()) if ratio.size else 0.0

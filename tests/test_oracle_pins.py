@@ -1,0 +1,265 @@
+"""Pins for the CPU oracle: values fixed by the pages or by mathematics.
+
+None of these re-type the oracle's own loop.  Each case is chosen so that a
+plausible slip in the oracle (a dropped alpha/beta term, a sign, a swapped
+index or a transposed operand, a wrong rounding rule) fails at least one test:
+
+* hand products (tests/golden/hand_*.txt) with non-symmetric operands and
+  alpha/beta not in {0, 1}: catch transposition, A.B vs B.A, beta dropped;
+* identity / permutation matrices: exact data movement, index mapping;
+* the rank-1 closed form (u v^T)(w z^T) = (v.w) u z^T;
+* numpy's float64 matmul on integer-valued data (exact in double);
+* IEEE round-to-nearest-even cases for bfloat16 and its ulp;
+* the FLOP count printed by "Operator & Runtime" section 5.2.1.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from dense_gemm_sm_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def read_golden(name):
+    vals = {}
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            parts = line.split()
+            try:
+                float(parts[0])
+                rows.append([float(p) for p in parts])
+            except ValueError:
+                key = parts[0]
+                nums = [float(p) for p in parts[1:]]
+                vals[key] = nums if len(nums) > 1 else nums[0]
+    return vals, rows
+
+
+def test_hand_2x2():
+    g, _ = read_golden("hand_2x2.txt")
+    A = np.array(g["A"], dtype=np.float32)
+    B = np.array(g["B"], dtype=np.float32)
+    C = oracle.gemm(2, 2, 2, g["alpha"], A, 2, B, 2)[0]
+    assert C.ravel().tolist() == g["C"]
+
+
+@pytest.mark.parametrize("op_b", [0, 1])
+def test_hand_3x3_alpha_beta(op_b):
+    g, _ = read_golden("hand_3x3.txt")
+    A = np.array(g["A"], dtype=np.float32)
+    B = np.array(g["B"], dtype=np.float32).reshape(3, 3)
+    Bstore = B if op_b == 0 else np.ascontiguousarray(B.T)  # op(B)[k][j] = B[j][k]
+    C0 = np.array(g["C0"], dtype=np.float32)
+    C = oracle.gemm(3, 3, 3, g["alpha"], A, 3, Bstore.ravel(), 3, g["beta"], C0, 3, op_b=op_b)[0]
+    assert C.ravel().tolist() == g["C"]
+    AB = oracle.gemm(3, 3, 3, 1.0, A, 3, Bstore.ravel(), 3, op_b=op_b)[0]
+    assert AB.ravel().tolist() == g["AB"]
+
+
+def test_identity_and_zero():
+    A = inputs.uniform_f32(1, (37, 23))
+    I = np.eye(23, dtype=np.float32)
+    C = oracle.gemm(37, 23, 23, 1.0, A, 23, I, 23)[0]
+    assert np.array_equal(C, A.astype(np.float64))
+    I2 = np.eye(37, dtype=np.float32)
+    C2 = oracle.gemm(37, 23, 37, 1.0, I2, 37, A, 23)[0]
+    assert np.array_equal(C2, A.astype(np.float64))
+    Z = np.zeros((23, 11), dtype=np.float32)
+    assert np.all(oracle.gemm(37, 11, 23, 1.0, A, 23, Z, 11)[0] == 0)
+
+
+def test_permutations():
+    r = inputs.rng(7)
+    A = inputs.uniform_f32(2, (9, 13))
+    p_rows = r.permutation(9)
+    P = np.zeros((9, 9), dtype=np.float32)
+    P[np.arange(9), p_rows] = 1.0          # (P A)[i] = A[p_rows[i]]
+    C = oracle.gemm(9, 13, 9, 1.0, P, 9, A, 13)[0]
+    assert np.array_equal(C, A[p_rows].astype(np.float64))
+    p_cols = r.permutation(13)
+    Q = np.zeros((13, 13), dtype=np.float32)
+    Q[p_cols, np.arange(13)] = 1.0         # (A Q)[:, j] = A[:, p_cols[j]]
+    C = oracle.gemm(9, 13, 13, 1.0, A, 13, Q, 13)[0]
+    assert np.array_equal(C, A[:, p_cols].astype(np.float64))
+
+
+def test_rank1_closed_form():
+    M, K, N = 17, 29, 11
+    u = inputs.uniform_f32(3, M).astype(np.float64)
+    v = inputs.uniform_f32(4, K).astype(np.float64)
+    w = inputs.uniform_f32(5, K).astype(np.float64)
+    z = inputs.uniform_f32(6, N).astype(np.float64)
+    A = np.outer(u, v)
+    B = np.outer(w, z)
+    C = oracle.gemm(M, N, K, 1.0, A, K, B, N)[0]
+    expect = float(v @ w) * np.outer(u, z)
+    assert np.max(np.abs(C - expect)) <= 1e-12 * np.max(np.abs(expect))
+
+
+def test_alpha_beta_special_cases():
+    M, N, K = 6, 5, 4
+    A = inputs.uniform_f32(8, (M, K))
+    B = inputs.uniform_f32(9, (K, N))
+    C0 = inputs.uniform_f32(10, (M, N))
+    # alpha = 0: C = beta * C0 exactly
+    C = oracle.gemm(M, N, K, 0.0, A, K, B, N, 0.75, C0, N)[0]
+    assert np.array_equal(C, 0.75 * C0.astype(np.float64))
+    # beta = 0: C0 is never read (NaN does not propagate)
+    nan_c0 = np.full((M, N), np.nan, dtype=np.float32)
+    C = oracle.gemm(M, N, K, 1.0, A, K, B, N, 0.0, nan_c0, N)[0]
+    assert np.all(np.isfinite(C))
+    # B = 0, alpha = beta = 1: C = C0
+    C = oracle.gemm(M, N, K, 1.0, A, K, np.zeros((K, N), np.float32), N, 1.0, C0, N)[0]
+    assert np.array_equal(C, C0.astype(np.float64))
+    # K = 0: C = beta * C0
+    C = oracle.gemm(M, N, 0, 1.0, A, K, B, N, -2.0, C0, N)[0]
+    assert np.array_equal(C, -2.0 * C0.astype(np.float64))
+
+
+@pytest.mark.parametrize("op_b", [0, 1])
+def test_integer_data_matches_numpy_exactly(op_b):
+    M, N, K = 37, 53, 29
+    A = inputs.integer_f32(11, (M, K))
+    B = inputs.integer_f32(12, (K, N))
+    Bstore = B if op_b == 0 else np.ascontiguousarray(B.T)
+    C = oracle.gemm(M, N, K, 1.0, A, K, Bstore, N if op_b == 0 else K, op_b=op_b)[0]
+    assert np.array_equal(C, A.astype(np.float64) @ B.astype(np.float64))
+
+
+def test_leading_dimension_padding_not_read():
+    M, N, K = 7, 9, 5
+    A = inputs.integer_f32(13, (M, K))
+    B = inputs.integer_f32(14, (K, N))
+    C0 = inputs.integer_f32(15, (M, N))
+    Ap = inputs.pad_rows(A, 8)
+    Bp = inputs.pad_rows(B, 12)
+    C0p = inputs.pad_rows(C0, 10)
+    C = oracle.gemm(M, N, K, 1.0, Ap, 8, Bp, 12, 1.0, C0p, 10)[0]
+    assert np.array_equal(C, A.astype(np.float64) @ B.astype(np.float64) + C0)
+
+
+def test_batched_strides():
+    batch, M, N, K = 3, 5, 4, 6
+    sA, sB, sC = M * K + 3, K * N + 1, M * N + 2
+    A = inputs.integer_f32(16, (batch * sA,))
+    B = inputs.integer_f32(17, (batch * sB,))
+    C0 = inputs.integer_f32(18, (batch * sC,))
+    C = oracle.gemm(M, N, K, 2.0, A, K, B, N, -1.0, C0, N, batch=batch, strideA=sA, strideB=sB,
+                    strideC=sC)
+    for b in range(batch):
+        Ab = A[b * sA:b * sA + M * K].reshape(M, K).astype(np.float64)
+        Bb = B[b * sB:b * sB + K * N].reshape(K, N).astype(np.float64)
+        C0b = C0[b * sC:b * sC + M * N].reshape(M, N).astype(np.float64)
+        assert np.array_equal(C[b], 2.0 * (Ab @ Bb) - C0b)
+
+
+def test_bf16_inputs_widen_exactly():
+    vals = np.array([1.0, -1.5, 0.0078125, 3.0e38, -2.0 ** -130], dtype=np.float32)
+    bits = inputs.f32_to_bf16_bits(vals[:4])
+    assert bits.tolist() == [0x3F80, 0xBFC0, 0x3C00, 0x7F62]
+    w = oracle.bf16_to_f64(bits)
+    assert w[:3].tolist() == [1.0, -1.5, 0.0078125]
+    # bf16 GEMM == GEMM of the widened values
+    X = inputs.f32_to_bf16_bits(inputs.normal_f32(19, (8, 16)))
+    W = inputs.f32_to_bf16_bits(inputs.normal_f32(20, (16, 12)))
+    C1 = oracle.gemm(8, 12, 16, 1.0, X, 16, W, 12)[0]
+    C2 = oracle.gemm(8, 12, 16, 1.0, oracle.bf16_to_f64(X), 16, oracle.bf16_to_f64(W), 12)[0]
+    assert np.array_equal(C1, C2)
+
+
+def test_round_bf16_ieee_cases():
+    one = 1.0
+    cases = [
+        (1.0, 0x3F80),
+        (-2.0, 0xC000),
+        (one + 2.0 ** -8, 0x3F80),             # exact tie -> even (down)
+        (one + 3 * 2.0 ** -8, 0x3F82),         # exact tie -> even (up)
+        (one + 2.0 ** -8 + 2.0 ** -30, 0x3F81),  # just above the tie -> up
+        (one + 2.0 ** -9, 0x3F80),             # below half -> down
+        (0.0, 0x0000),
+        (-0.0, 0x8000),
+        (2.0 ** -133, 0x0001),                 # smallest subnormal
+        (2.0 ** -134, 0x0000),                 # tie between 0 and 2^-133 -> even (0)
+        (3 * 2.0 ** -134, 0x0002),             # tie between 1 and 2 quanta -> 2
+        ((2 - 2.0 ** -7) * 2.0 ** 127, 0x7F7F),  # largest finite
+        ((2 - 2.0 ** -8) * 2.0 ** 127, 0x7F80),  # tie at the top rounds to infinity
+        (float("inf"), 0x7F80),
+        (-float("inf"), 0xFF80),
+        (3.140625, 0x4049),                    # exactly representable
+        (0.1, 0x3DCD),                         # 0.1 = 0x3DCCCCCD (f32) -> 0x3DCD
+    ]
+    xs = np.array([c[0] for c in cases], dtype=np.float64)
+    got = oracle.round_bf16(xs)
+    assert got.tolist() == [c[1] for c in cases]
+    nan = oracle.round_bf16(np.array([np.nan]))[0]
+    assert (nan & 0x7F80) == 0x7F80 and (nan & 0x7F) != 0
+
+
+def test_round_bf16_agrees_with_float32_path_on_f32_values():
+    # For values that are already float32, rounding the double directly and the
+    # integer-rounding of the float32 bits (the input converter) must agree.
+    x = inputs.normal_f32(21, 20000) * np.float32(1000)
+    assert np.array_equal(oracle.round_bf16(x.astype(np.float64)), inputs.f32_to_bf16_bits(x))
+
+
+def test_ulp_bf16():
+    got = oracle.ulp_bf16(np.array([1.0, 1.99, 2.0, 0.75, -3.0, 0.0, 2.0 ** -140]))
+    assert got.tolist() == [2.0 ** -7, 2.0 ** -7, 2.0 ** -6, 2.0 ** -8, 2.0 ** -6, 2.0 ** -133,
+                            2.0 ** -133]
+
+
+def test_entries_and_error_scale():
+    g, _ = read_golden("hand_3x3.txt")
+    A = np.array(g["A"], dtype=np.float32)
+    B = np.array(g["B"], dtype=np.float32)
+    C0 = np.array(g["C0"], dtype=np.float32)
+    rows = np.array([0, 1, 2, 2])
+    cols = np.array([0, 1, 2, 0])
+    out, den = oracle.gemm_entries(3, 3, 3, g["alpha"], A, 3, B, 3, g["beta"], C0, 3, rows, cols)
+    C = np.array(g["C"]).reshape(3, 3)
+    assert out.tolist() == [C[r, c] for r, c in zip(rows, cols)]
+    # error scale by hand: D_00 = 2*(|1*2|+|2*1|+|3*0|) + |-1*1| = 9
+    assert den[0] == 9.0
+    full, D = oracle.gemm(3, 3, 3, g["alpha"], A, 3, B, 3, g["beta"], C0, 3, absden=True)
+    assert D[0, 0, 0] == 9.0
+    assert den.tolist() == [D[0, r, c] for r, c in zip(rows, cols)]
+
+
+def test_flop_count_of_ffn_example():
+    g, _ = read_golden("ffn_counts.txt")
+    f = oracle.flops(1, int(g["M"]), int(g["N"]), int(g["K"]))
+    assert f == 103_079_215_104
+    assert round(f / 1e9) == g["F_gemm_GFLOP_approx"]
+    e = g["bytes_per_element"]
+    mib = 2 ** 20
+    M, K, N = g["M"], g["K"], g["N"]
+    assert (e * M * K / mib, e * K * N / mib, e * M * N / mib) == (g["X_MiB"], g["W_MiB"], g["C_MiB"])
+    assert e * (M * K + K * N + M * N) / mib == g["V_once_MiB"]
+
+
+def test_fp32_order_example_from_pages():
+    g, _ = read_golden("fp32_order.txt")
+    one, t = np.float32(1.0), np.float32(2.0 ** -24)
+    assert float((one + t) + t) == g["left_to_right"]
+    assert float(one + (t + t)) == g["small_first"]
+
+
+def test_acceptance_checkers():
+    ref = np.array([1.0, -2.0, 0.0])
+    den = np.array([10.0, 10.0, 0.0])
+    ok, worst = oracle.check_f32(np.array([1.0 + 0.5e-4, -2.0 - 0.9e-4, 0.0]), ref, den)
+    assert ok and worst <= 1e-5
+    ok, _ = oracle.check_f32(np.array([1.0 + 1.5e-4, -2.0, 0.0]), ref, den)
+    assert not ok
+    ok, _ = oracle.check_f32(np.array([1.0, -2.0, 1e-30]), ref, den)
+    assert not ok  # D == 0 demands exact equality
+    bits = oracle.round_bf16(ref)
+    ok, worst = oracle.check_bf16(bits, ref, den)
+    assert ok and worst == 0.0
