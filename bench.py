@@ -1,0 +1,500 @@
+#!/usr/bin/env python3
+"""Benchmark of the dense GEMM hot path on GB300.
+
+One "step" is one call of the library's public C ABI on one batch of synthetic input
+(resident in HBM).  The default workload is the FP32 SGEMM M = N = K = 4096,
+alpha = 1, beta = 0.5; --workload picks another of the path's configurations
+(ffn_bf16, decode_m1 / decode_m4 / decode_m16, qk_batched, sgemm_ragged, sgemm_256).
+
+Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier and
+torch.cuda.synchronize() on both sides, CUDA events on the launching stream; rotating
+copies of the inputs make the working set larger than L2 between successive steps.
+Rank 0 prints one JSON line.  Under torchrun each rank runs an independent replica of
+the workload (the path is one problem; ranks exchange nothing) and `value` is the sum
+of the ranks' work divided by the slowest rank's time.
+
+--impl reference times the CPU oracle (the repository's FP64 reference) on a bounded
+sample of the same workload, on the host cores, and prints the same kind of line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOPS (2MNK/s) and % of GB300 BF16/FP32 roofline; GB/s at M=1..16"
+L2_BYTES = 126.5 * 2 ** 20
+SM_COUNT_NOMINAL = 152
+FP32_LANES_PER_SM = 128          # FP32 FMA units per SM (4 partitions x 32)
+SM_MAX_MHZ_NOMINAL = 2070.0
+
+# ncu DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum), keyed by
+# workload, valid only while the kernel source hash matches the one it was taken with.
+MEASURED_TRAFFIC = {}
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=d["hbm_gbs"], bf16=d["bf16_tflops"],
+                    bf16_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                    sm_max_mhz=d.get("sm_max_mhz", SM_MAX_MHZ_NOMINAL), source="measured")
+    return dict(hbm_gbs=6800.0, bf16=1900.0, bf16_sustained=1700.0, sm_max_mhz=SM_MAX_MHZ_NOMINAL,
+                source="fallback")
+
+
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "dense_gemm_sm_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+# --------------------------------------------------------------------------- workloads
+
+class Workload:
+    """Device buffers (rotating copies) + one step = one library call."""
+
+    def __init__(self, name, torch, dg, inputs):
+        self.name = name
+        self.torch = torch
+        self.dg = dg
+        spec = self.spec(name, inputs)
+        self.__dict__.update(spec)
+
+    # ---- description of each configuration
+    @staticmethod
+    def spec(name, inputs):
+        if name in ("sgemm_4096", "sgemm_ragged", "sgemm_256"):
+            w = {"sgemm_4096": inputs.sgemm_4096, "sgemm_ragged": inputs.sgemm_ragged,
+                 "sgemm_256": inputs.sgemm_256}[name]()
+            M, N, K = w["M"], w["N"], w["K"]
+            return dict(kind="f32", w=w, batch=1, flops=2.0 * M * N * K,
+                        algo_bytes=4.0 * (M * K + K * N + (2 if w["beta"] != 0 else 1) * M * N),
+                        bound="alu", unit="TFLOPS", kernel="sgemm_simt_kernel",
+                        sources=["sgemm_simt.cu"],
+                        desc=f"FP32 SGEMM M={M} N={N} K={K} lda={w['lda']} ldb={w['ldb']} "
+                             f"ldc={w['ldc']} alpha={float(w['alpha'])} beta={float(w['beta'])}")
+        if name == "ffn_bf16":
+            w = inputs.ffn_bf16()
+            M, N, K = w["M"], w["N"], w["K"]
+            return dict(kind="bf16", w=w, batch=1, flops=2.0 * M * N * K,
+                        algo_bytes=2.0 * (M * K + K * N + M * N), bound="tensor", unit="TFLOPS",
+                        kernel="gemm_tc_kernel", sources=["gemm_tc.cu", "ptx.cuh"],
+                        desc=f"BF16 FFN projection C=XW M={M} N={N} K={K}, FP32 accumulate, BF16 out")
+        if name.startswith("decode_m"):
+            m = int(name[len("decode_m"):])
+            w = inputs.decode_bf16(m)
+            M, N, K = w["M"], w["N"], w["K"]
+            return dict(kind="bf16", w=w, batch=1, flops=2.0 * M * N * K,
+                        algo_bytes=2.0 * (M * K + K * N + M * N), bound="hbm", unit="GB/s",
+                        kernel="gemm_thin_kernel", sources=["gemm_thin.cu", "ptx.cuh"],
+                        desc=f"BF16 decode GEMM M={M} N={N} K={K}, BF16 out")
+        if name == "qk_batched":
+            w = inputs.qk_batched()
+            b, S, D = w["batch"], w["M"], w["K"]
+            return dict(kind="bf16b", w=w, batch=b, flops=2.0 * b * S * S * D,
+                        algo_bytes=2.0 * b * (2 * S * D) + 4.0 * b * S * S, bound="hbm",
+                        unit="TFLOPS", kernel="gemm_tc_kernel", sources=["gemm_tc.cu", "ptx.cuh"],
+                        desc=f"strided-batched BF16 S=QK^T*alpha batch={b} S={S} d={D}, FP32 out")
+        raise ValueError(f"unknown workload {name}")
+
+    def setup(self, copies=None):
+        torch = self.torch
+        w = self.w
+        per_copy = self.algo_bytes
+        if copies is None:
+            copies = max(2, int(np.ceil(2.0 * L2_BYTES / per_copy)) + 1)
+            copies = min(copies, 8)
+        self.copies = copies
+        self.bufs = []
+        if self.kind == "f32":
+            for i in range(copies):
+                A = torch.from_numpy(w["A"]).cuda()
+                B = torch.from_numpy(w["B"]).cuda()
+                C = torch.from_numpy(w["C0"]).cuda() if w["C0"] is not None else \
+                    torch.zeros((w["M"], w["ldc"]), dtype=torch.float32, device="cuda")
+                self.bufs.append((A, B, C))
+        else:
+            def bf(bits):
+                return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+            for i in range(copies):
+                A, B = bf(w["A"]), bf(w["B"])
+                if self.kind == "bf16b":
+                    C = torch.empty((w["batch"], w["M"], w["N"]), dtype=torch.float32, device="cuda")
+                else:
+                    C = torch.empty((w["M"], w["N"]), dtype=torch.bfloat16, device="cuda")
+                self.bufs.append((A, B, C))
+        torch.cuda.synchronize()
+
+    def step(self, i, bufs=None):
+        A, B, C = bufs if bufs is not None else self.bufs[i % self.copies]
+        w, dg = self.w, self.dg
+        if self.kind == "f32":
+            dg.gemm_f32(w["M"], w["N"], w["K"], float(w["alpha"]), A, w["lda"], B, w["ldb"],
+                        float(w["beta"]), C, w["ldc"])
+        elif self.kind == "bf16":
+            dg.gemm_bf16(w["M"], w["N"], w["K"], float(w["alpha"]), A, w["lda"], B, w["ldb"],
+                         float(w["beta"]), C, w["ldc"], dg.DG_OUT_BF16)
+        else:
+            dg.gemm_bf16_strided_batched(w["M"], w["N"], w["K"], float(w["alpha"]), A, w["lda"],
+                                         w["strideA"], B, w["ldb"], w["strideB"], w["op_b"],
+                                         float(w["beta"]), C, w["ldc"], w["strideC"], w["batch"],
+                                         dg.DG_OUT_F32)
+
+    def metric_value(self, seconds_per_step):
+        if self.unit == "GB/s":
+            return self.algo_bytes / seconds_per_step / 1e9
+        return self.flops / seconds_per_step / 1e12
+
+    def roofline(self, sec_per_launch, peaks, sm_mhz):
+        if self.bound == "alu":
+            peak = SM_COUNT_NOMINAL * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+            achieved = self.flops / sec_per_launch / 1e12
+            unit = "TFLOP/s"
+            note = (f"FP32 CUDA-core peak = {SM_COUNT_NOMINAL} SMs x {FP32_LANES_PER_SM} FMA/clk x 2 "
+                    f"x {peaks['sm_max_mhz']:.0f} MHz")
+        elif self.bound == "tensor":
+            peak = peaks["bf16_sustained"]
+            achieved = self.flops / sec_per_launch / 1e12
+            unit = "TFLOP/s"
+            note = f"bf16 dense, sustained cuBLAS figure of {peaks['source']} peaks"
+        else:
+            peak = peaks["hbm_gbs"]
+            achieved = self.algo_bytes / sec_per_launch / 1e9
+            unit = "GB/s"
+            note = f"HBM copy bandwidth of {peaks['source']} peaks"
+        traffic = None
+        t = MEASURED_TRAFFIC.get(self.name)
+        if t and t["source_hash"] == kernel_source_hash(self.sources):
+            traffic = t["bytes_per_launch"]
+        return {"bound": self.bound, "achieved": round(achieved, 3), "peak": round(peak, 1),
+                "unit": unit, "frac": round(achieved / peak, 4), "traffic": traffic,
+                "kernel": self.kernel, "algorithmic": {"flops": self.flops, "bytes": self.algo_bytes},
+                "peak_note": note}
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.samples:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((ts, float(parts[1]), float(parts[2]), parts))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"],
+                    "samples": 0}
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        use = inside if inside else sorted(rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))[:3]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in use:
+            for k, name in enumerate(names):
+                if r[3][5 + k].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median([r[1] for r in use])), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+# --------------------------------------------------------------------------- runs
+
+def time_steps(torch, wl, steps, warmup, barrier):
+    for i in range(warmup):
+        wl.step(i)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        ev[i][0].record(stream)
+        wl.step(warmup + i)
+        ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    t1 = time.time()
+    total_ms = start.elapsed_time(end)
+    per_launch_ms = [a.elapsed_time(b) for a, b in ev]
+    return total_ms, per_launch_ms, t0, t1
+
+
+def time_e2e(torch, wl, steps, warmup):
+    """Same workload through the public API with host inputs: each step copies that step's
+    inputs from pinned host memory, calls the library and reads the result back."""
+    w = wl.w
+    A0, B0, C0 = wl.bufs[0]
+    hA = A0.cpu().pin_memory()
+    hB = B0.cpu().pin_memory()
+    hC = C0.cpu().pin_memory()
+    out = torch.empty_like(hC).pin_memory()
+    h2d = hA.numel() * hA.element_size() + hB.numel() * hB.element_size()
+    reads_c = wl.kind == "f32" and w.get("beta", 0) != 0
+    if reads_c:
+        h2d += hC.numel() * hC.element_size()
+    d2h = out.numel() * out.element_size()
+    dA, dB, dC = torch.empty_like(A0), torch.empty_like(B0), torch.empty_like(C0)
+    stream = torch.cuda.current_stream()
+
+    def one():
+        dA.copy_(hA, non_blocking=True)
+        dB.copy_(hB, non_blocking=True)
+        if reads_c:
+            dC.copy_(hC, non_blocking=True)
+        wl.step(0, bufs=(dA, dB, dC))
+        out.copy_(dC, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        one()
+    end.record(stream)
+    torch.cuda.synchronize()
+    sec = start.elapsed_time(end) / 1e3 / steps
+    return {"value": round(wl.metric_value(sec), 3), "unit": wl.unit, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": round(sec * 1e3, 4)}
+
+
+def cpu_baseline(wl, budget_s=15.0, nthreads=None):
+    """The oracle, as it stands, on a bounded sample (the first R rows of C) of the workload."""
+    import oracle
+    w = wl.w
+    nthreads = nthreads or os.cpu_count() or 1
+    M, N, K = w["M"], w["N"], w["K"]
+    batch = w.get("batch", 1)
+    op_b = w.get("op_b", 0)
+
+    def run(rows):
+        A = w["A"].reshape(-1)[: rows * w["lda"]] if batch == 1 else w["A"].reshape(-1)
+        C0 = w["C0"]
+        if C0 is not None:
+            C0 = C0.reshape(-1)[: rows * w["ldc"]]
+        t = time.perf_counter()
+        oracle.gemm(rows, N, K, w["alpha"], A, w["lda"], w["B"].reshape(-1), w["ldb"], w["beta"],
+                    C0, w["ldc"], op_b=op_b, nthreads=nthreads)
+        return time.perf_counter() - t
+
+    rows = min(M, max(nthreads, 16))
+    dt = run(rows)
+    target = int(rows * budget_s / max(dt, 1e-6) * 0.8)
+    rows2 = max(rows, min(M, target))
+    if rows2 > rows:
+        rows, dt = rows2, run(rows2)
+    flops = 2.0 * rows * N * K
+    byts = wl.algo_bytes * rows / M / batch
+    value = byts / dt / 1e9 if wl.unit == "GB/s" else flops / dt / 1e12
+    return {"value": round(value, 6), "unit": wl.unit, "cores": nthreads, "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of C ({rows}/{M} rows{' of batch 0' if batch > 1 else ''}), "
+                      f"FP64 triple loop, {dt:.2f} s"}
+
+
+def reference_arm(args):
+    """--impl reference: the oracle timed as the reference on this workload's metric."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from dense_gemm_sm_gb300 import inputs
+    spec = Workload.spec(args.workload, inputs)
+
+    class W:  # minimal stand-in with the fields cpu_baseline needs
+        pass
+
+    wl = W()
+    wl.__dict__.update(spec)
+    per_step = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_baseline(wl, budget_s=per_step)
+    vals = [cpu_baseline(wl, budget_s=per_step) for _ in range(args.steps)]
+    value = float(np.median([v["value"] for v in vals]))
+    cb = dict(vals[-1])
+    cb["value"] = round(value, 6)
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": wl.unit,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded PCG64)", "config": {"workload": args.workload, "desc": wl.desc},
+            "cpu_baseline": cb,
+            "e2e": {"value": round(value, 6), "unit": wl.unit, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="sgemm_4096")
+    ap.add_argument("--no-suite", action="store_true", help="skip the other workloads' summary")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return reference_arm(args)
+
+    import torch
+    import dense_gemm_sm_gb300 as dg
+    from dense_gemm_sm_gb300 import inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    dg.load()
+    peaks = read_peaks()
+    wl = Workload(args.workload, torch, dg, inputs)
+    wl.setup()
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    total_ms, per_launch, t0, t1 = time_steps(torch, wl, args.steps, args.warmup, barrier)
+    if sampler:
+        time.sleep(0.2)
+        sampler.stop()
+    st = dg.dg_device_status()
+    if st != dg.DG_OK:
+        raise SystemExit(f"device status after the timed region: {dg.status_string(st)}")
+
+    ms = total_ms / args.steps
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    per_rank_value = wl.metric_value(ms / 1e3)
+    value = per_rank_value * world
+    launch_ms = float(np.mean(per_launch))
+
+    e2e = None if args.no_e2e else time_e2e(torch, wl, max(3, min(args.steps, 20)), 2)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    clocks = sampler.summary(t0, t1) if sampler else None
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": wl.unit, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if wl.kind == "f32" else "bf16",
+        "data": "synthetic (seeded PCG64; shapes and distributions of the pages' workloads)",
+        "config": {"workload": args.workload, "desc": wl.desc,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"{wl.copies} rotating input copies "
+                         f"({wl.copies * wl.algo_bytes / 2 ** 20:.0f} MiB) > L2 between steps"},
+        "roofline": wl.roofline(launch_ms / 1e3, peaks, clocks and clocks["sm_mhz"]),
+        "clocks": clocks,
+        "gpu_launches": args.steps,
+        "e2e": e2e,
+    }
+    if not args.no_suite:
+        suite = {}
+        for name in ("ffn_bf16", "decode_m1", "decode_m4", "decode_m16", "qk_batched",
+                     "sgemm_ragged"):
+            if name == args.workload:
+                continue
+            other = Workload(name, torch, dg, inputs)
+            other.setup()
+            tot, per, _, _ = time_steps(torch, other, 20, 3, barrier)
+            s = tot / 20 / 1e3
+            rf = other.roofline(float(np.mean(per)) / 1e3, peaks, None)
+            suite[name] = {"value": round(other.metric_value(s), 3), "unit": other.unit,
+                           "ms_per_step": round(s * 1e3, 4), "roofline_frac": rf["frac"],
+                           "bound": rf["bound"]}
+            del other
+            torch.cuda.empty_cache()
+        st = dg.dg_device_status()
+        if st != dg.DG_OK:
+            raise SystemExit(f"device status after the suite: {dg.status_string(st)}")
+        line["suite"] = suite
+    if not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,474 @@
+// api.cu -- the C ABI: argument checks, shape-based dispatch, workspace, status word.
+//
+// Dispatch (a static table keyed on dtype and shape class; chosen by measurement):
+//   FP32                       -> SIMT kernel (vector-copy variant when rows are aligned)
+//   BF16, batch == 1, M <= 32  -> thin stream-K kernel (HBM-bound decode shapes)
+//   BF16 otherwise             -> persistent tcgen05 tile kernel, BN = 256 (128 when the
+//                                 256-wide tiling leaves most SMs idle)
+//   K == 0 or alpha == 0       -> C = beta*C (scale kernel)
+// This is the "specialise per shape class with precompiled kernels" option of
+// "Operator & Runtime" section 5.5.3: no run-time compilation, a fixed table.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "dg_internal.h"
+#include "tile_sched.h"
+
+namespace dg {
+
+int g_fault_injection = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kRasterGroup = 8;
+constexpr int64_t kThinMaxM = 32;
+
+// Device status word: kernels record the first bounded-wait expiry here.
+__device__ uint32_t g_status_word;
+
+std::mutex g_mu;
+uint32_t* g_status_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+
+struct Workspace {
+  float* ws = nullptr;
+  size_t ws_floats = 0;
+  uint32_t* counters = nullptr;
+  size_t n_counters = 0;
+};
+std::map<std::pair<int, cudaStream_t>, Workspace> g_workspaces;
+
+bool log_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("DG_LOG");
+    return e && e[0] == '1';
+  }();
+  return on;
+}
+
+cudaError_t current_device(int* dev) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return e;
+  if (*dev < 0 || *dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  return cudaSuccess;
+}
+
+// Status-word address and SM count of the current device (cached per device).
+cudaError_t device_info(int dev, uint32_t** status, int* sms) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_status_word);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    g_status_ptr[dev] = static_cast<uint32_t*>(p);
+    g_num_sms[dev] = n;
+  }
+  *status = g_status_ptr[dev];
+  *sms = g_num_sms[dev];
+  return cudaSuccess;
+}
+
+// Workspace of (device, stream), grown to at least the requested sizes.  New counters are
+// zeroed on the stream; the kernels leave them at zero when they finish.
+dg_status get_workspace(int dev, cudaStream_t s, size_t ws_floats, size_t n_counters,
+                        Workspace* out) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  Workspace& w = g_workspaces[{dev, s}];
+  if (w.ws_floats < ws_floats || w.n_counters < n_counters) {
+    if (w.ws || w.counters) {
+      // Earlier work on this stream may still use the old buffers.
+      if (cudaStreamSynchronize(s) != cudaSuccess) return DG_ERR_CUDA;
+      cudaFree(w.ws);
+      cudaFree(w.counters);
+      w = Workspace{};
+    }
+    const size_t nf = ws_floats > 0 ? ws_floats : 1;
+    const size_t nc = n_counters > 0 ? n_counters : 1;
+    if (cudaMalloc(&w.ws, nf * sizeof(float)) != cudaSuccess) {
+      w = Workspace{};
+      return DG_ERR_NO_MEMORY;
+    }
+    if (cudaMalloc(&w.counters, nc * sizeof(uint32_t)) != cudaSuccess) {
+      cudaFree(w.ws);
+      w = Workspace{};
+      return DG_ERR_NO_MEMORY;
+    }
+    if (cudaMemsetAsync(w.counters, 0, nc * sizeof(uint32_t), s) != cudaSuccess)
+      return DG_ERR_CUDA;
+    w.ws_floats = nf;
+    w.n_counters = nc;
+  }
+  *out = w;
+  return DG_OK;
+}
+
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ------------------------------------------------------------------ planning
+void plan_f32(int64_t M, int64_t N, int64_t K, int64_t batch, dg_plan* pl) {
+  pl->kernel = DG_KERNEL_SIMT_F32;
+  pl->tile_m = kSimtBM;
+  pl->tile_n = kSimtBN;
+  pl->tile_k = kSimtBK;
+  pl->stages = kSimtStages;
+  pl->group = kRasterGroup;
+  pl->tiles = batch * cdiv(M, kSimtBM) * cdiv(N, kSimtBN);
+  pl->grid = pl->tiles;
+  pl->kblocks = cdiv(K, kSimtBK);
+  pl->vec = 1;
+}
+
+void plan_bf16(int64_t M, int64_t N, int64_t K, int64_t batch, int sms, dg_plan* pl) {
+  if (batch == 1 && M <= kThinMaxM) {
+    pl->kernel = DG_KERNEL_THIN_BF16;
+    pl->ntok = M <= 16 ? 16 : 32;
+    pl->tile_m = pl->ntok;
+    pl->tile_n = kThinBN;
+    pl->tile_k = kThinBK;
+    pl->stages = 8;
+    pl->group = 1;
+    pl->tiles = cdiv(N, kThinBN);
+    pl->kblocks = cdiv(K, kThinBK);
+    const int64_t units = pl->tiles * pl->kblocks;
+    pl->grid = units < sms ? units : sms;
+    pl->workspace_bytes =
+        thin_ws_floats(pl->grid, pl->ntok) * 4 + pl->tiles * static_cast<int64_t>(sizeof(uint32_t));
+    return;
+  }
+  pl->kernel = DG_KERNEL_TC_BF16;
+  int bn = 256;
+  const int64_t tiles256 = batch * cdiv(M, kTcBM) * cdiv(N, 256);
+  if (N <= 128 || tiles256 * 2 <= sms) bn = 128;
+  pl->tile_m = kTcBM;
+  pl->tile_n = bn;
+  pl->tile_k = kTcBK;
+  pl->stages = bn == 256 ? 4 : 6;
+  pl->group = kRasterGroup;
+  pl->tiles = batch * cdiv(M, kTcBM) * cdiv(N, bn);
+  pl->grid = pl->tiles < sms ? pl->tiles : sms;
+  pl->kblocks = cdiv(K, kTcBK);
+}
+
+dg_status plan(int32_t dtype, int64_t M, int64_t N, int64_t K, int64_t batch, float alpha,
+               int sms, dg_plan* pl) {
+  *pl = dg_plan{};
+  if (M == 0 || N == 0 || batch == 0) {
+    pl->kernel = DG_KERNEL_NONE;
+    return DG_OK;
+  }
+  if (K == 0 || alpha == 0.f) {
+    pl->kernel = DG_KERNEL_SCALE;
+    return DG_OK;
+  }
+  if (dtype == 0) plan_f32(M, N, K, batch, pl);
+  else plan_bf16(M, N, K, batch, sms, pl);
+  return DG_OK;
+}
+
+void log_plan(const char* who, int64_t M, int64_t N, int64_t K, int64_t batch, const dg_plan& pl) {
+  if (!log_enabled()) return;
+  std::fprintf(stderr,
+               "[dgemm] %s M=%lld N=%lld K=%lld batch=%lld -> kernel=%d tile=%dx%dx%d stages=%d "
+               "grid=%lld tiles=%lld ntok=%d\n",
+               who, (long long)M, (long long)N, (long long)K, (long long)batch, pl.kernel,
+               pl.tile_m, pl.tile_n, pl.tile_k, pl.stages, (long long)pl.grid, (long long)pl.tiles,
+               pl.ntok);
+}
+
+dg_status check_common(int64_t M, int64_t N, int64_t K, int64_t batch, int64_t lda, int64_t ldb,
+                       int64_t ldc, dg_op op_b, int64_t sA, int64_t sB, int64_t sC) {
+  if (M < 0 || N < 0 || K < 0 || batch < 0) return DG_ERR_INVALID_ARG;
+  if (op_b != DG_OP_N && op_b != DG_OP_T) return DG_ERR_INVALID_ARG;
+  if (M == 0 || N == 0 || batch == 0) return DG_OK;
+  if (ldc < N) return DG_ERR_INVALID_ARG;
+  if (K > 0) {
+    if (lda < K) return DG_ERR_INVALID_ARG;
+    if (op_b == DG_OP_N ? ldb < N : ldb < K) return DG_ERR_INVALID_ARG;
+  }
+  if (batch > 1 && (sA < 0 || sB < 0 || sC < 0)) return DG_ERR_INVALID_ARG;
+  // Tile coordinates and TMA coordinates are 32-bit.
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX || batch > INT32_MAX)
+    return DG_ERR_UNSUPPORTED;
+  return DG_OK;
+}
+
+dg_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DG_OK : DG_ERR_CUDA; }
+
+dg_status run_scale(void* C, bool f32, int64_t M, int64_t N, int64_t ldc, int64_t sC, int64_t batch,
+                    float beta, cudaStream_t s) {
+  if (!C) return DG_ERR_INVALID_ARG;
+  return from_cuda(launch_scale(C, f32, M, N, ldc, sC, batch, beta, s));
+}
+
+dg_status f32_impl(int64_t M, int64_t N, int64_t K, float alpha, const float* A, int64_t lda,
+                   int64_t sA, const float* B, int64_t ldb, int64_t sB, dg_op op_b, float beta,
+                   float* C, int64_t ldc, int64_t sC, int64_t batch, void* stream) {
+  dg_status st = check_common(M, N, K, batch, lda, ldb, ldc, op_b, sA, sB, sC);
+  if (st != DG_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  dg_plan pl;
+  plan(0, M, N, K, batch, alpha, 0, &pl);
+  log_plan("gemm_f32", M, N, K, batch, pl);
+  if (pl.kernel == DG_KERNEL_NONE) return DG_OK;
+  if (pl.kernel == DG_KERNEL_SCALE) return run_scale(C, true, M, N, ldc, sC, batch, beta, s);
+  if (!A || !B || !C) return DG_ERR_INVALID_ARG;
+  if (pl.tiles > INT32_MAX) return DG_ERR_UNSUPPORTED;
+  const bool vec = aligned16(A) && aligned16(B) && aligned16(C) && lda % 4 == 0 &&
+                   ldb % 4 == 0 && ldc % 4 == 0 &&
+                   (batch <= 1 || (sA % 4 == 0 && sB % 4 == 0 && sC % 4 == 0));
+  SimtParams p;
+  p.M = M; p.N = N; p.K = K;
+  p.alpha = alpha; p.beta = beta;
+  p.A = A; p.lda = lda; p.strideA = batch > 1 ? sA : 0;
+  p.B = B; p.ldb = ldb; p.strideB = batch > 1 ? sB : 0;
+  p.C = C; p.ldc = ldc; p.strideC = batch > 1 ? sC : 0;
+  p.batch = batch;
+  p.tiles_m = cdiv(M, kSimtBM);
+  p.tiles_n = cdiv(N, kSimtBN);
+  p.group = kRasterGroup;
+  return from_cuda(launch_sgemm_simt(p, op_b == DG_OP_T, vec, s));
+}
+
+dg_status bf16_impl(int64_t M, int64_t N, int64_t K, float alpha, const uint16_t* A, int64_t lda,
+                    int64_t sA, const uint16_t* B, int64_t ldb, int64_t sB, dg_op op_b,
+                    float beta, void* C, int64_t ldc, int64_t sC, int64_t batch, dg_out c_type,
+                    void* stream) {
+  dg_status st = check_common(M, N, K, batch, lda, ldb, ldc, op_b, sA, sB, sC);
+  if (st != DG_OK) return st;
+  if (c_type != DG_OUT_BF16 && c_type != DG_OUT_F32) return DG_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool c_f32 = c_type == DG_OUT_F32;
+  int dev = 0;
+  if (current_device(&dev) != cudaSuccess) return DG_ERR_CUDA;
+  uint32_t* status = nullptr;
+  int sms = 0;
+  if (device_info(dev, &status, &sms) != cudaSuccess) return DG_ERR_CUDA;
+  dg_plan pl;
+  plan(1, M, N, K, batch, alpha, sms, &pl);
+  log_plan("gemm_bf16", M, N, K, batch, pl);
+  if (pl.kernel == DG_KERNEL_NONE) return DG_OK;
+  if (pl.kernel == DG_KERNEL_SCALE) return run_scale(C, c_f32, M, N, ldc, sC, batch, beta, s);
+  if (!A || !B || !C) return DG_ERR_INVALID_ARG;
+  // TMA: 16-byte aligned bases and row / batch strides that are multiples of 16 bytes.
+  if (!aligned16(A) || !aligned16(B) || lda % 8 != 0 || ldb % 8 != 0) return DG_ERR_MISALIGNED;
+  if (batch > 1 && (sA % 8 != 0 || sB % 8 != 0)) return DG_ERR_MISALIGNED;
+  const int esz = c_f32 ? 4 : 2;
+  const bool c_vec = aligned16(C) && (ldc * esz) % 16 == 0 && (batch <= 1 || (sC * esz) % 16 == 0);
+
+  if (pl.kernel == DG_KERNEL_THIN_BF16) {
+    Workspace w;
+    st = get_workspace(dev, s, static_cast<size_t>(thin_ws_floats(pl.grid, pl.ntok)),
+                       static_cast<size_t>(pl.tiles), &w);
+    if (st != DG_OK) return st;
+    ThinParams p;
+    p.M = M; p.N = N; p.K = K;
+    p.n_tiles = pl.tiles;
+    p.kblocks = pl.kblocks;
+    p.units = pl.tiles * pl.kblocks;
+    p.ctas = pl.grid;
+    p.alpha = alpha; p.beta = beta;
+    p.C = C; p.ldc = ldc;
+    p.c_f32 = c_f32 ? 1 : 0;
+    p.ws = w.ws;
+    p.counters = w.counters;
+    p.status = status;
+    return from_cuda(launch_gemm_thin(p, pl.ntok, A, lda, B, ldb, op_b == DG_OP_T, s));
+  }
+
+  TcParams p;
+  p.M = M; p.N = N; p.K = K;
+  p.batch = batch;
+  p.tiles_m = cdiv(M, kTcBM);
+  p.tiles_n = cdiv(N, pl.tile_n);
+  p.total_tiles = pl.tiles;
+  p.kblocks = static_cast<int32_t>(pl.kblocks);
+  p.group = pl.group;
+  p.alpha = alpha; p.beta = beta;
+  p.C = C; p.ldc = ldc; p.strideC = batch > 1 ? sC : 0;
+  p.c_f32 = c_f32 ? 1 : 0;
+  p.c_vec = c_vec ? 1 : 0;
+  p.status = status;
+  return from_cuda(launch_gemm_tc(p, pl.tile_n, A, lda, batch > 1 ? sA : 0, B, ldb,
+                                  batch > 1 ? sB : 0, op_b == DG_OP_T,
+                                  static_cast<int>(pl.grid), s));
+}
+
+// ------------------------------------------------------------------ scale kernel
+template <typename T>
+__global__ void scale_kernel(T* C, int64_t M, int64_t N, int64_t ldc, int64_t sC, int64_t batch,
+                             float beta) {
+  const int64_t total = batch * M * N;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t b = i / (M * N);
+    const int64_t r = i - b * M * N;
+    const int64_t m = r / N, n = r - m * N;
+    T* c = C + b * sC + m * ldc + n;
+    if constexpr (sizeof(T) == 4) {
+      *c = beta != 0.f ? beta * *c : 0.f;
+    } else {
+      const float v = beta != 0.f ? beta * __bfloat162float(*c) : 0.f;
+      *c = __float2bfloat16_rn(v);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_scale(void* C, bool c_f32, int64_t M, int64_t N, int64_t ldc, int64_t strideC,
+                         int64_t batch, float beta, cudaStream_t s) {
+  const int64_t total = batch * M * N;
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > 152 * 32) blocks = 152 * 32;
+  if (blocks < 1) blocks = 1;
+  if (c_f32)
+    scale_kernel<float><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        static_cast<float*>(C), M, N, ldc, strideC, batch, beta);
+  else
+    scale_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        static_cast<__nv_bfloat16*>(C), M, N, ldc, strideC, batch, beta);
+  return cudaGetLastError();
+}
+
+}  // namespace dg
+
+// ==================================================================== C ABI
+using namespace dg;
+
+extern "C" {
+
+dg_status gemm_f32(int64_t M, int64_t N, int64_t K, float alpha, const float* A, int64_t lda,
+                   const float* B, int64_t ldb, float beta, float* C, int64_t ldc, void* stream) {
+  return f32_impl(M, N, K, alpha, A, lda, 0, B, ldb, 0, DG_OP_N, beta, C, ldc, 0, 1, stream);
+}
+
+dg_status gemm_f32_strided_batched(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                                   int64_t lda, int64_t strideA, const float* B, int64_t ldb,
+                                   int64_t strideB, dg_op op_b, float beta, float* C, int64_t ldc,
+                                   int64_t strideC, int64_t batch, void* stream) {
+  return f32_impl(M, N, K, alpha, A, lda, strideA, B, ldb, strideB, op_b, beta, C, ldc, strideC,
+                  batch, stream);
+}
+
+dg_status gemm_bf16(int64_t M, int64_t N, int64_t K, float alpha, const uint16_t* A, int64_t lda,
+                    const uint16_t* B, int64_t ldb, float beta, void* C, int64_t ldc,
+                    dg_out c_type, void* stream) {
+  return bf16_impl(M, N, K, alpha, A, lda, 0, B, ldb, 0, DG_OP_N, beta, C, ldc, 0, 1, c_type,
+                   stream);
+}
+
+dg_status gemm_bf16_strided_batched(int64_t M, int64_t N, int64_t K, float alpha,
+                                    const uint16_t* A, int64_t lda, int64_t strideA,
+                                    const uint16_t* B, int64_t ldb, int64_t strideB, dg_op op_b,
+                                    float beta, void* C, int64_t ldc, int64_t strideC,
+                                    int64_t batch, dg_out c_type, void* stream) {
+  return bf16_impl(M, N, K, alpha, A, lda, strideA, B, ldb, strideB, op_b, beta, C, ldc, strideC,
+                   batch, c_type, stream);
+}
+
+const char* dg_status_string(dg_status s) {
+  switch (s) {
+    case DG_OK: return "DG_OK";
+    case DG_ERR_INVALID_ARG: return "DG_ERR_INVALID_ARG: invalid argument";
+    case DG_ERR_MISALIGNED: return "DG_ERR_MISALIGNED: pointer or leading dimension violates the 16-byte TMA rule";
+    case DG_ERR_UNSUPPORTED: return "DG_ERR_UNSUPPORTED: shape not covered by the kernels";
+    case DG_ERR_CUDA: return "DG_ERR_CUDA: a CUDA runtime call failed";
+    case DG_ERR_TIMEOUT: return "DG_ERR_TIMEOUT: a kernel gave up a bounded wait";
+    case DG_ERR_NO_MEMORY: return "DG_ERR_NO_MEMORY: workspace allocation failed";
+  }
+  return "unknown dg_status";
+}
+
+dg_status dg_device_status(void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int dev = 0;
+  if (current_device(&dev) != cudaSuccess) return DG_ERR_CUDA;
+  uint32_t* status = nullptr;
+  int sms = 0;
+  if (device_info(dev, &status, &sms) != cudaSuccess) return DG_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DG_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DG_ERR_CUDA;
+  if (word == 0) return DG_OK;
+  const uint32_t zero = 0;
+  if (cudaMemcpy(status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    return DG_ERR_CUDA;
+  // A CTA that gave up may have left split-K arrival counters non-zero.
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (auto& kv : g_workspaces)
+      if (kv.first.first == dev && kv.second.counters)
+        cudaMemset(kv.second.counters, 0, kv.second.n_counters * sizeof(uint32_t));
+  }
+  if (cudaDeviceSynchronize() != cudaSuccess) return DG_ERR_CUDA;
+  return DG_ERR_TIMEOUT;
+}
+
+dg_status dg_release_workspace(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_workspaces.empty()) return DG_OK;
+  if (cudaDeviceSynchronize() != cudaSuccess) return DG_ERR_CUDA;
+  int cur = 0;
+  cudaGetDevice(&cur);
+  for (auto& kv : g_workspaces) {
+    cudaSetDevice(kv.first.first);
+    cudaFree(kv.second.ws);
+    cudaFree(kv.second.counters);
+  }
+  cudaSetDevice(cur);
+  g_workspaces.clear();
+  return DG_OK;
+}
+
+dg_status dg_plan_gemm(int32_t dtype, int64_t M, int64_t N, int64_t K, int64_t batch, dg_op op_b,
+                       dg_out c_type, int32_t num_sms, dg_plan* out) {
+  if (!out || (dtype != 0 && dtype != 1)) return DG_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0 || batch < 0) return DG_ERR_INVALID_ARG;
+  if (op_b != DG_OP_N && op_b != DG_OP_T) return DG_ERR_INVALID_ARG;
+  if (c_type != DG_OUT_BF16 && c_type != DG_OUT_F32) return DG_ERR_INVALID_ARG;
+  int sms = num_sms;
+  if (sms <= 0) {
+    int dev = 0;
+    uint32_t* status = nullptr;
+    if (current_device(&dev) != cudaSuccess || device_info(dev, &status, &sms) != cudaSuccess)
+      return DG_ERR_CUDA;
+  }
+  return plan(dtype, M, N, K, batch, 1.0f, sms, out);
+}
+
+void dg_raster_tile(int64_t t, int64_t tiles_m, int64_t tiles_n, int32_t group, int64_t* b,
+                    int64_t* tm, int64_t* tn) {
+  raster_tile(t, tiles_m, tiles_n, group, b, tm, tn);
+}
+
+int64_t dg_streamk_start(int64_t c, int64_t units, int64_t ctas) { return sk_start(c, units, ctas); }
+
+double dg_model_traffic_bytes(int64_t M, int64_t N, int64_t K, int64_t tile_m, int64_t tile_n,
+                              int32_t elem_bytes, int32_t out_bytes) {
+  const double e = elem_bytes, Md = M, Nd = N, Kd = K;
+  return e * Md * Kd * (Nd / tile_n) + e * Kd * Nd * (Md / tile_m) + out_bytes * Md * Nd;
+}
+
+int64_t dg_model_local_bytes(int64_t tile_m, int64_t tile_n, int64_t tile_k, int32_t elem_bytes) {
+  return elem_bytes * tile_m * tile_k + elem_bytes * tile_k * tile_n + 4 * tile_m * tile_n;
+}
+
+const char* dg_version(void) { return "dgemm-sm103a 0.1.0"; }
+
+void dg_set_fault_injection(int32_t mode) { g_fault_injection = mode; }
+
+}  // extern "C"

@@ -1,0 +1,72 @@
+// dg_internal.h -- declarations shared by the C-ABI layer and the kernel translation units.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "../../include/dgemm.h"
+
+namespace dg {
+
+// ------------------------------------------------------------------ FP32 SIMT path
+struct SimtParams {
+  int64_t M, N, K;
+  float alpha, beta;
+  const float* A; int64_t lda, strideA;
+  const float* B; int64_t ldb, strideB;
+  float* C; int64_t ldc, strideC;
+  int64_t batch;
+  int64_t tiles_m, tiles_n;
+  int32_t group;
+};
+// vec: all rows 16-byte aligned (bases aligned, ld % 4 == 0) so 16-byte copies are legal.
+cudaError_t launch_sgemm_simt(const SimtParams& p, bool trans_b, bool vec, cudaStream_t s);
+constexpr int kSimtBM = 128, kSimtBN = 128, kSimtBK = 16, kSimtThreads = 256, kSimtStages = 3;
+
+// ------------------------------------------------------------------ BF16 tcgen05 tile path
+struct TcParams {
+  int64_t M, N, K;
+  int64_t batch;
+  int64_t tiles_m, tiles_n, total_tiles;
+  int32_t kblocks;
+  int32_t group;
+  float alpha, beta;
+  void* C; int64_t ldc, strideC;
+  int32_t c_f32;     // 1: C is float32, 0: bfloat16
+  int32_t c_vec;     // 1: 16-byte vector stores/loads of C rows are legal
+  uint32_t* status;  // device status word
+};
+// A: [batch][M][lda] bf16 (K contiguous).  B: op N -> [batch][K][ldb] (N contiguous),
+// op T -> [batch][N][ldb] (K contiguous).
+cudaError_t launch_gemm_tc(const TcParams& p, int bn, const void* A, int64_t lda, int64_t strideA,
+                           const void* B, int64_t ldb, int64_t strideB, bool b_kmajor,
+                           int num_ctas, cudaStream_t s);
+constexpr int kTcBM = 128, kTcBK = 64;
+
+// ------------------------------------------------------------------ BF16 thin (decode) path
+struct ThinParams {
+  int64_t M, N, K;
+  int64_t n_tiles;     // ceil(N / 128)
+  int64_t kblocks;     // ceil(K / 64)
+  int64_t units;       // n_tiles * kblocks
+  int64_t ctas;        // grid size G
+  float alpha, beta;
+  void* C; int64_t ldc;
+  int32_t c_f32;
+  float* ws;           // partials: [ctas][2][ntok][128] fp32
+  uint32_t* counters;  // [n_tiles], zero between calls
+  uint32_t* status;
+};
+cudaError_t launch_gemm_thin(const ThinParams& p, int ntok, const void* X, int64_t ldx,
+                             const void* W, int64_t ldw, bool w_kmajor, cudaStream_t s);
+constexpr int kThinBN = 128, kThinBK = 64;
+inline int64_t thin_ws_floats(int64_t ctas, int ntok) { return ctas * 2 * ntok * 128; }
+
+// ------------------------------------------------------------------ misc
+// C = beta * C over a (batch, M, N) strided view (K == 0 or alpha == 0).
+cudaError_t launch_scale(void* C, bool c_f32, int64_t M, int64_t N, int64_t ldc, int64_t strideC,
+                         int64_t batch, float beta, cudaStream_t s);
+
+// Fault injection for the bounded-wait tests (host-set, read by the kernels at launch).
+extern int g_fault_injection;
+
+}  // namespace dg

@@ -1,0 +1,371 @@
+// gemm_tc.cu -- BF16-in / FP32-accumulate GEMM on the 5th-generation tensor cores (sm_103a).
+//
+// Structure (the pages' ideas, set for tcgen05):
+//   * The output is cut into 128 x BN tiles (BN = 256 or 128) and walked by a persistent
+//     grid (one CTA per SM) in the grouped raster order of tile_sched.h; the linear tile index
+//     is the "fuse the tile grid into one linear index" transform of "Operator & Runtime"
+//     section 5.4.2.
+//   * Operands move global -> shared with TMA (cp.async.bulk.tensor, 128-byte swizzle)
+//     into a STAGES-deep ring guarded by "full" and "empty" mbarriers with byte-counted
+//     completion: the producer / consumer warp specialisation of "Operator & Runtime"
+//     section 5.1.5 and the async-transaction barrier of the MUSA lesson m11-l5.  The
+//     swizzle replaces padding, which a tensor-descriptor copy cannot do (section 5.1.5).
+//   * One thread issues tcgen05.mma (M = 128, N = BN, K = 16) into an FP32 accumulator in
+//     tensor memory; tcgen05.commit releases each smem stage when its MMAs finish.
+//   * Two accumulators in TMEM (2 x BN columns) let the epilogue of tile i overlap the
+//     main loop of tile i+1.
+//   * Epilogue warps read the accumulator with tcgen05.ld, apply C = alpha*acc + beta*C_old
+//     in FP32 and round once to the output type (BF16 nearest-even or FP32), after the
+//     whole K reduction ("Operator & Runtime" sections 5.4.2-5.4.3).
+//   * Every mbarrier wait is bounded; a CTA that gives up records an error in the status
+//     word, waits (bounded) for its in-flight copies and MMAs, frees TMEM and exits.
+// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM owner + MMA issuer,
+// warps 2-5 = epilogue (warp w reads TMEM lanes 32*(w%4) .. 32*(w%4)+31).
+#include <cuda_bf16.h>
+
+#include "dg_internal.h"
+#include "ptx.cuh"
+#include "tile_sched.h"
+
+namespace dg {
+namespace {
+
+constexpr int BM = kTcBM, BK = kTcBK;
+constexpr uint32_t A_BYTES = BM * BK * 2;  // 16 KiB per stage
+constexpr int NUM_THREADS = 192;
+
+template <int BN>
+struct TcCfg {
+  static constexpr uint32_t B_BYTES = BN * BK * 2;
+  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators, power of two
+  static constexpr uint32_t RING_BYTES = STAGES * (A_BYTES + B_BYTES);
+  static constexpr uint32_t BAR_BYTES = 256;
+  static constexpr uint32_t SMEM_BYTES = 1024 /*alignment slack*/ + RING_BYTES + BAR_BYTES;
+  static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of two");
+};
+
+struct SmemCtl {
+  uint64_t full[8];
+  uint64_t empty[8];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  uint32_t abort;
+};
+
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint32_t* status) {
+  uint32_t never = 0;
+  return mbar_wait(bar, parity, &never, status, kDevTimeoutDrain);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Writes 32 consecutive outputs of one row: out[j] = alpha*acc[j] + beta*old[j], j < 32,
+// columns gn0 .. gn0+31 (masked against N).
+__device__ __forceinline__ void store_row_chunk(const TcParams& p, void* crow_v, int64_t gn0,
+                                                const uint32_t (&r)[32]) {
+  const float alpha = p.alpha, beta = p.beta;
+  const bool full = p.c_vec && gn0 + 32 <= p.N;
+  if (p.c_f32) {
+    float* crow = static_cast<float*>(crow_v) + gn0;
+    if (full) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (beta != 0.f) o = reinterpret_cast<const float4*>(crow)[q];
+        float4 v;
+        v.x = fmaf(alpha, __uint_as_float(r[4 * q + 0]), beta * o.x);
+        v.y = fmaf(alpha, __uint_as_float(r[4 * q + 1]), beta * o.y);
+        v.z = fmaf(alpha, __uint_as_float(r[4 * q + 2]), beta * o.z);
+        v.w = fmaf(alpha, __uint_as_float(r[4 * q + 3]), beta * o.w);
+        reinterpret_cast<float4*>(crow)[q] = v;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (gn0 + j < p.N) {
+          const float a = __uint_as_float(r[j]);
+          crow[j] = beta != 0.f ? fmaf(alpha, a, beta * crow[j]) : alpha * a;
+        }
+      }
+    }
+  } else {
+    __nv_bfloat16* crow = static_cast<__nv_bfloat16*>(crow_v) + gn0;
+    if (full) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 o = make_uint4(0u, 0u, 0u, 0u);
+        if (beta != 0.f) o = reinterpret_cast<const uint4*>(crow)[q];
+        const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+        uint32_t w[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const float a0 = __uint_as_float(r[8 * q + 2 * h]);
+          const float a1 = __uint_as_float(r[8 * q + 2 * h + 1]);
+          w[h] = pack_bf16x2(fmaf(alpha, a0, beta * bf16_lo(ow[h])),
+                             fmaf(alpha, a1, beta * bf16_hi(ow[h])));
+        }
+        reinterpret_cast<uint4*>(crow)[q] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (gn0 + j < p.N) {
+          const float a = __uint_as_float(r[j]);
+          const float v = beta != 0.f ? fmaf(alpha, a, beta * __bfloat162float(crow[j])) : alpha * a;
+          crow[j] = __float2bfloat16_rn(v);
+        }
+      }
+    }
+  }
+}
+
+template <int BN, bool B_KMAJOR, bool RANK3>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const TcParams p, const int fault) {
+  using Cfg = TcCfg<BN>;
+  constexpr int STAGES = Cfg::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t ring = (raw + 1023u) & ~1023u;            // 1024-byte aligned swizzle atoms
+  const uint32_t a_ring = ring;
+  const uint32_t b_ring = ring + STAGES * A_BYTES;
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem_raw + (ring - raw) + Cfg::RING_BYTES);
+  volatile uint32_t* abort = &ctl->abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&ctl->full[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&ctl->tfull[a]), 1);
+      mbar_init(smem_u32(&ctl->tempty[a]), 4);
+    }
+    mbar_init(smem_u32(&ctl->drain), 1);
+    ctl->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ctl->tmem_base;
+
+  const int64_t total = p.total_tiles;
+  const int kblocks = p.kblocks;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_map(&tmA);
+      tma_prefetch_map(&tmB);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        int64_t b, tm, tn;
+        raster_tile(t, p.tiles_m, p.tiles_n, p.group, &b, &tm, &tn);
+        const int32_t ym = static_cast<int32_t>(tm * BM);
+        const int32_t xn = static_cast<int32_t>(tn * BN);
+        const int32_t zb = static_cast<int32_t>(b);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+          if (!mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort, p.status, kDevTimeoutProducer)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&ctl->full[s]);
+          mbar_arrive_expect_tx(fb, A_BYTES + Cfg::B_BYTES);
+          const int32_t kx = kb * BK;
+          const uint32_t adst = a_ring + s * A_BYTES, bdst = b_ring + s * Cfg::B_BYTES;
+          if (RANK3) tma_load_3d(adst, &tmA, fb, kx, ym, zb);
+          else tma_load_2d(adst, &tmA, fb, kx, ym);
+          if (B_KMAJOR) {
+            if (RANK3) tma_load_3d(bdst, &tmB, fb, kx, xn, zb);
+            else tma_load_2d(bdst, &tmB, fb, kx, xn);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j) {
+              if (RANK3) tma_load_3d(bdst + j * 8192u, &tmB, fb, xn + 64 * j, kx, zb);
+              else tma_load_2d(bdst + j * 8192u, &tmB, fb, xn + 64 * j, kx);
+            }
+          }
+          ++it;
+        }
+      }
+      if (!ok) {
+        // Do not leave copies landing in shared memory after exit.
+        const uint32_t first = it > static_cast<uint32_t>(STAGES) ? it - STAGES : 0u;
+        for (uint32_t j = first; j < it; ++j)
+          wait_drain(smem_u32(&ctl->full[j % STAGES]), (j / STAGES) & 1u, p.status);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, false, !B_KMAJOR);
+      uint32_t it = 0, lt = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x, ++lt) {
+        const uint32_t acc = lt & 1u, aph = (lt >> 1) & 1u;
+        if (!mbar_wait(smem_u32(&ctl->tempty[acc]), aph ^ 1u, abort, p.status, kDevTimeoutMma)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * BN;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+          if (!mbar_wait(smem_u32(&ctl->full[s]), ph, abort, p.status, kDevTimeoutMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = a_ring + s * A_BYTES, b0 = b_ring + s * Cfg::B_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            // A (K-major, 128B swizzle): K step of 16 elements = 32 bytes inside the atom.
+            const uint64_t adesc = sdesc_sw128(a0 + k * 32, 16, 1024);
+            // B: K-major like A, or N-major: 64-column atoms 8 KiB apart (LBO), 8-row
+            // groups 1 KiB apart (SBO), K step of 16 rows = 2 KiB.
+            const uint64_t bdesc = B_KMAJOR ? sdesc_sw128(b0 + k * 32, 16, 1024)
+                                            : sdesc_sw128(b0 + k * 2048, 8192, 1024);
+            umma_bf16(d, adesc, bdesc, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          if (fault != 1) umma_commit(smem_u32(&ctl->empty[s]));
+          ++it;
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(&ctl->tfull[acc]));
+      }
+      // All MMAs of this CTA finished before TMEM is released.
+      umma_commit(smem_u32(&ctl->drain));
+      wait_drain(smem_u32(&ctl->drain), 0, p.status);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int row = q * 32 + lane;
+    uint32_t lt = 0;
+    for (int64_t t = blockIdx.x; t < total; t += gridDim.x, ++lt) {
+      int64_t b, tm, tn;
+      raster_tile(t, p.tiles_m, p.tiles_n, p.group, &b, &tm, &tn);
+      const uint32_t acc = lt & 1u, aph = (lt >> 1) & 1u;
+      if (!mbar_wait(smem_u32(&ctl->tfull[acc]), aph, abort, p.status, kDevTimeoutEpilogue)) break;
+      tc_fence_after();
+      const int64_t gm = tm * BM + row;
+      uint8_t* cbase = static_cast<uint8_t*>(p.C) +
+                       (b * p.strideC + gm * p.ldc) * (p.c_f32 ? 4 : 2);
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(taddr + c * 32, r);
+        tmem_ld_wait();
+        if (gm < p.M) store_row_chunk(p, cbase, tn * BN + c * 32, r);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+}  // namespace
+
+EncodeTiledFn get_encode_tiled();
+
+// Builds a BF16 tensor map over a (batch x) outer x inner row-major view with a
+// box_inner x box_outer box and 128-byte swizzle.  Out-of-range elements read as zero.
+bool make_bf16_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
+                   uint64_t batch, uint64_t stride, uint32_t box_inner, uint32_t box_outer) {
+  static EncodeTiledFn fn = get_encode_tiled();
+  if (!fn) return false;
+  const bool rank3 = batch > 1;
+  cuuint64_t dims[3] = {inner, outer, batch};
+  cuuint64_t strides[2] = {ld * 2, stride * 2};
+  cuuint32_t box[3] = {box_inner, box_outer, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank3 ? 3 : 2, const_cast<void*>(base),
+                  dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+EncodeTiledFn get_encode_tiled() {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<EncodeTiledFn>(p);
+}
+
+namespace {
+template <int BN, bool B_KMAJOR, bool RANK3>
+cudaError_t launch_tc_variant(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p,
+                              int num_ctas, cudaStream_t s) {
+  auto kern = gemm_tc_kernel<BN, B_KMAJOR, RANK3>;
+  constexpr uint32_t smem = TcCfg<BN>::SMEM_BYTES;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<num_ctas, NUM_THREADS, smem, s>>>(ma, mb, p, g_fault_injection);
+  return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_gemm_tc(const TcParams& p, int bn, const void* A, int64_t lda, int64_t strideA,
+                           const void* B, int64_t ldb, int64_t strideB, bool b_kmajor,
+                           int num_ctas, cudaStream_t s) {
+  CUtensorMap ma, mb;
+  const uint64_t batch = static_cast<uint64_t>(p.batch);
+  if (!make_bf16_map(&ma, A, p.K, p.M, lda, batch, strideA, BK, BM)) return cudaErrorInvalidValue;
+  const bool ok_b = b_kmajor ? make_bf16_map(&mb, B, p.K, p.N, ldb, batch, strideB, BK, bn)
+                             : make_bf16_map(&mb, B, p.N, p.K, ldb, batch, strideB, 64, BK);
+  if (!ok_b) return cudaErrorInvalidValue;
+  const bool rank3 = batch > 1;
+#define DG_TC_CASE(BNV, KM, R3)                                                     \
+  if (bn == BNV && b_kmajor == KM && rank3 == R3)                                   \
+    return launch_tc_variant<BNV, KM, R3>(ma, mb, p, num_ctas, s);
+  DG_TC_CASE(256, false, false)
+  DG_TC_CASE(256, false, true)
+  DG_TC_CASE(256, true, false)
+  DG_TC_CASE(256, true, true)
+  DG_TC_CASE(128, false, false)
+  DG_TC_CASE(128, false, true)
+  DG_TC_CASE(128, true, false)
+  DG_TC_CASE(128, true, true)
+#undef DG_TC_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dg

@@ -1,0 +1,340 @@
+// gemm_thin.cu -- decode-shaped BF16 GEMM (M <= 32 rows of X) on tcgen05, stream-K split.
+//
+// C[M,N] = alpha * X[M,K] * W[K,N] + beta * C with M tiny: every weight element is used
+// by at most 32 rows, so the cost is streaming W (K*N*2 bytes) from HBM once; the MUSA
+// lesson m11-l5 ("Batch GEMV" for [m,k] x [k,4]) and the Little's-law argument of
+// "Operator & Runtime" section 5.1.5 (enough bytes in flight per SM) drive the design:
+//   * swap A/B: the MMA's M dimension (128) runs over 128 columns of W, its N dimension
+//     (16 or 32) over the rows of X, so D^T = W^T X^T sits in TMEM as 128 lanes x ntok;
+//   * the (W column tile, K block) pairs are flattened into U units and split evenly over
+//     one CTA per SM (stream-K); each CTA streams its contiguous range of W through a deep
+//     TMA ring (8 stages x 16 KiB of W);
+//   * a tile split across CTAs ("split K", "Operator & Runtime" section 5.2.4) is combined
+//     by the last CTA to arrive: partial sums go to a workspace, an atomic counter per
+//     tile detects the last arrival, which adds the partials in CTA order (= K order) --
+//     a fixed order, so results are identical run to run (same section: atomics give
+//     arrival-dependent rounding, a fixed combination order does not);
+//   * alpha/beta and the single rounding to BF16 (or FP32 output) happen after the full
+//     K reduction (sections 5.4.2-5.4.3).
+// Warp roles (192 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer,
+// warps 2-5 epilogue / combine (thread = one W column of the tile).
+#include <cuda_bf16.h>
+
+#include "dg_internal.h"
+#include "ptx.cuh"
+#include "tile_sched.h"
+
+namespace dg {
+
+bool make_bf16_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
+                   uint64_t batch, uint64_t stride, uint32_t box_inner, uint32_t box_outer);
+
+namespace {
+
+constexpr int BNW = kThinBN, BK = kThinBK;
+constexpr uint32_t W_BYTES = BNW * BK * 2;  // 16 KiB per stage
+constexpr int STAGES = 8;
+constexpr int NUM_THREADS = 192;
+
+template <int NTOK>
+struct ThinCfg {
+  static constexpr uint32_t X_BYTES = NTOK * BK * 2;  // 2 or 4 KiB (multiple of 1 KiB)
+  static constexpr uint32_t RING_BYTES = STAGES * (W_BYTES + X_BYTES);
+  static constexpr uint32_t TMEM_COLS = NTOK == 16 ? 32 : 64;  // two accumulators
+  static constexpr uint32_t SMEM_BYTES = 1024 + RING_BYTES + 256;
+};
+
+struct SmemCtl {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  uint32_t abort;
+  uint32_t is_last;
+  uint32_t seg_ok;
+};
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// One contiguous piece of a CTA's stream-K range that lies in a single W column tile.
+struct Segment {
+  int64_t tile;
+  int64_t kbeg, kend;  // K blocks [kbeg, kend) of that tile
+};
+
+// Walks CTA c's range [u0, u1) tile by tile.
+struct SegmentWalk {
+  int64_t u, u1, kb;
+  __device__ SegmentWalk(const ThinParams& p, int64_t c)
+      : u(sk_start(c, p.units, p.ctas)), u1(sk_start(c + 1, p.units, p.ctas)), kb(p.kblocks) {}
+  __device__ bool next(Segment* s) {
+    if (u >= u1) return false;
+    s->tile = u / kb;
+    s->kbeg = u - s->tile * kb;
+    const int64_t lim = u1 - s->tile * kb;
+    s->kend = lim < kb ? lim : kb;
+    u = s->tile * kb + s->kend;
+    return true;
+  }
+};
+
+__device__ __forceinline__ void store_out(const ThinParams& p, int64_t t, int64_t n, float acc) {
+  const float alpha = p.alpha, beta = p.beta;
+  if (p.c_f32) {
+    float* c = static_cast<float*>(p.C) + t * p.ldc + n;
+    *c = beta != 0.f ? fmaf(alpha, acc, beta * *c) : alpha * acc;
+  } else {
+    __nv_bfloat16* c = static_cast<__nv_bfloat16*>(p.C) + t * p.ldc + n;
+    const float v = beta != 0.f ? fmaf(alpha, acc, beta * __bfloat162float(*c)) : alpha * acc;
+    *c = __float2bfloat16_rn(v);
+  }
+}
+
+template <int NTOK, bool W_KMAJOR>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_thin_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                     const ThinParams p) {
+  using Cfg = ThinCfg<NTOK>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t ring = (raw + 1023u) & ~1023u;
+  const uint32_t w_ring = ring;
+  const uint32_t x_ring = ring + STAGES * W_BYTES;
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem_raw + (ring - raw) + Cfg::RING_BYTES);
+  volatile uint32_t* abort = &ctl->abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t c = blockIdx.x;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&ctl->full[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&ctl->tfull[a]), 1);
+      mbar_init(smem_u32(&ctl->tempty[a]), 4);
+    }
+    mbar_init(smem_u32(&ctl->drain), 1);
+    ctl->abort = 0;
+    ctl->is_last = 0;
+    ctl->seg_ok = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ctl->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_map(&tmW);
+      tma_prefetch_map(&tmX);
+      SegmentWalk walk(p, c);
+      Segment sg;
+      uint32_t it = 0;
+      bool ok = true;
+      while (ok && walk.next(&sg)) {
+        const int32_t xn = static_cast<int32_t>(sg.tile * BNW);
+        for (int64_t kbi = sg.kbeg; kbi < sg.kend; ++kbi) {
+          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+          if (!mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort, p.status, kDevTimeoutProducer)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&ctl->full[s]);
+          mbar_arrive_expect_tx(fb, W_BYTES + Cfg::X_BYTES);
+          const int32_t kx = static_cast<int32_t>(kbi * BK);
+          const uint32_t wdst = w_ring + s * W_BYTES;
+          if (W_KMAJOR) {
+            tma_load_2d(wdst, &tmW, fb, kx, xn);
+          } else {
+            tma_load_2d(wdst, &tmW, fb, xn, kx);
+            tma_load_2d(wdst + 8192u, &tmW, fb, xn + 64, kx);
+          }
+          tma_load_2d(x_ring + s * Cfg::X_BYTES, &tmX, fb, kx, 0);
+          ++it;
+        }
+      }
+      if (!ok) {
+        const uint32_t first = it > static_cast<uint32_t>(STAGES) ? it - STAGES : 0u;
+        uint32_t never = 0;
+        for (uint32_t j = first; j < it; ++j)
+          mbar_wait(smem_u32(&ctl->full[j % STAGES]), (j / STAGES) & 1u, &never, p.status,
+                    kDevTimeoutDrain);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      // A = W^T tile (128 W columns x 64 K): N-contiguous W is "MN-major" for the MMA.
+      constexpr uint32_t idesc = idesc_bf16_f32(128, NTOK, !W_KMAJOR, false);
+      SegmentWalk walk(p, c);
+      Segment sg;
+      uint32_t it = 0, lt = 0;
+      bool ok = true;
+      while (ok && walk.next(&sg)) {
+        const uint32_t acc = lt & 1u, aph = (lt >> 1) & 1u;
+        if (!mbar_wait(smem_u32(&ctl->tempty[acc]), aph ^ 1u, abort, p.status, kDevTimeoutMma)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * NTOK;
+        for (int64_t kbi = sg.kbeg; kbi < sg.kend; ++kbi) {
+          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+          if (!mbar_wait(smem_u32(&ctl->full[s]), ph, abort, p.status, kDevTimeoutMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t w0 = w_ring + s * W_BYTES, x0 = x_ring + s * Cfg::X_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t adesc = W_KMAJOR ? sdesc_sw128(w0 + k * 32, 16, 1024)
+                                            : sdesc_sw128(w0 + k * 2048, 8192, 1024);
+            const uint64_t bdesc = sdesc_sw128(x0 + k * 32, 16, 1024);
+            umma_bf16(d, adesc, bdesc, idesc, (kbi > sg.kbeg || k > 0) ? 1u : 0u);
+          }
+          umma_commit(smem_u32(&ctl->empty[s]));
+          ++it;
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(&ctl->tfull[acc]));
+        ++lt;
+      }
+      umma_commit(smem_u32(&ctl->drain));
+      uint32_t never = 0;
+      mbar_wait(smem_u32(&ctl->drain), 0, &never, p.status, kDevTimeoutDrain);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue / combine
+    const int q = warp & 3;
+    const int row = q * 32 + lane;  // W column within the tile
+    const int etid = threadIdx.x - 64;
+    SegmentWalk walk(p, c);
+    Segment sg;
+    uint32_t lt = 0;
+    while (walk.next(&sg)) {
+      const uint32_t acc = lt & 1u, aph = (lt >> 1) & 1u;
+      // One thread waits (bounded) and the 128 epilogue threads take the same decision
+      // after the group barrier, so no thread is ever left alone in a barrier.
+      if (etid == 0)
+        ctl->seg_ok = mbar_wait(smem_u32(&ctl->tfull[acc]), aph, abort, p.status,
+                                kDevTimeoutEpilogue) ? 1u : 0u;
+      epi_bar();
+      if (!ctl->seg_ok) break;
+      tc_fence_after();
+      float v[NTOK];
+      {
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * NTOK;
+        if (NTOK == 16) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(taddr, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int t = 0; t < NTOK && t < 16; ++t) v[t] = __uint_as_float(r[t]);
+        } else {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(taddr, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int t = 0; t < NTOK; ++t) v[t] = __uint_as_float(r[t]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
+      ++lt;
+
+      const int64_t n = sg.tile * BNW + row;
+      if (sg.kbeg == 0 && sg.kend == p.kblocks) {
+        // This CTA computed the whole K range of the tile: write C directly.
+        if (n < p.N) {
+#pragma unroll
+          for (int t = 0; t < NTOK; ++t)
+            if (t < p.M) store_out(p, t, n, v[t]);
+        }
+        epi_bar();  // seg_ok is rewritten for the next segment only after everyone read it
+        continue;
+      }
+      // Partial K range: publish the partial sums, then count arrivals for the tile.
+      const int slot = sk_slot(c, sg.tile, p.kblocks, p.units, p.ctas);
+      float* mine = p.ws + ((c * 2 + slot) * NTOK) * BNW;
+#pragma unroll
+      for (int t = 0; t < NTOK; ++t) mine[t * BNW + row] = v[t];
+      __threadfence();
+      epi_bar();
+      if (etid == 0) {
+        const uint32_t need = static_cast<uint32_t>(
+            sk_contributors(sg.tile, p.kblocks, p.units, p.ctas));
+        const uint32_t prev = atomicAdd(&p.counters[sg.tile], 1u);
+        ctl->is_last = (prev + 1u == need) ? 1u : 0u;
+      }
+      epi_bar();
+      if (ctl->is_last) {
+        __threadfence();
+        const int64_t first = sk_cta_of(sg.tile * p.kblocks, p.units, p.ctas);
+        const int64_t last = sk_cta_of((sg.tile + 1) * p.kblocks - 1, p.units, p.ctas);
+        if (n < p.N) {
+          for (int64_t t = 0; t < p.M; ++t) {
+            float s = 0.f;
+            for (int64_t cc = first; cc <= last; ++cc) {
+              const int sl = sk_slot(cc, sg.tile, p.kblocks, p.units, p.ctas);
+              s += __ldcg(p.ws + ((cc * 2 + sl) * NTOK + t) * BNW + row);
+            }
+            store_out(p, t, n, s);
+          }
+        }
+        if (etid == 0) p.counters[sg.tile] = 0u;  // ready for the next call
+      }
+      epi_bar();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+  }
+}
+
+template <int NTOK, bool W_KMAJOR>
+cudaError_t launch_thin_variant(const CUtensorMap& mw, const CUtensorMap& mx, const ThinParams& p,
+                                cudaStream_t s) {
+  auto kern = gemm_thin_kernel<NTOK, W_KMAJOR>;
+  constexpr uint32_t smem = ThinCfg<NTOK>::SMEM_BYTES;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<static_cast<unsigned>(p.ctas), NUM_THREADS, smem, s>>>(mw, mx, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_thin(const ThinParams& p, int ntok, const void* X, int64_t ldx,
+                             const void* W, int64_t ldw, bool w_kmajor, cudaStream_t s) {
+  CUtensorMap mw, mx;
+  const bool ok_w = w_kmajor ? make_bf16_map(&mw, W, p.K, p.N, ldw, 1, 0, BK, BNW)
+                             : make_bf16_map(&mw, W, p.N, p.K, ldw, 1, 0, 64, BK);
+  if (!ok_w) return cudaErrorInvalidValue;
+  if (!make_bf16_map(&mx, X, p.K, p.M, ldx, 1, 0, BK, ntok)) return cudaErrorInvalidValue;
+  if (ntok == 16)
+    return w_kmajor ? launch_thin_variant<16, true>(mw, mx, p, s)
+                    : launch_thin_variant<16, false>(mw, mx, p, s);
+  if (ntok == 32)
+    return w_kmajor ? launch_thin_variant<32, true>(mw, mx, p, s)
+                    : launch_thin_variant<32, false>(mw, mx, p, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dg

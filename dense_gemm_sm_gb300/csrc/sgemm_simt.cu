@@ -1,0 +1,250 @@
+// sgemm_simt.cu -- FP32 SGEMM on CUDA cores for sm_103a.
+//
+// The SGEMM tutorial ("4.1 Toi uu hieu nang toan tu GEMM tren CUDA") builds the kernel in
+// steps: block tiling in shared memory along K (section 4), a register-blocked outer
+// product per thread (section 5), a 4 x 8 lane arrangement per warp (section 6), 16-byte
+// vector accesses (section 7), a bank-conflict-free shared layout (section 8) and
+// asynchronous multistage copies (sections 9-10).  This kernel keeps those ideas and sets
+// them for this GPU:
+//   * 128 x 128 block tile, BK = 16, 256 threads, an 8 x 8 FP32 accumulator per thread
+//     (4 x 8 lanes per warp, warp tile 32 x 64);
+//   * a 3-stage cp.async ring (global -> shared without registers), zero-filled edges;
+//   * A is kept K-contiguous in shared memory (row stride 20 floats).  Each thread reads
+//     4 K-steps of one A row with one 16-byte load; the 4 distinct rows a warp reads
+//     fall in 4 different bank quads, and the 8 lanes of a quarter-warp share a row, so
+//     the reads are conflict-free without the register transpose of the tutorial;
+//   * B rows are read as two 16-byte vectors per K-step, 8 lanes covering 128 contiguous
+//     bytes (conflict-free);
+//   * thread rows are interleaved (row = base + 4*i) so C rows are written by 8 lanes
+//     with 16-byte stores, 128 contiguous bytes per row segment;
+//   * strictly FP32 fused multiply-add; no TF32.
+// Epilogue: C = fma(alpha, acc, beta*C_old) in FP32 (C_old not read when beta == 0), masked
+// at the edges.
+#include "dg_internal.h"
+#include "ptx.cuh"
+#include "tile_sched.h"
+
+namespace dg {
+namespace {
+
+constexpr int BM = kSimtBM, BN = kSimtBN, BK = kSimtBK, NT = kSimtThreads, STAGES = kSimtStages;
+constexpr int LDS_K = BK + 4;            // K-contiguous tile row stride (floats)
+constexpr int A_STAGE = BM * LDS_K;      // floats per A stage
+constexpr int B_STAGE = BM * LDS_K;      // floats per B stage (>= BK*BN for the N layout)
+static_assert(BK * BN <= B_STAGE, "B stage too small");
+constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) * 4;
+
+__device__ __forceinline__ int clamp_bytes(int64_t remaining_elems) {
+  return remaining_elems <= 0 ? 0 : (remaining_elems >= 4 ? 16 : static_cast<int>(remaining_elems) * 4);
+}
+
+// Copies one BM x BK tile of a K-contiguous matrix (rows r0.., columns k0..) into a
+// [BM][LDS_K] shared tile, zero-filling outside [0,rows) x [0,K).
+template <bool VEC>
+__device__ __forceinline__ void load_kmajor(float* dst, const float* src, int64_t ld, int64_t r0,
+                                            int64_t rows, int64_t k0, int64_t K, int tid) {
+  if (VEC) {
+#pragma unroll
+    for (int h = 0; h < (BM * BK / 4) / NT; ++h) {
+      const int q = tid + h * NT;
+      const int r = q >> 2, c4 = q & 3;
+      const int64_t gr = r0 + r, gk = k0 + c4 * 4;
+      const int bytes = gr < rows ? clamp_bytes(K - gk) : 0;
+      const float* g = bytes ? src + gr * ld + gk : src;
+      cp_async_16(smem_u32(dst + r * LDS_K + c4 * 4), g, bytes);
+    }
+  } else {
+#pragma unroll
+    for (int h = 0; h < (BM * BK) / NT; ++h) {
+      const int e = tid + h * NT;
+      const int r = e >> 4, k = e & 15;
+      const int64_t gr = r0 + r, gk = k0 + k;
+      const bool ok = gr < rows && gk < K;
+      cp_async_4(smem_u32(dst + r * LDS_K + k), ok ? src + gr * ld + gk : src, ok ? 4 : 0);
+    }
+  }
+}
+
+// Copies one BK x BN tile of an N-contiguous matrix (rows k0.., columns n0..) into a
+// [BK][BN] shared tile, zero-filling outside [0,K) x [0,N).
+template <bool VEC>
+__device__ __forceinline__ void load_nmajor(float* dst, const float* src, int64_t ld, int64_t k0,
+                                            int64_t K, int64_t n0, int64_t N, int tid) {
+  if (VEC) {
+#pragma unroll
+    for (int h = 0; h < (BK * BN / 4) / NT; ++h) {
+      const int q = tid + h * NT;
+      const int r = q >> 5, c = q & 31;
+      const int64_t gk = k0 + r, gn = n0 + c * 4;
+      const int bytes = gk < K ? clamp_bytes(N - gn) : 0;
+      const float* g = bytes ? src + gk * ld + gn : src;
+      cp_async_16(smem_u32(dst + r * BN + c * 4), g, bytes);
+    }
+  } else {
+#pragma unroll
+    for (int h = 0; h < (BK * BN) / NT; ++h) {
+      const int e = tid + h * NT;
+      const int r = e >> 7, n = e & 127;
+      const int64_t gk = k0 + r, gn = n0 + n;
+      const bool ok = gk < K && gn < N;
+      cp_async_4(smem_u32(dst + r * BN + n), ok ? src + gk * ld + gn : src, ok ? 4 : 0);
+    }
+  }
+}
+
+__device__ __forceinline__ float f4get(const float4& v, int i) {
+  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+template <bool TRANS_B, bool VEC>
+__global__ void __launch_bounds__(NT, 2) sgemm_simt_kernel(const SimtParams p) {
+  extern __shared__ __align__(16) float smem[];
+  float* As = smem;
+  float* Bs = smem + STAGES * A_STAGE;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int wm = warp >> 1, wn = warp & 1;
+  const int lm = lane >> 3, ln = lane & 7;
+
+  int64_t b, tm, tn;
+  raster_tile(blockIdx.x, p.tiles_m, p.tiles_n, p.group, &b, &tm, &tn);
+  const int64_t m0 = tm * BM, n0 = tn * BN;
+  const float* A = p.A + b * p.strideA;
+  const float* B = p.B + b * p.strideB;
+  float* C = p.C + b * p.strideC;
+
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+  const int64_t KT = (p.K + BK - 1) / BK;
+  auto load_stage = [&](int stage, int64_t kt) {
+    const int64_t k0 = kt * BK;
+    load_kmajor<VEC>(As + stage * A_STAGE, A, p.lda, m0, p.M, k0, p.K, tid);
+    if (TRANS_B)
+      load_kmajor<VEC>(Bs + stage * B_STAGE, B, p.ldb, n0, p.N, k0, p.K, tid);
+    else
+      load_nmajor<VEC>(Bs + stage * B_STAGE, B, p.ldb, k0, p.K, n0, p.N, tid);
+  };
+
+#pragma unroll
+  for (int s = 0; s < STAGES - 1; ++s) {
+    if (s < KT) load_stage(s, s);
+    cp_async_commit();
+  }
+
+  const int row_base = wm * 32 + lm;          // thread rows: row_base + 4*i
+  const int col_base_n = wn * 64 + ln * 4;    // N layout: cols col_base_n + {0..3}, +32
+  const int col_base_t = wn * 64 + ln;        // T layout: cols col_base_t + 8*j
+
+  for (int64_t kt = 0; kt < KT; ++kt) {
+    cp_async_wait<STAGES - 2>();
+    __syncthreads();
+    {
+      const int64_t nk = kt + STAGES - 1;
+      if (nk < KT) load_stage(static_cast<int>(nk % STAGES), nk);
+      cp_async_commit();
+    }
+    const int stage = static_cast<int>(kt % STAGES);
+    const float* as = As + stage * A_STAGE;
+    const float* bs = Bs + stage * B_STAGE;
+#pragma unroll
+    for (int kk = 0; kk < BK / 4; ++kk) {
+      float4 a[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        a[i] = *reinterpret_cast<const float4*>(as + (row_base + 4 * i) * LDS_K + kk * 4);
+      if (TRANS_B) {
+        float4 bt[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          bt[j] = *reinterpret_cast<const float4*>(bs + (col_base_t + 8 * j) * LDS_K + kk * 4);
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4)
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              acc[i][j] = fmaf(f4get(a[i], k4), f4get(bt[j], k4), acc[i][j]);
+      } else {
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const int k = kk * 4 + k4;
+          const float4 b0 = *reinterpret_cast<const float4*>(bs + k * BN + col_base_n);
+          const float4 b1 = *reinterpret_cast<const float4*>(bs + k * BN + col_base_n + 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float av = f4get(a[i], k4);
+            acc[i][0] = fmaf(av, b0.x, acc[i][0]);
+            acc[i][1] = fmaf(av, b0.y, acc[i][1]);
+            acc[i][2] = fmaf(av, b0.z, acc[i][2]);
+            acc[i][3] = fmaf(av, b0.w, acc[i][3]);
+            acc[i][4] = fmaf(av, b1.x, acc[i][4]);
+            acc[i][5] = fmaf(av, b1.y, acc[i][5]);
+            acc[i][6] = fmaf(av, b1.z, acc[i][6]);
+            acc[i][7] = fmaf(av, b1.w, acc[i][7]);
+          }
+        }
+      }
+    }
+  }
+  cp_async_wait<0>();
+
+  // Epilogue: C = alpha*acc + beta*C_old, one FP32 rounding per operation.
+  const float alpha = p.alpha, beta = p.beta;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int64_t gm = m0 + row_base + 4 * i;
+    if (gm >= p.M) continue;
+    float* crow = C + gm * p.ldc;
+    if (TRANS_B) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int64_t gn = n0 + col_base_t + 8 * j;
+        if (gn < p.N)
+          crow[gn] = beta != 0.f ? fmaf(alpha, acc[i][j], beta * crow[gn]) : alpha * acc[i][j];
+      }
+    } else {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t gn = n0 + col_base_n + 32 * h;
+        const float* a4 = &acc[i][4 * h];
+        if (VEC && gn + 3 < p.N) {
+          float4* dst = reinterpret_cast<float4*>(crow + gn);
+          float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (beta != 0.f) o = *dst;
+          *dst = make_float4(fmaf(alpha, a4[0], beta * o.x), fmaf(alpha, a4[1], beta * o.y),
+                             fmaf(alpha, a4[2], beta * o.z), fmaf(alpha, a4[3], beta * o.w));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (gn + j < p.N)
+              crow[gn + j] = beta != 0.f ? fmaf(alpha, a4[j], beta * crow[gn + j]) : alpha * a4[j];
+          }
+        }
+      }
+    }
+  }
+}
+
+template <bool TRANS_B, bool VEC>
+cudaError_t launch_variant(const SimtParams& p, cudaStream_t s) {
+  auto kern = sgemm_simt_kernel<TRANS_B, VEC>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const int64_t tiles = p.batch * p.tiles_m * p.tiles_n;
+  kern<<<static_cast<unsigned>(tiles), NT, SMEM_BYTES, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_sgemm_simt(const SimtParams& p, bool trans_b, bool vec, cudaStream_t s) {
+  if (trans_b) return vec ? launch_variant<true, true>(p, s) : launch_variant<true, false>(p, s);
+  return vec ? launch_variant<false, true>(p, s) : launch_variant<false, false>(p, s);
+}
+
+}  // namespace dg

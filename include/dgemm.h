@@ -1,0 +1,190 @@
+/*
+ * dgemm.h -- C ABI of the GB300 (sm_103a) dense GEMM library.
+ *
+ * Operation (every entry point):
+ *
+ *     C = alpha * A * op(B) + beta * C          (row-major matrices)
+ *
+ *   - GEMM definition: "4.1 Toi uu hieu nang toan tu GEMM tren CUDA"
+ *     (infra-guide), section 1.1, and MUSA learning centre lesson m11-l5,
+ *     Case 4 "GEMM" (C_ij = sum_k A_ik B_kj).  Row-major element addressing
+ *     follows section 3.1 of the GEMM page: A[i*lda + k], B[k*ldb + j],
+ *     C[i*ldc + j].
+ *   - Work: 2*M*N*K floating-point operations ("Operator & Runtime", AI infra
+ *     book ch. 5, section 5.2.1, F_gemm = 2MKN).
+ *   - BF16 path: BF16 inputs, FP32 accumulation over the whole K reduction,
+ *     then alpha/beta and one rounding to the output type ("Operator &
+ *     Runtime" chapter introduction: X, W, C in BF16 with FP32 accumulation;
+ *     sections 5.4.2-5.4.3: round to BF16 once, after the K loop).
+ *   - Strided-batched variants: `batch` independent problems whose operands
+ *     start `stride*` elements apart ("Batched GEMM" in multi-head attention,
+ *     GEMM page section 1.2).
+ *
+ * Conventions shared by all entry points:
+ *   - Pointers A, B, C are DEVICE pointers (cudaMalloc / torch CUDA memory) on
+ *     the current device, owned by the caller.  The library never frees them.
+ *   - Dimensions and leading dimensions are in elements.  op(B) = B (DG_OP_N):
+ *     B is K x N with B[k*ldb + j]; op(B) = B^T (DG_OP_T): B is stored N x K
+ *     with op(B)[k][j] = B[j*ldb + k].
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and the call returns without waiting.  Faults in the kernels
+ *     surface at the caller's next synchronisation; a kernel that gives up a
+ *     bounded wait records DG_ERR_TIMEOUT, read with dg_device_status().
+ *   - BLAS edge semantics (the pages are silent): M == 0, N == 0 or
+ *     batch == 0 is a no-op; K == 0 or alpha == 0 gives C = beta*C; when
+ *     beta == 0, C is not read (NaN/Inf in it do not propagate).
+ *   - Return value: DG_OK, or an error status with nothing enqueued.  No
+ *     exceptions cross the ABI.
+ *   - Thread safety: calls may come from several host threads.  Calls that
+ *     use the split-K workspace (thin BF16 shapes) on the SAME stream are
+ *     ordered by the stream; each stream gets its own workspace.
+ */
+#ifndef DGEMM_SM103_H
+#define DGEMM_SM103_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DG_OK = 0,
+  DG_ERR_INVALID_ARG = 1,  /* negative size, ld smaller than a row, null pointer, bad enum */
+  DG_ERR_MISALIGNED = 2,   /* BF16 path: a base pointer not 16-byte aligned, or an ld or
+                              batch stride not a multiple of 8 elements (TMA rule) */
+  DG_ERR_UNSUPPORTED = 3,  /* shape the kernels do not cover (e.g. > 2^31-1 rows) */
+  DG_ERR_CUDA = 4,         /* a CUDA runtime call failed (launch, allocation, query) */
+  DG_ERR_TIMEOUT = 5,      /* a kernel gave up a bounded wait; results are invalid */
+  DG_ERR_NO_MEMORY = 6     /* workspace allocation failed */
+} dg_status;
+
+typedef enum { DG_OP_N = 0, DG_OP_T = 1 } dg_op;
+typedef enum { DG_OUT_BF16 = 0, DG_OUT_F32 = 1 } dg_out;
+
+/*
+ * FP32 SGEMM on CUDA cores: C = alpha*A*B + beta*C, all float32, row-major.
+ * A: M x K (lda >= K), B: K x N (ldb >= N), C: M x N (ldc >= N).
+ * FP32 multiply-add throughout; no TF32 or other reduced-precision
+ * substitution.  Any alignment is accepted (rows that are 16-byte aligned
+ * take the vector-copy variant of the kernel).
+ * Defined by: GEMM page sections 1.1, 3-10 (the SGEMM this path implements).
+ */
+dg_status gemm_f32(int64_t M, int64_t N, int64_t K, float alpha, const float* A, int64_t lda,
+                   const float* B, int64_t ldb, float beta, float* C, int64_t ldc, void* stream);
+
+/*
+ * Strided-batched FP32 SGEMM: for b < batch,
+ *   C_b = alpha*A_b*op(B_b) + beta*C_b with X_b = X + b*strideX.
+ * op_b = DG_OP_T reads B_b as N x K (ldb >= K).
+ */
+dg_status gemm_f32_strided_batched(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                                   int64_t lda, int64_t strideA, const float* B, int64_t ldb,
+                                   int64_t strideB, dg_op op_b, float beta, float* C, int64_t ldc,
+                                   int64_t strideC, int64_t batch, void* stream);
+
+/*
+ * BF16 GEMM with FP32 accumulation on the 5th-generation tensor cores:
+ * C = alpha*A*B + beta*C.  A: M x K bfloat16 (lda >= K), B: K x N bfloat16
+ * (ldb >= N), C: M x N of type c_type (bfloat16 rounded to nearest-even, or
+ * float32), ldc >= N.  bfloat16 values are passed as their 16-bit patterns.
+ * Requirements (TMA): A and B 16-byte aligned, lda and ldb multiples of 8.
+ * Shapes with M <= 32 use the split-K decode kernel and a library-owned
+ * workspace (see dg_release_workspace).
+ * Defined by: "Operator & Runtime" chapter introduction and section 5.2.1
+ * (the FFN projection C = XW, BF16 with FP32 accumulate), sections 5.4.2-5.4.3.
+ */
+dg_status gemm_bf16(int64_t M, int64_t N, int64_t K, float alpha, const uint16_t* A, int64_t lda,
+                    const uint16_t* B, int64_t ldb, float beta, void* C, int64_t ldc,
+                    dg_out c_type, void* stream);
+
+/*
+ * Strided-batched BF16 GEMM: for b < batch, C_b = alpha*A_b*op(B_b) + beta*C_b.
+ * op_b = DG_OP_T reads B_b as N x K (ldb >= K), e.g. attention scores
+ * S = Q K^T / sqrt(d) with Q_b, K_b stored [seq][d].  strideA/strideB must
+ * be multiples of 8 elements when batch > 1.
+ */
+dg_status gemm_bf16_strided_batched(int64_t M, int64_t N, int64_t K, float alpha,
+                                    const uint16_t* A, int64_t lda, int64_t strideA,
+                                    const uint16_t* B, int64_t ldb, int64_t strideB, dg_op op_b,
+                                    float beta, void* C, int64_t ldc, int64_t strideC,
+                                    int64_t batch, dg_out c_type, void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* dg_status_string(dg_status s);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word.  Returns DG_ERR_TIMEOUT if a kernel gave up a bounded wait since the
+ * last call, DG_ERR_CUDA if the stream reported an error, DG_OK otherwise.
+ * After a timeout the split-K workspace counters are re-zeroed.
+ */
+dg_status dg_device_status(void* stream);
+
+/* Synchronises the device and frees every library-owned workspace. */
+dg_status dg_release_workspace(void);
+
+/* ----------------------------------------------------------------------
+ * Introspection (host only; no GPU needed).  Used by the tests and the bench.
+ * ---------------------------------------------------------------------- */
+
+typedef enum {
+  DG_KERNEL_NONE = 0,      /* no-op (empty problem) */
+  DG_KERNEL_SCALE = 1,     /* C = beta*C only (K == 0 or alpha == 0) */
+  DG_KERNEL_SIMT_F32 = 2,  /* FP32 CUDA-core SGEMM */
+  DG_KERNEL_TC_BF16 = 3,   /* tcgen05 tile kernel (persistent, TMA ring, TMEM accumulators) */
+  DG_KERNEL_THIN_BF16 = 4  /* tcgen05 stream-K decode kernel (M <= 32) */
+} dg_kernel;
+
+typedef struct {
+  int32_t kernel;          /* dg_kernel */
+  int32_t tile_m, tile_n, tile_k;
+  int32_t stages;          /* shared-memory ring depth */
+  int32_t group;           /* raster group height, in tile rows */
+  int32_t ntok;            /* thin path: MMA N (tokens padded to 16 or 32) */
+  int32_t vec;             /* SIMT path: 16-byte copy variant */
+  int64_t tiles;           /* output tiles over all batches */
+  int64_t grid;            /* CTAs launched */
+  int64_t kblocks;         /* K blocks per tile */
+  int64_t workspace_bytes; /* library workspace needed (thin path) */
+} dg_plan;
+
+/*
+ * The kernel choice and launch shape for a problem, without running it.
+ * dtype: 0 = FP32 path, 1 = BF16 path.  num_sms <= 0 queries the current
+ * device (needs a GPU); pass the SM count explicitly to plan on a CPU.
+ * Pointer alignment is not considered (vec assumes aligned rows).
+ */
+dg_status dg_plan_gemm(int32_t dtype, int64_t M, int64_t N, int64_t K, int64_t batch, dg_op op_b,
+                       dg_out c_type, int32_t num_sms, dg_plan* out);
+
+/* Tile raster: linear tile id -> (batch, tile row, tile column). */
+void dg_raster_tile(int64_t t, int64_t tiles_m, int64_t tiles_n, int32_t group, int64_t* b,
+                    int64_t* tm, int64_t* tn);
+
+/* Stream-K partition of `units` work units over `ctas` CTAs: first unit of CTA c. */
+int64_t dg_streamk_start(int64_t c, int64_t units, int64_t ctas);
+
+/*
+ * Interface-traffic model of a tiled GEMM ("Operator & Runtime" section 5.2.2,
+ * Example 5-3): every m x n output tile reads its own A and B panels once,
+ * V = e*M*K*(N/n) + e*K*N*(M/m) + e_out*M*N bytes, and needs
+ * S = e*m*k + e*k*n + 4*m*n bytes of local memory (FP32 accumulator).
+ */
+double dg_model_traffic_bytes(int64_t M, int64_t N, int64_t K, int64_t tile_m, int64_t tile_n,
+                              int32_t elem_bytes, int32_t out_bytes);
+int64_t dg_model_local_bytes(int64_t tile_m, int64_t tile_n, int64_t tile_k, int32_t elem_bytes);
+
+/* Library version string. */
+const char* dg_version(void);
+
+/* Test hook: 0 = off.  1 = the tcgen05 tile kernel's MMA issuer skips its stage
+ * releases, so the bounded waits expire and DG_ERR_TIMEOUT is reported (no hang,
+ * no fault).  Affects launches made after the call. */
+void dg_set_fault_injection(int32_t mode);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DGEMM_SM103_H */

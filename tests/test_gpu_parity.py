@@ -1,0 +1,341 @@
+"""GPU parity: the CUDA path (called through the C ABI) against the CPU oracle.
+
+Acceptance (the stated tolerance):
+  * small-integer inputs: bit-exact (sums are exact in FP32 for any order);
+  * FP32 output:  |C - C_ref| <= 1e-5 * D,  D = sum_k |alpha a b| + |beta c0|;
+  * BF16 output:  |C - C_ref| <= 2e-4 * D + ulp_bf16(|C_ref|).
+Sizes the oracle finishes in seconds are compared element by element; the full-size
+workloads are compared on sampled outputs computed one dot product at a time.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import dense_gemm_sm_gb300 as dg
+from dense_gemm_sm_gb300 import inputs
+
+from .helpers import (assert_bf16_close, assert_f32_close, dev_bf16, dev_f32, host_bf16_bits,
+                      host_f32, sample_indices, torch_mod)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch():
+    t = torch_mod()
+    if not t.cuda.is_available():
+        pytest.skip("no CUDA device")
+    dg.load()
+    return t
+
+
+def sync(torch):
+    torch.cuda.synchronize()
+    st = dg.dg_device_status()
+    assert st == dg.DG_OK, dg.status_string(st)
+
+
+# ------------------------------------------------------------------------- FP32 path
+
+def run_f32(torch, M, N, K, alpha, A, lda, B, ldb, beta, C0, ldc):
+    dA, dB = dev_f32(A), dev_f32(B)
+    dC = dev_f32(C0) if C0 is not None else torch.full((M * ldc,), float("nan"), device="cuda")
+    dg.gemm_f32(M, N, K, float(alpha), dA, lda, dB, ldb, float(beta), dC, ldc)
+    sync(torch)
+    return host_f32(dC).reshape(-1)
+
+
+def check_f32_full(torch, w):
+    M, N, K, lda, ldb, ldc = w["M"], w["N"], w["K"], w["lda"], w["ldb"], w["ldc"]
+    C = run_f32(torch, M, N, K, w["alpha"], w["A"], lda, w["B"], ldb, w["beta"], w["C0"], ldc)
+    ref, den = oracle.gemm(M, N, K, w["alpha"], w["A"], lda, w["B"], ldb, w["beta"], w["C0"], ldc,
+                           absden=True)
+    Cv = C.reshape(-1, ldc)[:M, :N] if ldc != N else C.reshape(M, N)
+    return Cv, ref[0], den[0]
+
+
+def test_f32_256_integer_bit_exact(torch):
+    w = inputs.sgemm_256(integer=True)
+    C, ref, _ = check_f32_full(torch, w)
+    assert np.array_equal(C.astype(np.float64), ref)
+
+
+def test_f32_256_uniform(torch):
+    w = inputs.sgemm_256()
+    C, ref, den = check_f32_full(torch, w)
+    assert_f32_close(C, ref, den, "sgemm 256^3")
+
+
+def test_f32_ragged_padded_ld(torch):
+    w = inputs.sgemm_ragged()
+    C, ref, den = check_f32_full(torch, w)
+    assert_f32_close(C, ref, den, "sgemm 1000x3000x777")
+    # padding columns of C (beyond N) are not written
+    M, ldc, N = w["M"], w["ldc"], w["N"]
+    assert ldc == N or np.all(np.isnan(C.reshape(M, -1)[:, N:]))
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (7, 9, 5), (127, 129, 33), (129, 127, 17),
+                                   (1, 300, 64), (300, 1, 64), (64, 64, 1), (200, 136, 1000)])
+@pytest.mark.parametrize("aligned", [True, False])
+def test_f32_edge_shapes(torch, M, N, K, aligned):
+    pad = 4 if aligned else 3
+    lda = ((K + 3) // 4) * 4 + (0 if aligned else 1)
+    ldb = ((N + 3) // 4) * 4 + (0 if aligned else 1)
+    ldc = ((N + 3) // 4) * 4 + (0 if aligned else pad)
+    A = inputs.pad_rows(inputs.uniform_f32(M * 7 + K, (M, K)), lda)
+    B = inputs.pad_rows(inputs.uniform_f32(N * 3 + K, (K, N)), ldb)
+    C0 = inputs.pad_rows(inputs.uniform_f32(M + N, (M, N)), ldc)
+    w = dict(M=M, N=N, K=K, alpha=np.float32(0.75), beta=np.float32(-1.25), A=A, lda=lda, B=B,
+             ldb=ldb, C0=C0, ldc=ldc)
+    C, ref, den = check_f32_full(torch, w)
+    assert_f32_close(C, ref, den, f"sgemm {M}x{N}x{K} aligned={aligned}")
+
+
+def test_f32_alpha_zero_and_k_zero(torch):
+    M, N, K = 33, 65, 17
+    A = inputs.uniform_f32(1, (M, K))
+    B = inputs.uniform_f32(2, (K, N))
+    C0 = inputs.uniform_f32(3, (M, N))
+    C = run_f32(torch, M, N, K, 0.0, A, K, B, N, 0.5, C0, N).reshape(M, N)
+    assert np.array_equal(C, (np.float32(0.5) * C0))
+    C = run_f32(torch, M, N, 0, 1.0, A, K, B, N, -2.0, C0, N).reshape(M, N)
+    assert np.array_equal(C, (np.float32(-2.0) * C0))
+    # beta = 0: NaN in C is not read
+    C = run_f32(torch, M, N, K, 1.0, A, K, B, N, 0.0, None, N).reshape(M, N)
+    assert np.all(np.isfinite(C))
+
+
+def test_f32_no_tf32_substitution(torch):
+    # A = 1 + r * 2^-18 (r small integers), B = 1: the sum keeps r exactly in FP32, while a
+    # 10-bit-mantissa (TF32) product would drop it and miss the 1e-5 bound by ~10x.
+    M, N, K = 128, 128, 256
+    r = np.random.Generator(np.random.PCG64(5)).integers(1, 8, size=(M, K))
+    A = (1.0 + r * 2.0 ** -18).astype(np.float32)
+    B = np.ones((K, N), dtype=np.float32)
+    C = run_f32(torch, M, N, K, 1.0, A, K, B, N, 0.0, None, N).reshape(M, N)
+    ref = oracle.gemm(M, N, K, 1.0, A, K, B, N)[0]
+    assert np.array_equal(C.astype(np.float64), ref)
+
+
+@pytest.mark.parametrize("op_b", [dg.DG_OP_N, dg.DG_OP_T])
+def test_f32_strided_batched(torch, op_b):
+    batch, M, N, K = 3, 130, 70, 45
+    lda, ldc = 48, 72
+    ldb = 72 if op_b == dg.DG_OP_N else 48
+    brows = K if op_b == dg.DG_OP_N else N
+    sA, sB, sC = M * lda + 8, brows * ldb + 4, M * ldc + 12
+    A = inputs.uniform_f32(10, (batch * sA,))
+    B = inputs.uniform_f32(11, (batch * sB,))
+    C0 = inputs.uniform_f32(12, (batch * sC,))
+    dA, dB, dC = dev_f32(A), dev_f32(B), dev_f32(C0)
+    dg.gemm_f32_strided_batched(M, N, K, 1.5, dA, lda, sA, dB, ldb, sB, op_b, 0.25, dC, ldc, sC,
+                                batch)
+    sync(torch)
+    C = host_f32(dC)
+    ref, den = oracle.gemm(M, N, K, 1.5, A, lda, B, ldb, 0.25, C0, ldc, op_b=op_b, batch=batch,
+                           strideA=sA, strideB=sB, strideC=sC, absden=True)
+    for b in range(batch):
+        Cb = C[b * sC:b * sC + M * ldc].reshape(M, ldc)[:, :N]
+        assert_f32_close(Cb, ref[b], den[b], f"batched f32 b={b}")
+
+
+def test_f32_4096_sampled(torch):
+    w = inputs.sgemm_4096()
+    M, N, K = w["M"], w["N"], w["K"]
+    dA, dB, dC = dev_f32(w["A"]), dev_f32(w["B"]), dev_f32(w["C0"])
+    dg.gemm_f32(M, N, K, float(w["alpha"]), dA, K, dB, N, float(w["beta"]), dC, N)
+    sync(torch)
+    C = host_f32(dC).reshape(M, N)
+    rows, cols = sample_indices(41, 3000, M, N)
+    ref, den = oracle.gemm_entries(M, N, K, w["alpha"], w["A"], K, w["B"], N, w["beta"], w["C0"],
+                                   N, rows, cols)
+    assert_f32_close(C[rows, cols], ref, den, "sgemm 4096^3 (sampled)")
+
+
+# ------------------------------------------------------------------------- BF16 path
+
+def run_bf16(torch, M, N, K, alpha, A, lda, B, ldb, beta, C0, ldc, out_f32=False):
+    dA, dB = dev_bf16(A), dev_bf16(B)
+    if out_f32:
+        dC = dev_f32(C0) if C0 is not None else torch.full((M * ldc,), float("nan"), device="cuda")
+    else:
+        dC = dev_bf16(C0) if C0 is not None else torch.full((M * ldc,), float("nan"), device="cuda",
+                                                             dtype=torch.bfloat16)
+    dg.gemm_bf16(M, N, K, float(alpha), dA, lda, dB, ldb, float(beta), dC, ldc,
+                 dg.DG_OUT_F32 if out_f32 else dg.DG_OUT_BF16)
+    sync(torch)
+    if out_f32:
+        return host_f32(dC).reshape(M, ldc)[:, :N]
+    return host_bf16_bits(dC).reshape(M, ldc)[:, :N]
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 384, 320), (1, 256, 128), (16, 12288, 4096),
+                                   (40, 520, 136)])
+def test_bf16_integer_bit_exact(torch, M, N, K):
+    A = inputs.f32_to_bf16_bits(inputs.integer_f32(M + K, (M, K)))
+    B = inputs.f32_to_bf16_bits(inputs.integer_f32(N + K, (K, N)))
+    C = run_bf16(torch, M, N, K, 1.0, A, K, B, N, 0.0, None, N)
+    ref = oracle.gemm(M, N, K, 1.0, A, K, B, N)[0]
+    assert np.array_equal(C, oracle.round_bf16(ref))
+
+
+def test_bf16_ffn_reduced_full_compare(torch):
+    w = inputs.ffn_bf16(M=512, K=1024, N=2048)
+    M, N, K = w["M"], w["N"], w["K"]
+    C = run_bf16(torch, M, N, K, w["alpha"], w["A"], K, w["B"], N, 0.0, None, N)
+    ref, den = oracle.gemm(M, N, K, w["alpha"], w["A"], K, w["B"], N, absden=True)
+    assert_bf16_close(C, ref[0], den[0], "ffn-shaped 512x2048x1024")
+
+
+@pytest.mark.parametrize("M,N,K", [(129, 264, 72), (300, 1000, 200), (200, 136, 8), (33, 8, 16),
+                                   (128, 256, 64), (255, 520, 4104)])
+@pytest.mark.parametrize("out_f32", [False, True])
+def test_bf16_edge_shapes(torch, M, N, K, out_f32):
+    lda = ((K + 7) // 8) * 8
+    ldb = ((N + 7) // 8) * 8 + 8
+    ldc = N + 3
+    A = inputs.pad_rows(inputs.f32_to_bf16_bits(inputs.normal_f32(M + 1, (M, K))), lda, 0)
+    B = inputs.pad_rows(inputs.f32_to_bf16_bits(inputs.normal_f32(N + 2, (K, N), 0.1)), ldb, 0)
+    c0 = inputs.normal_f32(M + N, (M, N))
+    C0 = inputs.pad_rows(c0 if out_f32 else inputs.f32_to_bf16_bits(c0), ldc, 0)
+    alpha, beta = np.float32(0.5), np.float32(-0.75)
+    C = run_bf16(torch, M, N, K, alpha, A, lda, B, ldb, beta, C0, ldc, out_f32)
+    ref, den = oracle.gemm(M, N, K, alpha, A, lda, B, ldb, beta, C0, ldc, absden=True)
+    if out_f32:
+        assert_f32_close(C, ref[0], den[0], f"bf16->f32 {M}x{N}x{K}")
+    else:
+        assert_bf16_close(C, ref[0], den[0], f"bf16 {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M", [1, 4, 16, 17, 32])
+def test_bf16_decode_full_size(torch, M):
+    W = inputs.ffn_weight()
+    w = inputs.decode_bf16(M, W=W)
+    N, K = w["N"], w["K"]
+    C = run_bf16(torch, M, N, K, 1.0, w["A"], K, W, N, 0.0, None, N)
+    ref, den = oracle.gemm(M, N, K, 1.0, w["A"], K, W, N, absden=True)
+    assert_bf16_close(C, ref[0], den[0], f"decode M={M}")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 8, 8), (3, 136, 200), (16, 1000, 4104), (5, 128, 64),
+                                   (9, 4096, 64), (32, 264, 2056)])
+def test_bf16_thin_ragged(torch, M, N, K):
+    lda = ((K + 7) // 8) * 8
+    ldb = ((N + 7) // 8) * 8
+    A = inputs.pad_rows(inputs.f32_to_bf16_bits(inputs.normal_f32(K + M, (M, K))), lda, 0)
+    B = inputs.pad_rows(inputs.f32_to_bf16_bits(inputs.normal_f32(N + K, (K, N), 0.05)), ldb, 0)
+    c0 = inputs.f32_to_bf16_bits(inputs.normal_f32(7, (M, N)))
+    C = run_bf16(torch, M, N, K, 1.25, A, lda, B, ldb, 0.5, c0, N)
+    ref, den = oracle.gemm(M, N, K, 1.25, A, lda, B, ldb, 0.5, c0, N, absden=True)
+    assert_bf16_close(C, ref[0], den[0], f"thin {M}x{N}x{K}")
+
+
+def test_bf16_decode_deterministic(torch):
+    W = inputs.ffn_weight()
+    w = inputs.decode_bf16(16, W=W)
+    dA, dB = dev_bf16(w["A"]), dev_bf16(W)
+    outs = []
+    for _ in range(3):
+        dC = torch.empty((16, 12288), dtype=torch.bfloat16, device="cuda")
+        dg.gemm_bf16(16, 12288, 4096, 1.0, dA, 4096, dB, 12288, 0.0, dC, 12288)
+        sync(torch)
+        outs.append(host_bf16_bits(dC))
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
+
+
+def test_bf16_ffn_full_size_sampled(torch):
+    w = inputs.ffn_bf16()
+    M, N, K = w["M"], w["N"], w["K"]
+    dA, dB = dev_bf16(w["A"]), dev_bf16(w["B"])
+    dC = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    dg.gemm_bf16(M, N, K, 1.0, dA, K, dB, N, 0.0, dC, N)
+    sync(torch)
+    C = host_bf16_bits(dC)
+    rows, cols = sample_indices(43, 4000, M, N)
+    ref, den = oracle.gemm_entries(M, N, K, 1.0, w["A"], K, w["B"], N, 0.0, None, N, rows, cols)
+    assert_bf16_close(C[rows, cols], ref, den, "FFN 1024x12288x4096 (sampled)")
+    # a whole 128 x 256 tile in the middle, every element
+    r0, c0 = 384, 4096
+    rr, cc = np.meshgrid(np.arange(r0, r0 + 128), np.arange(c0, c0 + 256), indexing="ij")
+    ref, den = oracle.gemm_entries(M, N, K, 1.0, w["A"], K, w["B"], N, 0.0, None, N, rr.ravel(),
+                                   cc.ravel())
+    assert_bf16_close(C[rr, cc].ravel(), ref, den, "FFN one full tile")
+
+
+def run_qk(torch, w):
+    batch, S, D = w["batch"], w["M"], w["K"]
+    dQ, dK = dev_bf16(w["A"]), dev_bf16(w["B"])
+    dC = torch.empty((batch, S, S), dtype=torch.float32, device="cuda")
+    dg.gemm_bf16_strided_batched(S, S, D, float(w["alpha"]), dQ, D, S * D, dK, D, S * D,
+                                 dg.DG_OP_T, 0.0, dC, S, S * S, batch, dg.DG_OUT_F32)
+    sync(torch)
+    return dC
+
+
+def test_bf16_batched_qk_reduced_full_compare(torch):
+    w = inputs.qk_batched(batch=3, S=384, D=128)
+    batch, S, D = w["batch"], w["M"], w["K"]
+    C = host_f32(run_qk(torch, w))
+    ref, den = oracle.gemm(S, S, D, w["alpha"], w["A"], D, w["B"], D, op_b=1, batch=batch,
+                           strideA=S * D, strideB=S * D, absden=True)
+    for b in range(batch):
+        assert_f32_close(C[b], ref[b], den[b], f"QK^T batch {b}")
+
+
+def test_bf16_batched_qk_full_size_sampled(torch):
+    w = inputs.qk_batched()
+    batch, S, D = w["batch"], w["M"], w["K"]
+    C = host_f32(run_qk(torch, w))
+    bidx, rows, cols = sample_indices(44, 4000, batch, S, S)
+    ref, den = oracle.gemm_entries(S, S, D, w["alpha"], w["A"], D, w["B"], D, 0.0, None, S, rows,
+                                   cols, op_b=1, bidx=bidx, strideA=S * D, strideB=S * D,
+                                   strideC=S * S)
+    assert_f32_close(C[bidx, rows, cols], ref, den, "QK^T 64x2048x2048x128 (sampled)")
+
+
+@pytest.mark.parametrize("op_b", [dg.DG_OP_N, dg.DG_OP_T])
+def test_bf16_strided_batched_bf16_out(torch, op_b):
+    batch, M, N, K = 5, 200, 264, 136
+    brows, bcols = (K, N) if op_b == dg.DG_OP_N else (N, K)
+    sA, sB, sC = M * K + 64, brows * bcols + 8, M * N + 40
+    A = inputs.f32_to_bf16_bits(inputs.normal_f32(30, (batch * sA,)))
+    B = inputs.f32_to_bf16_bits(inputs.normal_f32(31, (batch * sB,), 0.1))
+    C0 = inputs.f32_to_bf16_bits(inputs.normal_f32(32, (batch * sC,)))
+    dA, dB, dC = dev_bf16(A), dev_bf16(B), dev_bf16(C0)
+    dg.gemm_bf16_strided_batched(M, N, K, 0.5, dA, K, sA, dB, bcols, sB, op_b, 2.0, dC, N, sC,
+                                 batch, dg.DG_OUT_BF16)
+    sync(torch)
+    C = host_bf16_bits(dC)
+    ref, den = oracle.gemm(M, N, K, 0.5, A, K, B, bcols, 2.0, C0, N, op_b=op_b, batch=batch,
+                           strideA=sA, strideB=sB, strideC=sC, absden=True)
+    for b in range(batch):
+        Cb = C[b * sC:b * sC + M * N].reshape(M, N)
+        assert_bf16_close(Cb, ref[b], den[b], f"batched bf16 op_b={op_b} b={b}")
+
+
+def test_bf16_tile_kernel_deterministic(torch):
+    w = inputs.ffn_bf16(M=384, K=2048, N=1536)
+    dA, dB = dev_bf16(w["A"]), dev_bf16(w["B"])
+    outs = []
+    for _ in range(2):
+        dC = torch.empty((384, 1536), dtype=torch.bfloat16, device="cuda")
+        dg.gemm_bf16(384, 1536, 2048, 1.0, dA, 2048, dB, 1536, 0.0, dC, 1536)
+        sync(torch)
+        outs.append(host_bf16_bits(dC))
+    assert np.array_equal(outs[0], outs[1])
+
+
+def test_bf16_argument_errors(torch):
+    A = torch.zeros(64 * 64, dtype=torch.bfloat16, device="cuda")
+    C = torch.zeros(64 * 64, dtype=torch.bfloat16, device="cuda")
+    st = dg.gemm_bf16(64, 64, 60, 1.0, A, 60, A, 64, 0.0, C, 64, check=False)
+    assert st == dg.DG_ERR_MISALIGNED                              # lda % 8 != 0
+    st = dg.gemm_bf16(64, 64, 64, 1.0, A.data_ptr() + 2, 64, A, 64, 0.0, C, 64, check=False)
+    assert st == dg.DG_ERR_MISALIGNED                              # base not 16-byte aligned
+    assert dg.gemm_bf16(-1, 64, 64, 1.0, A, 64, A, 64, 0.0, C, 64, check=False) == dg.DG_ERR_INVALID_ARG
+    assert dg.gemm_bf16(64, 64, 64, 1.0, A, 32, A, 64, 0.0, C, 64, check=False) == dg.DG_ERR_INVALID_ARG
+    assert dg.gemm_bf16(64, 64, 64, 1.0, A, 64, A, 64, 0.0, C, 64, c_type=7,
+                        check=False) == dg.DG_ERR_INVALID_ARG
+    assert dg.gemm_bf16(0, 64, 64, 1.0, None, 64, None, 64, 0.0, None, 64, check=False) == dg.DG_OK
+    sync(torch)

@@ -1,0 +1,109 @@
+"""Host-side checks (no GPU): the library loads and exports the declared ABI, and the
+planner / raster / stream-K / traffic-model logic matches the pages' numbers."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import dense_gemm_sm_gb300 as dg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "dgemm.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w[\w\s\*]*?\b(\w+)\s*\(", src, flags=re.M)) - {"if"})
+
+
+def test_library_exports_every_declared_symbol():
+    lib = dg.load()
+    names = declared_functions()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/dgemm.h but not exported"
+    assert set(names) == set(dg.EXPORTED)
+
+
+def test_status_strings():
+    for s in range(7):
+        assert dg.status_string(s).startswith("DG_")
+
+
+def test_plan_dispatch_table():
+    ffn = dg.dg_plan_gemm(1, 1024, 12288, 4096, num_sms=152)
+    assert ffn["kernel"] == dg.DG_KERNEL_TC_BF16 and ffn["tile_n"] == 256 and ffn["tiles"] == 384
+    assert ffn["grid"] == 152
+    for m in (1, 4, 16):
+        p = dg.dg_plan_gemm(1, m, 12288, 4096, num_sms=152)
+        assert p["kernel"] == dg.DG_KERNEL_THIN_BF16 and p["ntok"] == 16
+    assert dg.dg_plan_gemm(1, 32, 12288, 4096, num_sms=152)["ntok"] == 32
+    assert dg.dg_plan_gemm(1, 33, 12288, 4096, num_sms=152)["kernel"] == dg.DG_KERNEL_TC_BF16
+    qk = dg.dg_plan_gemm(1, 2048, 2048, 128, batch=64, op_b=dg.DG_OP_T, c_type=dg.DG_OUT_F32,
+                         num_sms=152)
+    assert qk["kernel"] == dg.DG_KERNEL_TC_BF16 and qk["tiles"] == 64 * 16 * 8
+    assert dg.dg_plan_gemm(0, 4096, 4096, 4096, num_sms=152)["kernel"] == dg.DG_KERNEL_SIMT_F32
+    assert dg.dg_plan_gemm(0, 10, 10, 0, num_sms=152)["kernel"] == dg.DG_KERNEL_SCALE
+    assert dg.dg_plan_gemm(1, 0, 10, 10, num_sms=152)["kernel"] == dg.DG_KERNEL_NONE
+
+
+@pytest.mark.parametrize("tiles_m,tiles_n,group", [(10, 10, 8), (8, 48, 8), (32, 16, 8), (3, 7, 8),
+                                                    (17, 5, 4), (1, 1, 8), (9, 1, 8)])
+def test_raster_is_a_bijection(tiles_m, tiles_n, group):
+    # Swizzle bijection and range property (MUSA lesson m11-l5, Block ID Swizzle discussion).
+    batch = 2
+    seen = set()
+    for t in range(batch * tiles_m * tiles_n):
+        b, tm, tn = dg.dg_raster_tile(t, tiles_m, tiles_n, group)
+        assert 0 <= b < batch and 0 <= tm < tiles_m and 0 <= tn < tiles_n
+        seen.add((b, tm, tn))
+    assert len(seen) == batch * tiles_m * tiles_n
+
+
+def test_raster_locality_matches_swizzle_example():
+    # MUSA lesson m11-l5: changing row every 8 blocks, 64 blocks need 8 tile_m and 8 tile_n
+    # operand tiles: amplification (64+64)/(8+8) = 8 versus ~2 for the plain row order.
+    tiles_m, tiles_n = 64, 64
+    for start in range(0, tiles_m * tiles_n, 64):
+        ids = [dg.dg_raster_tile(t, tiles_m, tiles_n, 8) for t in range(start, start + 64)]
+        rows = {tm for _, tm, _ in ids}
+        cols = {tn for _, _, tn in ids}
+        assert len(rows) == 8 and len(cols) == 8
+        assert (64 + 64) / (len(rows) + len(cols)) == 8
+
+
+def test_streamk_partition_covers_units_once():
+    for units, ctas in [(6144, 152), (96, 152), (7, 3), (1000, 152), (152, 152)]:
+        starts = [dg.dg_streamk_start(c, units, ctas) for c in range(ctas + 1)]
+        assert starts[0] == 0 and starts[-1] == units
+        assert all(a <= b for a, b in zip(starts, starts[1:]))
+        sizes = [b - a for a, b in zip(starts, starts[1:])]
+        assert max(sizes) - min(sizes) <= 1
+
+
+def read_tile_table():
+    rows = []
+    for line in open(os.path.join(GOLDEN, "tile_traffic.txt")):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            rows.append([float(x) for x in line.split()])
+    return rows
+
+
+def test_tile_traffic_model_reproduces_pages_table():
+    # "Operator & Runtime" section 5.2.2, Example 5-3 and its table (k = 32).
+    M, K, N = 1024, 4096, 12288
+    flops = 2 * M * N * K
+    for m, n, kib, mib, intensity in read_tile_table():
+        assert dg.dg_model_local_bytes(int(m), int(n), 32, 2) == kib * 1024
+        v = dg.dg_model_traffic_bytes(M, N, K, int(m), int(n), 2, 2)
+        assert v == mib * 2 ** 20
+        assert abs(flops / v - intensity) < 0.06
+
+
+def test_ffn_counts_from_chapter_intro():
+    # 128 MiB once-through bytes = the traffic model with one tile covering everything.
+    v = dg.dg_model_traffic_bytes(1024, 12288, 4096, 1024, 12288, 2, 2)
+    assert v == 128 * 2 ** 20
