@@ -107,15 +107,19 @@ def test_f32_alpha_zero_and_k_zero(torch):
 
 
 def test_f32_no_tf32_substitution(torch):
-    # A = 1 + r * 2^-18 (r small integers), B = 1: the sum keeps r exactly in FP32, while a
-    # 10-bit-mantissa (TF32) product would drop it and miss the 1e-5 bound by ~10x.
-    M, N, K = 128, 128, 256
+    # A = 1 + r * 2^-12 (r in 1..7), B = 1, K = 64: every partial sum is a multiple of 2^-12
+    # below 128, so FP32 accumulation is exact and the result must match bit for bit.  A
+    # TF32 (10-bit mantissa) operand would round r * 2^-12 away, an error of about
+    # 2.4e-4 * D, 24 times the FP32 bound.
+    M, N, K = 128, 128, 64
     r = np.random.Generator(np.random.PCG64(5)).integers(1, 8, size=(M, K))
-    A = (1.0 + r * 2.0 ** -18).astype(np.float32)
+    A = (1.0 + r * 2.0 ** -12).astype(np.float32)
     B = np.ones((K, N), dtype=np.float32)
     C = run_f32(torch, M, N, K, 1.0, A, K, B, N, 0.0, None, N).reshape(M, N)
-    ref = oracle.gemm(M, N, K, 1.0, A, K, B, N)[0]
-    assert np.array_equal(C.astype(np.float64), ref)
+    ref, den = oracle.gemm(M, N, K, 1.0, A, K, B, N, absden=True)
+    assert np.array_equal(C.astype(np.float64), ref[0])
+    tf32_like = oracle.gemm(M, N, K, 1.0, np.ones_like(A), K, B, N)[0]  # r * 2^-12 rounded away
+    assert not oracle.check_f32(tf32_like, ref[0], den[0])[0]
 
 
 @pytest.mark.parametrize("op_b", [dg.DG_OP_N, dg.DG_OP_T])
