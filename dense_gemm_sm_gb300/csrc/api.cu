@@ -328,6 +328,10 @@ __global__ void scale_kernel(T* C, int64_t M, int64_t N, int64_t ldc, int64_t sC
 
 }  // namespace
 
+cudaError_t device_status_word(int dev, uint32_t** status, int* sms) {
+  return device_info(dev, status, sms);
+}
+
 cudaError_t launch_scale(void* C, bool c_f32, int64_t M, int64_t N, int64_t ldc, int64_t strideC,
                          int64_t batch, float beta, cudaStream_t s) {
   const int64_t total = batch * M * N;

@@ -110,6 +110,31 @@ dg_status gemm_bf16_strided_batched(int64_t M, int64_t N, int64_t K, float alpha
                                     float beta, void* C, int64_t ldc, int64_t strideC,
                                     int64_t batch, dg_out c_type, void* stream);
 
+/*
+ * gemm_bf16 for decode shapes, without any allocation.  The pages have no counterpart: this
+ * entry point exists for callers that cannot let a library call cudaMalloc -- a framework
+ * whose caching allocator already holds the device memory (a new cudaMalloc may fail or
+ * fragment its pool), or a latency-critical decode loop that cannot take cudaMalloc's
+ * implicit device-wide synchronisation.  gemm_bf16 gives its split-K decode kernel a
+ * workspace it allocates on first use; this variant runs the same kernel with its scratch
+ * (FP32 partial sums, per-tile arrival counters) in a fixed array inside the library's
+ * device image, 2.5 MiB + 32 KiB, which every GPU that loads the library holds until exit.
+ *   - Arguments, layout and result are those of gemm_bf16 (op(B) = B), restricted to
+ *     M <= 16 and N <= 1,048,576; larger sizes return DG_ERR_UNSUPPORTED and enqueue
+ *     nothing.  Alignment rules as gemm_bf16 (DG_ERR_MISALIGNED).
+ *   - Calls no cudaMalloc, cudaFree or other allocating routine.  The first call on a
+ *     device looks up the array's device address (cudaGetSymbolAddress) for that device;
+ *     make that first call before any stream capture.
+ *   - Every call shares the one array and leaves its contents behind; each call zeroes the
+ *     counters it uses (cudaMemsetAsync on `stream`) before its kernel.  Calls whose work
+ *     overlaps on the GPU (other streams, other host threads) race on the array and give
+ *     wrong results: serialise them.
+ */
+dg_status gemm_bf16_decode_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
+                                   const uint16_t* A, int64_t lda, const uint16_t* B,
+                                   int64_t ldb, float beta, void* C, int64_t ldc, dg_out c_type,
+                                   void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* dg_status_string(dg_status s);
 
