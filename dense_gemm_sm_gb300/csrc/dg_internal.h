@@ -1,6 +1,8 @@
 // dg_internal.h -- declarations shared by the C-ABI layer and the kernel translation units.
 #pragma once
 #include <cuda_runtime.h>
+
+#include <atomic>
 #include <cstdint>
 
 #include "../../include/dgemm.h"
@@ -52,7 +54,7 @@ struct ThinParams {
   float alpha, beta;
   void* C; int64_t ldc;
   int32_t c_f32;
-  float* ws;           // partials: [ctas][2][ntok][128] fp32
+  float* ws;           // partials: [ctas][2][128 columns][ntok] fp32
   uint32_t* counters;  // [n_tiles], zero between calls
   uint32_t* status;
 };
@@ -65,6 +67,20 @@ inline int64_t thin_ws_floats(int64_t ctas, int ntok) { return ctas * 2 * ntok *
 // C = beta * C over a (batch, M, N) strided view (K == 0 or alpha == 0).
 cudaError_t launch_scale(void* C, bool c_f32, int64_t M, int64_t N, int64_t ldc, int64_t strideC,
                          int64_t batch, float beta, cudaStream_t s);
+
+// Sets the dynamic shared-memory limit of a kernel once per device (the attribute is
+// per function and context; setting it on every call costs host time on the launch path).
+template <typename Kernel>
+inline cudaError_t ensure_smem_attr(Kernel kern, int bytes, std::atomic<uint64_t>& done_mask) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done_mask.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done_mask.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 // Fault injection for the bounded-wait tests (host-set, read by the kernels at launch).
 extern int g_fault_injection;

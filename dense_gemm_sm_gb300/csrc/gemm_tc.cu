@@ -23,6 +23,10 @@
 // warps 2-5 = epilogue (warp w reads TMEM lanes 32*(w%4) .. 32*(w%4)+31).
 #include <cuda_bf16.h>
 
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
 #include "dg_internal.h"
 #include "ptx.cuh"
 #include "tile_sched.h"
@@ -302,10 +306,44 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 
 EncodeTiledFn get_encode_tiled();
 
+namespace {
+struct MapKey {
+  const void* base;
+  uint64_t inner, outer, ld, batch, stride;
+  uint32_t box_inner, box_outer;
+  bool operator==(const MapKey& o) const { return std::memcmp(this, &o, sizeof(MapKey)) == 0; }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey& k) const {
+    uint64_t h = reinterpret_cast<uintptr_t>(k.base);
+    const uint64_t v[7] = {k.inner, k.outer, k.ld, k.batch, k.stride, k.box_inner, k.box_outer};
+    for (uint64_t x : v) h = (h ^ x) * 0x100000001B3ull;
+    return static_cast<size_t>(h);
+  }
+};
+std::mutex g_map_mu;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_map_cache;
+}  // namespace
+
 // Builds a BF16 tensor map over a (batch x) outer x inner row-major view with a
 // box_inner x box_outer box and 128-byte swizzle.  Out-of-range elements read as zero.
+// Encoded maps are cached by (address, shape, box): repeated calls on the same buffers
+// (the usual inference loop) skip the encoding on the launch path.
 bool make_bf16_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
                    uint64_t batch, uint64_t stride, uint32_t box_inner, uint32_t box_outer) {
+  MapKey key;
+  std::memset(&key, 0, sizeof key);
+  key.base = base; key.inner = inner; key.outer = outer; key.ld = ld;
+  key.batch = batch > 1 ? batch : 1; key.stride = batch > 1 ? stride : 0;
+  key.box_inner = box_inner; key.box_outer = box_outer;
+  {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    auto it = g_map_cache.find(key);
+    if (it != g_map_cache.end()) {
+      *map = it->second;
+      return true;
+    }
+  }
   static EncodeTiledFn fn = get_encode_tiled();
   if (!fn) return false;
   const bool rank3 = batch > 1;
@@ -317,7 +355,11 @@ bool make_bf16_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t 
                   dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  if (r != CUDA_SUCCESS) return false;
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  if (g_map_cache.size() >= 4096) g_map_cache.clear();
+  g_map_cache.emplace(key, *map);
+  return true;
 }
 
 EncodeTiledFn get_encode_tiled() {
@@ -336,7 +378,8 @@ cudaError_t launch_tc_variant(const CUtensorMap& ma, const CUtensorMap& mb, cons
                               int num_ctas, cudaStream_t s) {
   auto kern = gemm_tc_kernel<BN, B_KMAJOR, RANK3>;
   constexpr uint32_t smem = TcCfg<BN>::SMEM_BYTES;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t e = ensure_smem_attr(kern, smem, attr_done);
   if (e != cudaSuccess) return e;
   kern<<<num_ctas, NUM_THREADS, smem, s>>>(ma, mb, p, g_fault_injection);
   return cudaGetLastError();

@@ -266,11 +266,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         epi_bar();  // seg_ok is rewritten for the next segment only after everyone read it
         continue;
       }
-      // Partial K range: publish the partial sums, then count arrivals for the tile.
+      // Partial K range: publish the partial sums (one thread = one W column, its ntok
+      // values contiguous, so the stores and the combine's loads are 16-byte vectors),
+      // then count arrivals for the tile.
       const int slot = sk_slot(c, sg.tile, p.kblocks, p.units, p.ctas);
-      float* mine = p.ws + ((c * 2 + slot) * NTOK) * BNW;
+      float4* mine = reinterpret_cast<float4*>(p.ws + ((c * 2 + slot) * BNW + row) * NTOK);
 #pragma unroll
-      for (int t = 0; t < NTOK; ++t) mine[t * BNW + row] = v[t];
+      for (int q4 = 0; q4 < NTOK / 4; ++q4)
+        mine[q4] = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
       __threadfence();
       epi_bar();
       if (etid == 0) {
@@ -284,15 +287,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __threadfence();
         const int64_t first = sk_cta_of(sg.tile * p.kblocks, p.units, p.ctas);
         const int64_t last = sk_cta_of((sg.tile + 1) * p.kblocks - 1, p.units, p.ctas);
-        if (n < p.N) {
-          for (int64_t t = 0; t < p.M; ++t) {
-            float s = 0.f;
-            for (int64_t cc = first; cc <= last; ++cc) {
-              const int sl = sk_slot(cc, sg.tile, p.kblocks, p.units, p.ctas);
-              s += __ldcg(p.ws + ((cc * 2 + sl) * NTOK + t) * BNW + row);
-            }
-            store_out(p, t, n, s);
+        // Sum the contributors' partials in CTA order (= K order): a fixed order.
+        float s[NTOK];
+#pragma unroll
+        for (int t = 0; t < NTOK; ++t) s[t] = 0.f;
+        for (int64_t cc = first; cc <= last; ++cc) {
+          const int sl = sk_slot(cc, sg.tile, p.kblocks, p.units, p.ctas);
+          const float4* src = reinterpret_cast<const float4*>(p.ws + ((cc * 2 + sl) * BNW + row) * NTOK);
+          float4 part[NTOK / 4];
+#pragma unroll
+          for (int q4 = 0; q4 < NTOK / 4; ++q4) part[q4] = __ldcg(src + q4);
+#pragma unroll
+          for (int q4 = 0; q4 < NTOK / 4; ++q4) {
+            s[4 * q4 + 0] += part[q4].x;
+            s[4 * q4 + 1] += part[q4].y;
+            s[4 * q4 + 2] += part[q4].z;
+            s[4 * q4 + 3] += part[q4].w;
           }
+        }
+        if (n < p.N) {
+#pragma unroll
+          for (int t = 0; t < NTOK; ++t)
+            if (t < p.M) store_out(p, t, n, s[t]);
         }
         if (etid == 0) p.counters[sg.tile] = 0u;  // ready for the next call
       }
@@ -313,7 +329,8 @@ cudaError_t launch_thin_variant(const CUtensorMap& mw, const CUtensorMap& mx, co
                                 cudaStream_t s) {
   auto kern = gemm_thin_kernel<NTOK, W_KMAJOR>;
   constexpr uint32_t smem = ThinCfg<NTOK>::SMEM_BYTES;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t e = ensure_smem_attr(kern, smem, attr_done);
   if (e != cudaSuccess) return e;
   kern<<<static_cast<unsigned>(p.ctas), NUM_THREADS, smem, s>>>(mw, mx, p);
   return cudaGetLastError();

@@ -17,7 +17,8 @@
 //     bytes (conflict-free);
 //   * thread rows are interleaved (row = base + 4*i) so C rows are written by 8 lanes
 //     with 16-byte stores, 128 contiguous bytes per row segment;
-//   * strictly FP32 fused multiply-add; no TF32.
+//   * strictly FP32 fused multiply-add (packed two per instruction with fma.rn.f32x2, which
+//     halves the issue slots the FMAs take); no TF32.
 // Epilogue: C = fma(alpha, acc, beta*C_old) in FP32 (C_old not read when beta == 0), masked
 // at the edges.
 #include "dg_internal.h"
@@ -96,8 +97,34 @@ __device__ __forceinline__ float f4get(const float4& v, int i) {
   return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }
 
+#ifndef DG_SIMT_FFMA2
+#define DG_SIMT_FFMA2 1
+#endif
+#ifndef DG_SIMT_MIN_BLOCKS
+#define DG_SIMT_MIN_BLOCKS 2
+#endif
+
+// (d0, d1) += (a, a) * (b0, b1) with one packed FP32 instruction (fma.rn.f32x2): two IEEE
+// single-precision fused multiply-adds, the same arithmetic as two fmaf calls, half the
+// issue slots.
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a, float b0, float b1) {
+#if DG_SIMT_FFMA2
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %2};\n\t"
+      "mov.b64 rb, {%3, %4};\n\t"
+      "mov.b64 rd, {%0, %1};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rd;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a), "f"(b0), "f"(b1));
+#else
+  d0 = fmaf(a, b0, d0);
+  d1 = fmaf(a, b1, d1);
+#endif
+}
+
 template <bool TRANS_B, bool VEC>
-__global__ void __launch_bounds__(NT, 2) sgemm_simt_kernel(const SimtParams p) {
+__global__ void __launch_bounds__(NT, DG_SIMT_MIN_BLOCKS) sgemm_simt_kernel(const SimtParams p) {
   extern __shared__ __align__(16) float smem[];
   float* As = smem;
   float* Bs = smem + STAGES * A_STAGE;
@@ -120,19 +147,57 @@ __global__ void __launch_bounds__(NT, 2) sgemm_simt_kernel(const SimtParams p) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
 
-  const int64_t KT = (p.K + BK - 1) / BK;
-  auto load_stage = [&](int stage, int64_t kt) {
-    const int64_t k0 = kt * BK;
-    load_kmajor<VEC>(As + stage * A_STAGE, A, p.lda, m0, p.M, k0, p.K, tid);
-    if (TRANS_B)
-      load_kmajor<VEC>(Bs + stage * B_STAGE, B, p.ldb, n0, p.N, k0, p.K, tid);
-    else
-      load_nmajor<VEC>(Bs + stage * B_STAGE, B, p.ldb, k0, p.K, n0, p.N, tid);
+  const int KT = static_cast<int>((p.K + BK - 1) / BK);
+  const int K = static_cast<int>(p.K);
+
+  // Copy plan of this thread for the 16-byte path: chunks (rows ar, ar+64; K offset ac) of
+  // the A tile and, for B, (rows br, br+8; column bc) in the N layout or (rows ar, ar+64)
+  // in the T layout.  Only two running global pointers are kept; the second chunk of each
+  // operand is reached through the leading dimension (a kernel parameter), so few
+  // registers stay live across the main loop.
+  const int ar = tid >> 2, ac = (tid & 3) * 4;
+  const int br = tid >> 5, bc = (tid & 31) * 4;
+  const bool a_ok0 = m0 + ar < p.M, a_ok1 = m0 + ar + 64 < p.M;
+  const bool bt_ok0 = n0 + ar < p.N, bt_ok1 = n0 + ar + 64 < p.N;
+  const int b_nbytes = TRANS_B ? 0 : clamp_bytes(p.N - (n0 + bc));
+  const float* ga = A + (m0 + ar) * p.lda + ac;
+  const float* gb = TRANS_B ? B + (n0 + ar) * p.ldb + ac : B + br * p.ldb + n0 + bc;
+
+  int next_tile = 0;  // K tile the next issued stage copies
+  auto load_stage = [&](int stage) {
+    const int k0 = next_tile * BK;
+    if (VEC) {
+      const uint32_t as_ = smem_u32(As + stage * A_STAGE);
+      const uint32_t bs_ = smem_u32(Bs + stage * B_STAGE);
+      const int ka = clamp_bytes(K - (k0 + ac));
+      const int a0 = a_ok0 ? ka : 0, a1 = a_ok1 ? ka : 0;
+      cp_async_16(as_ + (ar * LDS_K + ac) * 4, a0 ? ga : A, a0);
+      cp_async_16(as_ + ((ar + 64) * LDS_K + ac) * 4, a1 ? ga + 64 * p.lda : A, a1);
+      ga += BK;
+      if (TRANS_B) {
+        const int b0 = bt_ok0 ? ka : 0, b1 = bt_ok1 ? ka : 0;
+        cp_async_16(bs_ + (ar * LDS_K + ac) * 4, b0 ? gb : B, b0);
+        cp_async_16(bs_ + ((ar + 64) * LDS_K + ac) * 4, b1 ? gb + 64 * p.ldb : B, b1);
+        gb += BK;
+      } else {
+        const int b0 = k0 + br < K ? b_nbytes : 0, b1 = k0 + br + 8 < K ? b_nbytes : 0;
+        cp_async_16(bs_ + (br * BN + bc) * 4, b0 ? gb : B, b0);
+        cp_async_16(bs_ + ((br + 8) * BN + bc) * 4, b1 ? gb + 8 * p.ldb : B, b1);
+        gb += BK * p.ldb;
+      }
+    } else {
+      load_kmajor<false>(As + stage * A_STAGE, A, p.lda, m0, p.M, k0, p.K, tid);
+      if (TRANS_B)
+        load_kmajor<false>(Bs + stage * B_STAGE, B, p.ldb, n0, p.N, k0, p.K, tid);
+      else
+        load_nmajor<false>(Bs + stage * B_STAGE, B, p.ldb, k0, p.K, n0, p.N, tid);
+    }
+    ++next_tile;
   };
 
 #pragma unroll
   for (int s = 0; s < STAGES - 1; ++s) {
-    if (s < KT) load_stage(s, s);
+    if (s < KT) load_stage(s);
     cp_async_commit();
   }
 
@@ -140,15 +205,14 @@ __global__ void __launch_bounds__(NT, 2) sgemm_simt_kernel(const SimtParams p) {
   const int col_base_n = wn * 64 + ln * 4;    // N layout: cols col_base_n + {0..3}, +32
   const int col_base_t = wn * 64 + ln;        // T layout: cols col_base_t + 8*j
 
-  for (int64_t kt = 0; kt < KT; ++kt) {
+  int stage = 0;                  // stage computed this iteration
+  int load_slot = STAGES - 1;     // stage the next copy goes to
+  for (int kt = 0; kt < KT; ++kt) {
     cp_async_wait<STAGES - 2>();
     __syncthreads();
-    {
-      const int64_t nk = kt + STAGES - 1;
-      if (nk < KT) load_stage(static_cast<int>(nk % STAGES), nk);
-      cp_async_commit();
-    }
-    const int stage = static_cast<int>(kt % STAGES);
+    if (kt + STAGES - 1 < KT) load_stage(load_slot);
+    cp_async_commit();
+    load_slot = load_slot + 1 == STAGES ? 0 : load_slot + 1;
     const float* as = As + stage * A_STAGE;
     const float* bs = Bs + stage * B_STAGE;
 #pragma unroll
@@ -167,8 +231,8 @@ __global__ void __launch_bounds__(NT, 2) sgemm_simt_kernel(const SimtParams p) {
 #pragma unroll
           for (int i = 0; i < 8; ++i)
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              acc[i][j] = fmaf(f4get(a[i], k4), f4get(bt[j], k4), acc[i][j]);
+            for (int j = 0; j < 8; j += 2)
+              ffma2(acc[i][j], acc[i][j + 1], f4get(a[i], k4), f4get(bt[j], k4), f4get(bt[j + 1], k4));
       } else {
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
@@ -178,18 +242,15 @@ __global__ void __launch_bounds__(NT, 2) sgemm_simt_kernel(const SimtParams p) {
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const float av = f4get(a[i], k4);
-            acc[i][0] = fmaf(av, b0.x, acc[i][0]);
-            acc[i][1] = fmaf(av, b0.y, acc[i][1]);
-            acc[i][2] = fmaf(av, b0.z, acc[i][2]);
-            acc[i][3] = fmaf(av, b0.w, acc[i][3]);
-            acc[i][4] = fmaf(av, b1.x, acc[i][4]);
-            acc[i][5] = fmaf(av, b1.y, acc[i][5]);
-            acc[i][6] = fmaf(av, b1.z, acc[i][6]);
-            acc[i][7] = fmaf(av, b1.w, acc[i][7]);
+            ffma2(acc[i][0], acc[i][1], av, b0.x, b0.y);
+            ffma2(acc[i][2], acc[i][3], av, b0.z, b0.w);
+            ffma2(acc[i][4], acc[i][5], av, b1.x, b1.y);
+            ffma2(acc[i][6], acc[i][7], av, b1.z, b1.w);
           }
         }
       }
     }
+    stage = stage + 1 == STAGES ? 0 : stage + 1;
   }
   cp_async_wait<0>();
 
@@ -233,7 +294,8 @@ __global__ void __launch_bounds__(NT, 2) sgemm_simt_kernel(const SimtParams p) {
 template <bool TRANS_B, bool VEC>
 cudaError_t launch_variant(const SimtParams& p, cudaStream_t s) {
   auto kern = sgemm_simt_kernel<TRANS_B, VEC>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t e = ensure_smem_attr(kern, SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;
   const int64_t tiles = p.batch * p.tiles_m * p.tiles_n;
   kern<<<static_cast<unsigned>(tiles), NT, SMEM_BYTES, s>>>(p);
