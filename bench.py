@@ -140,21 +140,22 @@ class Workload:
                     C = torch.empty((w["M"], w["N"]), dtype=torch.bfloat16, device="cuda")
                 self.bufs.append((A, B, C))
         torch.cuda.synchronize()
+        self.stream = torch.cuda.current_stream().cuda_stream
 
     def step(self, i, bufs=None):
         A, B, C = bufs if bufs is not None else self.bufs[i % self.copies]
-        w, dg = self.w, self.dg
+        w, dg, s = self.w, self.dg, self.stream
         if self.kind == "f32":
             dg.gemm_f32(w["M"], w["N"], w["K"], float(w["alpha"]), A, w["lda"], B, w["ldb"],
-                        float(w["beta"]), C, w["ldc"])
+                        float(w["beta"]), C, w["ldc"], stream=s)
         elif self.kind == "bf16":
             dg.gemm_bf16(w["M"], w["N"], w["K"], float(w["alpha"]), A, w["lda"], B, w["ldb"],
-                         float(w["beta"]), C, w["ldc"], dg.DG_OUT_BF16)
+                         float(w["beta"]), C, w["ldc"], dg.DG_OUT_BF16, stream=s)
         else:
             dg.gemm_bf16_strided_batched(w["M"], w["N"], w["K"], float(w["alpha"]), A, w["lda"],
                                          w["strideA"], B, w["ldb"], w["strideB"], w["op_b"],
                                          float(w["beta"]), C, w["ldc"], w["strideC"], w["batch"],
-                                         dg.DG_OUT_F32)
+                                         dg.DG_OUT_F32, stream=s)
 
     def metric_value(self, seconds_per_step):
         if self.unit == "GB/s":
@@ -257,12 +258,14 @@ class ClockSampler:
 # --------------------------------------------------------------------------- runs
 
 def time_steps(torch, wl, steps, warmup, barrier):
+    """Warm-up, then exactly `steps` back-to-back steps between one pair of CUDA events on
+    the launching stream (events between the launches would add their own gaps).  Each
+    step is one kernel launch, so total / steps is the kernel's average launch duration
+    over the timed region."""
     for i in range(warmup):
         wl.step(i)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(steps)]
     barrier()
     torch.cuda.synchronize()
     t0 = time.time()
@@ -270,16 +273,13 @@ def time_steps(torch, wl, steps, warmup, barrier):
     end = torch.cuda.Event(enable_timing=True)
     start.record(stream)
     for i in range(steps):
-        ev[i][0].record(stream)
         wl.step(warmup + i)
-        ev[i][1].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
     barrier()
     t1 = time.time()
     total_ms = start.elapsed_time(end)
-    per_launch_ms = [a.elapsed_time(b) for a, b in ev]
-    return total_ms, per_launch_ms, t0, t1
+    return total_ms, [total_ms / steps], t0, t1
 
 
 def time_e2e(torch, wl, steps, warmup):

@@ -82,6 +82,25 @@ inline cudaError_t ensure_smem_attr(Kernel kern, int bytes, std::atomic<uint64_t
   return e;
 }
 
+// Launches `kern` with programmatic stream serialisation: the launch may overlap the tail of
+// the previous kernel in the stream; the kernel itself waits (griddepcontrol.wait) before it
+// touches global memory, so stream order is kept for every memory effect.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // Fault injection for the bounded-wait tests (host-set, read by the kernels at launch).
 extern int g_fault_injection;
 

@@ -166,10 +166,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tmem_alloc(smem_u32(&ctl->tmem_base), Cfg::TMEM_COLS);
     tmem_relinquish();
   }
+  if (threadIdx.x == 0) {
+    tma_prefetch_map(&tmA);
+    tma_prefetch_map(&tmB);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
+  // Only shared memory, TMEM and parameters above: this may overlap the previous kernel.
+  pdl_trigger();
+  pdl_wait();
 
   const int64_t total = p.total_tiles;
   const int kblocks = p.kblocks;
@@ -177,8 +184,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      tma_prefetch_map(&tmA);
-      tma_prefetch_map(&tmB);
       uint32_t it = 0;
       bool ok = true;
       for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
@@ -381,8 +386,8 @@ cudaError_t launch_tc_variant(const CUtensorMap& ma, const CUtensorMap& mb, cons
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = ensure_smem_attr(kern, smem, attr_done);
   if (e != cudaSuccess) return e;
-  kern<<<num_ctas, NUM_THREADS, smem, s>>>(ma, mb, p, g_fault_injection);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(num_ctas), dim3(NUM_THREADS), smem, s, ma, mb, p,
+                    g_fault_injection);
 }
 }  // namespace
 

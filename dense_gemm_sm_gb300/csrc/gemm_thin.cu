@@ -128,16 +128,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tmem_alloc(smem_u32(&ctl->tmem_base), Cfg::TMEM_COLS);
     tmem_relinquish();
   }
+  if (threadIdx.x == 0) {
+    tma_prefetch_map(&tmW);
+    tma_prefetch_map(&tmX);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
+  // Everything above touches only shared memory, TMEM and kernel parameters; it may overlap
+  // the previous kernel of the stream.  Global memory is touched only after the wait.
+  pdl_trigger();
+  pdl_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      tma_prefetch_map(&tmW);
-      tma_prefetch_map(&tmX);
       SegmentWalk walk(p, c);
       Segment sg;
       uint32_t it = 0;
@@ -332,8 +338,7 @@ cudaError_t launch_thin_variant(const CUtensorMap& mw, const CUtensorMap& mx, co
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = ensure_smem_attr(kern, smem, attr_done);
   if (e != cudaSuccess) return e;
-  kern<<<static_cast<unsigned>(p.ctas), NUM_THREADS, smem, s>>>(mw, mx, p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(static_cast<unsigned>(p.ctas)), dim3(NUM_THREADS), smem, s, mw, mx, p);
 }
 
 }  // namespace

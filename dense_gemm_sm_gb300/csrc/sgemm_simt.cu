@@ -134,6 +134,11 @@ __global__ void __launch_bounds__(NT, DG_SIMT_MIN_BLOCKS) sgemm_simt_kernel(cons
   const int wm = warp >> 1, wn = warp & 1;
   const int lm = lane >> 3, ln = lane & 7;
 
+  // Launched with programmatic serialisation: wait for the previous kernel before the first
+  // global access, and let the next one launch early.
+  pdl_trigger();
+  pdl_wait();
+
   int64_t b, tm, tn;
   raster_tile(blockIdx.x, p.tiles_m, p.tiles_n, p.group, &b, &tm, &tn);
   const int64_t m0 = tm * BM, n0 = tn * BN;
@@ -298,8 +303,7 @@ cudaError_t launch_variant(const SimtParams& p, cudaStream_t s) {
   cudaError_t e = ensure_smem_attr(kern, SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;
   const int64_t tiles = p.batch * p.tiles_m * p.tiles_n;
-  kern<<<static_cast<unsigned>(tiles), NT, SMEM_BYTES, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(static_cast<unsigned>(tiles)), dim3(NT), SMEM_BYTES, s, p);
 }
 
 }  // namespace
