@@ -459,7 +459,9 @@ void dg_raster_tile(int64_t t, int64_t tiles_m, int64_t tiles_n, int32_t group, 
   raster_tile(t, tiles_m, tiles_n, group, b, tm, tn);
 }
 
-int64_t dg_streamk_start(int64_t c, int64_t units, int64_t ctas) { return sk_start(c, units, ctas); }
+int64_t dg_streamk_start(int64_t c, int64_t units, int64_t ctas) {
+  return sk_start<int64_t>(c, units, ctas);
+}
 
 double dg_model_traffic_bytes(int64_t M, int64_t N, int64_t K, int64_t tile_m, int64_t tile_n,
                               int32_t elem_bytes, int32_t out_bytes) {

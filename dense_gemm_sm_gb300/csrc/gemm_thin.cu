@@ -33,7 +33,10 @@ namespace {
 
 constexpr int BNW = kThinBN, BK = kThinBK;
 constexpr uint32_t W_BYTES = BNW * BK * 2;  // 16 KiB per stage
-constexpr int STAGES = 8;
+#ifndef DG_THIN_STAGES
+#define DG_THIN_STAGES 8
+#endif
+constexpr int STAGES = DG_THIN_STAGES;
 constexpr int NUM_THREADS = 192;
 
 template <int NTOK>
@@ -59,21 +62,26 @@ struct SmemCtl {
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 // One contiguous piece of a CTA's stream-K range that lies in a single W column tile.
+template <typename IDX>
 struct Segment {
-  int64_t tile;
-  int64_t kbeg, kend;  // K blocks [kbeg, kend) of that tile
+  IDX tile;
+  IDX kbeg, kend;  // K blocks [kbeg, kend) of that tile
 };
 
-// Walks CTA c's range [u0, u1) tile by tile.
+// Walks CTA c's range [u0, u1) tile by tile.  IDX is uint32_t when units * ctas < 2^32, so
+// the divisions on this path are 32-bit.
+template <typename IDX>
 struct SegmentWalk {
-  int64_t u, u1, kb;
-  __device__ SegmentWalk(const ThinParams& p, int64_t c)
-      : u(sk_start(c, p.units, p.ctas)), u1(sk_start(c + 1, p.units, p.ctas)), kb(p.kblocks) {}
-  __device__ bool next(Segment* s) {
+  IDX u, u1, kb;
+  __device__ SegmentWalk(const ThinParams& p, IDX c)
+      : u(sk_start<IDX>(c, static_cast<IDX>(p.units), static_cast<IDX>(p.ctas))),
+        u1(sk_start<IDX>(c + 1, static_cast<IDX>(p.units), static_cast<IDX>(p.ctas))),
+        kb(static_cast<IDX>(p.kblocks)) {}
+  __device__ bool next(Segment<IDX>* s) {
     if (u >= u1) return false;
     s->tile = u / kb;
     s->kbeg = u - s->tile * kb;
-    const int64_t lim = u1 - s->tile * kb;
+    const IDX lim = u1 - s->tile * kb;
     s->kend = lim < kb ? lim : kb;
     u = s->tile * kb + s->kend;
     return true;
@@ -92,7 +100,7 @@ __device__ __forceinline__ void store_out(const ThinParams& p, int64_t t, int64_
   }
 }
 
-template <int NTOK, bool W_KMAJOR>
+template <int NTOK, bool W_KMAJOR, typename IDX>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_thin_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                      const ThinParams p) {
@@ -107,7 +115,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int64_t c = blockIdx.x;
+  const IDX c = blockIdx.x;
+  const IDX units = static_cast<IDX>(p.units), ctas = static_cast<IDX>(p.ctas);
+  const IDX kblocks = static_cast<IDX>(p.kblocks);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -137,20 +147,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
   // Everything above touches only shared memory, TMEM and kernel parameters; it may overlap
-  // the previous kernel of the stream.  Global memory is touched only after the wait.
+  // the previous kernel of the stream.  The producer and the epilogue wait for the previous
+  // grid (pdl_wait) before their first global access; the MMA issuer reads only shared
+  // memory and TMEM that the producer fills, so it needs no wait.
   pdl_trigger();
-  pdl_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      SegmentWalk walk(p, c);
-      Segment sg;
+      SegmentWalk<IDX> walk(p, c);
+      Segment<IDX> sg;
       uint32_t it = 0;
       bool ok = true;
-      while (ok && walk.next(&sg)) {
+      bool have = walk.next(&sg);  // index arithmetic before the wait
+      pdl_wait();
+      for (; ok && have; have = walk.next(&sg)) {
         const int32_t xn = static_cast<int32_t>(sg.tile * BNW);
-        for (int64_t kbi = sg.kbeg; kbi < sg.kend; ++kbi) {
+        for (IDX kbi = sg.kbeg; kbi < sg.kend; ++kbi) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
           if (!mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort, p.status, kDevTimeoutProducer)) {
             ok = false;
@@ -183,8 +196,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       // A = W^T tile (128 W columns x 64 K): N-contiguous W is "MN-major" for the MMA.
       constexpr uint32_t idesc = idesc_bf16_f32(128, NTOK, !W_KMAJOR, false);
-      SegmentWalk walk(p, c);
-      Segment sg;
+      SegmentWalk<IDX> walk(p, c);
+      Segment<IDX> sg;
       uint32_t it = 0, lt = 0;
       bool ok = true;
       while (ok && walk.next(&sg)) {
@@ -195,7 +208,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_after();
         const uint32_t d = tmem_base + acc * NTOK;
-        for (int64_t kbi = sg.kbeg; kbi < sg.kend; ++kbi) {
+        for (IDX kbi = sg.kbeg; kbi < sg.kend; ++kbi) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
           if (!mbar_wait(smem_u32(&ctl->full[s]), ph, abort, p.status, kDevTimeoutMma)) {
             ok = false;
@@ -226,9 +239,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int q = warp & 3;
     const int row = q * 32 + lane;  // W column within the tile
     const int etid = threadIdx.x - 64;
-    SegmentWalk walk(p, c);
-    Segment sg;
+    SegmentWalk<IDX> walk(p, c);
+    Segment<IDX> sg;
     uint32_t lt = 0;
+    pdl_wait();
     while (walk.next(&sg)) {
       const uint32_t acc = lt & 1u, aph = (lt >> 1) & 1u;
       // One thread waits (bounded) and the 128 epilogue threads take the same decision
@@ -261,8 +275,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
       ++lt;
 
-      const int64_t n = sg.tile * BNW + row;
-      if (sg.kbeg == 0 && sg.kend == p.kblocks) {
+      const int64_t n = static_cast<int64_t>(sg.tile) * BNW + row;
+      if (sg.kbeg == 0 && sg.kend == kblocks) {
         // This CTA computed the whole K range of the tile: write C directly.
         if (n < p.N) {
 #pragma unroll
@@ -275,31 +289,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // Partial K range: publish the partial sums (one thread = one W column, its ntok
       // values contiguous, so the stores and the combine's loads are 16-byte vectors),
       // then count arrivals for the tile.
-      const int slot = sk_slot(c, sg.tile, p.kblocks, p.units, p.ctas);
-      float4* mine = reinterpret_cast<float4*>(p.ws + ((c * 2 + slot) * BNW + row) * NTOK);
+      const int slot = sk_slot<IDX>(c, sg.tile, kblocks, units, ctas);
+      float4* mine = reinterpret_cast<float4*>(p.ws + ((static_cast<int64_t>(c) * 2 + slot) * BNW + row) * NTOK);
 #pragma unroll
       for (int q4 = 0; q4 < NTOK / 4; ++q4)
         mine[q4] = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
-      __threadfence();
+      // Publish: the barrier orders the 128 threads' stores before thread 0's fence, and the
+      // fence (cumulative) orders them before the arrival count.  On the reading side the
+      // last arriver fences after observing the count, before the group reads.
       epi_bar();
       if (etid == 0) {
-        const uint32_t need = static_cast<uint32_t>(
-            sk_contributors(sg.tile, p.kblocks, p.units, p.ctas));
+        const uint32_t need = static_cast<uint32_t>(sk_contributors<IDX>(sg.tile, kblocks, units, ctas));
+        __threadfence();
         const uint32_t prev = atomicAdd(&p.counters[sg.tile], 1u);
-        ctl->is_last = (prev + 1u == need) ? 1u : 0u;
+        const bool last = prev + 1u == need;
+        if (last) __threadfence();
+        ctl->is_last = last ? 1u : 0u;
       }
       epi_bar();
       if (ctl->is_last) {
-        __threadfence();
-        const int64_t first = sk_cta_of(sg.tile * p.kblocks, p.units, p.ctas);
-        const int64_t last = sk_cta_of((sg.tile + 1) * p.kblocks - 1, p.units, p.ctas);
+        const IDX first = sk_cta_of<IDX>(sg.tile * kblocks, units, ctas);
+        const IDX last = sk_cta_of<IDX>((sg.tile + 1) * kblocks - 1, units, ctas);
         // Sum the contributors' partials in CTA order (= K order): a fixed order.
         float s[NTOK];
 #pragma unroll
         for (int t = 0; t < NTOK; ++t) s[t] = 0.f;
-        for (int64_t cc = first; cc <= last; ++cc) {
-          const int sl = sk_slot(cc, sg.tile, p.kblocks, p.units, p.ctas);
-          const float4* src = reinterpret_cast<const float4*>(p.ws + ((cc * 2 + sl) * BNW + row) * NTOK);
+        for (IDX cc = first; cc <= last; ++cc) {
+          const int sl = sk_slot<IDX>(cc, sg.tile, kblocks, units, ctas);
+          const float4* src = reinterpret_cast<const float4*>(
+              p.ws + ((static_cast<int64_t>(cc) * 2 + sl) * BNW + row) * NTOK);
           float4 part[NTOK / 4];
 #pragma unroll
           for (int q4 = 0; q4 < NTOK / 4; ++q4) part[q4] = __ldcg(src + q4);
@@ -330,10 +348,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-template <int NTOK, bool W_KMAJOR>
+template <int NTOK, bool W_KMAJOR, typename IDX>
 cudaError_t launch_thin_variant(const CUtensorMap& mw, const CUtensorMap& mx, const ThinParams& p,
                                 cudaStream_t s) {
-  auto kern = gemm_thin_kernel<NTOK, W_KMAJOR>;
+  auto kern = gemm_thin_kernel<NTOK, W_KMAJOR, IDX>;
   constexpr uint32_t smem = ThinCfg<NTOK>::SMEM_BYTES;
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = ensure_smem_attr(kern, smem, attr_done);
@@ -350,12 +368,16 @@ cudaError_t launch_gemm_thin(const ThinParams& p, int ntok, const void* X, int64
                              : make_bf16_map(&mw, W, p.N, p.K, ldw, 1, 0, 64, BK);
   if (!ok_w) return cudaErrorInvalidValue;
   if (!make_bf16_map(&mx, X, p.K, p.M, ldx, 1, 0, BK, ntok)) return cudaErrorInvalidValue;
-  if (ntok == 16)
-    return w_kmajor ? launch_thin_variant<16, true>(mw, mx, p, s)
-                    : launch_thin_variant<16, false>(mw, mx, p, s);
-  if (ntok == 32)
-    return w_kmajor ? launch_thin_variant<32, true>(mw, mx, p, s)
-                    : launch_thin_variant<32, false>(mw, mx, p, s);
+  const bool small = sk_fits_u32(p.units, p.ctas);
+#define DG_THIN_CASE(NT, KM)                                                          \
+  if (ntok == NT && w_kmajor == KM)                                                   \
+    return small ? launch_thin_variant<NT, KM, uint32_t>(mw, mx, p, s)                \
+                 : launch_thin_variant<NT, KM, int64_t>(mw, mx, p, s);
+  DG_THIN_CASE(16, false)
+  DG_THIN_CASE(16, true)
+  DG_THIN_CASE(32, false)
+  DG_THIN_CASE(32, true)
+#undef DG_THIN_CASE
   return cudaErrorInvalidValue;
 }
 

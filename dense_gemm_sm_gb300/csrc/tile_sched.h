@@ -48,24 +48,34 @@ DG_HD void raster_tile(int64_t t, int64_t tiles_m, int64_t tiles_n, int32_t grou
   *tn = n;
 }
 
+// The stream-K helpers are written for an index type T: int64_t in general, uint32_t when
+// units * ctas < 2^32 (the kernels pick it at launch), where the divisions are 32-bit.
+
 // First unit of CTA c's stream-K range.
-DG_HD int64_t sk_start(int64_t c, int64_t units, int64_t ctas) { return c * units / ctas; }
+template <typename T>
+DG_HD T sk_start(T c, T units, T ctas) { return c * units / ctas; }
 
 // The CTA whose range contains unit x (the largest c with sk_start(c) <= x).
-DG_HD int64_t sk_cta_of(int64_t x, int64_t units, int64_t ctas) {
-  return ((x + 1) * ctas - 1) / units;
-}
+template <typename T>
+DG_HD T sk_cta_of(T x, T units, T ctas) { return ((x + 1) * ctas - 1) / units; }
 
 // Number of CTAs that contribute to output tile `tile` (kblocks units per tile).
-DG_HD int64_t sk_contributors(int64_t tile, int64_t kblocks, int64_t units, int64_t ctas) {
-  return sk_cta_of((tile + 1) * kblocks - 1, units, ctas) - sk_cta_of(tile * kblocks, units, ctas) +
+template <typename T>
+DG_HD T sk_contributors(T tile, T kblocks, T units, T ctas) {
+  return sk_cta_of<T>((tile + 1) * kblocks - 1, units, ctas) - sk_cta_of<T>(tile * kblocks, units, ctas) +
          1;
 }
 
 // Partial-result slot used by CTA c for tile `tile`: 0 when c's range starts inside the
 // tile (its first segment), 1 when the range began in an earlier tile (its last segment).
-DG_HD int sk_slot(int64_t c, int64_t tile, int64_t kblocks, int64_t units, int64_t ctas) {
-  return sk_start(c, units, ctas) >= tile * kblocks ? 0 : 1;
+template <typename T>
+DG_HD int sk_slot(T c, T tile, T kblocks, T units, T ctas) {
+  return sk_start<T>(c, units, ctas) >= tile * kblocks ? 0 : 1;
+}
+
+// True when the 32-bit helpers are exact for this partition.
+inline bool sk_fits_u32(int64_t units, int64_t ctas) {
+  return units > 0 && ctas > 0 && (units + 1) * (ctas + 1) < (int64_t(1) << 32);
 }
 
 }  // namespace dg
