@@ -4,7 +4,8 @@
 One "step" is one call of the library's public C ABI on one batch of synthetic input
 (resident in HBM).  The default workload is the FP32 SGEMM M = N = K = 4096,
 alpha = 1, beta = 0.5; --workload picks another of the path's configurations
-(ffn_bf16, decode_m1 / decode_m4 / decode_m16, qk_batched, sgemm_ragged, sgemm_256).
+(ffn_bf16, bf16_4096, decode_m1 / decode_m4 / decode_m16, qk_batched, sgemm_ragged,
+sgemm_256).
 
 Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier and
 torch.cuda.synchronize() on both sides, CUDA events on the launching stream; rotating
@@ -96,6 +97,13 @@ class Workload:
                         algo_bytes=2.0 * (M * K + K * N + M * N), bound="tensor", unit="TFLOPS",
                         kernel="gemm_tc_kernel", sources=["gemm_tc.cu", "ptx.cuh"],
                         desc=f"BF16 FFN projection C=XW M={M} N={N} K={K}, FP32 accumulate, BF16 out")
+        if name == "bf16_4096":
+            w = inputs.bf16_square(4096)
+            M, N, K = w["M"], w["N"], w["K"]
+            return dict(kind="bf16", w=w, batch=1, flops=2.0 * M * N * K,
+                        algo_bytes=2.0 * (M * K + K * N + M * N), bound="tensor", unit="TFLOPS",
+                        kernel="gemm_tc_kernel", sources=["gemm_tc.cu", "ptx.cuh"],
+                        desc=f"BF16 GEMM M=N=K={M}, FP32 accumulate, BF16 out")
         if name.startswith("decode_m"):
             m = int(name[len("decode_m"):])
             w = inputs.decode_bf16(m)
@@ -470,8 +478,8 @@ def main():
     }
     if not args.no_suite:
         suite = {}
-        for name in ("ffn_bf16", "decode_m1", "decode_m4", "decode_m16", "qk_batched",
-                     "sgemm_ragged"):
+        for name in ("ffn_bf16", "bf16_4096", "decode_m1", "decode_m4", "decode_m16",
+                     "qk_batched", "sgemm_ragged"):
             if name == args.workload:
                 continue
             other = Workload(name, torch, dg, inputs)

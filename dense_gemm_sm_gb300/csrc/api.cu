@@ -300,6 +300,7 @@ dg_status bf16_impl(int64_t M, int64_t N, int64_t K, float alpha, const uint16_t
   p.C = C; p.ldc = ldc; p.strideC = batch > 1 ? sC : 0;
   p.c_f32 = c_f32 ? 1 : 0;
   p.c_vec = c_vec ? 1 : 0;
+  p.c_tma = (c_vec && beta == 0.f) ? 1 : 0;
   p.status = status;
   return from_cuda(launch_gemm_tc(p, pl.tile_n, A, lda, batch > 1 ? sA : 0, B, ldb,
                                   batch > 1 ? sB : 0, op_b == DG_OP_T,

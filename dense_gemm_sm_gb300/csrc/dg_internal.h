@@ -35,6 +35,7 @@ struct TcParams {
   void* C; int64_t ldc, strideC;
   int32_t c_f32;     // 1: C is float32, 0: bfloat16
   int32_t c_vec;     // 1: 16-byte vector stores/loads of C rows are legal
+  int32_t c_tma;     // 1: epilogue writes C with TMA tensor stores (beta == 0, aligned C)
   uint32_t* status;  // device status word
 };
 // A: [batch][M][lda] bf16 (K contiguous).  B: op N -> [batch][K][ldb] (N contiguous),

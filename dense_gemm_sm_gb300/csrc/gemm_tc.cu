@@ -44,8 +44,11 @@ struct TcCfg {
   static constexpr int STAGES = BN == 256 ? 4 : 6;
   static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators, power of two
   static constexpr uint32_t RING_BYTES = STAGES * (A_BYTES + B_BYTES);
+  // Epilogue staging for TMA stores: 4 warps x 2 buffers x (32 rows x 128 bytes).
+  static constexpr uint32_t STAGE_OUT_BYTES = 4 * 2 * 4096;
   static constexpr uint32_t BAR_BYTES = 256;
-  static constexpr uint32_t SMEM_BYTES = 1024 /*alignment slack*/ + RING_BYTES + BAR_BYTES;
+  static constexpr uint32_t SMEM_BYTES =
+      1024 /*alignment slack*/ + RING_BYTES + STAGE_OUT_BYTES + BAR_BYTES;
   static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of two");
 };
 
@@ -135,7 +138,7 @@ __device__ __forceinline__ void store_row_chunk(const TcParams& p, void* crow_v,
 template <int BN, bool B_KMAJOR, bool RANK3>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const TcParams p, const int fault) {
+                   const __grid_constant__ CUtensorMap tmC, const TcParams p, const int fault) {
   using Cfg = TcCfg<BN>;
   constexpr int STAGES = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -143,7 +146,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t ring = (raw + 1023u) & ~1023u;            // 1024-byte aligned swizzle atoms
   const uint32_t a_ring = ring;
   const uint32_t b_ring = ring + STAGES * A_BYTES;
-  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem_raw + (ring - raw) + Cfg::RING_BYTES);
+  const uint32_t out_stage = ring + Cfg::RING_BYTES;  // 1024-byte aligned
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem_raw + (ring - raw) + Cfg::RING_BYTES +
+                                            Cfg::STAGE_OUT_BYTES);
   volatile uint32_t* abort = &ctl->abort;
 
   const int warp = threadIdx.x >> 5;
@@ -169,6 +174,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     tma_prefetch_map(&tmA);
     tma_prefetch_map(&tmB);
+    if (p.c_tma) tma_prefetch_map(&tmC);
   }
   tc_fence_before();
   __syncthreads();
@@ -270,6 +276,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------------ epilogue (warps 2..5)
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     const int row = q * 32 + lane;
+    // Two 4 KiB staging buffers per warp for the TMA-store path (32 rows x 128 bytes each,
+    // 128-byte swizzled like the tensor map's box).
+    const uint32_t stg = out_stage + static_cast<uint32_t>(warp - 2) * 8192u;
+    uint32_t sbuf = 0;
     uint32_t lt = 0;
     for (int64_t t = blockIdx.x; t < total; t += gridDim.x, ++lt) {
       int64_t b, tm, tn;
@@ -277,21 +287,80 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t acc = lt & 1u, aph = (lt >> 1) & 1u;
       if (!mbar_wait(smem_u32(&ctl->tfull[acc]), aph, abort, p.status, kDevTimeoutEpilogue)) break;
       tc_fence_after();
-      const int64_t gm = tm * BM + row;
-      uint8_t* cbase = static_cast<uint8_t*>(p.C) +
-                       (b * p.strideC + gm * p.ldc) * (p.c_f32 ? 4 : 2);
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      if (p.c_tma) {
+        // C = alpha * acc: each 32 x (128 bytes) piece goes registers -> swizzled shared
+        // staging -> one TMA tensor store (rows / columns beyond M / N are clipped).
+        const int32_t y = static_cast<int32_t>(tm * BM + q * 32);
+        const int32_t zb = static_cast<int32_t>(b);
+        constexpr int COLS = 32;  // FP32 columns per piece (BF16 pieces hold 64)
+        const int pieces = p.c_f32 ? BN / COLS : BN / (2 * COLS);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(taddr + c * 32, r);
-        tmem_ld_wait();
-        if (gm < p.M) store_row_chunk(p, cbase, tn * BN + c * 32, r);
+        for (int c = 0; c < pieces; ++c) {
+          uint32_t w[32];
+          if (p.c_f32) {
+            tmem_ld_32x32b_x32(taddr + c * 32, w);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(p.alpha * __uint_as_float(w[j]));
+          } else {
+            uint32_t r0[32], r1[32];
+            tmem_ld_32x32b_x32(taddr + c * 64, r0);
+            tmem_ld_32x32b_x32(taddr + c * 64 + 32, r1);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              w[j] = pack_bf16x2(p.alpha * __uint_as_float(r0[2 * j]),
+                                 p.alpha * __uint_as_float(r0[2 * j + 1]));
+              w[16 + j] = pack_bf16x2(p.alpha * __uint_as_float(r1[2 * j]),
+                                      p.alpha * __uint_as_float(r1[2 * j + 1]));
+            }
+          }
+          if (c == pieces - 1) {
+            // The accumulator is in registers now: hand TMEM back to the MMA issuer.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
+          }
+          // The store issued from this buffer two pieces ago must have finished reading it.
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
+          const uint32_t buf = stg + sbuf * 4096u;
+          const uint32_t rowaddr = buf + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            st_shared_v4(rowaddr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4), w[4 * j],
+                         w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int32_t x = static_cast<int32_t>(tn * BN + c * (p.c_f32 ? COLS : 2 * COLS));
+            if (y < p.M && x < p.N) {  // skip pieces wholly outside C
+              if (RANK3) tma_store_3d(&tmC, buf, x, y, zb);
+              else tma_store_2d(&tmC, buf, x, y);
+            }
+            bulk_commit();
+          }
+          sbuf ^= 1u;
+        }
+      } else {
+        const int64_t gm = tm * BM + row;
+        uint8_t* cbase = static_cast<uint8_t*>(p.C) +
+                         (b * p.strideC + gm * p.ldc) * (p.c_f32 ? 4 : 2);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(taddr + c * 32, r);
+          tmem_ld_wait();
+          if (gm < p.M) store_row_chunk(p, cbase, tn * BN + c * 32, r);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
     }
+    // Stores must have finished reading shared memory (and landed) before the CTA exits.
+    if (p.c_tma && lane == 0) bulk_wait<0>();
   }
 
   tc_fence_before();
@@ -330,17 +399,19 @@ std::mutex g_map_mu;
 std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_map_cache;
 }  // namespace
 
-// Builds a BF16 tensor map over a (batch x) outer x inner row-major view with a
-// box_inner x box_outer box and 128-byte swizzle.  Out-of-range elements read as zero.
-// Encoded maps are cached by (address, shape, box): repeated calls on the same buffers
-// (the usual inference loop) skip the encoding on the launch path.
-bool make_bf16_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
-                   uint64_t batch, uint64_t stride, uint32_t box_inner, uint32_t box_outer) {
+// Builds a tensor map over a (batch x) outer x inner row-major view of elements of `esz`
+// bytes with a box_inner x box_outer box and 128-byte swizzle.  Out-of-range elements read
+// as zero (and are not written by stores).  Encoded maps are cached by (address, shape,
+// type, box): repeated calls on the same buffers (the usual inference loop) skip the
+// encoding on the launch path.
+bool make_tile_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t esz, const void* base,
+                   uint64_t inner, uint64_t outer, uint64_t ld, uint64_t batch, uint64_t stride,
+                   uint32_t box_inner, uint32_t box_outer) {
   MapKey key;
   std::memset(&key, 0, sizeof key);
   key.base = base; key.inner = inner; key.outer = outer; key.ld = ld;
   key.batch = batch > 1 ? batch : 1; key.stride = batch > 1 ? stride : 0;
-  key.box_inner = box_inner; key.box_outer = box_outer;
+  key.box_inner = box_inner | (static_cast<uint32_t>(dtype) << 16); key.box_outer = box_outer;
   {
     std::lock_guard<std::mutex> lock(g_map_mu);
     auto it = g_map_cache.find(key);
@@ -353,18 +424,23 @@ bool make_bf16_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t 
   if (!fn) return false;
   const bool rank3 = batch > 1;
   cuuint64_t dims[3] = {inner, outer, batch};
-  cuuint64_t strides[2] = {ld * 2, stride * 2};
+  cuuint64_t strides[2] = {ld * esz, stride * esz};
   cuuint32_t box[3] = {box_inner, box_outer, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank3 ? 3 : 2, const_cast<void*>(base),
-                  dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = fn(map, dtype, rank3 ? 3 : 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return false;
   std::lock_guard<std::mutex> lock(g_map_mu);
   if (g_map_cache.size() >= 4096) g_map_cache.clear();
   g_map_cache.emplace(key, *map);
   return true;
+}
+
+bool make_bf16_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
+                   uint64_t batch, uint64_t stride, uint32_t box_inner, uint32_t box_outer) {
+  return make_tile_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, inner, outer, ld, batch,
+                       stride, box_inner, box_outer);
 }
 
 EncodeTiledFn get_encode_tiled() {
@@ -379,14 +455,14 @@ EncodeTiledFn get_encode_tiled() {
 
 namespace {
 template <int BN, bool B_KMAJOR, bool RANK3>
-cudaError_t launch_tc_variant(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p,
-                              int num_ctas, cudaStream_t s) {
+cudaError_t launch_tc_variant(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
+                              const TcParams& p, int num_ctas, cudaStream_t s) {
   auto kern = gemm_tc_kernel<BN, B_KMAJOR, RANK3>;
   constexpr uint32_t smem = TcCfg<BN>::SMEM_BYTES;
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = ensure_smem_attr(kern, smem, attr_done);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(num_ctas), dim3(NUM_THREADS), smem, s, ma, mb, p,
+  return launch_pdl(kern, dim3(num_ctas), dim3(NUM_THREADS), smem, s, ma, mb, mc, p,
                     g_fault_injection);
 }
 }  // namespace
@@ -400,10 +476,21 @@ cudaError_t launch_gemm_tc(const TcParams& p, int bn, const void* A, int64_t lda
   const bool ok_b = b_kmajor ? make_bf16_map(&mb, B, p.K, p.N, ldb, batch, strideB, BK, bn)
                              : make_bf16_map(&mb, B, p.N, p.K, ldb, batch, strideB, 64, BK);
   if (!ok_b) return cudaErrorInvalidValue;
+  CUtensorMap mc;
+  std::memset(&mc, 0, sizeof mc);
+  TcParams q = p;
+  if (q.c_tma) {
+    // 32 rows x 128 bytes per store: 32 FP32 or 64 BF16 columns.
+    const bool ok_c = q.c_f32 ? make_tile_map(&mc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, q.C, q.N, q.M,
+                                              q.ldc, batch, q.strideC, 32, 32)
+                              : make_tile_map(&mc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q.C, q.N,
+                                              q.M, q.ldc, batch, q.strideC, 64, 32);
+    if (!ok_c) q.c_tma = 0;  // fall back to direct stores from registers
+  }
   const bool rank3 = batch > 1;
 #define DG_TC_CASE(BNV, KM, R3)                                                     \
   if (bn == BNV && b_kmajor == KM && rank3 == R3)                                   \
-    return launch_tc_variant<BNV, KM, R3>(ma, mb, p, num_ctas, s);
+    return launch_tc_variant<BNV, KM, R3>(ma, mb, mc, q, num_ctas, s);
   DG_TC_CASE(256, false, false)
   DG_TC_CASE(256, false, true)
   DG_TC_CASE(256, true, false)

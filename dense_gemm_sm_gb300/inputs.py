@@ -13,6 +13,7 @@ Workloads (shapes and distributions from the FFN running example of
   sgemm_ragged   FP32 1000x3000x777, lda=780, ldb=ldc=3000, alpha=1, beta=0.5
   ffn_bf16       X[1024,4096] ~ N(0,1), W[4096,12288] ~ N(0,1/4096), BF16
   decode_bf16    X[M,4096] ~ N(0,1), same W, M in {1,4,16}
+  bf16_square    BF16 4096^3 with the same operand distributions
   qk_batched     64 x (Q[2048,128] . K[2048,128]^T), alpha=fp32(1/sqrt(128)), FP32 out
 """
 from __future__ import annotations
@@ -114,6 +115,15 @@ def ffn_bf16(M=1024, K=4096, N=12288, W=None) -> dict:
         W = ffn_weight(K, N)
     return dict(M=M, N=N, K=K, alpha=np.float32(1.0), beta=np.float32(0.0), A=X, lda=K, B=W,
                 ldb=N, C0=None, ldc=N)
+
+
+def bf16_square(n=4096) -> dict:
+    """BF16 n^3 GEMM with the FFN operand distributions (the "4096-class" square shape)."""
+    s = BASE_SEED + 5
+    X = f32_to_bf16_bits(normal_f32(s, (n, n)))
+    W = f32_to_bf16_bits(normal_f32(s + 100, (n, n), std=1.0 / np.sqrt(n)))
+    return dict(M=n, N=n, K=n, alpha=np.float32(1.0), beta=np.float32(0.0), A=X, lda=n, B=W,
+                ldb=n, C0=None, ldc=n)
 
 
 def decode_bf16(M: int, K=4096, N=12288, W=None) -> dict:

@@ -212,6 +212,37 @@ def test_bf16_edge_shapes(torch, M, N, K, out_f32):
         assert_bf16_close(C, ref[0], den[0], f"bf16 {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M,N,K", [(129, 264, 72), (300, 1000, 200), (33, 8, 16), (255, 520, 4104),
+                                   (1000, 136, 64)])
+@pytest.mark.parametrize("out_f32", [False, True])
+def test_bf16_beta_zero_edge_shapes(torch, M, N, K, out_f32):
+    # beta = 0 with 16-byte aligned C rows: the epilogue's TMA-store path (edge tiles clipped
+    # by the tensor map); the NaN-filled C checks that nothing outside M x N is written.
+    lda = ((K + 7) // 8) * 8
+    A = inputs.pad_rows(inputs.f32_to_bf16_bits(inputs.normal_f32(M + 5, (M, K))), lda, 0)
+    B = inputs.f32_to_bf16_bits(inputs.normal_f32(N + 6, (K, N), 0.1))
+    ldc = N + 8
+    C = run_bf16(torch, M, N, K, 0.75, A, lda, B, N, 0.0, None, ldc, out_f32)
+    ref, den = oracle.gemm(M, N, K, 0.75, A, lda, B, N, absden=True)
+    if out_f32:
+        assert_f32_close(C, ref[0], den[0], f"bf16->f32 beta=0 {M}x{N}x{K}")
+    else:
+        assert_bf16_close(C, ref[0], den[0], f"bf16 beta=0 {M}x{N}x{K}")
+
+
+def test_bf16_tma_store_leaves_padding_untouched(torch):
+    M, N, K, ldc = 200, 264, 128, 272
+    A = inputs.f32_to_bf16_bits(inputs.normal_f32(50, (M, K)))
+    B = inputs.f32_to_bf16_bits(inputs.normal_f32(51, (K, N)))
+    dA, dB = dev_bf16(A), dev_bf16(B)
+    dC = torch.full((M + 3, ldc), float("nan"), dtype=torch.float32, device="cuda")
+    dg.gemm_bf16(M, N, K, 1.0, dA, K, dB, N, 0.0, dC, ldc, dg.DG_OUT_F32)
+    sync(torch)
+    C = host_f32(dC)
+    assert np.all(np.isnan(C[:, N:])) and np.all(np.isnan(C[M:, :]))
+    assert np.all(np.isfinite(C[:M, :N]))
+
+
 @pytest.mark.parametrize("M", [1, 4, 16, 17, 32])
 def test_bf16_decode_full_size(torch, M):
     W = inputs.ffn_weight()
@@ -265,6 +296,19 @@ def test_bf16_ffn_full_size_sampled(torch):
     ref, den = oracle.gemm_entries(M, N, K, 1.0, w["A"], K, w["B"], N, 0.0, None, N, rr.ravel(),
                                    cc.ravel())
     assert_bf16_close(C[rr, cc].ravel(), ref, den, "FFN one full tile")
+
+
+def test_bf16_square_4096_sampled(torch):
+    w = inputs.bf16_square(4096)
+    n = 4096
+    dA, dB = dev_bf16(w["A"]), dev_bf16(w["B"])
+    dC = torch.empty((n, n), dtype=torch.bfloat16, device="cuda")
+    dg.gemm_bf16(n, n, n, 1.0, dA, n, dB, n, 0.0, dC, n)
+    sync(torch)
+    C = host_bf16_bits(dC)
+    rows, cols = sample_indices(45, 3000, n, n)
+    ref, den = oracle.gemm_entries(n, n, n, 1.0, w["A"], n, w["B"], n, 0.0, None, n, rows, cols)
+    assert_bf16_close(C[rows, cols], ref, den, "BF16 4096^3 (sampled)")
 
 
 def run_qk(torch, w):
