@@ -38,18 +38,22 @@ constexpr int BM = kTcBM, BK = kTcBK;
 constexpr uint32_t A_BYTES = BM * BK * 2;  // 16 KiB per stage
 constexpr int NUM_THREADS = 192;
 
-template <int BN>
+template <int BN, bool B_KMAJOR>
 struct TcCfg {
-  static constexpr uint32_t B_BYTES = BN * BK * 2;
-  static constexpr int STAGES = BN == 256 ? 4 : 6;
-  static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators, power of two
+  // N-major B arrives as 64-column boxes (8 KiB each), K-major B as one BN-row box.
+  static constexpr int NBOX = (BN + 63) / 64;
+  static constexpr uint32_t B_BYTES = NBOX * 8192;  // stage footprint
+  static constexpr uint32_t B_LOAD_BYTES = B_KMAJOR ? BN * BK * 2 : NBOX * 8192;  // expect_tx
+  static constexpr int STAGES = BN >= 192 ? 4 : 6;
+  // Two accumulators of BN columns; the allocation is a power of two.
+  static constexpr uint32_t TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
   static constexpr uint32_t RING_BYTES = STAGES * (A_BYTES + B_BYTES);
   // Epilogue staging for TMA stores: 4 warps x 2 buffers x (32 rows x 128 bytes).
   static constexpr uint32_t STAGE_OUT_BYTES = 4 * 2 * 4096;
   static constexpr uint32_t BAR_BYTES = 256;
   static constexpr uint32_t SMEM_BYTES =
       1024 /*alignment slack*/ + RING_BYTES + STAGE_OUT_BYTES + BAR_BYTES;
-  static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of two");
+  static_assert(BN % 32 == 0 && BN <= 256 && 2 * BN <= 512, "tile width");
 };
 
 struct SmemCtl {
@@ -139,7 +143,7 @@ template <int BN, bool B_KMAJOR, bool RANK3>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const TcParams p, const int fault) {
-  using Cfg = TcCfg<BN>;
+  using Cfg = TcCfg<BN, B_KMAJOR>;
   constexpr int STAGES = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -205,7 +209,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           const uint32_t fb = smem_u32(&ctl->full[s]);
-          mbar_arrive_expect_tx(fb, A_BYTES + Cfg::B_BYTES);
+          mbar_arrive_expect_tx(fb, A_BYTES + Cfg::B_LOAD_BYTES);
           const int32_t kx = kb * BK;
           const uint32_t adst = a_ring + s * A_BYTES, bdst = b_ring + s * Cfg::B_BYTES;
           if (RANK3) tma_load_3d(adst, &tmA, fb, kx, ym, zb);
@@ -215,7 +219,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             else tma_load_2d(bdst, &tmB, fb, kx, xn);
           } else {
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j) {
+            for (int j = 0; j < Cfg::NBOX; ++j) {
               if (RANK3) tma_load_3d(bdst + j * 8192u, &tmB, fb, xn + 64 * j, kx, zb);
               else tma_load_2d(bdst + j * 8192u, &tmB, fb, xn + 64 * j, kx);
             }
@@ -289,34 +293,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       if (p.c_tma) {
-        // C = alpha * acc: each 32 x (128 bytes) piece goes registers -> swizzled shared
-        // staging -> one TMA tensor store (rows / columns beyond M / N are clipped).
+        // C = alpha * acc, in pieces of 32 rows x 32 columns: registers -> swizzled shared
+        // staging -> one TMA tensor store (rows / columns beyond M / N are clipped).  An FP32
+        // piece is 32 x 128 bytes (128-byte swizzle), a BF16 piece 32 x 64 bytes (64-byte).
         const int32_t y = static_cast<int32_t>(tm * BM + q * 32);
         const int32_t zb = static_cast<int32_t>(b);
-        constexpr int COLS = 32;  // FP32 columns per piece (BF16 pieces hold 64)
-        const int pieces = p.c_f32 ? BN / COLS : BN / (2 * COLS);
 #pragma unroll 1
-        for (int c = 0; c < pieces; ++c) {
+        for (int c = 0; c < BN / 32; ++c) {
           uint32_t w[32];
-          if (p.c_f32) {
-            tmem_ld_32x32b_x32(taddr + c * 32, w);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(p.alpha * __uint_as_float(w[j]));
-          } else {
-            uint32_t r0[32], r1[32];
-            tmem_ld_32x32b_x32(taddr + c * 64, r0);
-            tmem_ld_32x32b_x32(taddr + c * 64 + 32, r1);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              w[j] = pack_bf16x2(p.alpha * __uint_as_float(r0[2 * j]),
-                                 p.alpha * __uint_as_float(r0[2 * j + 1]));
-              w[16 + j] = pack_bf16x2(p.alpha * __uint_as_float(r1[2 * j]),
-                                      p.alpha * __uint_as_float(r1[2 * j + 1]));
-            }
-          }
-          if (c == pieces - 1) {
+          tmem_ld_32x32b_x32(taddr + c * 32, w);
+          tmem_ld_wait();
+          if (c == BN / 32 - 1) {
             // The accumulator is in registers now: hand TMEM back to the MMA issuer.
             tc_fence_before();
             __syncwarp();
@@ -326,15 +313,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (lane == 0) bulk_wait_read<1>();
           __syncwarp();
           const uint32_t buf = stg + sbuf * 4096u;
-          const uint32_t rowaddr = buf + static_cast<uint32_t>(lane) * 128u;
+          if (p.c_f32) {
+            const uint32_t rowaddr = buf + static_cast<uint32_t>(lane) * 128u;
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            st_shared_v4(rowaddr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4), w[4 * j],
-                         w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+            for (int j = 0; j < 8; ++j) {
+              const float a0 = p.alpha * __uint_as_float(w[4 * j]);
+              const float a1 = p.alpha * __uint_as_float(w[4 * j + 1]);
+              const float a2 = p.alpha * __uint_as_float(w[4 * j + 2]);
+              const float a3 = p.alpha * __uint_as_float(w[4 * j + 3]);
+              st_shared_v4(rowaddr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4),
+                           __float_as_uint(a0), __float_as_uint(a1), __float_as_uint(a2),
+                           __float_as_uint(a3));
+            }
+          } else {
+            const uint32_t rowaddr = buf + static_cast<uint32_t>(lane) * 64u;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint32_t h[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                h[e] = pack_bf16x2(p.alpha * __uint_as_float(w[8 * j + 2 * e]),
+                                   p.alpha * __uint_as_float(w[8 * j + 2 * e + 1]));
+              st_shared_v4(rowaddr + ((static_cast<uint32_t>(j) ^ ((lane >> 1) & 3u)) << 4), h[0],
+                           h[1], h[2], h[3]);
+            }
+          }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            const int32_t x = static_cast<int32_t>(tn * BN + c * (p.c_f32 ? COLS : 2 * COLS));
+            const int32_t x = static_cast<int32_t>(tn * BN + c * 32);
             if (y < p.M && x < p.N) {  // skip pieces wholly outside C
               if (RANK3) tma_store_3d(&tmC, buf, x, y, zb);
               else tma_store_2d(&tmC, buf, x, y);
@@ -406,12 +413,14 @@ std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_map_cache;
 // encoding on the launch path.
 bool make_tile_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t esz, const void* base,
                    uint64_t inner, uint64_t outer, uint64_t ld, uint64_t batch, uint64_t stride,
-                   uint32_t box_inner, uint32_t box_outer) {
+                   uint32_t box_inner, uint32_t box_outer,
+                   CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   MapKey key;
   std::memset(&key, 0, sizeof key);
   key.base = base; key.inner = inner; key.outer = outer; key.ld = ld;
   key.batch = batch > 1 ? batch : 1; key.stride = batch > 1 ? stride : 0;
-  key.box_inner = box_inner | (static_cast<uint32_t>(dtype) << 16); key.box_outer = box_outer;
+  key.box_inner = box_inner | (static_cast<uint32_t>(dtype) << 16);
+  key.box_outer = box_outer | (static_cast<uint32_t>(swizzle) << 16);
   {
     std::lock_guard<std::mutex> lock(g_map_mu);
     auto it = g_map_cache.find(key);
@@ -428,8 +437,8 @@ bool make_tile_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t esz, co
   cuuint32_t box[3] = {box_inner, box_outer, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, dtype, rank3 ? 3 : 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return false;
   std::lock_guard<std::mutex> lock(g_map_mu);
   if (g_map_cache.size() >= 4096) g_map_cache.clear();
@@ -458,7 +467,7 @@ template <int BN, bool B_KMAJOR, bool RANK3>
 cudaError_t launch_tc_variant(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
                               const TcParams& p, int num_ctas, cudaStream_t s) {
   auto kern = gemm_tc_kernel<BN, B_KMAJOR, RANK3>;
-  constexpr uint32_t smem = TcCfg<BN>::SMEM_BYTES;
+  constexpr uint32_t smem = TcCfg<BN, B_KMAJOR>::SMEM_BYTES;
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = ensure_smem_attr(kern, smem, attr_done);
   if (e != cudaSuccess) return e;
@@ -480,11 +489,13 @@ cudaError_t launch_gemm_tc(const TcParams& p, int bn, const void* A, int64_t lda
   std::memset(&mc, 0, sizeof mc);
   TcParams q = p;
   if (q.c_tma) {
-    // 32 rows x 128 bytes per store: 32 FP32 or 64 BF16 columns.
+    // Stores of 32 rows x 32 columns: 128-byte FP32 rows, 64-byte BF16 rows.
     const bool ok_c = q.c_f32 ? make_tile_map(&mc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, q.C, q.N, q.M,
-                                              q.ldc, batch, q.strideC, 32, 32)
+                                              q.ldc, batch, q.strideC, 32, 32,
+                                              CU_TENSOR_MAP_SWIZZLE_128B)
                               : make_tile_map(&mc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q.C, q.N,
-                                              q.M, q.ldc, batch, q.strideC, 64, 32);
+                                              q.M, q.ldc, batch, q.strideC, 32, 32,
+                                              CU_TENSOR_MAP_SWIZZLE_64B);
     if (!ok_c) q.c_tma = 0;  // fall back to direct stores from registers
   }
   const bool rank3 = batch > 1;
@@ -495,6 +506,14 @@ cudaError_t launch_gemm_tc(const TcParams& p, int bn, const void* A, int64_t lda
   DG_TC_CASE(256, false, true)
   DG_TC_CASE(256, true, false)
   DG_TC_CASE(256, true, true)
+  DG_TC_CASE(224, false, false)
+  DG_TC_CASE(224, false, true)
+  DG_TC_CASE(224, true, false)
+  DG_TC_CASE(224, true, true)
+  DG_TC_CASE(192, false, false)
+  DG_TC_CASE(192, false, true)
+  DG_TC_CASE(192, true, false)
+  DG_TC_CASE(192, true, true)
   DG_TC_CASE(128, false, false)
   DG_TC_CASE(128, false, true)
   DG_TC_CASE(128, true, false)
