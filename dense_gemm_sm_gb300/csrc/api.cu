@@ -30,6 +30,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int kRasterGroup = 8;
 constexpr int64_t kThinMaxM = 32;
+constexpr int kSimtCtasPerSmPlan = 2;  // occupancy of the SIMT kernel (launch bounds 256 x 2)
 
 // Device status word: kernels record the first bounded-wait expiry here.
 __device__ uint32_t g_status_word;
@@ -118,7 +119,13 @@ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // ------------------------------------------------------------------ planning
-void plan_f32(int64_t M, int64_t N, int64_t K, int64_t batch, dg_plan* pl) {
+// FP32: whole waves of tiles run data-parallel (one tile per CTA).  The tiles of the last,
+// partial wave are split along K into S equal chunks, one CTA each, S chosen so that the
+// tail takes the fewest tile-times: ceil(tail * S / resident) / S, with at least 16 K tiles
+// (256 of K) per chunk and at most three waves of tail CTAs; the chunks of a tile are summed
+// in K order by the last one to finish (a fixed order).
+void plan_f32(int64_t M, int64_t N, int64_t K, int64_t batch, int64_t resident, dg_plan* pl,
+              int64_t* dp_tiles, int64_t* sk_tiles, int* sk_splits) {
   pl->kernel = DG_KERNEL_SIMT_F32;
   pl->tile_m = kSimtBM;
   pl->tile_n = kSimtBN;
@@ -126,9 +133,26 @@ void plan_f32(int64_t M, int64_t N, int64_t K, int64_t batch, dg_plan* pl) {
   pl->stages = kSimtStages;
   pl->group = kRasterGroup;
   pl->tiles = batch * cdiv(M, kSimtBM) * cdiv(N, kSimtBN);
-  pl->grid = pl->tiles;
   pl->kblocks = cdiv(K, kSimtBK);
   pl->vec = 1;
+  const int64_t T = pl->tiles, KT = pl->kblocks, G = resident > 0 ? resident : 1;
+  const int64_t tail = T % G;
+  int best_s = 1;
+  if (tail > 0) {
+    double best = 1.0;  // tail time (in tile times) without splitting
+    for (int64_t S = 2; S <= KT / 16 && tail * S <= 3 * G; ++S) {
+      const double t = static_cast<double>(cdiv(tail * S, G)) / static_cast<double>(S);
+      if (t < best - 1e-9) {
+        best = t;
+        best_s = static_cast<int>(S);
+      }
+    }
+  }
+  *sk_splits = best_s;
+  *sk_tiles = best_s > 1 ? tail : 0;
+  *dp_tiles = T - *sk_tiles;
+  pl->grid = *dp_tiles + *sk_tiles * best_s;
+  pl->workspace_bytes = *sk_tiles > 0 ? simt_ws_floats(*sk_tiles * best_s) * 4 + *sk_tiles * 4 : 0;
 }
 
 void plan_bf16(int64_t M, int64_t N, int64_t K, int64_t batch, int sms, dg_plan* pl) {
@@ -184,8 +208,14 @@ dg_status plan(int32_t dtype, int64_t M, int64_t N, int64_t K, int64_t batch, fl
     pl->kernel = DG_KERNEL_SCALE;
     return DG_OK;
   }
-  if (dtype == 0) plan_f32(M, N, K, batch, pl);
-  else plan_bf16(M, N, K, batch, sms, pl);
+  if (dtype == 0) {
+    int64_t dp = 0, sk = 0;
+    int splits = 1;
+    plan_f32(M, N, K, batch, static_cast<int64_t>(sms) * kSimtCtasPerSmPlan, pl, &dp, &sk,
+             &splits);
+  } else {
+    plan_bf16(M, N, K, batch, sms, pl);
+  }
   return DG_OK;
 }
 
@@ -230,16 +260,26 @@ dg_status f32_impl(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
   dg_status st = check_common(M, N, K, batch, lda, ldb, ldc, op_b, sA, sB, sC);
   if (st != DG_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  dg_plan pl;
-  plan(0, M, N, K, batch, alpha, 0, &pl);
-  log_plan("gemm_f32", M, N, K, batch, pl);
-  if (pl.kernel == DG_KERNEL_NONE) return DG_OK;
-  if (pl.kernel == DG_KERNEL_SCALE) return run_scale(C, true, M, N, ldc, sC, batch, beta, s);
+  if (M == 0 || N == 0 || batch == 0) return DG_OK;
+  if (K == 0 || alpha == 0.f) return run_scale(C, true, M, N, ldc, sC, batch, beta, s);
   if (!A || !B || !C) return DG_ERR_INVALID_ARG;
-  if (pl.tiles > INT32_MAX) return DG_ERR_UNSUPPORTED;
+  int dev = 0;
+  if (current_device(&dev) != cudaSuccess) return DG_ERR_CUDA;
+  uint32_t* status = nullptr;
+  int sms = 0;
+  if (device_info(dev, &status, &sms) != cudaSuccess) return DG_ERR_CUDA;
   const bool vec = aligned16(A) && aligned16(B) && aligned16(C) && lda % 4 == 0 &&
                    ldb % 4 == 0 && ldc % 4 == 0 &&
                    (batch <= 1 || (sA % 4 == 0 && sB % 4 == 0 && sC % 4 == 0));
+  const bool trans_b = op_b == DG_OP_T;
+  const int64_t resident =
+      static_cast<int64_t>(sms) * sgemm_simt_ctas_per_sm(trans_b, vec);
+  dg_plan pl = dg_plan{};
+  int64_t dp = 0, sk = 0;
+  int splits = 1;
+  plan_f32(M, N, K, batch, resident, &pl, &dp, &sk, &splits);
+  log_plan("gemm_f32", M, N, K, batch, pl);
+  if (pl.tiles > INT32_MAX) return DG_ERR_UNSUPPORTED;
   SimtParams p;
   p.M = M; p.N = N; p.K = K;
   p.alpha = alpha; p.beta = beta;
@@ -250,7 +290,20 @@ dg_status f32_impl(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
   p.tiles_m = cdiv(M, kSimtBM);
   p.tiles_n = cdiv(N, kSimtBN);
   p.group = kRasterGroup;
-  return from_cuda(launch_sgemm_simt(p, op_b == DG_OP_T, vec, s));
+  p.dp_tiles = dp;
+  p.sk_tiles = sk;
+  p.sk_splits = splits;
+  p.ws = nullptr;
+  p.counters = nullptr;
+  if (sk > 0) {
+    Workspace w;
+    st = get_workspace(dev, s, static_cast<size_t>(simt_ws_floats(sk * splits)),
+                       static_cast<size_t>(sk), &w);
+    if (st != DG_OK) return st;
+    p.ws = w.ws;
+    p.counters = w.counters;
+  }
+  return from_cuda(launch_sgemm_simt(p, trans_b, vec, s));
 }
 
 dg_status bf16_impl(int64_t M, int64_t N, int64_t K, float alpha, const uint16_t* A, int64_t lda,

@@ -19,9 +19,19 @@ struct SimtParams {
   int64_t batch;
   int64_t tiles_m, tiles_n;
   int32_t group;
+  // Schedule: the first dp_tiles CTAs of the grid compute one whole tile each; the next
+  // sk_tiles * sk_splits CTAs each compute one of sk_splits equal K chunks of the remaining
+  // (tail) tiles.  Grid = dp_tiles + sk_tiles * sk_splits.
+  int64_t dp_tiles, sk_tiles;
+  int32_t sk_splits;
+  float* ws;           // split-K partials: [sk_tiles][sk_splits][16][256] float4
+  uint32_t* counters;  // [sk_tiles], zero between calls
 };
 // vec: all rows 16-byte aligned (bases aligned, ld % 4 == 0) so 16-byte copies are legal.
 cudaError_t launch_sgemm_simt(const SimtParams& p, bool trans_b, bool vec, cudaStream_t s);
+// CTAs of the SIMT kernel that fit on one SM at once (occupancy query, cached).
+int sgemm_simt_ctas_per_sm(bool trans_b, bool vec);
+inline int64_t simt_ws_floats(int64_t partial_tiles) { return partial_tiles * 16 * 256 * 4; }
 constexpr int kSimtBM = 128, kSimtBN = 128, kSimtBK = 16, kSimtThreads = 256, kSimtStages = 3;
 
 // ------------------------------------------------------------------ BF16 tcgen05 tile path

@@ -123,37 +123,32 @@ __device__ __forceinline__ void ffma2(float& d0, float& d1, float a, float b0, f
 #endif
 }
 
+// One work item: the K tiles [kbeg, kend) of output tile `tile`.  sk_cta < 0 marks a
+// data-parallel tile (always the whole K range); otherwise the item is stream-K CTA
+// sk_cta's piece of the tile and, when it covers only part of K, goes through the partial
+// protocol (publish, count arrivals, the last arriver sums in CTA order).
 template <bool TRANS_B, bool VEC>
-__global__ void __launch_bounds__(NT, DG_SIMT_MIN_BLOCKS) sgemm_simt_kernel(const SimtParams p) {
-  extern __shared__ __align__(16) float smem[];
-  float* As = smem;
-  float* Bs = smem + STAGES * A_STAGE;
-
+__device__ __forceinline__ void simt_item(const SimtParams& p, float* As, float* Bs,
+                                          const int64_t tile, const int kbeg, const int kend,
+                                          const int chunk, uint32_t* s_is_last) {
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int wm = warp >> 1, wn = warp & 1;
   const int lm = lane >> 3, ln = lane & 7;
-
-  // Launched with programmatic serialisation: wait for the previous kernel before the first
-  // global access, and let the next one launch early.
-  pdl_trigger();
-  pdl_wait();
+  const int KT = static_cast<int>((p.K + BK - 1) / BK);
+  const int K = static_cast<int>(p.K);
 
   int64_t b, tm, tn;
-  raster_tile(blockIdx.x, p.tiles_m, p.tiles_n, p.group, &b, &tm, &tn);
+  raster_tile(tile, p.tiles_m, p.tiles_n, p.group, &b, &tm, &tn);
   const int64_t m0 = tm * BM, n0 = tn * BN;
   const float* A = p.A + b * p.strideA;
   const float* B = p.B + b * p.strideB;
-  float* C = p.C + b * p.strideC;
 
   float acc[8][8];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-
-  const int KT = static_cast<int>((p.K + BK - 1) / BK);
-  const int K = static_cast<int>(p.K);
 
   // Copy plan of this thread for the 16-byte path: chunks (rows ar, ar+64; K offset ac) of
   // the A tile and, for B, (rows br, br+8; column bc) in the N layout or (rows ar, ar+64)
@@ -165,10 +160,12 @@ __global__ void __launch_bounds__(NT, DG_SIMT_MIN_BLOCKS) sgemm_simt_kernel(cons
   const bool a_ok0 = m0 + ar < p.M, a_ok1 = m0 + ar + 64 < p.M;
   const bool bt_ok0 = n0 + ar < p.N, bt_ok1 = n0 + ar + 64 < p.N;
   const int b_nbytes = TRANS_B ? 0 : clamp_bytes(p.N - (n0 + bc));
-  const float* ga = A + (m0 + ar) * p.lda + ac;
-  const float* gb = TRANS_B ? B + (n0 + ar) * p.ldb + ac : B + br * p.ldb + n0 + bc;
+  const int64_t kofs = static_cast<int64_t>(kbeg) * BK;
+  const float* ga = A + (m0 + ar) * p.lda + ac + kofs;
+  const float* gb = TRANS_B ? B + (n0 + ar) * p.ldb + ac + kofs
+                            : B + (br + kofs) * p.ldb + n0 + bc;
 
-  int next_tile = 0;  // K tile the next issued stage copies
+  int next_tile = kbeg;  // K tile the next issued stage copies
   auto load_stage = [&](int stage) {
     const int k0 = next_tile * BK;
     if (VEC) {
@@ -176,18 +173,18 @@ __global__ void __launch_bounds__(NT, DG_SIMT_MIN_BLOCKS) sgemm_simt_kernel(cons
       const uint32_t bs_ = smem_u32(Bs + stage * B_STAGE);
       const int ka = clamp_bytes(K - (k0 + ac));
       const int a0 = a_ok0 ? ka : 0, a1 = a_ok1 ? ka : 0;
-      cp_async_16(as_ + (ar * LDS_K + ac) * 4, a0 ? ga : A, a0);
-      cp_async_16(as_ + ((ar + 64) * LDS_K + ac) * 4, a1 ? ga + 64 * p.lda : A, a1);
+      cp_async_16(as_ + (ar * LDS_K + ac) * 4, a0 ? ga : p.A, a0);
+      cp_async_16(as_ + ((ar + 64) * LDS_K + ac) * 4, a1 ? ga + 64 * p.lda : p.A, a1);
       ga += BK;
       if (TRANS_B) {
         const int b0 = bt_ok0 ? ka : 0, b1 = bt_ok1 ? ka : 0;
-        cp_async_16(bs_ + (ar * LDS_K + ac) * 4, b0 ? gb : B, b0);
-        cp_async_16(bs_ + ((ar + 64) * LDS_K + ac) * 4, b1 ? gb + 64 * p.ldb : B, b1);
+        cp_async_16(bs_ + (ar * LDS_K + ac) * 4, b0 ? gb : p.B, b0);
+        cp_async_16(bs_ + ((ar + 64) * LDS_K + ac) * 4, b1 ? gb + 64 * p.ldb : p.B, b1);
         gb += BK;
       } else {
         const int b0 = k0 + br < K ? b_nbytes : 0, b1 = k0 + br + 8 < K ? b_nbytes : 0;
-        cp_async_16(bs_ + (br * BN + bc) * 4, b0 ? gb : B, b0);
-        cp_async_16(bs_ + ((br + 8) * BN + bc) * 4, b1 ? gb + 8 * p.ldb : B, b1);
+        cp_async_16(bs_ + (br * BN + bc) * 4, b0 ? gb : p.B, b0);
+        cp_async_16(bs_ + ((br + 8) * BN + bc) * 4, b1 ? gb + 8 * p.ldb : p.B, b1);
         gb += BK * p.ldb;
       }
     } else {
@@ -202,7 +199,7 @@ __global__ void __launch_bounds__(NT, DG_SIMT_MIN_BLOCKS) sgemm_simt_kernel(cons
 
 #pragma unroll
   for (int s = 0; s < STAGES - 1; ++s) {
-    if (s < KT) load_stage(s);
+    if (kbeg + s < kend) load_stage(s);
     cp_async_commit();
   }
 
@@ -212,10 +209,10 @@ __global__ void __launch_bounds__(NT, DG_SIMT_MIN_BLOCKS) sgemm_simt_kernel(cons
 
   int stage = 0;                  // stage computed this iteration
   int load_slot = STAGES - 1;     // stage the next copy goes to
-  for (int kt = 0; kt < KT; ++kt) {
+  for (int kt = kbeg; kt < kend; ++kt) {
     cp_async_wait<STAGES - 2>();
     __syncthreads();
-    if (kt + STAGES - 1 < KT) load_stage(load_slot);
+    if (kt + STAGES - 1 < kend) load_stage(load_slot);
     cp_async_commit();
     load_slot = load_slot + 1 == STAGES ? 0 : load_slot + 1;
     const float* as = As + stage * A_STAGE;
@@ -258,6 +255,52 @@ __global__ void __launch_bounds__(NT, DG_SIMT_MIN_BLOCKS) sgemm_simt_kernel(cons
     stage = stage + 1 == STAGES ? 0 : stage + 1;
   }
   cp_async_wait<0>();
+  {
+  float* C = p.C + b * p.strideC;
+
+  if (chunk >= 0) {
+    // One of the sk_splits K chunks of a tail tile: publish the partial accumulator; the last
+    // chunk to arrive sums all chunks in chunk (= K) order -- a fixed order -- and writes C.
+    const int64_t sk_tile = tile - p.dp_tiles;
+    const int S = p.sk_splits;
+    float4* mine = reinterpret_cast<float4*>(p.ws) + ((sk_tile * S + chunk) * 16) * NT + tid;
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+      mine[q * NT] = make_float4(acc[q >> 1][4 * (q & 1)], acc[q >> 1][4 * (q & 1) + 1],
+                                 acc[q >> 1][4 * (q & 1) + 2], acc[q >> 1][4 * (q & 1) + 3]);
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      const uint32_t prev = atomicAdd(&p.counters[sk_tile], 1u);
+      const bool last = prev + 1u == static_cast<uint32_t>(S);
+      if (last) __threadfence();
+      *s_is_last = last ? 1u : 0u;
+    }
+    __syncthreads();
+    if (!*s_is_last) return;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    for (int cc = 0; cc < S; ++cc) {
+      const float4* src = reinterpret_cast<const float4*>(p.ws) + ((sk_tile * S + cc) * 16) * NT + tid;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {  // 8 independent 16-byte loads in flight
+        float4 part[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) part[q] = __ldcg(src + (8 * half + q) * NT);
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8) {
+          const int q = 8 * half + q8;
+          acc[q >> 1][4 * (q & 1)] += part[q8].x;
+          acc[q >> 1][4 * (q & 1) + 1] += part[q8].y;
+          acc[q >> 1][4 * (q & 1) + 2] += part[q8].z;
+          acc[q >> 1][4 * (q & 1) + 3] += part[q8].w;
+        }
+      }
+    }
+    if (tid == 0) p.counters[sk_tile] = 0u;  // ready for the next call
+  }
 
   // Epilogue: C = alpha*acc + beta*C_old, one FP32 rounding per operation.
   const float alpha = p.alpha, beta = p.beta;
@@ -294,6 +337,34 @@ __global__ void __launch_bounds__(NT, DG_SIMT_MIN_BLOCKS) sgemm_simt_kernel(cons
       }
     }
   }
+  }
+}
+
+template <bool TRANS_B, bool VEC>
+__global__ void __launch_bounds__(NT, DG_SIMT_MIN_BLOCKS) sgemm_simt_kernel(const SimtParams p) {
+  extern __shared__ __align__(16) float smem[];
+  float* As = smem;
+  float* Bs = smem + STAGES * A_STAGE;
+  __shared__ uint32_t s_is_last;
+
+  // Launched with programmatic serialisation: wait for the previous kernel before the first
+  // global access, and let the next one launch early.
+  pdl_trigger();
+  pdl_wait();
+
+  const int KT = static_cast<int>((p.K + BK - 1) / BK);
+  if (blockIdx.x < p.dp_tiles) {
+    // Data-parallel part of the grid: one whole tile per CTA.
+    simt_item<TRANS_B, VEC>(p, As, Bs, blockIdx.x, 0, KT, -1, &s_is_last);
+    return;
+  }
+  // Tail of the grid: tile dp_tiles + j / S, K chunk j % S (S = sk_splits equal chunks).
+  const int64_t j = blockIdx.x - p.dp_tiles;
+  const int S = p.sk_splits;
+  const int chunk = static_cast<int>(j % S);
+  const int kbeg = static_cast<int>(static_cast<int64_t>(chunk) * KT / S);
+  const int kend = static_cast<int>(static_cast<int64_t>(chunk + 1) * KT / S);
+  simt_item<TRANS_B, VEC>(p, As, Bs, p.dp_tiles + j / S, kbeg, kend, chunk, &s_is_last);
 }
 
 template <bool TRANS_B, bool VEC>
@@ -302,11 +373,34 @@ cudaError_t launch_variant(const SimtParams& p, cudaStream_t s) {
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = ensure_smem_attr(kern, SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;
-  const int64_t tiles = p.batch * p.tiles_m * p.tiles_n;
-  return launch_pdl(kern, dim3(static_cast<unsigned>(tiles)), dim3(NT), SMEM_BYTES, s, p);
+  const int64_t grid = p.dp_tiles + p.sk_tiles * p.sk_splits;
+  return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(NT), SMEM_BYTES, s, p);
 }
 
 }  // namespace
+
+namespace {
+template <bool TRANS_B, bool VEC>
+int ctas_per_sm_variant() {
+  static std::atomic<int> cached{0};
+  int n = cached.load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  auto kern = sgemm_simt_kernel<TRANS_B, VEC>;
+  static std::atomic<uint64_t> attr_done{0};
+  n = 0;
+  if (ensure_smem_attr(kern, SMEM_BYTES, attr_done) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, NT, SMEM_BYTES) != cudaSuccess ||
+      n < 1)
+    n = 1;
+  cached.store(n, std::memory_order_relaxed);
+  return n;
+}
+}  // namespace
+
+int sgemm_simt_ctas_per_sm(bool trans_b, bool vec) {
+  if (trans_b) return vec ? ctas_per_sm_variant<true, true>() : ctas_per_sm_variant<true, false>();
+  return vec ? ctas_per_sm_variant<false, true>() : ctas_per_sm_variant<false, false>();
+}
 
 cudaError_t launch_sgemm_simt(const SimtParams& p, bool trans_b, bool vec, cudaStream_t s) {
   if (trans_b) return vec ? launch_variant<true, true>(p, s) : launch_variant<true, false>(p, s);
