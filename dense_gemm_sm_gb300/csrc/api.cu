@@ -173,19 +173,14 @@ void plan_bf16(int64_t M, int64_t N, int64_t K, int64_t batch, int sms, dg_plan*
     return;
   }
   pl->kernel = DG_KERNEL_TC_BF16;
-  // Tile width: the one that minimises (waves of the persistent grid) x (time per tile, which
-  // is proportional to the width); ties go to the wider tile.  Widths that are not a multiple
-  // of 64 (224, 192) are built but not chosen: on the FFN shape 128 x 224 tiles measured
-  // slower than 128 x 256 despite fewer idle SMs in the last wave.
-  int bn = 256;
-  int64_t best = -1;
-  for (int cand : {256, 128}) {
-    const int64_t tiles = batch * cdiv(M, kTcBM) * cdiv(N, cand);
-    const int64_t cost = cdiv(tiles, sms > 0 ? sms : 1) * cand;
-    if (best < 0 || cost < best) {
-      best = cost;
-      bn = cand;
-    }
+  // Tile width, from a measured sweep over 128..256 on FFN, square (2048..8192) and wide
+  // shapes: 256 is fastest everywhere (narrower tiles load more B bytes per FLOP, which
+  // costs more than the better wave fill they buy), so 128 is used only when N <= 128.
+  int bn = N <= 128 ? 128 : 256;
+  // Tuning override (bench and sweeps): DG_TC_BN=256|224|192|128 forces the tile width.
+  if (const char* e = std::getenv("DG_TC_BN")) {
+    const int f = std::atoi(e);
+    if (f == 256 || f == 224 || f == 192 || f == 128) bn = f;
   }
   pl->tile_m = kTcBM;
   pl->tile_n = bn;
