@@ -40,9 +40,17 @@ SM_COUNT_NOMINAL = 152
 FP32_LANES_PER_SM = 128          # FP32 FMA units per SM (4 partitions x 32)
 SM_MAX_MHZ_NOMINAL = 2070.0
 
-# ncu DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum), keyed by
-# workload, valid only while the kernel source hash matches the one it was taken with.
-MEASURED_TRAFFIC = {}
+# ncu DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum, one capture of
+# the workload's kernel), keyed by workload; an entry is used only while the hash of the
+# kernel's sources (kernel file, planner, headers) matches the one it was taken with.
+COMMON_SOURCES = ["api.cu", "dg_internal.h", "ptx.cuh", "tile_sched.h"]
+MEASURED_TRAFFIC = {
+    "sgemm_4096": {"bytes_per_launch": 445_493_760, "source_hash": "054294bebacd30bd"},
+    "ffn_bf16": {"bytes_per_launch": 119_055_360, "source_hash": "6dabc67fef36a803"},
+    "bf16_4096": {"bytes_per_launch": 88_940_288, "source_hash": "6dabc67fef36a803"},
+    "qk_batched": {"bytes_per_launch": 1_079_842_520, "source_hash": "6dabc67fef36a803"},
+    "decode_m16": {"bytes_per_launch": 104_747_008, "source_hash": "fc7a372324f51032"},
+}
 
 
 def read_peaks():
@@ -87,7 +95,7 @@ class Workload:
             return dict(kind="f32", w=w, batch=1, flops=2.0 * M * N * K,
                         algo_bytes=4.0 * (M * K + K * N + (2 if w["beta"] != 0 else 1) * M * N),
                         bound="alu", unit="TFLOPS", kernel="sgemm_simt_kernel",
-                        sources=["sgemm_simt.cu"],
+                        sources=["sgemm_simt.cu"] + COMMON_SOURCES,
                         desc=f"FP32 SGEMM M={M} N={N} K={K} lda={w['lda']} ldb={w['ldb']} "
                              f"ldc={w['ldc']} alpha={float(w['alpha'])} beta={float(w['beta'])}")
         if name == "ffn_bf16":
@@ -95,14 +103,14 @@ class Workload:
             M, N, K = w["M"], w["N"], w["K"]
             return dict(kind="bf16", w=w, batch=1, flops=2.0 * M * N * K,
                         algo_bytes=2.0 * (M * K + K * N + M * N), bound="tensor", unit="TFLOPS",
-                        kernel="gemm_tc_kernel", sources=["gemm_tc.cu", "ptx.cuh"],
+                        kernel="gemm_tc_kernel", sources=["gemm_tc.cu"] + COMMON_SOURCES,
                         desc=f"BF16 FFN projection C=XW M={M} N={N} K={K}, FP32 accumulate, BF16 out")
         if name == "bf16_4096":
             w = inputs.bf16_square(4096)
             M, N, K = w["M"], w["N"], w["K"]
             return dict(kind="bf16", w=w, batch=1, flops=2.0 * M * N * K,
                         algo_bytes=2.0 * (M * K + K * N + M * N), bound="tensor", unit="TFLOPS",
-                        kernel="gemm_tc_kernel", sources=["gemm_tc.cu", "ptx.cuh"],
+                        kernel="gemm_tc_kernel", sources=["gemm_tc.cu"] + COMMON_SOURCES,
                         desc=f"BF16 GEMM M=N=K={M}, FP32 accumulate, BF16 out")
         if name.startswith("decode_m"):
             m = int(name[len("decode_m"):])
@@ -110,14 +118,14 @@ class Workload:
             M, N, K = w["M"], w["N"], w["K"]
             return dict(kind="bf16", w=w, batch=1, flops=2.0 * M * N * K,
                         algo_bytes=2.0 * (M * K + K * N + M * N), bound="hbm", unit="GB/s",
-                        kernel="gemm_thin_kernel", sources=["gemm_thin.cu", "ptx.cuh"],
+                        kernel="gemm_thin_kernel", sources=["gemm_thin.cu"] + COMMON_SOURCES,
                         desc=f"BF16 decode GEMM M={M} N={N} K={K}, BF16 out")
         if name == "qk_batched":
             w = inputs.qk_batched()
             b, S, D = w["batch"], w["M"], w["K"]
             return dict(kind="bf16b", w=w, batch=b, flops=2.0 * b * S * S * D,
                         algo_bytes=2.0 * b * (2 * S * D) + 4.0 * b * S * S, bound="hbm",
-                        unit="TFLOPS", kernel="gemm_tc_kernel", sources=["gemm_tc.cu", "ptx.cuh"],
+                        unit="TFLOPS", kernel="gemm_tc_kernel", sources=["gemm_tc.cu"] + COMMON_SOURCES,
                         desc=f"strided-batched BF16 S=QK^T*alpha batch={b} S={S} d={D}, FP32 out")
         raise ValueError(f"unknown workload {name}")
 
@@ -290,6 +298,18 @@ def time_steps(torch, wl, steps, warmup, barrier):
     return total_ms, [total_ms / steps], t0, t1
 
 
+def aggregate_ranks(ms_local, metric_of_seconds, world, dist, device):
+    """Whole-job figure of N independent replicas: the slowest rank's time per step (max
+    over ranks) and the work of all ranks divided by that time."""
+    ms = ms_local
+    if dist is not None and world > 1:
+        import torch
+        t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, metric_of_seconds(ms / 1e3) * world
+
+
 def time_e2e(torch, wl, steps, warmup):
     """Same workload through the public API with host inputs: each step copies that step's
     inputs from pinned host memory, calls the library and reads the result back."""
@@ -444,13 +464,8 @@ def main():
     if st != dg.DG_OK:
         raise SystemExit(f"device status after the timed region: {dg.status_string(st)}")
 
-    ms = total_ms / args.steps
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    per_rank_value = wl.metric_value(ms / 1e3)
-    value = per_rank_value * world
+    ms, value = aggregate_ranks(total_ms / args.steps, wl.metric_value, world, dist,
+                                torch.device("cuda"))
     launch_ms = float(np.mean(per_launch))
 
     e2e = None if args.no_e2e else time_e2e(torch, wl, max(3, min(args.steps, 20)), 2)
@@ -489,7 +504,7 @@ def main():
             rf = other.roofline(float(np.mean(per)) / 1e3, peaks, None)
             suite[name] = {"value": round(other.metric_value(s), 3), "unit": other.unit,
                            "ms_per_step": round(s * 1e3, 4), "roofline_frac": rf["frac"],
-                           "bound": rf["bound"]}
+                           "bound": rf["bound"], "traffic": rf["traffic"]}
             del other
             torch.cuda.empty_cache()
         st = dg.dg_device_status()
