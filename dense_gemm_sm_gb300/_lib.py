@@ -37,7 +37,8 @@ class dg_plan(ctypes.Structure):
     _fields_ = [
         ("kernel", ctypes.c_int32), ("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32),
         ("tile_k", ctypes.c_int32), ("stages", ctypes.c_int32), ("group", ctypes.c_int32),
-        ("ntok", ctypes.c_int32), ("vec", ctypes.c_int32), ("tiles", ctypes.c_int64),
+        ("ntok", ctypes.c_int32), ("vec", ctypes.c_int32), ("splits", ctypes.c_int32),
+        ("tiles", ctypes.c_int64), ("tail_tiles", ctypes.c_int64),
         ("grid", ctypes.c_int64), ("kblocks", ctypes.c_int64),
         ("workspace_bytes", ctypes.c_int64),
     ]

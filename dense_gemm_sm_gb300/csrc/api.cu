@@ -151,6 +151,8 @@ void plan_f32(int64_t M, int64_t N, int64_t K, int64_t batch, int64_t resident, 
   *sk_splits = best_s;
   *sk_tiles = best_s > 1 ? tail : 0;
   *dp_tiles = T - *sk_tiles;
+  pl->splits = best_s;
+  pl->tail_tiles = *sk_tiles;
   pl->grid = *dp_tiles + *sk_tiles * best_s;
   pl->workspace_bytes = *sk_tiles > 0 ? simt_ws_floats(*sk_tiles * best_s) * 4 + *sk_tiles * 4 : 0;
 }
@@ -190,6 +192,10 @@ void plan_bf16(int64_t M, int64_t N, int64_t K, int64_t batch, int sms, dg_plan*
   pl->tiles = batch * cdiv(M, kTcBM) * cdiv(N, bn);
   pl->grid = pl->tiles < sms ? pl->tiles : sms;
   pl->kblocks = cdiv(K, kTcBK);
+  // No K split of a partial last wave here: combining 128 x 256 FP32 partial tiles costs
+  // about as much as the idle SMs it would fill (measured slower on the FFN shape).
+  pl->splits = 1;
+  pl->tail_tiles = 0;
 }
 
 dg_status plan(int32_t dtype, int64_t M, int64_t N, int64_t K, int64_t batch, float alpha,

@@ -135,7 +135,6 @@ __device__ __forceinline__ void simt_item(const SimtParams& p, float* As, float*
   const int warp = tid >> 5, lane = tid & 31;
   const int wm = warp >> 1, wn = warp & 1;
   const int lm = lane >> 3, ln = lane & 7;
-  const int KT = static_cast<int>((p.K + BK - 1) / BK);
   const int K = static_cast<int>(p.K);
 
   int64_t b, tm, tn;
