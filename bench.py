@@ -45,11 +45,14 @@ SM_MAX_MHZ_NOMINAL = 2070.0
 # kernel's sources (kernel file, planner, headers) matches the one it was taken with.
 COMMON_SOURCES = ["api.cu", "dg_internal.h", "ptx.cuh", "tile_sched.h"]
 MEASURED_TRAFFIC = {
-    "sgemm_4096": {"bytes_per_launch": 445_493_760, "source_hash": "054294bebacd30bd"},
-    "ffn_bf16": {"bytes_per_launch": 119_055_360, "source_hash": "6dabc67fef36a803"},
-    "bf16_4096": {"bytes_per_launch": 88_940_288, "source_hash": "6dabc67fef36a803"},
-    "qk_batched": {"bytes_per_launch": 1_079_842_520, "source_hash": "6dabc67fef36a803"},
-    "decode_m16": {"bytes_per_launch": 104_747_008, "source_hash": "fc7a372324f51032"},
+    "sgemm_4096": {"bytes_per_launch": 457_874_944, "source_hash": "984861a5fc06cc06"},
+    "sgemm_ragged": {"bytes_per_launch": 25_527_040, "source_hash": "984861a5fc06cc06"},
+    "ffn_bf16": {"bytes_per_launch": 118_126_592, "source_hash": "f994967f4f7fd9f4"},
+    "bf16_4096": {"bytes_per_launch": 93_359_872, "source_hash": "f994967f4f7fd9f4"},
+    "qk_batched": {"bytes_per_launch": 1_078_761_984, "source_hash": "f994967f4f7fd9f4"},
+    "decode_m1": {"bytes_per_launch": 103_844_608, "source_hash": "e6325cabd77eb51b"},
+    "decode_m4": {"bytes_per_launch": 103_601_152, "source_hash": "e6325cabd77eb51b"},
+    "decode_m16": {"bytes_per_launch": 103_616_000, "source_hash": "e6325cabd77eb51b"},
 }
 
 
