@@ -45,14 +45,14 @@ SM_MAX_MHZ_NOMINAL = 2070.0
 # kernel's sources (kernel file, planner, headers) matches the one it was taken with.
 COMMON_SOURCES = ["api.cu", "dg_internal.h", "ptx.cuh", "tile_sched.h"]
 MEASURED_TRAFFIC = {
-    "sgemm_4096": {"bytes_per_launch": 457_874_944, "source_hash": "984861a5fc06cc06"},
-    "sgemm_ragged": {"bytes_per_launch": 25_527_040, "source_hash": "984861a5fc06cc06"},
-    "ffn_bf16": {"bytes_per_launch": 118_126_592, "source_hash": "f994967f4f7fd9f4"},
-    "bf16_4096": {"bytes_per_launch": 93_359_872, "source_hash": "f994967f4f7fd9f4"},
-    "qk_batched": {"bytes_per_launch": 1_078_761_984, "source_hash": "f994967f4f7fd9f4"},
-    "decode_m1": {"bytes_per_launch": 103_844_608, "source_hash": "e6325cabd77eb51b"},
-    "decode_m4": {"bytes_per_launch": 103_601_152, "source_hash": "e6325cabd77eb51b"},
-    "decode_m16": {"bytes_per_launch": 103_616_000, "source_hash": "e6325cabd77eb51b"},
+    "sgemm_4096": {"bytes_per_launch": 464_984_832, "source_hash": "1fd602b20102736c"},
+    "sgemm_ragged": {"bytes_per_launch": 25_963_520, "source_hash": "1fd602b20102736c"},
+    "ffn_bf16": {"bytes_per_launch": 118_251_776, "source_hash": "fd094a58433ac027"},
+    "bf16_4096": {"bytes_per_launch": 89_063_680, "source_hash": "fd094a58433ac027"},
+    "qk_batched": {"bytes_per_launch": 1_079_800_320, "source_hash": "fd094a58433ac027"},
+    "decode_m1": {"bytes_per_launch": 103_823_616, "source_hash": "ae40842cb74ac8ea"},
+    "decode_m4": {"bytes_per_launch": 104_187_392, "source_hash": "ae40842cb74ac8ea"},
+    "decode_m16": {"bytes_per_launch": 103_992_832, "source_hash": "ae40842cb74ac8ea"},
 }
 
 

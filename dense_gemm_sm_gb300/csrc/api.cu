@@ -121,8 +121,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // ------------------------------------------------------------------ planning
 // FP32: whole waves of tiles run data-parallel (one tile per CTA).  The tiles of the last,
 // partial wave are split along K into S equal chunks, one CTA each, S chosen so that the
-// tail takes the fewest tile-times: ceil(tail * S / resident) / S, with at least 16 K tiles
-// (256 of K) per chunk and at most three waves of tail CTAs; the chunks of a tile are summed
+// tail takes the fewest tile-times: ceil(tail * S / resident) / S, with at least 256 of K
+// per chunk and at most three waves of tail CTAs; the chunks of a tile are summed
 // in K order by the last one to finish (a fixed order).
 void plan_f32(int64_t M, int64_t N, int64_t K, int64_t batch, int64_t resident, dg_plan* pl,
               int64_t* dp_tiles, int64_t* sk_tiles, int* sk_splits) {
@@ -140,7 +140,8 @@ void plan_f32(int64_t M, int64_t N, int64_t K, int64_t batch, int64_t resident, 
   int best_s = 1;
   if (tail > 0) {
     double best = 1.0;  // tail time (in tile times) without splitting
-    for (int64_t S = 2; S <= KT / 16 && tail * S <= 3 * G; ++S) {
+    const int64_t min_chunk = cdiv(256, kSimtBK);  // K tiles in 256 of K
+    for (int64_t S = 2; S <= KT / min_chunk && tail * S <= 3 * G; ++S) {
       const double t = static_cast<double>(cdiv(tail * S, G)) / static_cast<double>(S);
       if (t < best - 1e-9) {
         best = t;

@@ -32,7 +32,15 @@ cudaError_t launch_sgemm_simt(const SimtParams& p, bool trans_b, bool vec, cudaS
 // CTAs of the SIMT kernel that fit on one SM at once (occupancy query, cached).
 int sgemm_simt_ctas_per_sm(bool trans_b, bool vec);
 inline int64_t simt_ws_floats(int64_t partial_tiles) { return partial_tiles * 16 * 256 * 4; }
-constexpr int kSimtBM = 128, kSimtBN = 128, kSimtBK = 16, kSimtThreads = 256, kSimtStages = 3;
+#ifndef DG_SIMT_BK
+#define DG_SIMT_BK 32
+#endif
+#ifndef DG_SIMT_STAGES
+#define DG_SIMT_STAGES 2
+#endif
+constexpr int kSimtBM = 128, kSimtBN = 128, kSimtBK = DG_SIMT_BK, kSimtThreads = 256,
+              kSimtStages = DG_SIMT_STAGES;
+static_assert(kSimtBK == 16 || kSimtBK == 32, "SIMT K tile");
 
 // ------------------------------------------------------------------ BF16 tcgen05 tile path
 struct TcParams {

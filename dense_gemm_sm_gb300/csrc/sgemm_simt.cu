@@ -6,10 +6,10 @@
 // vector accesses (section 7), a bank-conflict-free shared layout (section 8) and
 // asynchronous multistage copies (sections 9-10).  This kernel keeps those ideas and sets
 // them for this GPU:
-//   * 128 x 128 block tile, BK = 16, 256 threads, an 8 x 8 FP32 accumulator per thread
+//   * 128 x 128 block tile, BK = 32, 256 threads, an 8 x 8 FP32 accumulator per thread
 //     (4 x 8 lanes per warp, warp tile 32 x 64);
-//   * a 3-stage cp.async ring (global -> shared without registers), zero-filled edges;
-//   * A is kept K-contiguous in shared memory (row stride 20 floats).  Each thread reads
+//   * a 2-stage cp.async ring (global -> shared without registers), zero-filled edges;
+//   * A is kept K-contiguous in shared memory (row stride BK + 4 floats).  Each thread reads
 //     4 K-steps of one A row with one 16-byte load; the 4 distinct rows a warp reads
 //     fall in 4 different bank quads, and the 8 lanes of a quarter-warp share a row, so
 //     the reads are conflict-free without the register transpose of the tutorial;
@@ -48,7 +48,7 @@ __device__ __forceinline__ void load_kmajor(float* dst, const float* src, int64_
 #pragma unroll
     for (int h = 0; h < (BM * BK / 4) / NT; ++h) {
       const int q = tid + h * NT;
-      const int r = q >> 2, c4 = q & 3;
+      const int r = q / (BK / 4), c4 = q % (BK / 4);
       const int64_t gr = r0 + r, gk = k0 + c4 * 4;
       const int bytes = gr < rows ? clamp_bytes(K - gk) : 0;
       const float* g = bytes ? src + gr * ld + gk : src;
@@ -58,7 +58,7 @@ __device__ __forceinline__ void load_kmajor(float* dst, const float* src, int64_
 #pragma unroll
     for (int h = 0; h < (BM * BK) / NT; ++h) {
       const int e = tid + h * NT;
-      const int r = e >> 4, k = e & 15;
+      const int r = e / BK, k = e % BK;
       const int64_t gr = r0 + r, gk = k0 + k;
       const bool ok = gr < rows && gk < K;
       cp_async_4(smem_u32(dst + r * LDS_K + k), ok ? src + gr * ld + gk : src, ok ? 4 : 0);
@@ -149,15 +149,15 @@ __device__ __forceinline__ void simt_item(const SimtParams& p, float* As, float*
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
 
-  // Copy plan of this thread for the 16-byte path: chunks (rows ar, ar+64; K offset ac) of
-  // the A tile and, for B, (rows br, br+8; column bc) in the N layout or (rows ar, ar+64)
-  // in the T layout.  Only two running global pointers are kept; the second chunk of each
-  // operand is reached through the leading dimension (a kernel parameter), so few
-  // registers stay live across the main loop.
-  const int ar = tid >> 2, ac = (tid & 3) * 4;
+  // Copy plan of this thread for the 16-byte path.  A (and B in the T layout): CPR = BK/4
+  // chunks per row, rows ar + h*RS (RS = NT/CPR) at K offset ac.  B in the N layout: rows
+  // br + 8h of the K tile, column bc.  Only two running global pointers are kept; the other
+  // chunks are reached through the leading dimension (a kernel parameter), so few registers
+  // stay live across the main loop.
+  constexpr int CPR = BK / 4, RS = NT / CPR, HA = BM / RS, HB = BK / 8;
+  const int ar = tid / CPR, ac = (tid % CPR) * 4;
   const int br = tid >> 5, bc = (tid & 31) * 4;
-  const bool a_ok0 = m0 + ar < p.M, a_ok1 = m0 + ar + 64 < p.M;
-  const bool bt_ok0 = n0 + ar < p.N, bt_ok1 = n0 + ar + 64 < p.N;
+  const int64_t a_rows_left = p.M - (m0 + ar), bt_rows_left = p.N - (n0 + ar);
   const int b_nbytes = TRANS_B ? 0 : clamp_bytes(p.N - (n0 + bc));
   const int64_t kofs = static_cast<int64_t>(kbeg) * BK;
   const float* ga = A + (m0 + ar) * p.lda + ac + kofs;
@@ -171,19 +171,25 @@ __device__ __forceinline__ void simt_item(const SimtParams& p, float* As, float*
       const uint32_t as_ = smem_u32(As + stage * A_STAGE);
       const uint32_t bs_ = smem_u32(Bs + stage * B_STAGE);
       const int ka = clamp_bytes(K - (k0 + ac));
-      const int a0 = a_ok0 ? ka : 0, a1 = a_ok1 ? ka : 0;
-      cp_async_16(as_ + (ar * LDS_K + ac) * 4, a0 ? ga : p.A, a0);
-      cp_async_16(as_ + ((ar + 64) * LDS_K + ac) * 4, a1 ? ga + 64 * p.lda : p.A, a1);
+#pragma unroll
+      for (int h = 0; h < HA; ++h) {
+        const int a = a_rows_left > h * RS ? ka : 0;
+        cp_async_16(as_ + ((ar + h * RS) * LDS_K + ac) * 4, a ? ga + h * RS * p.lda : p.A, a);
+      }
       ga += BK;
       if (TRANS_B) {
-        const int b0 = bt_ok0 ? ka : 0, b1 = bt_ok1 ? ka : 0;
-        cp_async_16(bs_ + (ar * LDS_K + ac) * 4, b0 ? gb : p.B, b0);
-        cp_async_16(bs_ + ((ar + 64) * LDS_K + ac) * 4, b1 ? gb + 64 * p.ldb : p.B, b1);
+#pragma unroll
+        for (int h = 0; h < HA; ++h) {
+          const int bb = bt_rows_left > h * RS ? ka : 0;
+          cp_async_16(bs_ + ((ar + h * RS) * LDS_K + ac) * 4, bb ? gb + h * RS * p.ldb : p.B, bb);
+        }
         gb += BK;
       } else {
-        const int b0 = k0 + br < K ? b_nbytes : 0, b1 = k0 + br + 8 < K ? b_nbytes : 0;
-        cp_async_16(bs_ + (br * BN + bc) * 4, b0 ? gb : p.B, b0);
-        cp_async_16(bs_ + ((br + 8) * BN + bc) * 4, b1 ? gb + 8 * p.ldb : p.B, b1);
+#pragma unroll
+        for (int h = 0; h < HB; ++h) {
+          const int bb = k0 + br + 8 * h < K ? b_nbytes : 0;
+          cp_async_16(bs_ + ((br + 8 * h) * BN + bc) * 4, bb ? gb + 8 * h * p.ldb : p.B, bb);
+        }
         gb += BK * p.ldb;
       }
     } else {
