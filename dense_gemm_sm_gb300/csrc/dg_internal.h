@@ -73,7 +73,7 @@ struct ThinParams {
   float alpha, beta;
   void* C; int64_t ldc;
   int32_t c_f32;
-  float* ws;           // partials: [ctas][2][128 columns][ntok] fp32
+  float* ws;           // partials: [ctas][2][ntok / 4][128 columns] float4
   uint32_t* counters;  // [n_tiles], zero between calls
   uint32_t* status;
 };

@@ -10,10 +10,15 @@
 //     one CTA per SM (stream-K); each CTA streams its contiguous range of W through a deep
 //     TMA ring (8 stages x 16 KiB of W);
 //   * a tile split across CTAs ("split K", "Operator & Runtime" section 5.2.4) is combined
-//     by the last CTA to arrive: partial sums go to a workspace, an atomic counter per
-//     tile detects the last arrival, which adds the partials in CTA order (= K order) --
-//     a fixed order, so results are identical run to run (same section: atomics give
-//     arrival-dependent rounding, a fixed combination order does not);
+//     by one of its contributors.  Each contributor stores its part, fences and takes a
+//     ticket from the tile's atomic counter; the last to take one adds the parts in a fixed
+//     order -- the contributors after the tile's first CTA in CTA order, then the first
+//     CTA's part -- so results are identical run to run whoever combines (same section:
+//     atomics give arrival-dependent rounding, a fixed combination order does not).  The
+//     tile's first CTA reaches its part at the very end of its range, when the others have
+//     usually finished theirs: while its own part still streams it watches the counter, and
+//     once every other contributor holds a ticket it adds their parts ahead of time,
+//     leaving only its own for the end;
 //   * alpha/beta and the single rounding to BF16 (or FP32 output) happen after the full
 //     K reduction (sections 5.4.2-5.4.3).
 // Warp roles (192 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer,
@@ -37,6 +42,13 @@ constexpr uint32_t W_BYTES = BNW * BK * 2;  // 16 KiB per stage
 #define DG_THIN_STAGES 8
 #endif
 constexpr int STAGES = DG_THIN_STAGES;
+// W blocks of its range a CTA asks L2 for before the previous grid of the stream has
+// finished (0: none).
+#ifndef DG_THIN_PREFETCH
+#define DG_THIN_PREFETCH 12
+#endif
+constexpr int PREFETCH = DG_THIN_PREFETCH;
+
 constexpr int NUM_THREADS = 192;
 
 template <int NTOK>
@@ -57,7 +69,78 @@ struct SmemCtl {
   uint32_t abort;
   uint32_t is_last;
   uint32_t seg_ok;
+  uint32_t pre;  // the tile's other parts were added ahead of this CTA's own
 };
+
+// Brings one box of the tensor into L2 (no shared memory, no completion signal).  The
+// prefetch returns nothing to the program, so it may run before the previous grid of the
+// stream has finished: L2 is the device's point of coherence, and writes that the previous
+// grid makes later land there too, so loads issued after the wait still see them.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* a) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed(uint32_t* a, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+// A split-K part is [ntok / 4 float4 groups][128 columns]: a warp's stores and loads of one
+// group cover 512 contiguous bytes.  Adds one column's values of one or two parts into s[],
+// A's before B's (srcB may be null; the first nq groups carry rows of X), with all loads in
+// flight together: under a full HBM stream an L2 round trip costs about a microsecond.
+template <int NTOK, bool TWO>
+__device__ __forceinline__ void add_parts(float (&s)[NTOK], const float4* srcA, const float4* srcB,
+                                          int nq) {
+  float4 a[NTOK / 4], b[TWO ? NTOK / 4 : 1];
+  const bool two = TWO && srcB != nullptr;
+#pragma unroll
+  for (int q = 0; q < NTOK / 4; ++q)
+    if (q < nq) a[q] = __ldcg(srcA + q * BNW);
+  if (TWO && two) {
+#pragma unroll
+    for (int q = 0; q < NTOK / 4; ++q)
+      if (q < nq) b[q] = __ldcg(srcB + q * BNW);
+  }
+#pragma unroll
+  for (int q = 0; q < NTOK / 4; ++q) {
+    if (q < nq) {
+      s[4 * q] += a[q].x; s[4 * q + 1] += a[q].y; s[4 * q + 2] += a[q].z; s[4 * q + 3] += a[q].w;
+    }
+  }
+  if (TWO && two) {
+#pragma unroll
+    for (int q = 0; q < NTOK / 4; ++q) {
+      if (q < nq) {
+        s[4 * q] += b[q].x; s[4 * q + 1] += b[q].y; s[4 * q + 2] += b[q].z; s[4 * q + 3] += b[q].w;
+      }
+    }
+  }
+}
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -88,15 +171,28 @@ struct SegmentWalk {
   }
 };
 
-__device__ __forceinline__ void store_out(const ThinParams& p, int64_t t, int64_t n, float acc) {
+// Writes column n of C for rows 0..M-1 from vals[] (one value per row of X).
+template <int NTOK>
+__device__ __forceinline__ void store_row(const ThinParams& p, int64_t n, const float (&vals)[NTOK]) {
+  const int m = p.M < NTOK ? static_cast<int>(p.M) : NTOK;
   const float alpha = p.alpha, beta = p.beta;
   if (p.c_f32) {
-    float* c = static_cast<float*>(p.C) + t * p.ldc + n;
-    *c = beta != 0.f ? fmaf(alpha, acc, beta * *c) : alpha * acc;
+    float* c = static_cast<float*>(p.C) + n;
+#pragma unroll
+    for (int t = 0; t < NTOK; ++t) {
+      if (t < m) *c = beta != 0.f ? fmaf(alpha, vals[t], beta * *c) : alpha * vals[t];
+      c += p.ldc;
+    }
   } else {
-    __nv_bfloat16* c = static_cast<__nv_bfloat16*>(p.C) + t * p.ldc + n;
-    const float v = beta != 0.f ? fmaf(alpha, acc, beta * __bfloat162float(*c)) : alpha * acc;
-    *c = __float2bfloat16_rn(v);
+    __nv_bfloat16* c = static_cast<__nv_bfloat16*>(p.C) + n;
+#pragma unroll
+    for (int t = 0; t < NTOK; ++t) {
+      if (t < m) {
+        const float x = beta != 0.f ? fmaf(alpha, vals[t], beta * __bfloat162float(*c)) : alpha * vals[t];
+        *c = __float2bfloat16_rn(x);
+      }
+      c += p.ldc;
+    }
   }
 }
 
@@ -132,6 +228,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ctl->abort = 0;
     ctl->is_last = 0;
     ctl->seg_ok = 0;
+    ctl->pre = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -160,6 +257,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t it = 0;
       bool ok = true;
       bool have = walk.next(&sg);  // index arithmetic before the wait
+      if (PREFETCH > 0) {
+        // The head of this CTA's range goes to L2 while the previous grid drains; the
+        // loads below then find it there.
+        const IDX u0 = sk_start<IDX>(c, units, ctas), u1 = sk_start<IDX>(c + 1, units, ctas);
+        const IDX ue = u1 - u0 > static_cast<IDX>(PREFETCH) ? u0 + static_cast<IDX>(PREFETCH) : u1;
+        for (IDX u = u0; u < ue; ++u) {
+          const IDX tile = u / kblocks;
+          const int32_t xn = static_cast<int32_t>(tile * BNW);
+          const int32_t kx = static_cast<int32_t>((u - tile * kblocks) * BK);
+          if (W_KMAJOR) {
+            tma_prefetch_l2_2d(&tmW, kx, xn);
+          } else {
+            tma_prefetch_l2_2d(&tmW, xn, kx);
+            if (xn + 64 < p.N) tma_prefetch_l2_2d(&tmW, xn + 64, kx);
+          }
+        }
+      }
       pdl_wait();
       for (; ok && have; have = walk.next(&sg)) {
         const int32_t xn = static_cast<int32_t>(sg.tile * BNW);
@@ -239,12 +353,74 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int q = warp & 3;
     const int row = q * 32 + lane;  // W column within the tile
     const int etid = threadIdx.x - 64;
+    // float4 groups per column that carry rows of X; the rest are never stored or read.
+    const int nq = static_cast<int>(((p.M < NTOK ? p.M : NTOK) + 3) / 4);
     SegmentWalk<IDX> walk(p, c);
     Segment<IDX> sg;
     uint32_t lt = 0;
     pdl_wait();
     while (walk.next(&sg)) {
       const uint32_t acc = lt & 1u, aph = (lt >> 1) & 1u;
+      const bool whole = sg.kbeg == 0 && sg.kend == kblocks;
+      // kbeg == 0 on a shared tile: this CTA is the tile's first contributor, and this is
+      // the last segment of its range.
+      const bool head = sg.kbeg == 0 && !whole;
+      const IDX first = sk_cta_of<IDX>(sg.tile * kblocks, units, ctas);
+      const IDX last = sk_cta_of<IDX>((sg.tile + 1) * kblocks - 1, units, ctas);
+      auto part_of = [&](IDX cc) {
+        const int sl = sk_slot<IDX>(cc, sg.tile, kblocks, units, ctas);
+        return reinterpret_cast<float4*>(p.ws) + (static_cast<int64_t>(cc) * 2 + sl) * BNW * (NTOK / 4) + row;
+      };
+      // Adds the first nk parts of the fixed order -- the contributors after the first in
+      // CTA order, then the first CTA's part -- into acc_s[], this CTA's own from vals[] and
+      // the others from the workspace, two per round trip.
+      auto add_in_order = [&](float (&acc_s)[NTOK], const float (&vals)[NTOK], IDX nk) {
+        auto order = [&](IDX k) { return k < last - first ? first + 1 + k : first; };
+        for (IDX k = 0; k < nk;) {
+          const IDX cc = order(k);
+          if (cc == c) {
+#pragma unroll
+            for (int t = 0; t < NTOK; ++t) acc_s[t] += vals[t];
+            ++k;
+            continue;
+          }
+          const bool pair = k + 1 < nk && order(k + 1) != c;
+          add_parts<NTOK, true>(acc_s, part_of(cc), pair ? part_of(order(k + 1)) : nullptr, nq);
+          k += pair ? 2 : 1;
+        }
+      };
+      float s[NTOK], v[NTOK];  // the combined sum; this CTA's own part
+#pragma unroll
+      for (int t = 0; t < NTOK; ++t) s[t] = 0.f;
+      if (head) {
+        // Watch the counter while this CTA's own part streams.  Once all other contributors
+        // hold tickets none of them can be last, so this CTA combines: it resets the counter
+        // and adds their parts now, leaving only its own for the end.  If its own part is
+        // ready first, it takes a ticket like the others.
+        if (etid == 0) {
+          const uint32_t need = static_cast<uint32_t>(sk_contributors<IDX>(sg.tile, kblocks, units, ctas));
+          uint32_t pre = 0;
+          const uint64_t t0 = globaltimer_ns();
+          for (;;) {
+            if (ld_relaxed(&p.counters[sg.tile]) + 1u == need) {
+              pre = 1;
+              break;
+            }
+            if (mbar_test(smem_u32(&ctl->tfull[acc]), aph)) break;
+            if (*abort || globaltimer_ns() - t0 > kWaitLimitNs) break;  // the wait below reports
+            __nanosleep(128);
+          }
+          if (pre) {
+            fence_acq_rel_gpu();  // acquire: the parts are read after their tickets
+            st_relaxed(&p.counters[sg.tile], 0u);  // ready for the next call
+          }
+          ctl->pre = pre;
+        }
+        epi_bar();
+        if (ctl->pre) add_in_order(s, v, last - first);
+      }
+      const bool pre = head && ctl->pre;
+
       // One thread waits (bounded) and the 128 epilogue threads take the same decision
       // after the group barrier, so no thread is ever left alone in a barrier.
       if (etid == 0)
@@ -253,7 +429,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       epi_bar();
       if (!ctl->seg_ok) break;
       tc_fence_after();
-      float v[NTOK];
       {
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * NTOK;
         if (NTOK == 16) {
@@ -276,65 +451,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ++lt;
 
       const int64_t n = static_cast<int64_t>(sg.tile) * BNW + row;
-      if (sg.kbeg == 0 && sg.kend == kblocks) {
+      if (whole) {
         // This CTA computed the whole K range of the tile: write C directly.
-        if (n < p.N) {
-#pragma unroll
-          for (int t = 0; t < NTOK; ++t)
-            if (t < p.M) store_out(p, t, n, v[t]);
-        }
+        if (n < p.N) store_row(p, n, v);
         epi_bar();  // seg_ok is rewritten for the next segment only after everyone read it
         continue;
       }
-      // Partial K range: publish the partial sums (one thread = one W column, its ntok
-      // values contiguous, so the stores and the combine's loads are 16-byte vectors),
-      // then count arrivals for the tile.
-      const int slot = sk_slot<IDX>(c, sg.tile, kblocks, units, ctas);
-      float4* mine = reinterpret_cast<float4*>(p.ws + ((static_cast<int64_t>(c) * 2 + slot) * BNW + row) * NTOK);
+      if (pre) {
+        // The other parts are in s[]; the first CTA's own part comes last.
 #pragma unroll
-      for (int q4 = 0; q4 < NTOK / 4; ++q4)
-        mine[q4] = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
-      // Publish: the barrier orders the 128 threads' stores before thread 0's fence, and the
-      // fence (cumulative) orders them before the arrival count.  On the reading side the
-      // last arriver fences after observing the count, before the group reads.
+        for (int t = 0; t < NTOK; ++t) s[t] += v[t];
+        if (n < p.N) store_row(p, n, s);
+        epi_bar();
+        continue;
+      }
+      // Publish this CTA's part, then take a ticket.  The barrier orders the 128 threads'
+      // stores before thread 0's release fence, and the fence (cumulative) orders them
+      // before the ticket.  The last contributor to take a ticket combines (its own stored
+      // part goes unused); its acquire fence orders the others' parts before its loads, and
+      // it resets the counter at once, as every contributor already holds its ticket.
+      {
+        float4* dst = part_of(c);
+#pragma unroll
+        for (int g = 0; g < NTOK / 4; ++g)
+          if (g < nq) __stcg(dst + g * BNW, make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]));
+      }
       epi_bar();
       if (etid == 0) {
         const uint32_t need = static_cast<uint32_t>(sk_contributors<IDX>(sg.tile, kblocks, units, ctas));
-        __threadfence();
+        fence_acq_rel_gpu();
         const uint32_t prev = atomicAdd(&p.counters[sg.tile], 1u);
-        const bool last = prev + 1u == need;
-        if (last) __threadfence();
-        ctl->is_last = last ? 1u : 0u;
+        const bool is_last = prev + 1u == need;
+        if (is_last) {
+          fence_acq_rel_gpu();
+          st_relaxed(&p.counters[sg.tile], 0u);
+        }
+        ctl->is_last = is_last ? 1u : 0u;
       }
       epi_bar();
       if (ctl->is_last) {
-        const IDX first = sk_cta_of<IDX>(sg.tile * kblocks, units, ctas);
-        const IDX last = sk_cta_of<IDX>((sg.tile + 1) * kblocks - 1, units, ctas);
-        // Sum the contributors' partials in CTA order (= K order): a fixed order.
-        float s[NTOK];
-#pragma unroll
-        for (int t = 0; t < NTOK; ++t) s[t] = 0.f;
-        for (IDX cc = first; cc <= last; ++cc) {
-          const int sl = sk_slot<IDX>(cc, sg.tile, kblocks, units, ctas);
-          const float4* src = reinterpret_cast<const float4*>(
-              p.ws + ((static_cast<int64_t>(cc) * 2 + sl) * BNW + row) * NTOK);
-          float4 part[NTOK / 4];
-#pragma unroll
-          for (int q4 = 0; q4 < NTOK / 4; ++q4) part[q4] = __ldcg(src + q4);
-#pragma unroll
-          for (int q4 = 0; q4 < NTOK / 4; ++q4) {
-            s[4 * q4 + 0] += part[q4].x;
-            s[4 * q4 + 1] += part[q4].y;
-            s[4 * q4 + 2] += part[q4].z;
-            s[4 * q4 + 3] += part[q4].w;
-          }
-        }
-        if (n < p.N) {
-#pragma unroll
-          for (int t = 0; t < NTOK; ++t)
-            if (t < p.M) store_out(p, t, n, s[t]);
-        }
-        if (etid == 0) p.counters[sg.tile] = 0u;  // ready for the next call
+        add_in_order(s, v, last - first + 1);
+        if (n < p.N) store_row(p, n, s);
       }
       epi_bar();
     }

@@ -33,7 +33,7 @@ constexpr size_t kNaScratchBytes = kNaPartialBytes + kNaCounterBytes;
 static_assert(kNaPartialBytes % 256 == 0, "counters must stay 256-byte aligned");
 constexpr int kNaMaxDevices = 64;
 
-// The scratch: partials [ctas][2][128][16] FP32, then one uint32 counter per 128-column tile.
+// The scratch: partials [ctas][2][4][128] float4, then one uint32 counter per 128-column tile.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNaScratchBytes];
 
 std::mutex g_na_mu;

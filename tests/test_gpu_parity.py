@@ -266,17 +266,51 @@ def test_bf16_thin_ragged(torch, M, N, K):
     assert_bf16_close(C, ref[0], den[0], f"thin {M}x{N}x{K}")
 
 
-def test_bf16_decode_deterministic(torch):
+@pytest.mark.parametrize("M", [1, 6, 16])
+def test_bf16_decode_deterministic(torch, M):
+    # FP32 output shows any change in the order the split-K parts are added.  Which CTA
+    # combines a tile depends on arrival timing; the sum order must not.
     W = inputs.ffn_weight()
-    w = inputs.decode_bf16(16, W=W)
+    w = inputs.decode_bf16(M, W=W)
     dA, dB = dev_bf16(w["A"]), dev_bf16(W)
     outs = []
-    for _ in range(3):
-        dC = torch.empty((16, 12288), dtype=torch.bfloat16, device="cuda")
-        dg.gemm_bf16(16, 12288, 4096, 1.0, dA, 4096, dB, 12288, 0.0, dC, 12288)
+    for _ in range(4):
+        dC = torch.empty((M, 12288), dtype=torch.float32, device="cuda")
+        dg.gemm_bf16(M, 12288, 4096, 1.0, dA, 4096, dB, 12288, 0.0, dC, 12288, c_type=dg.DG_OUT_F32)
         sync(torch)
-        outs.append(host_bf16_bits(dC))
-    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
+        outs.append(host_f32(dC).view(np.uint32))
+    for o in outs[1:]:
+        assert np.array_equal(outs[0], o)
+    ref, den = oracle.gemm(M, 12288, 4096, 1.0, w["A"], 4096, W, 12288, 0.0, None, 12288,
+                           absden=True)
+    assert_f32_close(outs[0].view(np.float32), ref[0], den[0], f"decode M={M}, FP32 out")
+
+
+def test_bf16_decode_graph_replay(torch):
+    # A captured call replays its kernel parameters unchanged, split-K workspace included;
+    # every replay must still combine only the parts it wrote.  X changes between replays.
+    M, N, K = 16, 12288, 4096
+    W = inputs.ffn_weight()
+    dB = dev_bf16(W)
+    x0 = inputs.f32_to_bf16_bits(inputs.normal_f32(inputs.BASE_SEED + 900, (M, K)))
+    dX = dev_bf16(x0)
+    dC = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # first call on this stream sets up its workspace
+        dg.gemm_bf16(M, N, K, 1.0, dX, K, dB, N, 0.0, dC, N, c_type=dg.DG_OUT_F32)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        dg.gemm_bf16(M, N, K, 1.0, dX, K, dB, N, 0.0, dC, N, c_type=dg.DG_OUT_F32)
+    for seed in (901, 902, 903):
+        x = inputs.f32_to_bf16_bits(inputs.normal_f32(inputs.BASE_SEED + seed, (M, K)))
+        dX.copy_(dev_bf16(x))
+        g.replay()
+        sync(torch)
+        ref, den = oracle.gemm(M, N, K, 1.0, x, K, W, N, 0.0, None, N, absden=True)
+        assert_f32_close(host_f32(dC), ref[0], den[0], f"graph replay, X seed {seed}")
+    assert dg.dg_device_status() == dg.DG_OK
 
 
 def test_bf16_ffn_full_size_sampled(torch):
