@@ -45,14 +45,14 @@ SM_MAX_MHZ_NOMINAL = 2070.0
 # kernel's sources (kernel file, planner, headers) matches the one it was taken with.
 COMMON_SOURCES = ["api.cu", "dg_internal.h", "ptx.cuh", "tile_sched.h"]
 MEASURED_TRAFFIC = {
-    "sgemm_4096": {"bytes_per_launch": 464_984_832, "source_hash": "1fd602b20102736c"},
-    "sgemm_ragged": {"bytes_per_launch": 25_963_520, "source_hash": "1fd602b20102736c"},
-    "ffn_bf16": {"bytes_per_launch": 118_251_776, "source_hash": "fd094a58433ac027"},
-    "bf16_4096": {"bytes_per_launch": 89_063_680, "source_hash": "fd094a58433ac027"},
-    "qk_batched": {"bytes_per_launch": 1_079_800_320, "source_hash": "fd094a58433ac027"},
-    "decode_m1": {"bytes_per_launch": 103_823_616, "source_hash": "ae40842cb74ac8ea"},
-    "decode_m4": {"bytes_per_launch": 104_187_392, "source_hash": "ae40842cb74ac8ea"},
-    "decode_m16": {"bytes_per_launch": 103_992_832, "source_hash": "ae40842cb74ac8ea"},
+    "sgemm_4096": {"bytes_per_launch": 464_285_952, "source_hash": "4650a5a08dd58dfc"},
+    "sgemm_ragged": {"bytes_per_launch": 25_861_376, "source_hash": "4650a5a08dd58dfc"},
+    "ffn_bf16": {"bytes_per_launch": 118_262_272, "source_hash": "4a7cd78294d06df8"},
+    "bf16_4096": {"bytes_per_launch": 88_565_504, "source_hash": "4a7cd78294d06df8"},
+    "qk_batched": {"bytes_per_launch": 1_078_891_008, "source_hash": "4a7cd78294d06df8"},
+    "decode_m1": {"bytes_per_launch": 103_744_000, "source_hash": "8bd096eb41620b5d"},
+    "decode_m4": {"bytes_per_launch": 103_729_408, "source_hash": "8bd096eb41620b5d"},
+    "decode_m16": {"bytes_per_launch": 103_651_072, "source_hash": "8bd096eb41620b5d"},
 }
 
 

@@ -193,10 +193,21 @@ void plan_bf16(int64_t M, int64_t N, int64_t K, int64_t batch, int sms, dg_plan*
   pl->tiles = batch * cdiv(M, kTcBM) * cdiv(N, bn);
   pl->grid = pl->tiles < sms ? pl->tiles : sms;
   pl->kblocks = cdiv(K, kTcBK);
-  // No K split of a partial last wave here: combining 128 x 256 FP32 partial tiles costs
-  // about as much as the idle SMs it would fill (measured slower on the FFN shape).
+  // A partial last wave runs first, stream-K style (its tiles' K blocks spread over the
+  // CTAs), when the whole waves that follow are long enough to hide the combine: at least
+  // 96 K blocks per CTA (measured: 2 waves of K = 4096 hide it, 1 wave of K = 1024 does
+  // not, where the combine made the call 2.3x slower).  Each tail tile is shared by at
+  // most 4 CTAs.  tail_tiles = the stream-K tiles, splits = the CTAs sharing them.
+  const int64_t G = pl->grid;
   pl->splits = 1;
   pl->tail_tiles = 0;
+  if (pl->tiles > G && pl->tiles % G != 0 && (pl->tiles / G) * pl->kblocks >= 96) {
+    pl->tail_tiles = pl->tiles % G;
+    const int64_t c4 = 4 * pl->tail_tiles;
+    pl->splits = static_cast<int32_t>(c4 < G ? c4 : G);
+    pl->workspace_bytes = tc_ws_floats(pl->splits, bn) * 4 +
+                          pl->tail_tiles * static_cast<int64_t>(sizeof(uint32_t));
+  }
 }
 
 dg_status plan(int32_t dtype, int64_t M, int64_t N, int64_t K, int64_t batch, float alpha,
@@ -368,6 +379,19 @@ dg_status bf16_impl(int64_t M, int64_t N, int64_t K, float alpha, const uint16_t
   p.c_vec = c_vec ? 1 : 0;
   p.c_tma = (c_vec && beta == 0.f) ? 1 : 0;
   p.status = status;
+  p.sk_tiles = pl.tail_tiles;
+  p.dp_tiles = pl.tiles - pl.tail_tiles;
+  p.sk_ctas = pl.tail_tiles > 0 ? pl.splits : 0;
+  p.ws = nullptr;
+  p.counters = nullptr;
+  if (p.sk_tiles > 0) {
+    Workspace w;
+    st = get_workspace(dev, s, static_cast<size_t>(tc_ws_floats(p.sk_ctas, pl.tile_n)),
+                       static_cast<size_t>(p.sk_tiles), &w);
+    if (st != DG_OK) return st;
+    p.ws = w.ws;
+    p.counters = w.counters;
+  }
   return from_cuda(launch_gemm_tc(p, pl.tile_n, A, lda, batch > 1 ? sA : 0, B, ldb,
                                   batch > 1 ? sB : 0, op_b == DG_OP_T,
                                   static_cast<int>(pl.grid), s));

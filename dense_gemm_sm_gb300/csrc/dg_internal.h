@@ -55,7 +55,16 @@ struct TcParams {
   int32_t c_vec;     // 1: 16-byte vector stores/loads of C rows are legal
   int32_t c_tma;     // 1: epilogue writes C with TMA tensor stores (beta == 0, aligned C)
   uint32_t* status;  // device status word
+  // Stream-K phase: the last sk_tiles tiles of the raster order run first, their K blocks
+  // spread evenly over CTAs 0 .. sk_ctas-1 (sk_tiles = 0: none); then tiles 0 .. dp_tiles-1
+  // run one per CTA per wave.  Partial tiles go to ws, [sk_ctas][2][BN / 4][128] float4,
+  // and the last contributor of a tile adds them; counters[sk_tiles] are zero between calls.
+  int64_t dp_tiles, sk_tiles;
+  int32_t sk_ctas;
+  float* ws;
+  uint32_t* counters;
 };
+inline int64_t tc_ws_floats(int64_t sk_ctas, int bn) { return sk_ctas * 2 * 128 * bn; }
 // A: [batch][M][lda] bf16 (K contiguous).  B: op N -> [batch][K][ldb] (N contiguous),
 // op T -> [batch][N][ldb] (K contiguous).
 cudaError_t launch_gemm_tc(const TcParams& p, int bn, const void* A, int64_t lda, int64_t strideA,

@@ -17,6 +17,12 @@
 //   * Epilogue warps read the accumulator with tcgen05.ld, apply C = alpha*acc + beta*C_old
 //     in FP32 and round once to the output type (BF16 nearest-even or FP32), after the
 //     whole K reduction ("Operator & Runtime" sections 5.4.2-5.4.3).
+//   * When the tiles do not fill the last wave, the tail tiles are computed first, stream-K
+//     style: their (tile, K block) units are spread evenly over the CTAs, each CTA stores
+//     its partial tile, and the last contributor of a tile (atomic ticket, release/acquire
+//     fences) adds the partials in CTA (= K) order -- a fixed order, so results repeat run
+//     to run ("Operator & Runtime" section 5.2.4).  Done first, these combines overlap the
+//     whole-wave tiles that follow instead of extending the kernel.
 //   * Every mbarrier wait is bounded; a CTA that gives up records an error in the status
 //     word, waits (bounded) for its in-flight copies and MMAs, frees TMEM and exits.
 // Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM owner + MMA issuer,
@@ -64,7 +70,58 @@ struct SmemCtl {
   uint64_t drain;
   uint32_t tmem_base;
   uint32_t abort;
+  uint32_t is_last;
 };
+
+// One item of a CTA's work: K blocks [kbeg, kend) of output tile `tile` (raster order).
+struct TcItem {
+  int64_t tile;
+  int32_t kbeg, kend;
+  bool sk;  // a stream-K piece of a tail tile
+};
+
+// The work of CTA c, in order: its stream-K pieces of the tail tiles, then its whole-wave
+// tiles c, c + G, c + 2G, ... below dp_tiles.
+struct TcWalk {
+  int64_t u, u1, t, step;
+  __device__ TcWalk(const TcParams& p, int64_t c, int64_t G) : t(c), step(G) {
+    const int64_t units = p.sk_tiles * p.kblocks;
+    if (c < p.sk_ctas) {
+      u = sk_start<int64_t>(c, units, p.sk_ctas);
+      u1 = sk_start<int64_t>(c + 1, units, p.sk_ctas);
+    } else {
+      u = u1 = 0;
+    }
+  }
+  __device__ bool next(const TcParams& p, TcItem* it) {
+    if (u < u1) {
+      const int64_t kb = p.kblocks;
+      const int64_t st = u / kb;
+      const int64_t lim = u1 - st * kb;
+      it->tile = p.dp_tiles + st;
+      it->kbeg = static_cast<int32_t>(u - st * kb);
+      it->kend = static_cast<int32_t>(lim < kb ? lim : kb);
+      it->sk = true;
+      u = st * kb + it->kend;
+      return true;
+    }
+    if (t < p.dp_tiles) {
+      it->tile = t;
+      it->kbeg = 0;
+      it->kend = p.kblocks;
+      it->sk = false;
+      t += step;
+      return true;
+    }
+    return false;
+  }
+};
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
 
 __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint32_t* status) {
   uint32_t never = 0;
@@ -169,6 +226,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     mbar_init(smem_u32(&ctl->drain), 1);
     ctl->abort = 0;
+    ctl->is_last = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -188,7 +246,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   pdl_trigger();
   pdl_wait();
 
-  const int64_t total = p.total_tiles;
   const int kblocks = p.kblocks;
 
   if (warp == 0) {
@@ -196,13 +253,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      TcWalk walk(p, blockIdx.x, gridDim.x);
+      TcItem item;
+      while (ok && walk.next(p, &item)) {
         int64_t b, tm, tn;
-        raster_tile(t, p.tiles_m, p.tiles_n, p.group, &b, &tm, &tn);
+        raster_tile(item.tile, p.tiles_m, p.tiles_n, p.group, &b, &tm, &tn);
         const int32_t ym = static_cast<int32_t>(tm * BM);
         const int32_t xn = static_cast<int32_t>(tn * BN);
         const int32_t zb = static_cast<int32_t>(b);
-        for (int kb = 0; kb < kblocks; ++kb) {
+        for (int kb = item.kbeg; kb < item.kend; ++kb) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
           if (!mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort, p.status, kDevTimeoutProducer)) {
             ok = false;
@@ -240,7 +299,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, false, !B_KMAJOR);
       uint32_t it = 0, lt = 0;
       bool ok = true;
-      for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x, ++lt) {
+      TcWalk walk(p, blockIdx.x, gridDim.x);
+      TcItem item;
+      for (; ok && walk.next(p, &item); ++lt) {
         const uint32_t acc = lt & 1u, aph = (lt >> 1) & 1u;
         if (!mbar_wait(smem_u32(&ctl->tempty[acc]), aph ^ 1u, abort, p.status, kDevTimeoutMma)) {
           ok = false;
@@ -248,7 +309,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_after();
         const uint32_t d = tmem_base + acc * BN;
-        for (int kb = 0; kb < kblocks; ++kb) {
+        for (int kb = item.kbeg; kb < item.kend; ++kb) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
           if (!mbar_wait(smem_u32(&ctl->full[s]), ph, abort, p.status, kDevTimeoutMma)) {
             ok = false;
@@ -264,7 +325,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // groups 1 KiB apart (SBO), K step of 16 rows = 2 KiB.
             const uint64_t bdesc = B_KMAJOR ? sdesc_sw128(b0 + k * 32, 16, 1024)
                                             : sdesc_sw128(b0 + k * 2048, 8192, 1024);
-            umma_bf16(d, adesc, bdesc, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+            umma_bf16(d, adesc, bdesc, idesc, (kb > item.kbeg || k > 0) ? 1u : 0u);
           }
           if (fault != 1) umma_commit(smem_u32(&ctl->empty[s]));
           ++it;
@@ -285,13 +346,109 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t stg = out_stage + static_cast<uint32_t>(warp - 2) * 8192u;
     uint32_t sbuf = 0;
     uint32_t lt = 0;
-    for (int64_t t = blockIdx.x; t < total; t += gridDim.x, ++lt) {
+    const int etid = threadIdx.x - 64;
+    TcWalk walk(p, blockIdx.x, gridDim.x);
+    TcItem item;
+    for (; walk.next(p, &item); ++lt) {
       int64_t b, tm, tn;
-      raster_tile(t, p.tiles_m, p.tiles_n, p.group, &b, &tm, &tn);
+      raster_tile(item.tile, p.tiles_m, p.tiles_n, p.group, &b, &tm, &tn);
       const uint32_t acc = lt & 1u, aph = (lt >> 1) & 1u;
       if (!mbar_wait(smem_u32(&ctl->tfull[acc]), aph, abort, p.status, kDevTimeoutEpilogue)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      if (item.sk && !(item.kbeg == 0 && item.kend == kblocks)) {
+        // Stream-K piece of a tail tile: publish the partial tile, then take a ticket; the
+        // last contributor adds the partials in CTA order and writes C.
+        const int64_t kb = kblocks;
+        const int64_t units = p.sk_tiles * kb, ctas = p.sk_ctas;
+        const int64_t st = item.tile - p.dp_tiles;
+        const int64_t c = blockIdx.x;
+        float4* const ws4 = reinterpret_cast<float4*>(p.ws);
+        // Partial of CTA cc: [BN / 4 column groups][128 rows] float4, so a warp's stores and
+        // loads of one group cover 512 contiguous bytes.
+        auto part_of = [&](int64_t cc) {
+          const int sl = sk_slot<int64_t>(cc, st, kb, units, ctas);
+          return ws4 + (cc * 2 + sl) * (BN / 4) * BM + row;
+        };
+        {
+          float4* dst = part_of(c);
+#pragma unroll 1
+          for (int ch = 0; ch < BN / 32; ++ch) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + ch * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int g = 0; g < 8; ++g)
+              __stcg(dst + (ch * 8 + g) * BM,
+                     make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                                 __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3])));
+          }
+        }
+        // The accumulator is in the workspace now: hand TMEM back to the MMA issuer.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
+        // The barrier orders the 128 threads' stores before thread 0's release fence, and the
+        // fence (cumulative) orders them before the ticket; the last contributor's acquire
+        // fence orders the others' partials before its loads.
+        epi_bar();
+        if (etid == 0) {
+          const uint32_t need = static_cast<uint32_t>(sk_contributors<int64_t>(st, kb, units, ctas));
+          fence_acq_rel_gpu();
+          const uint32_t prev = atomicAdd(&p.counters[st], 1u);
+          const bool is_last = prev + 1u == need;
+          if (is_last) {
+            fence_acq_rel_gpu();
+            p.counters[st] = 0u;  // every contributor holds its ticket: ready for the next call
+          }
+          ctl->is_last = is_last ? 1u : 0u;
+        }
+        epi_bar();
+        if (ctl->is_last) {
+          const int64_t first = sk_cta_of<int64_t>(st * kb, units, ctas);
+          const int64_t lastc = sk_cta_of<int64_t>((st + 1) * kb - 1, units, ctas);
+          const int64_t gm = tm * BM + row;
+          uint8_t* cbase = static_cast<uint8_t*>(p.C) +
+                           (b * p.strideC + gm * p.ldc) * (p.c_f32 ? 4 : 2);
+#pragma unroll 1
+          for (int ch = 0; ch < BN / 32; ++ch) {
+            float sum[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) sum[j] = 0.f;
+            // Contributors in CTA order, two per round trip.
+            for (int64_t cc = first; cc <= lastc; cc += 2) {
+              const bool two = cc + 1 <= lastc;
+              const float4* pa = part_of(cc) + ch * 8 * BM;
+              const float4* pb = two ? part_of(cc + 1) + ch * 8 * BM : pa;
+              float4 va[8], vb[8];
+#pragma unroll
+              for (int g = 0; g < 8; ++g) va[g] = __ldcg(pa + g * BM);
+              if (two) {
+#pragma unroll
+                for (int g = 0; g < 8; ++g) vb[g] = __ldcg(pb + g * BM);
+              }
+#pragma unroll
+              for (int g = 0; g < 8; ++g) {
+                sum[4 * g] += va[g].x; sum[4 * g + 1] += va[g].y;
+                sum[4 * g + 2] += va[g].z; sum[4 * g + 3] += va[g].w;
+              }
+              if (two) {
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                  sum[4 * g] += vb[g].x; sum[4 * g + 1] += vb[g].y;
+                  sum[4 * g + 2] += vb[g].z; sum[4 * g + 3] += vb[g].w;
+                }
+              }
+            }
+            uint32_t r[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(sum[j]);
+            if (gm < p.M) store_row_chunk(p, cbase, tn * BN + ch * 32, r);
+          }
+        }
+        epi_bar();  // is_last is rewritten only after everyone read it
+        continue;
+      }
       if (p.c_tma) {
         // C = alpha * acc, in pieces of 32 rows x 32 columns: registers -> swizzled shared
         // staging -> one TMA tensor store (rows / columns beyond M / N are clipped).  An FP32

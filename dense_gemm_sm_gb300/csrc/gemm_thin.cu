@@ -45,7 +45,7 @@ constexpr int STAGES = DG_THIN_STAGES;
 // W blocks of its range a CTA asks L2 for before the previous grid of the stream has
 // finished (0: none).
 #ifndef DG_THIN_PREFETCH
-#define DG_THIN_PREFETCH 12
+#define DG_THIN_PREFETCH 32
 #endif
 constexpr int PREFETCH = DG_THIN_PREFETCH;
 

@@ -168,12 +168,14 @@ typedef struct {
   int32_t group;           /* raster group height, in tile rows */
   int32_t ntok;            /* thin path: MMA N (tokens padded to 16 or 32) */
   int32_t vec;             /* SIMT path: 16-byte copy variant */
-  int32_t splits;          /* K chunks of each tail tile (1: no split) */
+  int32_t splits;          /* SIMT: K chunks of each tail tile (1: no split);
+                              tile kernel: CTAs sharing the stream-K tail's K blocks */
   int64_t tiles;           /* output tiles over all batches */
-  int64_t tail_tiles;      /* tiles of the last partial wave that are split along K */
+  int64_t tail_tiles;      /* tiles of the last partial wave split along K (SIMT) or
+                              computed stream-K before the whole waves (tile kernel) */
   int64_t grid;            /* CTAs launched */
   int64_t kblocks;         /* K blocks per tile */
-  int64_t workspace_bytes; /* library workspace needed (thin path) */
+  int64_t workspace_bytes; /* library workspace needed (split-K partials and counters) */
 } dg_plan;
 
 /*

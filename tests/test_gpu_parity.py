@@ -192,6 +192,45 @@ def test_bf16_ffn_reduced_full_compare(torch):
     assert_bf16_close(C, ref[0], den[0], "ffn-shaped 512x2048x1024")
 
 
+# Shapes whose tiles overfill the last of the 152-CTA waves: the tail tiles run stream-K
+# first (8 tail tiles shared by 32 CTAs, K split 4 ways) before the whole-wave tiles.
+@pytest.mark.parametrize("M,N,K,ldc,beta,out_f32", [
+    (1280, 4096, 6144, 4096, 0.0, False),     # whole-wave tiles stored with TMA
+    (1280, 4096, 6144, 4096, 0.0, True),
+    (1200, 4000, 6104, 4003, -0.75, False),   # ragged tiles and K block, beta, direct stores
+    (1200, 4000, 6104, 4003, -0.75, True)])
+def test_bf16_stream_k_tail(torch, M, N, K, ldc, beta, out_f32):
+    plan = dg.dg_plan_gemm(1, M, N, K, c_type=dg.DG_OUT_F32 if out_f32 else dg.DG_OUT_BF16,
+                           num_sms=152)
+    assert plan["kernel"] == dg.DG_KERNEL_TC_BF16 and plan["tail_tiles"] > 0
+    A = inputs.f32_to_bf16_bits(inputs.normal_f32(M + 7, (M, K)))
+    B = inputs.f32_to_bf16_bits(inputs.normal_f32(N + 8, (K, N), 0.1))
+    c0 = inputs.normal_f32(M + N + 1, (M, N))
+    C0 = None
+    if beta != 0.0:
+        C0 = inputs.pad_rows(c0 if out_f32 else inputs.f32_to_bf16_bits(c0), ldc, 0)
+    alpha = np.float32(0.5)
+    C = run_bf16(torch, M, N, K, alpha, A, K, B, N, np.float32(beta), C0, ldc, out_f32)
+    ref, den = oracle.gemm(M, N, K, alpha, A, K, B, N, np.float32(beta), C0, ldc, absden=True)
+    if out_f32:
+        assert_f32_close(C, ref[0], den[0], f"stream-K tail {M}x{N}x{K}")
+    else:
+        assert_bf16_close(C, ref[0], den[0], f"stream-K tail {M}x{N}x{K}")
+
+
+def test_bf16_stream_k_tail_deterministic(torch):
+    M, N, K = 1280, 4096, 6144
+    A = dev_bf16(inputs.f32_to_bf16_bits(inputs.normal_f32(M + 7, (M, K))))
+    B = dev_bf16(inputs.f32_to_bf16_bits(inputs.normal_f32(N + 8, (K, N), 0.1)))
+    outs = []
+    for _ in range(3):
+        dC = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        dg.gemm_bf16(M, N, K, 1.0, A, K, B, N, 0.0, dC, N, c_type=dg.DG_OUT_F32)
+        sync(torch)
+        outs.append(host_f32(dC).view(np.uint32))
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
+
+
 @pytest.mark.parametrize("M,N,K", [(129, 264, 72), (300, 1000, 200), (200, 136, 8), (33, 8, 16),
                                    (128, 256, 64), (255, 520, 4104)])
 @pytest.mark.parametrize("out_f32", [False, True])
