@@ -45,14 +45,14 @@ SM_MAX_MHZ_NOMINAL = 2070.0
 # kernel's sources (kernel file, planner, headers) matches the one it was taken with.
 COMMON_SOURCES = ["api.cu", "dg_internal.h", "ptx.cuh", "tile_sched.h"]
 MEASURED_TRAFFIC = {
-    "sgemm_4096": {"bytes_per_launch": 464_285_952, "source_hash": "4650a5a08dd58dfc"},
-    "sgemm_ragged": {"bytes_per_launch": 25_861_376, "source_hash": "4650a5a08dd58dfc"},
-    "ffn_bf16": {"bytes_per_launch": 118_262_272, "source_hash": "4a7cd78294d06df8"},
-    "bf16_4096": {"bytes_per_launch": 88_565_504, "source_hash": "4a7cd78294d06df8"},
-    "qk_batched": {"bytes_per_launch": 1_078_891_008, "source_hash": "4a7cd78294d06df8"},
-    "decode_m1": {"bytes_per_launch": 103_744_000, "source_hash": "8bd096eb41620b5d"},
-    "decode_m4": {"bytes_per_launch": 103_729_408, "source_hash": "8bd096eb41620b5d"},
-    "decode_m16": {"bytes_per_launch": 103_651_072, "source_hash": "8bd096eb41620b5d"},
+    "sgemm_4096": {"bytes_per_launch": 449_025_280, "source_hash": "88002eb439e09a3e"},
+    "sgemm_ragged": {"bytes_per_launch": 25_864_448, "source_hash": "88002eb439e09a3e"},
+    "ffn_bf16": {"bytes_per_launch": 150_063_104, "source_hash": "5aa351fbf6f52108"},
+    "bf16_4096": {"bytes_per_launch": 136_358_400, "source_hash": "5aa351fbf6f52108"},
+    "qk_batched": {"bytes_per_launch": 1_079_062_272, "source_hash": "5aa351fbf6f52108"},
+    "decode_m1": {"bytes_per_launch": 105_169_152, "source_hash": "ecf5a400ad617af8"},
+    "decode_m4": {"bytes_per_launch": 104_963_584, "source_hash": "ecf5a400ad617af8"},
+    "decode_m16": {"bytes_per_launch": 105_434_368, "source_hash": "ecf5a400ad617af8"},
 }
 
 

@@ -194,14 +194,17 @@ void plan_bf16(int64_t M, int64_t N, int64_t K, int64_t batch, int sms, dg_plan*
   pl->grid = pl->tiles < sms ? pl->tiles : sms;
   pl->kblocks = cdiv(K, kTcBK);
   // A partial last wave runs first, stream-K style (its tiles' K blocks spread over the
-  // CTAs), when the whole waves that follow are long enough to hide the combine: at least
-  // 96 K blocks per CTA (measured: 2 waves of K = 4096 hide it, 1 wave of K = 1024 does
-  // not, where the combine made the call 2.3x slower).  Each tail tile is shared by at
+  // CTAs), when the whole waves that follow are long enough to hide the combine -- at
+  // least 96 K blocks per CTA (measured: 2 waves of K = 4096 hide it, 1 wave of K = 1024
+  // does not, where the combine made the call 2.3x slower) -- and a tile has at least 16
+  // K blocks, so a piece is worth its partial tile (with 2, as in attention scores with
+  // d = 128, the partials cost a quarter of the call).  Each tail tile is shared by at
   // most 4 CTAs.  tail_tiles = the stream-K tiles, splits = the CTAs sharing them.
   const int64_t G = pl->grid;
   pl->splits = 1;
   pl->tail_tiles = 0;
-  if (pl->tiles > G && pl->tiles % G != 0 && (pl->tiles / G) * pl->kblocks >= 96) {
+  if (pl->tiles > G && pl->tiles % G != 0 && pl->kblocks >= 16 &&
+      (pl->tiles / G) * pl->kblocks >= 96) {
     pl->tail_tiles = pl->tiles % G;
     const int64_t c4 = 4 * pl->tail_tiles;
     pl->splits = static_cast<int32_t>(c4 < G ? c4 : G);

@@ -45,6 +45,16 @@ def test_plan_dispatch_table():
                          num_sms=152)
     assert qk["kernel"] == dg.DG_KERNEL_TC_BF16 and qk["tiles"] == 64 * 16 * 8
     assert dg.dg_plan_gemm(0, 4096, 4096, 4096, num_sms=152)["kernel"] == dg.DG_KERNEL_SIMT_F32
+    # Stream-K tail of the tile kernel: on for FFN (2 whole waves of K = 4096 + 80 tail
+    # tiles, spread over all 152 CTAs); off where the whole waves are too short to hide the
+    # combine (one wave of K = 1024) or a tile has too few K blocks (QK^T, K = 128).
+    assert ffn["tail_tiles"] == 80 and ffn["splits"] == 152
+    assert ffn["workspace_bytes"] == 152 * 2 * 128 * 256 * 4 + 80 * 4
+    sk = dg.dg_plan_gemm(1, 1280, 4096, 6144, num_sms=152)
+    assert sk["tail_tiles"] == 8 and sk["splits"] == 32            # 4 CTAs per tail tile
+    assert dg.dg_plan_gemm(1, 1280, 4096, 1024, num_sms=152)["tail_tiles"] == 0
+    assert qk["tail_tiles"] == 0
+    assert dg.dg_plan_gemm(1, 2048, 2048, 4096, num_sms=152)["tail_tiles"] == 0  # one partial wave
     assert dg.dg_plan_gemm(0, 10, 10, 0, num_sms=152)["kernel"] == dg.DG_KERNEL_SCALE
     assert dg.dg_plan_gemm(1, 0, 10, 10, num_sms=152)["kernel"] == dg.DG_KERNEL_NONE
 
