@@ -196,7 +196,10 @@ __device__ __forceinline__ void store_row_chunk(const TcParams& p, void* crow_v,
   }
 }
 
-template <int BN, bool B_KMAJOR, bool RANK3>
+// B3D: N-major B is read through a 3-D view (64 columns, K rows, 64-column chunks), so one
+// TMA copy brings a stage's whole B tile instead of one per 64-column box (the copies per
+// stage, not the bytes, were the producer's limit).  Only when N is a multiple of 64.
+template <int BN, bool B_KMAJOR, bool RANK3, bool B3D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const TcParams p, const int fault) {
@@ -276,6 +279,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (B_KMAJOR) {
             if (RANK3) tma_load_3d(bdst, &tmB, fb, kx, xn, zb);
             else tma_load_2d(bdst, &tmB, fb, kx, xn);
+          } else if (B3D) {
+            tma_load_3d(bdst, &tmB, fb, 0, kx, xn / 64);
           } else {
 #pragma unroll
             for (int j = 0; j < Cfg::NBOX; ++j) {
@@ -571,13 +576,13 @@ std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_map_cache;
 bool make_tile_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t esz, const void* base,
                    uint64_t inner, uint64_t outer, uint64_t ld, uint64_t batch, uint64_t stride,
                    uint32_t box_inner, uint32_t box_outer,
-                   CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+                   CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B, uint32_t box_batch = 1) {
   MapKey key;
   std::memset(&key, 0, sizeof key);
   key.base = base; key.inner = inner; key.outer = outer; key.ld = ld;
   key.batch = batch > 1 ? batch : 1; key.stride = batch > 1 ? stride : 0;
   key.box_inner = box_inner | (static_cast<uint32_t>(dtype) << 16);
-  key.box_outer = box_outer | (static_cast<uint32_t>(swizzle) << 16);
+  key.box_outer = box_outer | (static_cast<uint32_t>(swizzle) << 16) | (box_batch << 20);
   {
     std::lock_guard<std::mutex> lock(g_map_mu);
     auto it = g_map_cache.find(key);
@@ -591,7 +596,7 @@ bool make_tile_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t esz, co
   const bool rank3 = batch > 1;
   cuuint64_t dims[3] = {inner, outer, batch};
   cuuint64_t strides[2] = {ld * esz, stride * esz};
-  cuuint32_t box[3] = {box_inner, box_outer, 1};
+  cuuint32_t box[3] = {box_inner, box_outer, box_batch};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, dtype, rank3 ? 3 : 2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -620,10 +625,10 @@ EncodeTiledFn get_encode_tiled() {
 }
 
 namespace {
-template <int BN, bool B_KMAJOR, bool RANK3>
+template <int BN, bool B_KMAJOR, bool RANK3, bool B3D = false>
 cudaError_t launch_tc_variant(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
                               const TcParams& p, int num_ctas, cudaStream_t s) {
-  auto kern = gemm_tc_kernel<BN, B_KMAJOR, RANK3>;
+  auto kern = gemm_tc_kernel<BN, B_KMAJOR, RANK3, B3D>;
   constexpr uint32_t smem = TcCfg<BN, B_KMAJOR>::SMEM_BYTES;
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = ensure_smem_attr(kern, smem, attr_done);
@@ -639,8 +644,18 @@ cudaError_t launch_gemm_tc(const TcParams& p, int bn, const void* A, int64_t lda
   CUtensorMap ma, mb;
   const uint64_t batch = static_cast<uint64_t>(p.batch);
   if (!make_bf16_map(&ma, A, p.K, p.M, lda, batch, strideA, BK, BM)) return cudaErrorInvalidValue;
-  const bool ok_b = b_kmajor ? make_bf16_map(&mb, B, p.K, p.N, ldb, batch, strideB, BK, bn)
-                             : make_bf16_map(&mb, B, p.N, p.K, ldb, batch, strideB, 64, BK);
+  // N-major B as one 3-D box per stage when the 64-column chunks tile N exactly (so no box
+  // reaches past a row) and the tile width is whole chunks.
+  const bool b3d = !b_kmajor && batch <= 1 && p.N % 64 == 0 && bn % 64 == 0 && p.N >= bn;
+  bool ok_b;
+  if (b_kmajor)
+    ok_b = make_bf16_map(&mb, B, p.K, p.N, ldb, batch, strideB, BK, bn);
+  else if (b3d)
+    ok_b = make_tile_map(&mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, 64, p.K, ldb,
+                         static_cast<uint64_t>(p.N / 64), 64, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B,
+                         static_cast<uint32_t>(bn / 64));
+  else
+    ok_b = make_bf16_map(&mb, B, p.N, p.K, ldb, batch, strideB, 64, BK);
   if (!ok_b) return cudaErrorInvalidValue;
   CUtensorMap mc;
   std::memset(&mc, 0, sizeof mc);
@@ -656,6 +671,11 @@ cudaError_t launch_gemm_tc(const TcParams& p, int bn, const void* A, int64_t lda
     if (!ok_c) q.c_tma = 0;  // fall back to direct stores from registers
   }
   const bool rank3 = batch > 1;
+  if (b3d) {
+    if (bn == 256) return launch_tc_variant<256, false, false, true>(ma, mb, mc, q, num_ctas, s);
+    if (bn == 192) return launch_tc_variant<192, false, false, true>(ma, mb, mc, q, num_ctas, s);
+    if (bn == 128) return launch_tc_variant<128, false, false, true>(ma, mb, mc, q, num_ctas, s);
+  }
 #define DG_TC_CASE(BNV, KM, R3)                                                     \
   if (bn == BNV && b_kmajor == KM && rank3 == R3)                                   \
     return launch_tc_variant<BNV, KM, R3>(ma, mb, mc, q, num_ctas, s);
