@@ -17,7 +17,8 @@ DG_OK, DG_ERR_INVALID_ARG, DG_ERR_MISALIGNED, DG_ERR_UNSUPPORTED = 0, 1, 2, 3
 DG_ERR_CUDA, DG_ERR_TIMEOUT, DG_ERR_NO_MEMORY = 4, 5, 6
 DG_OP_N, DG_OP_T = 0, 1
 DG_OUT_BF16, DG_OUT_F32 = 0, 1
-DG_KERNEL_NONE, DG_KERNEL_SCALE, DG_KERNEL_SIMT_F32, DG_KERNEL_TC_BF16, DG_KERNEL_THIN_BF16 = range(5)
+(DG_KERNEL_NONE, DG_KERNEL_SCALE, DG_KERNEL_SIMT_F32, DG_KERNEL_TC_BF16, DG_KERNEL_THIN_BF16,
+ DG_KERNEL_TC2_BF16) = range(6)
 
 EXPORTED = [
     "gemm_f32", "gemm_f32_strided_batched", "gemm_bf16", "gemm_bf16_strided_batched",

@@ -193,6 +193,22 @@ void plan_bf16(int64_t M, int64_t N, int64_t K, int64_t batch, int sms, dg_plan*
   pl->tiles = batch * cdiv(M, kTcBM) * cdiv(N, bn);
   pl->grid = pl->tiles < sms ? pl->tiles : sms;
   pl->kblocks = cdiv(K, kTcBK);
+  // CTA pairs (tcgen05 cta_group::2, 256 x 256 tiles) for one problem with at least two
+  // 128-row tile rows: each SM then moves half the B bytes per FLOP through its shared
+  // memory, which bounds the single-CTA tile.  DG_TC_PAIR=0 keeps single CTAs (sweeps).
+  const char* pe = std::getenv("DG_TC_PAIR");
+  const bool pair = batch == 1 && bn == 256 && cdiv(M, kTcBM) >= 2 && sms >= 2 &&
+                    !(pe && pe[0] == '0');
+  if (pair) {
+    pl->kernel = DG_KERNEL_TC2_BF16;
+    pl->tile_m = 2 * kTcBM;
+    pl->stages = 6;
+    pl->group = kRasterGroup / 2;  // in 256-row tile rows: the same 8 rows of 128
+    pl->tiles = cdiv(cdiv(M, kTcBM), 2) * cdiv(N, bn);
+    const int64_t clusters = pl->tiles < sms / 2 ? pl->tiles : sms / 2;
+    pl->grid = 2 * clusters;
+  }
+  const int64_t G = pair ? pl->grid / 2 : pl->grid;  // CTAs, or CTA pairs, that share the work
   // A partial last wave runs first, stream-K style (its tiles' K blocks spread over the
   // CTAs), when the whole waves that follow are long enough to hide the combine -- at
   // least 96 K blocks per CTA (measured: 2 waves of K = 4096 hide it, 1 wave of K = 1024
@@ -200,7 +216,6 @@ void plan_bf16(int64_t M, int64_t N, int64_t K, int64_t batch, int sms, dg_plan*
   // K blocks, so a piece is worth its partial tile (with 2, as in attention scores with
   // d = 128, the partials cost a quarter of the call).  Each tail tile is shared by at
   // most 4 CTAs.  tail_tiles = the stream-K tiles, splits = the CTAs sharing them.
-  const int64_t G = pl->grid;
   pl->splits = 1;
   pl->tail_tiles = 0;
   if (pl->tiles > G && pl->tiles % G != 0 && pl->kblocks >= 16 &&
@@ -208,8 +223,9 @@ void plan_bf16(int64_t M, int64_t N, int64_t K, int64_t batch, int sms, dg_plan*
     pl->tail_tiles = pl->tiles % G;
     const int64_t c4 = 4 * pl->tail_tiles;
     pl->splits = static_cast<int32_t>(c4 < G ? c4 : G);
-    pl->workspace_bytes = tc_ws_floats(pl->splits, bn) * 4 +
-                          pl->tail_tiles * static_cast<int64_t>(sizeof(uint32_t));
+    const int64_t per = pair ? 2 : 1;  // partials and counters per stream-K unit
+    pl->workspace_bytes = tc_ws_floats(per * pl->splits, bn) * 4 +
+                          per * pl->tail_tiles * static_cast<int64_t>(sizeof(uint32_t));
   }
 }
 
@@ -371,7 +387,8 @@ dg_status bf16_impl(int64_t M, int64_t N, int64_t K, float alpha, const uint16_t
   TcParams p;
   p.M = M; p.N = N; p.K = K;
   p.batch = batch;
-  p.tiles_m = cdiv(M, kTcBM);
+  const bool pair = pl.kernel == DG_KERNEL_TC2_BF16;
+  p.tiles_m = pair ? cdiv(cdiv(M, kTcBM), 2) : cdiv(M, kTcBM);
   p.tiles_n = cdiv(N, pl.tile_n);
   p.total_tiles = pl.tiles;
   p.kblocks = static_cast<int32_t>(pl.kblocks);
@@ -389,14 +406,15 @@ dg_status bf16_impl(int64_t M, int64_t N, int64_t K, float alpha, const uint16_t
   p.counters = nullptr;
   if (p.sk_tiles > 0) {
     Workspace w;
-    st = get_workspace(dev, s, static_cast<size_t>(tc_ws_floats(p.sk_ctas, pl.tile_n)),
-                       static_cast<size_t>(p.sk_tiles), &w);
+    const int64_t per = pair ? 2 : 1;
+    st = get_workspace(dev, s, static_cast<size_t>(tc_ws_floats(per * p.sk_ctas, pl.tile_n)),
+                       static_cast<size_t>(per * p.sk_tiles), &w);
     if (st != DG_OK) return st;
     p.ws = w.ws;
     p.counters = w.counters;
   }
   return from_cuda(launch_gemm_tc(p, pl.tile_n, A, lda, batch > 1 ? sA : 0, B, ldb,
-                                  batch > 1 ? sB : 0, op_b == DG_OP_T,
+                                  batch > 1 ? sB : 0, op_b == DG_OP_T, pair,
                                   static_cast<int>(pl.grid), s));
 }
 

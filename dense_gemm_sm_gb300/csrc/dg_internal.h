@@ -67,9 +67,11 @@ struct TcParams {
 inline int64_t tc_ws_floats(int64_t sk_ctas, int bn) { return sk_ctas * 2 * 128 * bn; }
 // A: [batch][M][lda] bf16 (K contiguous).  B: op N -> [batch][K][ldb] (N contiguous),
 // op T -> [batch][N][ldb] (K contiguous).
+// pair: launch clusters of two CTAs that each compute half of a 256 x bn tile (bn = 256,
+// batch 1, num_ctas even; p.tiles_m then counts 256-row tile rows).
 cudaError_t launch_gemm_tc(const TcParams& p, int bn, const void* A, int64_t lda, int64_t strideA,
                            const void* B, int64_t ldb, int64_t strideB, bool b_kmajor,
-                           int num_ctas, cudaStream_t s);
+                           bool pair, int num_ctas, cudaStream_t s);
 constexpr int kTcBM = 128, kTcBK = 64;
 
 // ------------------------------------------------------------------ BF16 thin (decode) path

@@ -44,13 +44,16 @@ constexpr int BM = kTcBM, BK = kTcBK;
 constexpr uint32_t A_BYTES = BM * BK * 2;  // 16 KiB per stage
 constexpr int NUM_THREADS = 192;
 
-template <int BN, bool B_KMAJOR>
+// PAIR: a CTA pair (cluster of 2) computes a 256 x BN tile with tcgen05.mma.cta_group::2;
+// each CTA holds its 128 rows of A and BN / 2 columns of B, so a stage is half as large.
+template <int BN, bool B_KMAJOR, bool PAIR = false>
 struct TcCfg {
-  // N-major B arrives as 64-column boxes (8 KiB each), K-major B as one BN-row box.
-  static constexpr int NBOX = (BN + 63) / 64;
+  static constexpr int BNC = PAIR ? BN / 2 : BN;  // B columns held by this CTA
+  // N-major B arrives as 64-column boxes (8 KiB each), K-major B as one BNC-row box.
+  static constexpr int NBOX = (BNC + 63) / 64;
   static constexpr uint32_t B_BYTES = NBOX * 8192;  // stage footprint
-  static constexpr uint32_t B_LOAD_BYTES = B_KMAJOR ? BN * BK * 2 : NBOX * 8192;  // expect_tx
-  static constexpr int STAGES = BN >= 192 ? 4 : 6;
+  static constexpr uint32_t B_LOAD_BYTES = B_KMAJOR ? BNC * BK * 2 : NBOX * 8192;  // expect_tx
+  static constexpr int STAGES = PAIR ? 6 : (BN >= 192 ? 4 : 6);
   // Two accumulators of BN columns; the allocation is a power of two.
   static constexpr uint32_t TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
   static constexpr uint32_t RING_BYTES = STAGES * (A_BYTES + B_BYTES);
@@ -62,6 +65,7 @@ struct TcCfg {
   static_assert(BN % 32 == 0 && BN <= 256 && 2 * BN <= 512, "tile width");
 };
 
+struct SmemCtl;
 struct SmemCtl {
   uint64_t full[8];
   uint64_t empty[8];
@@ -72,6 +76,7 @@ struct SmemCtl {
   uint32_t abort;
   uint32_t is_last;
 };
+static_assert(sizeof(SmemCtl) <= 256, "barrier block");
 
 // One item of a CTA's work: K blocks [kbeg, kend) of output tile `tile` (raster order).
 struct TcItem {
@@ -121,6 +126,117 @@ __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: 
 
 __device__ __forceinline__ void fence_acq_rel_gpu() {
   asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- CTA-pair (cluster of 2)
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                   "memory");
+}
+
+// Arrives (release, cluster scope) on the barrier at the same shared-memory offset in CTA
+// `rank` of the cluster.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(bar), "r"(rank));
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_wait for a barrier that the peer CTA arrives on: acquire at cluster scope.  Bounded
+// like mbar_wait.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
+                                                  volatile uint32_t* abort, uint32_t* status,
+                                                  uint32_t code) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((i & 31u) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort = 1;
+        atomicCAS(status, 0u, code);
+        return false;
+      }
+    }
+  }
+}
+
+// TMA loads into this CTA's shared memory whose completion counts on `bar`, a shared::cluster
+// barrier address that may be the pair peer's (rank 1 signals rank 0's stage barrier).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                                 int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                                 int32_t x, int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(local), "r"(rank));
+  return a;
+}
+
+// tcgen05 forms for the pair (every tcgen05 instruction of a kernel uses one CTA group).
+__device__ __forceinline__ void tmem_alloc2(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish2() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void umma2_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrives on the barrier at this offset in both CTAs of the pair once the issuing thread's
+// earlier MMAs have completed.
+__device__ __forceinline__ void umma2_commit_both(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+      "[%0], %1;" ::"r"(bar), "h"(static_cast<uint16_t>(3))
+      : "memory");
+}
+__device__ __forceinline__ void umma2_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
 }
 
 __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint32_t* status) {
@@ -199,11 +315,21 @@ __device__ __forceinline__ void store_row_chunk(const TcParams& p, void* crow_v,
 // B3D: N-major B is read through a 3-D view (64 columns, K rows, 64-column chunks), so one
 // TMA copy brings a stage's whole B tile instead of one per 64-column box (the copies per
 // stage, not the bytes, were the producer's limit).  Only when N is a multiple of 64.
-template <int BN, bool B_KMAJOR, bool RANK3, bool B3D>
+//
+// PAIR (launched as clusters of 2): tile i of the walk is a 256 x BN tile; CTA rank r of the
+// pair computes its rows 128r .. 128r + 127 into its own TMEM, from its own A rows and with
+// B split by columns between the two CTAs' shared memories.  Rank 0 issues the MMAs for both
+// (tcgen05.mma.cta_group::2) once both CTAs' stage has landed (rank 1's copies count on rank
+// 0's stage barrier), and its commits reach the stage and accumulator barriers of both CTAs.  Each CTA's epilogue writes its own rows;
+// both hand the accumulator back to rank 0.  Halving each CTA's B halves the bytes that
+// move through each SM's shared memory per FLOP (TMA writes plus MMA reads), which bounds
+// the single-CTA tile.
+template <int BN, bool B_KMAJOR, bool RANK3, bool B3D, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const TcParams p, const int fault) {
-  using Cfg = TcCfg<BN, B_KMAJOR>;
+  using Cfg = TcCfg<BN, B_KMAJOR, PAIR>;
+  static_assert(!PAIR || (BN == 256 && !RANK3), "pair tiles are 256 x 256, one problem");
   constexpr int STAGES = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -217,6 +343,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // Pair: rank in the cluster, the pair's index and count; otherwise the CTA's.
+  const uint32_t rank = PAIR ? cluster_rank() : 0u;
+  const int64_t cid = PAIR ? (blockIdx.x >> 1) : blockIdx.x;
+  const int64_t ncl = PAIR ? (gridDim.x >> 1) : gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -225,7 +355,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&ctl->tfull[a]), 1);
-      mbar_init(smem_u32(&ctl->tempty[a]), 4);
+      mbar_init(smem_u32(&ctl->tempty[a]), PAIR ? 8 : 4);  // pair: both CTAs' epilogue warps
     }
     mbar_init(smem_u32(&ctl->drain), 1);
     ctl->abort = 0;
@@ -233,8 +363,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&ctl->tmem_base), Cfg::TMEM_COLS);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc2(smem_u32(&ctl->tmem_base), Cfg::TMEM_COLS);  // one warp of each CTA, together
+      tmem_relinquish2();
+    } else {
+      tmem_alloc(smem_u32(&ctl->tmem_base), Cfg::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   if (threadIdx.x == 0) {
     tma_prefetch_map(&tmA);
@@ -243,6 +378,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // Pair: both CTAs' barriers are initialised and TMEM allocated before either signals the
+  // other or issues an MMA into it.
+  if (PAIR) cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
   // Only shared memory, TMEM and parameters above: this may overlap the previous kernel.
@@ -256,13 +394,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      TcWalk walk(p, blockIdx.x, gridDim.x);
+      TcWalk walk(p, cid, ncl);
       TcItem item;
       while (ok && walk.next(p, &item)) {
         int64_t b, tm, tn;
         raster_tile(item.tile, p.tiles_m, p.tiles_n, p.group, &b, &tm, &tn);
+        if (PAIR) tm = 2 * tm + rank;  // pair row -> this CTA's 128-row tile
         const int32_t ym = static_cast<int32_t>(tm * BM);
-        const int32_t xn = static_cast<int32_t>(tn * BN);
+        const int32_t xn = static_cast<int32_t>(tn * BN + rank * Cfg::BNC);  // this CTA's B columns
         const int32_t zb = static_cast<int32_t>(b);
         for (int kb = item.kbeg; kb < item.kend; ++kb) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
@@ -270,10 +409,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = false;
             break;
           }
-          const uint32_t fb = smem_u32(&ctl->full[s]);
-          mbar_arrive_expect_tx(fb, A_BYTES + Cfg::B_LOAD_BYTES);
           const int32_t kx = kb * BK;
           const uint32_t adst = a_ring + s * A_BYTES, bdst = b_ring + s * Cfg::B_BYTES;
+          if (PAIR) {
+            // Both CTAs' loads of stage s count on rank 0's full[s]; rank 0 posts the bytes
+            // of both (a load may land before the post: the count is signed within a phase).
+            const uint32_t fb = cluster_addr(smem_u32(&ctl->full[s]), 0u);
+            if (rank == 0) mbar_arrive_expect_tx(smem_u32(&ctl->full[s]), 2 * (A_BYTES + Cfg::B_LOAD_BYTES));
+            tma_load_2d_pair(adst, &tmA, fb, kx, ym);
+            if (B_KMAJOR) {
+              tma_load_2d_pair(bdst, &tmB, fb, kx, xn);
+            } else if (B3D) {
+              tma_load_3d_pair(bdst, &tmB, fb, 0, kx, xn / 64);
+            } else {
+#pragma unroll
+              for (int j = 0; j < Cfg::NBOX; ++j) tma_load_2d_pair(bdst + j * 8192u, &tmB, fb, xn + 64 * j, kx);
+            }
+            ++it;
+            continue;
+          }
+          const uint32_t fb = smem_u32(&ctl->full[s]);
+          mbar_arrive_expect_tx(fb, A_BYTES + Cfg::B_LOAD_BYTES);
           if (RANK3) tma_load_3d(adst, &tmA, fb, kx, ym, zb);
           else tma_load_2d(adst, &tmA, fb, kx, ym);
           if (B_KMAJOR) {
@@ -291,24 +447,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ++it;
         }
       }
-      if (!ok) {
-        // Do not leave copies landing in shared memory after exit.
+      if (!ok && (!PAIR || rank == 0)) {
+        // Do not leave copies landing in shared memory after exit (pair: rank 0's stage
+        // barriers count both CTAs' copies; the final cluster barrier holds rank 1 until
+        // rank 0 has seen them land).
         const uint32_t first = it > static_cast<uint32_t>(STAGES) ? it - STAGES : 0u;
         for (uint32_t j = first; j < it; ++j)
           wait_drain(smem_u32(&ctl->full[j % STAGES]), (j / STAGES) & 1u, p.status);
+      } else if (ok && PAIR) {
+        // Rank 0's last commits arrive on this CTA's stage barriers: see them land before
+        // the CTA can exit.
+        const uint32_t first = it > static_cast<uint32_t>(STAGES) ? it - STAGES : 0u;
+        for (uint32_t j = first; j < it; ++j)
+          mbar_wait(smem_u32(&ctl->empty[j % STAGES]), (j / STAGES) & 1u, abort, p.status,
+                    kDevTimeoutDrain);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, false, !B_KMAJOR);
+    if (lane == 0 && (!PAIR || rank == 0)) {
+      constexpr uint32_t idesc = idesc_bf16_f32(PAIR ? 2 * BM : BM, BN, false, !B_KMAJOR);
       uint32_t it = 0, lt = 0;
       bool ok = true;
-      TcWalk walk(p, blockIdx.x, gridDim.x);
+      TcWalk walk(p, cid, ncl);
       TcItem item;
       for (; ok && walk.next(p, &item); ++lt) {
         const uint32_t acc = lt & 1u, aph = (lt >> 1) & 1u;
-        if (!mbar_wait(smem_u32(&ctl->tempty[acc]), aph ^ 1u, abort, p.status, kDevTimeoutMma)) {
+        const uint32_t te = smem_u32(&ctl->tempty[acc]);
+        if (!(PAIR ? mbar_wait_cluster(te, aph ^ 1u, abort, p.status, kDevTimeoutMma)
+                   : mbar_wait(te, aph ^ 1u, abort, p.status, kDevTimeoutMma))) {
           ok = false;
           break;
         }
@@ -316,7 +483,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t d = tmem_base + acc * BN;
         for (int kb = item.kbeg; kb < item.kend; ++kb) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-          if (!mbar_wait(smem_u32(&ctl->full[s]), ph, abort, p.status, kDevTimeoutMma)) {
+          // Pair: full[s] counts the bytes of both CTAs' stage s (acquire at cluster scope).
+          if (!(PAIR ? mbar_wait_cluster(smem_u32(&ctl->full[s]), ph, abort, p.status, kDevTimeoutMma)
+                     : mbar_wait(smem_u32(&ctl->full[s]), ph, abort, p.status, kDevTimeoutMma))) {
             ok = false;
             break;
           }
@@ -327,19 +496,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // A (K-major, 128B swizzle): K step of 16 elements = 32 bytes inside the atom.
             const uint64_t adesc = sdesc_sw128(a0 + k * 32, 16, 1024);
             // B: K-major like A, or N-major: 64-column atoms 8 KiB apart (LBO), 8-row
-            // groups 1 KiB apart (SBO), K step of 16 rows = 2 KiB.
+            // groups 1 KiB apart (SBO), K step of 16 rows = 2 KiB.  For the pair the same
+            // offsets describe each CTA's share of A and B.
             const uint64_t bdesc = B_KMAJOR ? sdesc_sw128(b0 + k * 32, 16, 1024)
                                             : sdesc_sw128(b0 + k * 2048, 8192, 1024);
-            umma_bf16(d, adesc, bdesc, idesc, (kb > item.kbeg || k > 0) ? 1u : 0u);
+            const uint32_t accum = (kb > item.kbeg || k > 0) ? 1u : 0u;
+            if (PAIR) umma2_bf16(d, adesc, bdesc, idesc, accum);
+            else umma_bf16(d, adesc, bdesc, idesc, accum);
           }
-          if (fault != 1) umma_commit(smem_u32(&ctl->empty[s]));
+          if (fault != 1) {
+            if (PAIR) umma2_commit_both(smem_u32(&ctl->empty[s]));
+            else umma_commit(smem_u32(&ctl->empty[s]));
+          }
           ++it;
         }
         if (!ok) break;
-        umma_commit(smem_u32(&ctl->tfull[acc]));
+        if (PAIR) umma2_commit_both(smem_u32(&ctl->tfull[acc]));
+        else umma_commit(smem_u32(&ctl->tfull[acc]));
       }
-      // All MMAs of this CTA finished before TMEM is released.
-      umma_commit(smem_u32(&ctl->drain));
+      // All MMAs of this CTA (pair: of both CTAs) finished before TMEM is released.
+      if (PAIR) umma2_commit(smem_u32(&ctl->drain));
+      else umma_commit(smem_u32(&ctl->drain));
       wait_drain(smem_u32(&ctl->drain), 0, p.status);
     }
   } else {
@@ -352,11 +529,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t sbuf = 0;
     uint32_t lt = 0;
     const int etid = threadIdx.x - 64;
-    TcWalk walk(p, blockIdx.x, gridDim.x);
+    // Hands the accumulator back to the MMA issuer (pair: to rank 0, from both CTAs).
+    auto release_acc = [&](uint32_t acc) {
+      if (PAIR) mbar_arrive_remote(smem_u32(&ctl->tempty[acc]), 0u);
+      else mbar_arrive(smem_u32(&ctl->tempty[acc]));
+    };
+    TcWalk walk(p, cid, ncl);
     TcItem item;
     for (; walk.next(p, &item); ++lt) {
       int64_t b, tm, tn;
       raster_tile(item.tile, p.tiles_m, p.tiles_n, p.group, &b, &tm, &tn);
+      if (PAIR) tm = 2 * tm + rank;
       const uint32_t acc = lt & 1u, aph = (lt >> 1) & 1u;
       if (!mbar_wait(smem_u32(&ctl->tfull[acc]), aph, abort, p.status, kDevTimeoutEpilogue)) break;
       tc_fence_after();
@@ -367,14 +550,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int64_t kb = kblocks;
         const int64_t units = p.sk_tiles * kb, ctas = p.sk_ctas;
         const int64_t st = item.tile - p.dp_tiles;
-        const int64_t c = blockIdx.x;
+        const int64_t c = cid;
         float4* const ws4 = reinterpret_cast<float4*>(p.ws);
-        // Partial of CTA cc: [BN / 4 column groups][128 rows] float4, so a warp's stores and
-        // loads of one group cover 512 contiguous bytes.
+        // Partial of contributor cc (pair: cc's CTA of this rank): [BN / 4 column groups][128
+        // rows] float4, so a warp's stores and loads of one group cover 512 contiguous bytes.
         auto part_of = [&](int64_t cc) {
           const int sl = sk_slot<int64_t>(cc, st, kb, units, ctas);
-          return ws4 + (cc * 2 + sl) * (BN / 4) * BM + row;
+          const int64_t who = PAIR ? 2 * cc + rank : cc;
+          return ws4 + (who * 2 + sl) * (BN / 4) * BM + row;
         };
+        uint32_t* const counter = &p.counters[PAIR ? 2 * st + rank : st];
         {
           float4* dst = part_of(c);
 #pragma unroll 1
@@ -392,7 +577,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // The accumulator is in the workspace now: hand TMEM back to the MMA issuer.
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
+        if (lane == 0) release_acc(acc);
         // The barrier orders the 128 threads' stores before thread 0's release fence, and the
         // fence (cumulative) orders them before the ticket; the last contributor's acquire
         // fence orders the others' partials before its loads.
@@ -400,11 +585,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (etid == 0) {
           const uint32_t need = static_cast<uint32_t>(sk_contributors<int64_t>(st, kb, units, ctas));
           fence_acq_rel_gpu();
-          const uint32_t prev = atomicAdd(&p.counters[st], 1u);
+          const uint32_t prev = atomicAdd(counter, 1u);
           const bool is_last = prev + 1u == need;
           if (is_last) {
             fence_acq_rel_gpu();
-            p.counters[st] = 0u;  // every contributor holds its ticket: ready for the next call
+            *counter = 0u;  // every contributor holds its ticket: ready for the next call
           }
           ctl->is_last = is_last ? 1u : 0u;
         }
@@ -469,7 +654,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // The accumulator is in registers now: hand TMEM back to the MMA issuer.
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
+            if (lane == 0) release_acc(acc);
           }
           // The store issued from this buffer two pieces ago must have finished reading it.
           if (lane == 0) bulk_wait_read<1>();
@@ -525,7 +710,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
+        if (lane == 0) release_acc(acc);
       }
     }
     // Stores must have finished reading shared memory (and landed) before the CTA exits.
@@ -534,9 +719,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  // Pair: neither CTA frees TMEM or exits while the other may still touch its shared memory
+  // or barriers; the TMEM release is collective.
+  if (PAIR) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    if (PAIR) tmem_dealloc2(tmem_base, Cfg::TMEM_COLS);
+    else tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
   }
 }
 
@@ -625,35 +814,56 @@ EncodeTiledFn get_encode_tiled() {
 }
 
 namespace {
-template <int BN, bool B_KMAJOR, bool RANK3, bool B3D = false>
+template <int BN, bool B_KMAJOR, bool RANK3, bool B3D = false, bool PAIR = false>
 cudaError_t launch_tc_variant(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
                               const TcParams& p, int num_ctas, cudaStream_t s) {
-  auto kern = gemm_tc_kernel<BN, B_KMAJOR, RANK3, B3D>;
-  constexpr uint32_t smem = TcCfg<BN, B_KMAJOR>::SMEM_BYTES;
+  auto kern = gemm_tc_kernel<BN, B_KMAJOR, RANK3, B3D, PAIR>;
+  constexpr uint32_t smem = TcCfg<BN, B_KMAJOR, PAIR>::SMEM_BYTES;
+  static_assert(smem <= 232448, "shared memory per CTA");
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = ensure_smem_attr(kern, smem, attr_done);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(num_ctas), dim3(NUM_THREADS), smem, s, ma, mb, mc, p,
-                    g_fault_injection);
+  if (!PAIR)
+    return launch_pdl(kern, dim3(num_ctas), dim3(NUM_THREADS), smem, s, ma, mb, mc, p,
+                      g_fault_injection);
+  // Clusters of two CTAs, with programmatic stream serialisation as for the other kernels.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_ctas);
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, p, g_fault_injection);
 }
 }  // namespace
 
 cudaError_t launch_gemm_tc(const TcParams& p, int bn, const void* A, int64_t lda, int64_t strideA,
                            const void* B, int64_t ldb, int64_t strideB, bool b_kmajor,
-                           int num_ctas, cudaStream_t s) {
+                           bool pair, int num_ctas, cudaStream_t s) {
   CUtensorMap ma, mb;
   const uint64_t batch = static_cast<uint64_t>(p.batch);
+  if (pair && (bn != 256 || batch > 1 || num_ctas % 2 != 0)) return cudaErrorInvalidValue;
+  // B columns one CTA holds (the pair splits the tile's columns between its two CTAs).
+  const int bnc = pair ? bn / 2 : bn;
   if (!make_bf16_map(&ma, A, p.K, p.M, lda, batch, strideA, BK, BM)) return cudaErrorInvalidValue;
   // N-major B as one 3-D box per stage when the 64-column chunks tile N exactly (so no box
   // reaches past a row) and the tile width is whole chunks.
   const bool b3d = !b_kmajor && batch <= 1 && p.N % 64 == 0 && bn % 64 == 0 && p.N >= bn;
   bool ok_b;
   if (b_kmajor)
-    ok_b = make_bf16_map(&mb, B, p.K, p.N, ldb, batch, strideB, BK, bn);
+    ok_b = make_bf16_map(&mb, B, p.K, p.N, ldb, batch, strideB, BK, bnc);
   else if (b3d)
     ok_b = make_tile_map(&mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, 64, p.K, ldb,
                          static_cast<uint64_t>(p.N / 64), 64, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B,
-                         static_cast<uint32_t>(bn / 64));
+                         static_cast<uint32_t>(bnc / 64));
   else
     ok_b = make_bf16_map(&mb, B, p.N, p.K, ldb, batch, strideB, 64, BK);
   if (!ok_b) return cudaErrorInvalidValue;
@@ -671,6 +881,11 @@ cudaError_t launch_gemm_tc(const TcParams& p, int bn, const void* A, int64_t lda
     if (!ok_c) q.c_tma = 0;  // fall back to direct stores from registers
   }
   const bool rank3 = batch > 1;
+  if (pair) {
+    if (b_kmajor) return launch_tc_variant<256, true, false, false, true>(ma, mb, mc, q, num_ctas, s);
+    if (b3d) return launch_tc_variant<256, false, false, true, true>(ma, mb, mc, q, num_ctas, s);
+    return launch_tc_variant<256, false, false, false, true>(ma, mb, mc, q, num_ctas, s);
+  }
   if (b3d) {
     if (bn == 256) return launch_tc_variant<256, false, false, true>(ma, mb, mc, q, num_ctas, s);
     if (bn == 192) return launch_tc_variant<192, false, false, true>(ma, mb, mc, q, num_ctas, s);

@@ -158,7 +158,8 @@ typedef enum {
   DG_KERNEL_SCALE = 1,     /* C = beta*C only (K == 0 or alpha == 0) */
   DG_KERNEL_SIMT_F32 = 2,  /* FP32 CUDA-core SGEMM */
   DG_KERNEL_TC_BF16 = 3,   /* tcgen05 tile kernel (persistent, TMA ring, TMEM accumulators) */
-  DG_KERNEL_THIN_BF16 = 4  /* tcgen05 stream-K decode kernel (M <= 32) */
+  DG_KERNEL_THIN_BF16 = 4, /* tcgen05 stream-K decode kernel (M <= 32) */
+  DG_KERNEL_TC2_BF16 = 5   /* tile kernel on CTA pairs (cta_group::2, 256 x 256 tiles) */
 } dg_kernel;
 
 typedef struct {

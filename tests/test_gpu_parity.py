@@ -159,6 +159,17 @@ def test_f32_4096_sampled(torch):
 
 # ------------------------------------------------------------------------- BF16 path
 
+@pytest.fixture(params=["pair", "single"])
+def tile_mode(request, monkeypatch):
+    """Runs a BF16 tile-kernel test on CTA pairs (the default for M > 128) and on single
+    CTAs (DG_TC_PAIR=0, read by the planner at each call)."""
+    if request.param == "single":
+        monkeypatch.setenv("DG_TC_PAIR", "0")
+    else:
+        monkeypatch.delenv("DG_TC_PAIR", raising=False)
+    return request.param
+
+
 def run_bf16(torch, M, N, K, alpha, A, lda, B, ldb, beta, C0, ldc, out_f32=False):
     dA, dB = dev_bf16(A), dev_bf16(B)
     if out_f32:
@@ -176,7 +187,7 @@ def run_bf16(torch, M, N, K, alpha, A, lda, B, ldb, beta, C0, ldc, out_f32=False
 
 @pytest.mark.parametrize("M,N,K", [(256, 384, 320), (1, 256, 128), (16, 12288, 4096),
                                    (40, 520, 136)])
-def test_bf16_integer_bit_exact(torch, M, N, K):
+def test_bf16_integer_bit_exact(torch, tile_mode, M, N, K):
     A = inputs.f32_to_bf16_bits(inputs.integer_f32(M + K, (M, K)))
     B = inputs.f32_to_bf16_bits(inputs.integer_f32(N + K, (K, N)))
     C = run_bf16(torch, M, N, K, 1.0, A, K, B, N, 0.0, None, N)
@@ -184,7 +195,7 @@ def test_bf16_integer_bit_exact(torch, M, N, K):
     assert np.array_equal(C, oracle.round_bf16(ref))
 
 
-def test_bf16_ffn_reduced_full_compare(torch):
+def test_bf16_ffn_reduced_full_compare(torch, tile_mode):
     w = inputs.ffn_bf16(M=512, K=1024, N=2048)
     M, N, K = w["M"], w["N"], w["K"]
     C = run_bf16(torch, M, N, K, w["alpha"], w["A"], K, w["B"], N, 0.0, None, N)
@@ -192,17 +203,18 @@ def test_bf16_ffn_reduced_full_compare(torch):
     assert_bf16_close(C, ref[0], den[0], "ffn-shaped 512x2048x1024")
 
 
-# Shapes whose tiles overfill the last of the 152-CTA waves: the tail tiles run stream-K
-# first (8 tail tiles shared by 32 CTAs, K split 4 ways) before the whole-wave tiles.
+# Shapes whose tiles overfill the last wave (152 CTAs, or 76 pairs): the tail tiles run
+# stream-K first (K split 4 ways) before the whole-wave tiles.
 @pytest.mark.parametrize("M,N,K,ldc,beta,out_f32", [
     (1280, 4096, 6144, 4096, 0.0, False),     # whole-wave tiles stored with TMA
     (1280, 4096, 6144, 4096, 0.0, True),
     (1200, 4000, 6104, 4003, -0.75, False),   # ragged tiles and K block, beta, direct stores
     (1200, 4000, 6104, 4003, -0.75, True)])
-def test_bf16_stream_k_tail(torch, M, N, K, ldc, beta, out_f32):
+def test_bf16_stream_k_tail(torch, tile_mode, M, N, K, ldc, beta, out_f32):
     plan = dg.dg_plan_gemm(1, M, N, K, c_type=dg.DG_OUT_F32 if out_f32 else dg.DG_OUT_BF16,
                            num_sms=152)
-    assert plan["kernel"] == dg.DG_KERNEL_TC_BF16 and plan["tail_tiles"] > 0
+    assert plan["kernel"] in (dg.DG_KERNEL_TC_BF16, dg.DG_KERNEL_TC2_BF16)
+    assert plan["tail_tiles"] > 0
     A = inputs.f32_to_bf16_bits(inputs.normal_f32(M + 7, (M, K)))
     B = inputs.f32_to_bf16_bits(inputs.normal_f32(N + 8, (K, N), 0.1))
     c0 = inputs.normal_f32(M + N + 1, (M, N))
@@ -218,7 +230,7 @@ def test_bf16_stream_k_tail(torch, M, N, K, ldc, beta, out_f32):
         assert_bf16_close(C, ref[0], den[0], f"stream-K tail {M}x{N}x{K}")
 
 
-def test_bf16_stream_k_tail_deterministic(torch):
+def test_bf16_stream_k_tail_deterministic(torch, tile_mode):
     M, N, K = 1280, 4096, 6144
     A = dev_bf16(inputs.f32_to_bf16_bits(inputs.normal_f32(M + 7, (M, K))))
     B = dev_bf16(inputs.f32_to_bf16_bits(inputs.normal_f32(N + 8, (K, N), 0.1)))
@@ -234,7 +246,7 @@ def test_bf16_stream_k_tail_deterministic(torch):
 @pytest.mark.parametrize("M,N,K", [(129, 264, 72), (300, 1000, 200), (200, 136, 8), (33, 8, 16),
                                    (128, 256, 64), (255, 520, 4104)])
 @pytest.mark.parametrize("out_f32", [False, True])
-def test_bf16_edge_shapes(torch, M, N, K, out_f32):
+def test_bf16_edge_shapes(torch, tile_mode, M, N, K, out_f32):
     lda = ((K + 7) // 8) * 8
     ldb = ((N + 7) // 8) * 8 + 8
     ldc = N + 3
@@ -254,7 +266,7 @@ def test_bf16_edge_shapes(torch, M, N, K, out_f32):
 @pytest.mark.parametrize("M,N,K", [(129, 264, 72), (300, 1000, 200), (33, 8, 16), (255, 520, 4104),
                                    (1000, 136, 64)])
 @pytest.mark.parametrize("out_f32", [False, True])
-def test_bf16_beta_zero_edge_shapes(torch, M, N, K, out_f32):
+def test_bf16_beta_zero_edge_shapes(torch, tile_mode, M, N, K, out_f32):
     # beta = 0 with 16-byte aligned C rows: the epilogue's TMA-store path (edge tiles clipped
     # by the tensor map); the NaN-filled C checks that nothing outside M x N is written.
     lda = ((K + 7) // 8) * 8
@@ -269,7 +281,7 @@ def test_bf16_beta_zero_edge_shapes(torch, M, N, K, out_f32):
         assert_bf16_close(C, ref[0], den[0], f"bf16 beta=0 {M}x{N}x{K}")
 
 
-def test_bf16_tma_store_leaves_padding_untouched(torch):
+def test_bf16_tma_store_leaves_padding_untouched(torch, tile_mode):
     M, N, K, ldc = 200, 264, 128, 272
     A = inputs.f32_to_bf16_bits(inputs.normal_f32(50, (M, K)))
     B = inputs.f32_to_bf16_bits(inputs.normal_f32(51, (K, N)))
@@ -435,7 +447,7 @@ def test_bf16_strided_batched_bf16_out(torch, op_b):
         assert_bf16_close(Cb, ref[b], den[b], f"batched bf16 op_b={op_b} b={b}")
 
 
-def test_bf16_tile_kernel_deterministic(torch):
+def test_bf16_tile_kernel_deterministic(torch, tile_mode):
     w = inputs.ffn_bf16(M=384, K=2048, N=1536)
     dA, dB = dev_bf16(w["A"]), dev_bf16(w["B"])
     outs = []

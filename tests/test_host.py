@@ -34,8 +34,9 @@ def test_status_strings():
 
 def test_plan_dispatch_table():
     ffn = dg.dg_plan_gemm(1, 1024, 12288, 4096, num_sms=152)
-    assert ffn["kernel"] == dg.DG_KERNEL_TC_BF16 and ffn["tile_n"] == 256 and ffn["tiles"] == 384
-    assert ffn["grid"] == 152
+    # FFN on CTA pairs: 256 x 256 tiles, 4 x 48 of them, 76 pairs of CTAs.
+    assert ffn["kernel"] == dg.DG_KERNEL_TC2_BF16 and ffn["tile_m"] == 256 and ffn["tile_n"] == 256
+    assert ffn["tiles"] == 192 and ffn["grid"] == 152
     for m in (1, 4, 16):
         p = dg.dg_plan_gemm(1, m, 12288, 4096, num_sms=152)
         assert p["kernel"] == dg.DG_KERNEL_THIN_BF16 and p["ntok"] == 16
@@ -45,16 +46,20 @@ def test_plan_dispatch_table():
                          num_sms=152)
     assert qk["kernel"] == dg.DG_KERNEL_TC_BF16 and qk["tiles"] == 64 * 16 * 8
     assert dg.dg_plan_gemm(0, 4096, 4096, 4096, num_sms=152)["kernel"] == dg.DG_KERNEL_SIMT_F32
-    # Stream-K tail of the tile kernel: on for FFN (2 whole waves of K = 4096 + 80 tail
-    # tiles, spread over all 152 CTAs); off where the whole waves are too short to hide the
-    # combine (one wave of K = 1024) or a tile has too few K blocks (QK^T, K = 128).
-    assert ffn["tail_tiles"] == 80 and ffn["splits"] == 152
-    assert ffn["workspace_bytes"] == 152 * 2 * 128 * 256 * 4 + 80 * 4
+    # Stream-K tail of the tile kernel: on for FFN (2 whole waves of K = 4096 + 40 tail
+    # pair tiles, spread over all 76 pairs; partials and counters per CTA of a pair); off
+    # where the whole waves are too short to hide the combine (one wave of K = 1024) or a
+    # tile has too few K blocks (QK^T, K = 128).
+    assert ffn["tail_tiles"] == 40 and ffn["splits"] == 76
+    assert ffn["workspace_bytes"] == 2 * 76 * 2 * 128 * 256 * 4 + 2 * 40 * 4
     sk = dg.dg_plan_gemm(1, 1280, 4096, 6144, num_sms=152)
-    assert sk["tail_tiles"] == 8 and sk["splits"] == 32            # 4 CTAs per tail tile
+    assert sk["tail_tiles"] == 4 and sk["splits"] == 16            # 4 pairs per tail tile
     assert dg.dg_plan_gemm(1, 1280, 4096, 1024, num_sms=152)["tail_tiles"] == 0
     assert qk["tail_tiles"] == 0
     assert dg.dg_plan_gemm(1, 2048, 2048, 4096, num_sms=152)["tail_tiles"] == 0  # one partial wave
+    # Single CTAs where a pair would waste its second CTA (one 128-row tile row) or a batch.
+    assert dg.dg_plan_gemm(1, 128, 8192, 4096, num_sms=152)["kernel"] == dg.DG_KERNEL_TC_BF16
+    assert dg.dg_plan_gemm(1, 129, 8192, 4096, num_sms=152)["kernel"] == dg.DG_KERNEL_TC2_BF16
     assert dg.dg_plan_gemm(0, 10, 10, 0, num_sms=152)["kernel"] == dg.DG_KERNEL_SCALE
     assert dg.dg_plan_gemm(1, 0, 10, 10, num_sms=152)["kernel"] == dg.DG_KERNEL_NONE
 
