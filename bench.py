@@ -45,14 +45,14 @@ SM_MAX_MHZ_NOMINAL = 2070.0
 # kernel's sources (kernel file, planner, headers) matches the one it was taken with.
 COMMON_SOURCES = ["api.cu", "dg_internal.h", "ptx.cuh", "tile_sched.h"]
 MEASURED_TRAFFIC = {
-    "sgemm_4096": {"bytes_per_launch": 449_025_280, "source_hash": "88002eb439e09a3e"},
-    "sgemm_ragged": {"bytes_per_launch": 25_864_448, "source_hash": "88002eb439e09a3e"},
-    "ffn_bf16": {"bytes_per_launch": 150_063_104, "source_hash": "5aa351fbf6f52108"},
-    "bf16_4096": {"bytes_per_launch": 136_358_400, "source_hash": "5aa351fbf6f52108"},
-    "qk_batched": {"bytes_per_launch": 1_079_062_272, "source_hash": "5aa351fbf6f52108"},
-    "decode_m1": {"bytes_per_launch": 105_169_152, "source_hash": "ecf5a400ad617af8"},
-    "decode_m4": {"bytes_per_launch": 104_963_584, "source_hash": "ecf5a400ad617af8"},
-    "decode_m16": {"bytes_per_launch": 105_434_368, "source_hash": "ecf5a400ad617af8"},
+    "sgemm_4096": {"bytes_per_launch": 456_453_888, "source_hash": "4ab24ecfcb00ac6d"},
+    "sgemm_ragged": {"bytes_per_launch": 26_131_200, "source_hash": "4ab24ecfcb00ac6d"},
+    "ffn_bf16": {"bytes_per_launch": 164_043_008, "source_hash": "cdf45a12fbe2bbf9"},
+    "bf16_4096": {"bytes_per_launch": 147_007_232, "source_hash": "cdf45a12fbe2bbf9"},
+    "qk_batched": {"bytes_per_launch": 1_078_433_536, "source_hash": "cdf45a12fbe2bbf9"},
+    "decode_m1": {"bytes_per_launch": 105_056_512, "source_hash": "42cf33399a1b7eb4"},
+    "decode_m4": {"bytes_per_launch": 105_287_680, "source_hash": "42cf33399a1b7eb4"},
+    "decode_m16": {"bytes_per_launch": 105_511_680, "source_hash": "42cf33399a1b7eb4"},
 }
 
 
