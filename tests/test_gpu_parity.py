@@ -317,6 +317,25 @@ def test_bf16_thin_ragged(torch, M, N, K):
     assert_bf16_close(C, ref[0], den[0], f"thin {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("op_b", [dg.DG_OP_N, dg.DG_OP_T])
+@pytest.mark.parametrize("M", [1, 16, 32])
+def test_bf16_decode_w_layouts(torch, op_b, M):
+    # Decode with W as K x N (N-major) and as N x K, the nn.Linear layout (K-major); N = 3000
+    # leaves a ragged last 128-column tile.
+    N, K = 3000, 4096
+    brows, bcols = (K, N) if op_b == dg.DG_OP_N else (N, K)
+    X = inputs.f32_to_bf16_bits(inputs.normal_f32(M + 40, (M, K)))
+    W = inputs.f32_to_bf16_bits(inputs.normal_f32(M + 41, (brows, bcols), 0.05))
+    plan = dg.dg_plan_gemm(1, M, N, K, op_b=op_b, num_sms=152)
+    assert plan["kernel"] == dg.DG_KERNEL_THIN_BF16 and plan["tile_n"] == 128
+    dC = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    dg.gemm_bf16_strided_batched(M, N, K, 1.0, dev_bf16(X), K, 0, dev_bf16(W), bcols, 0, op_b,
+                                 0.0, dC, N, 0, 1, dg.DG_OUT_F32)
+    sync(torch)
+    ref, den = oracle.gemm(M, N, K, 1.0, X, K, W, bcols, op_b=op_b, absden=True)
+    assert_f32_close(host_f32(dC), ref[0], den[0], f"decode M={M} op_b={op_b}")
+
+
 @pytest.mark.parametrize("M", [1, 6, 16])
 def test_bf16_decode_deterministic(torch, M):
     # FP32 output shows any change in the order the split-K parts are added.  Which CTA
