@@ -4,8 +4,8 @@
 One "step" is one call of the library's public C ABI on one batch of synthetic input
 (resident in HBM).  The default workload is the FP32 SGEMM M = N = K = 4096,
 alpha = 1, beta = 0.5; --workload picks another of the path's configurations
-(ffn_bf16, bf16_4096, decode_m1 / decode_m4 / decode_m16, qk_batched, sgemm_ragged,
-sgemm_256).
+(ffn_bf16, ffn_gate_up, bf16_4096, decode_m1 / decode_m4 / decode_m16, qk_batched,
+sgemm_ragged, sgemm_256).
 
 Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier and
 torch.cuda.synchronize() on both sides, CUDA events on the launching stream; rotating
@@ -108,6 +108,17 @@ class Workload:
                         algo_bytes=2.0 * (M * K + K * N + M * N), bound="tensor", unit="TFLOPS",
                         kernel="gemm_tc_kernel", sources=["gemm_tc.cu"] + COMMON_SOURCES,
                         desc=f"BF16 FFN projection C=XW M={M} N={N} K={K}, FP32 accumulate, BF16 out")
+        if name == "ffn_gate_up":
+            w = inputs.ffn_gate_up()
+            M, N, K = w["M"], w["N"], w["K"]
+            w = dict(w, A=w["X"], B=w["Wg"], B2=w["Wu"], lda=K, ldb=N, ldc=N, C0=None,
+                     alpha=1.0, beta=0.0)
+            return dict(kind="gate_up", w=w, batch=1, flops=4.0 * M * N * K,
+                        algo_bytes=2.0 * (M * K + 2 * K * N + M * N), bound="tensor",
+                        unit="TFLOPS", kernel="gemm_tc_kernel",
+                        sources=["gemm_tc.cu"] + COMMON_SOURCES,
+                        desc=f"BF16 FFN gate/up Z=SiLU(XW_g)*(XW_u) M={M} N={N} K={K}, "
+                             f"FP32 accumulate, BF16 out")
         if name == "bf16_4096":
             w = inputs.bf16_square(4096)
             M, N, K = w["M"], w["N"], w["K"]
@@ -153,6 +164,8 @@ class Workload:
                 return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
             for i in range(copies):
                 A, B = bf(w["A"]), bf(w["B"])
+                if self.kind == "gate_up":
+                    B = torch.cat([B.reshape(-1), bf(w["B2"]).reshape(-1)])  # [W_g | W_u]
                 if self.kind == "bf16b":
                     C = torch.empty((w["batch"], w["M"], w["N"]), dtype=torch.float32, device="cuda")
                 else:
@@ -167,6 +180,10 @@ class Workload:
         if self.kind == "f32":
             dg.gemm_f32(w["M"], w["N"], w["K"], float(w["alpha"]), A, w["lda"], B, w["ldb"],
                         float(w["beta"]), C, w["ldc"], stream=s)
+        elif self.kind == "gate_up":
+            kn = w["K"] * w["N"]
+            dg.gemm_bf16_gate_up_silu(w["M"], w["N"], w["K"], A, w["lda"], B, w["ldb"],
+                                      B.data_ptr() + 2 * kn, w["ldb"], C, w["ldc"], stream=s)
         elif self.kind == "bf16":
             dg.gemm_bf16(w["M"], w["N"], w["K"], float(w["alpha"]), A, w["lda"], B, w["ldb"],
                          float(w["beta"]), C, w["ldc"], dg.DG_OUT_BF16, stream=s)
@@ -301,6 +318,42 @@ def time_steps(torch, wl, steps, warmup, barrier):
     return total_ms, [total_ms / steps], t0, t1
 
 
+def time_graph(torch, wl, steps, warmup):
+    """The same back-to-back steps captured once in a CUDA graph and replayed: one submission
+    launches all `steps` kernels, so the host's per-call cost drops out of the time.  The
+    capture stream gets its own library workspace, set up by warm-up calls on that stream
+    before the capture.  Returns milliseconds per step."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    saved = wl.stream
+    wl.stream = side.cuda_stream
+    try:
+        with torch.cuda.stream(side):
+            for i in range(warmup):
+                wl.step(i)
+        side.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            for i in range(steps):
+                wl.step(warmup + i)
+        graph.replay()  # once, untimed
+        torch.cuda.synchronize()
+        cur = torch.cuda.current_stream()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(cur)
+        graph.replay()
+        end.record(cur)
+        torch.cuda.synchronize()
+        return start.elapsed_time(end) / steps
+    finally:
+        wl.stream = saved
+
+
+# Short kernels also timed as a CUDA-graph replay (launch and submission cost removed).
+GRAPH_WORKLOADS = ("sgemm_256", "ffn_bf16", "ffn_gate_up", "decode_m1", "decode_m4", "decode_m16")
+
+
 def aggregate_ranks(ms_local, metric_of_seconds, world, dist, device):
     """Whole-job figure of N independent replicas: the slowest rank's time per step (max
     over ranks) and the work of all ranks divided by that time."""
@@ -368,6 +421,10 @@ def cpu_baseline(wl, budget_s=15.0, nthreads=None):
         if C0 is not None:
             C0 = C0.reshape(-1)[: rows * w["ldc"]]
         t = time.perf_counter()
+        if wl.kind == "gate_up":
+            oracle.gate_up_silu(rows, N, K, A, w["lda"], w["B"].reshape(-1), w["ldb"],
+                                w["B2"].reshape(-1), w["ldb"], nthreads=nthreads)
+            return time.perf_counter() - t
         oracle.gemm(rows, N, K, w["alpha"], A, w["lda"], w["B"].reshape(-1), w["ldb"], w["beta"],
                     C0, w["ldc"], op_b=op_b, nthreads=nthreads)
         return time.perf_counter() - t
@@ -378,7 +435,7 @@ def cpu_baseline(wl, budget_s=15.0, nthreads=None):
     rows2 = max(rows, min(M, target))
     if rows2 > rows:
         rows, dt = rows2, run(rows2)
-    flops = 2.0 * rows * N * K
+    flops = wl.flops * rows / M / batch
     byts = wl.algo_bytes * rows / M / batch
     value = byts / dt / 1e9 if wl.unit == "GB/s" else flops / dt / 1e12
     return {"value": round(value, 6), "unit": wl.unit, "cores": nthreads, "kind": "oracle",
@@ -496,8 +553,8 @@ def main():
     }
     if not args.no_suite:
         suite = {}
-        for name in ("ffn_bf16", "bf16_4096", "decode_m1", "decode_m4", "decode_m16",
-                     "qk_batched", "sgemm_ragged"):
+        for name in ("ffn_bf16", "ffn_gate_up", "bf16_4096", "decode_m1", "decode_m4",
+                     "decode_m16", "qk_batched", "sgemm_ragged", "sgemm_256"):
             if name == args.workload:
                 continue
             other = Workload(name, torch, dg, inputs)
@@ -508,6 +565,10 @@ def main():
             suite[name] = {"value": round(other.metric_value(s), 3), "unit": other.unit,
                            "ms_per_step": round(s * 1e3, 4), "roofline_frac": rf["frac"],
                            "bound": rf["bound"], "traffic": rf["traffic"]}
+            if name in GRAPH_WORKLOADS:
+                gms = time_graph(torch, other, 20, 3)
+                suite[name]["graph"] = {"value": round(other.metric_value(gms / 1e3), 3),
+                                        "ms_per_step": round(gms, 4)}
             del other
             torch.cuda.empty_cache()
         st = dg.dg_device_status()

@@ -24,7 +24,7 @@ EXPORTED = [
     "gemm_f32", "gemm_f32_strided_batched", "gemm_bf16", "gemm_bf16_strided_batched",
     "dg_status_string", "dg_device_status", "dg_release_workspace", "dg_plan_gemm",
     "dg_raster_tile", "dg_streamk_start", "dg_model_traffic_bytes", "dg_model_local_bytes",
-    "dg_version", "dg_set_fault_injection", "gemm_bf16_decode_noalloc",
+    "dg_version", "dg_set_fault_injection", "gemm_bf16_decode_noalloc", "gemm_bf16_gate_up_silu",
 ]
 
 
@@ -73,10 +73,11 @@ def load(build_if_missing: bool = True):
     lib.gemm_bf16.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, i32, vp]
     lib.gemm_bf16_strided_batched.argtypes = [i64, i64, i64, f32, vp, i64, i64, vp, i64, i64, i32,
                                               f32, vp, i64, i64, i64, i32, vp]
+    lib.gemm_bf16_gate_up_silu.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp]
     lib.gemm_bf16_decode_noalloc.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64,
                                              i32, vp]
     for f in ("gemm_f32", "gemm_f32_strided_batched", "gemm_bf16", "gemm_bf16_strided_batched",
-              "gemm_bf16_decode_noalloc"):
+              "gemm_bf16_decode_noalloc", "gemm_bf16_gate_up_silu"):
         getattr(lib, f).restype = ctypes.c_int
     lib.dg_status_string.argtypes = [ctypes.c_int]
     lib.dg_status_string.restype = ctypes.c_char_p
@@ -167,6 +168,15 @@ def gemm_bf16_decode_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, c_typ
     st = lib.gemm_bf16_decode_noalloc(M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, beta, _ptr(C),
                                       ldc, c_type, _stream(stream))
     return _ret(st, "gemm_bf16_decode_noalloc", check)
+
+
+def gemm_bf16_gate_up_silu(M, N, K, X, ldx, Wg, ldwg, Wu, ldwu, Z, ldz, stream=None,
+                           check=True) -> int:
+    """Z = bf16(SiLU(bf16(X Wg)) * bf16(X Wu)): FFN gate/up projections, activation fused."""
+    lib = load()
+    st = lib.gemm_bf16_gate_up_silu(M, N, K, _ptr(X), ldx, _ptr(Wg), ldwg, _ptr(Wu), ldwu,
+                                    _ptr(Z), ldz, _stream(stream))
+    return _ret(st, "gemm_bf16_gate_up_silu", check)
 
 
 def status_string(status: int) -> str:

@@ -158,8 +158,11 @@ void plan_f32(int64_t M, int64_t N, int64_t K, int64_t batch, int64_t resident, 
   pl->workspace_bytes = *sk_tiles > 0 ? simt_ws_floats(*sk_tiles * best_s) * 4 + *sk_tiles * 4 : 0;
 }
 
-void plan_bf16(int64_t M, int64_t N, int64_t K, int64_t batch, int sms, dg_plan* pl) {
-  if (batch == 1 && M <= kThinMaxM) {
+// dual: the FFN gate/up form, planned as one GEMM over [W_g | W_u] (N = 2 x the output
+// columns): always the tile kernel, 256-column tiles (128 output columns).
+void plan_bf16(int64_t M, int64_t N, int64_t K, int64_t batch, int sms, dg_plan* pl,
+               bool dual = false) {
+  if (!dual && batch == 1 && M <= kThinMaxM) {
     pl->kernel = DG_KERNEL_THIN_BF16;
     pl->ntok = M <= 16 ? 16 : 32;
     pl->tile_m = pl->ntok;
@@ -179,9 +182,9 @@ void plan_bf16(int64_t M, int64_t N, int64_t K, int64_t batch, int sms, dg_plan*
   // Tile width, from a measured sweep over 128..256 on FFN, square (2048..8192) and wide
   // shapes: 256 is fastest everywhere (narrower tiles load more B bytes per FLOP, which
   // costs more than the better wave fill they buy), so 128 is used only when N <= 128.
-  int bn = N <= 128 ? 128 : 256;
+  int bn = N <= 128 && !dual ? 128 : 256;
   // Tuning override (bench and sweeps): DG_TC_BN=256|224|192|128 forces the tile width.
-  if (const char* e = std::getenv("DG_TC_BN")) {
+  if (const char* e = dual ? nullptr : std::getenv("DG_TC_BN")) {
     const int f = std::atoi(e);
     if (f == 256 || f == 224 || f == 192 || f == 128) bn = f;
   }
@@ -338,6 +341,49 @@ dg_status f32_impl(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
   return from_cuda(launch_sgemm_simt(p, trans_b, vec, s));
 }
 
+// The tile kernels (single CTAs or pairs) for a planned BF16 problem.  B2 non-null selects
+// the FFN gate/up form (C = SiLU(bf16(A B)) * bf16(A B2), N output columns).
+dg_status run_tile(const dg_plan& pl, int64_t M, int64_t N, int64_t K, int64_t batch, float alpha,
+                   float beta, const uint16_t* A, int64_t lda, int64_t sA, const uint16_t* B,
+                   int64_t ldb, int64_t sB, dg_op op_b, void* C, int64_t ldc, int64_t sC,
+                   bool c_f32, bool c_vec, uint32_t* status, int dev, cudaStream_t s,
+                   const uint16_t* B2, int64_t ldb2) {
+  dg_status st = DG_OK;
+  TcParams p;
+  p.M = M; p.N = N; p.K = K;
+  p.batch = batch;
+  const bool pair = pl.kernel == DG_KERNEL_TC2_BF16;
+  p.tiles_m = pair ? cdiv(cdiv(M, kTcBM), 2) : cdiv(M, kTcBM);
+  p.tiles_n = cdiv(N, B2 ? pl.tile_n / 2 : pl.tile_n);  // gate/up: 128 output columns a tile
+  p.total_tiles = pl.tiles;
+  p.kblocks = static_cast<int32_t>(pl.kblocks);
+  p.group = pl.group;
+  p.alpha = alpha; p.beta = beta;
+  p.C = C; p.ldc = ldc; p.strideC = batch > 1 ? sC : 0;
+  p.c_f32 = c_f32 ? 1 : 0;
+  p.c_vec = c_vec ? 1 : 0;
+  p.c_tma = (c_vec && beta == 0.f) ? 1 : 0;
+  p.status = status;
+  p.sk_tiles = pl.tail_tiles;
+  p.dp_tiles = pl.tiles - pl.tail_tiles;
+  p.sk_ctas = pl.tail_tiles > 0 ? pl.splits : 0;
+  p.ws = nullptr;
+  p.counters = nullptr;
+  if (p.sk_tiles > 0) {
+    Workspace w;
+    const int64_t per = pair ? 2 : 1;
+    st = get_workspace(dev, s, static_cast<size_t>(tc_ws_floats(per * p.sk_ctas, pl.tile_n)),
+                       static_cast<size_t>(per * p.sk_tiles), &w);
+    if (st != DG_OK) return st;
+    p.ws = w.ws;
+    p.counters = w.counters;
+  }
+  return from_cuda(launch_gemm_tc(p, pl.tile_n, A, lda, batch > 1 ? sA : 0, B, ldb,
+                                  batch > 1 ? sB : 0, op_b == DG_OP_T, pair,
+                                  static_cast<int>(pl.grid), s, B2, ldb2));
+}
+
+
 dg_status bf16_impl(int64_t M, int64_t N, int64_t K, float alpha, const uint16_t* A, int64_t lda,
                     int64_t sA, const uint16_t* B, int64_t ldb, int64_t sB, dg_op op_b,
                     float beta, void* C, int64_t ldc, int64_t sC, int64_t batch, dg_out c_type,
@@ -384,38 +430,8 @@ dg_status bf16_impl(int64_t M, int64_t N, int64_t K, float alpha, const uint16_t
     return from_cuda(launch_gemm_thin(p, pl.ntok, A, lda, B, ldb, op_b == DG_OP_T, s));
   }
 
-  TcParams p;
-  p.M = M; p.N = N; p.K = K;
-  p.batch = batch;
-  const bool pair = pl.kernel == DG_KERNEL_TC2_BF16;
-  p.tiles_m = pair ? cdiv(cdiv(M, kTcBM), 2) : cdiv(M, kTcBM);
-  p.tiles_n = cdiv(N, pl.tile_n);
-  p.total_tiles = pl.tiles;
-  p.kblocks = static_cast<int32_t>(pl.kblocks);
-  p.group = pl.group;
-  p.alpha = alpha; p.beta = beta;
-  p.C = C; p.ldc = ldc; p.strideC = batch > 1 ? sC : 0;
-  p.c_f32 = c_f32 ? 1 : 0;
-  p.c_vec = c_vec ? 1 : 0;
-  p.c_tma = (c_vec && beta == 0.f) ? 1 : 0;
-  p.status = status;
-  p.sk_tiles = pl.tail_tiles;
-  p.dp_tiles = pl.tiles - pl.tail_tiles;
-  p.sk_ctas = pl.tail_tiles > 0 ? pl.splits : 0;
-  p.ws = nullptr;
-  p.counters = nullptr;
-  if (p.sk_tiles > 0) {
-    Workspace w;
-    const int64_t per = pair ? 2 : 1;
-    st = get_workspace(dev, s, static_cast<size_t>(tc_ws_floats(per * p.sk_ctas, pl.tile_n)),
-                       static_cast<size_t>(per * p.sk_tiles), &w);
-    if (st != DG_OK) return st;
-    p.ws = w.ws;
-    p.counters = w.counters;
-  }
-  return from_cuda(launch_gemm_tc(p, pl.tile_n, A, lda, batch > 1 ? sA : 0, B, ldb,
-                                  batch > 1 ? sB : 0, op_b == DG_OP_T, pair,
-                                  static_cast<int>(pl.grid), s));
+  return run_tile(pl, M, N, K, batch, alpha, beta, A, lda, sA, B, ldb, sB, op_b, C, ldc, sC,
+                  c_f32, c_vec, status, dev, s, nullptr, 0);
 }
 
 // ------------------------------------------------------------------ scale kernel
@@ -493,6 +509,33 @@ dg_status gemm_bf16_strided_batched(int64_t M, int64_t N, int64_t K, float alpha
                                     int64_t batch, dg_out c_type, void* stream) {
   return bf16_impl(M, N, K, alpha, A, lda, strideA, B, ldb, strideB, op_b, beta, C, ldc, strideC,
                    batch, c_type, stream);
+}
+
+dg_status gemm_bf16_gate_up_silu(int64_t M, int64_t N, int64_t K, const uint16_t* X, int64_t ldx,
+                                 const uint16_t* Wg, int64_t ldwg, const uint16_t* Wu,
+                                 int64_t ldwu, uint16_t* Z, int64_t ldz, void* stream) {
+  if (M < 0 || N < 0 || K < 0) return DG_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return DG_OK;
+  if (ldz < N || (K > 0 && (ldx < K || ldwg < N || ldwu < N))) return DG_ERR_INVALID_ARG;
+  if (!Z) return DG_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int dev = 0;
+  if (current_device(&dev) != cudaSuccess) return DG_ERR_CUDA;
+  uint32_t* status = nullptr;
+  int sms = 0;
+  if (device_info(dev, &status, &sms) != cudaSuccess) return DG_ERR_CUDA;
+  // K == 0: G = U = 0 and SiLU(0) * 0 = 0.
+  if (K == 0) return run_scale(Z, false, M, N, ldz, 0, 1, 0.f, s);
+  if (!X || !Wg || !Wu) return DG_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(Wg) || !aligned16(Wu) || ldx % 8 != 0 || ldwg % 8 != 0 ||
+      ldwu % 8 != 0)
+    return DG_ERR_MISALIGNED;
+  dg_plan pl;
+  plan_bf16(M, 2 * N, K, 1, sms, &pl, true);
+  log_plan("gemm_bf16_gate_up_silu", M, N, K, 1, pl);
+  const bool c_vec = aligned16(Z) && (ldz * 2) % 16 == 0;
+  return run_tile(pl, M, N, K, 1, 1.f, 0.f, X, ldx, 0, Wg, ldwg, 0, DG_OP_N, Z, ldz, 0, false,
+                  c_vec, status, dev, s, Wu, ldwu);
 }
 
 const char* dg_status_string(dg_status s) {

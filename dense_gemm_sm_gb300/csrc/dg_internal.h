@@ -69,9 +69,12 @@ inline int64_t tc_ws_floats(int64_t sk_ctas, int bn) { return sk_ctas * 2 * 128 
 // op T -> [batch][N][ldb] (K contiguous).
 // pair: launch clusters of two CTAs that each compute half of a 256 x bn tile (bn = 256,
 // batch 1, num_ctas even; p.tiles_m then counts 256-row tile rows).
+// B2 non-null: the FFN gate/up form -- B = W_g, B2 = W_u (both K x N, N-major, batch 1),
+// bn = 256 covers 128 output columns of each, and C = SiLU(bf16(X W_g)) * bf16(X W_u).
 cudaError_t launch_gemm_tc(const TcParams& p, int bn, const void* A, int64_t lda, int64_t strideA,
                            const void* B, int64_t ldb, int64_t strideB, bool b_kmajor,
-                           bool pair, int num_ctas, cudaStream_t s);
+                           bool pair, int num_ctas, cudaStream_t s, const void* B2 = nullptr,
+                           int64_t ldb2 = 0);
 constexpr int kTcBM = 128, kTcBK = 64;
 
 // ------------------------------------------------------------------ BF16 thin (decode) path

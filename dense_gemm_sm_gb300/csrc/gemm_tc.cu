@@ -250,6 +250,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+
+// FFN activation chain ("Operator & Runtime" sections 5.3.1 and 5.4.3): z = SiLU(G) * U
+// with G and U rounded to BF16 first (the unfused program stores them as BF16), SiLU(x) =
+// x / (1 + e^-x) and the product in FP32; the store rounds z to BF16 once more.
+__device__ __forceinline__ void silu_mul_bf16(uint32_t (&g)[32], const uint32_t (&u)[32]) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float gb = __bfloat162float(__float2bfloat16_rn(__uint_as_float(g[j])));
+    const float ub = __bfloat162float(__float2bfloat16_rn(__uint_as_float(u[j])));
+    g[j] = __float_as_uint(gb / (1.f + expf(-gb)) * ub);
+  }
+}
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // Writes 32 consecutive outputs of one row: out[j] = alpha*acc[j] + beta*old[j], j < 32,
@@ -324,12 +336,19 @@ __device__ __forceinline__ void store_row_chunk(const TcParams& p, void* crow_v,
 // both hand the accumulator back to rank 0.  Halving each CTA's B halves the bytes that
 // move through each SM's shared memory per FLOP (TMA writes plus MMA reads), which bounds
 // the single-CTA tile.
-template <int BN, bool B_KMAJOR, bool RANK3, bool B3D, bool PAIR>
+//
+// DUAL (FFN gate and up projections): B is [W_g tile | W_u tile], BN / 2 columns each, so the
+// accumulator holds G and U side by side; the epilogue writes z = SiLU(bf16(G)) * bf16(U),
+// BN / 2 output columns per tile.  Pair: rank 0 holds the W_g tile and rank 1 the W_u tile.
+template <int BN, bool B_KMAJOR, bool RANK3, bool B3D, bool PAIR, bool DUAL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, const TcParams p, const int fault) {
+                   const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC,
+                   const TcParams p, const int fault) {
   using Cfg = TcCfg<BN, B_KMAJOR, PAIR>;
   static_assert(!PAIR || (BN == 256 && !RANK3), "pair tiles are 256 x 256, one problem");
+  static_assert(!DUAL || (BN == 256 && !B_KMAJOR && !RANK3), "gate/up: 2 x 128 columns, N-major");
+  constexpr int OUT_N = DUAL ? BN / 2 : BN;  // output columns per tile
   constexpr int STAGES = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -374,6 +393,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     tma_prefetch_map(&tmA);
     tma_prefetch_map(&tmB);
+    if (DUAL) tma_prefetch_map(&tmB2);
     if (p.c_tma) tma_prefetch_map(&tmC);
   }
   tc_fence_before();
@@ -401,7 +421,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         raster_tile(item.tile, p.tiles_m, p.tiles_n, p.group, &b, &tm, &tn);
         if (PAIR) tm = 2 * tm + rank;  // pair row -> this CTA's 128-row tile
         const int32_t ym = static_cast<int32_t>(tm * BM);
-        const int32_t xn = static_cast<int32_t>(tn * BN + rank * Cfg::BNC);  // this CTA's B columns
+        // This CTA's B columns (gate/up: the output tile's columns in W_g and W_u).
+        const int32_t xn = static_cast<int32_t>(DUAL ? tn * OUT_N : tn * BN + rank * Cfg::BNC);
+        const CUtensorMap* mb1 = (DUAL && PAIR && rank == 1) ? &tmB2 : &tmB;
         const int32_t zb = static_cast<int32_t>(b);
         for (int kb = item.kbeg; kb < item.kend; ++kb) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
@@ -420,10 +442,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (B_KMAJOR) {
               tma_load_2d_pair(bdst, &tmB, fb, kx, xn);
             } else if (B3D) {
-              tma_load_3d_pair(bdst, &tmB, fb, 0, kx, xn / 64);
+              tma_load_3d_pair(bdst, mb1, fb, 0, kx, xn / 64);
             } else {
 #pragma unroll
-              for (int j = 0; j < Cfg::NBOX; ++j) tma_load_2d_pair(bdst + j * 8192u, &tmB, fb, xn + 64 * j, kx);
+              for (int j = 0; j < Cfg::NBOX; ++j) tma_load_2d_pair(bdst + j * 8192u, mb1, fb, xn + 64 * j, kx);
             }
             ++it;
             continue;
@@ -435,6 +457,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (B_KMAJOR) {
             if (RANK3) tma_load_3d(bdst, &tmB, fb, kx, xn, zb);
             else tma_load_2d(bdst, &tmB, fb, kx, xn);
+          } else if (DUAL) {
+            // W_g's columns into the first half of the stage's B, W_u's into the second.
+            if (B3D) {
+              tma_load_3d(bdst, &tmB, fb, 0, kx, xn / 64);
+              tma_load_3d(bdst + Cfg::B_BYTES / 2, &tmB2, fb, 0, kx, xn / 64);
+            } else {
+#pragma unroll
+              for (int j = 0; j < Cfg::NBOX / 2; ++j) {
+                tma_load_2d(bdst + j * 8192u, &tmB, fb, xn + 64 * j, kx);
+                tma_load_2d(bdst + Cfg::B_BYTES / 2 + j * 8192u, &tmB2, fb, xn + 64 * j, kx);
+              }
+            }
           } else if (B3D) {
             tma_load_3d(bdst, &tmB, fb, 0, kx, xn / 64);
           } else {
@@ -600,12 +634,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int64_t gm = tm * BM + row;
           uint8_t* cbase = static_cast<uint8_t*>(p.C) +
                            (b * p.strideC + gm * p.ldc) * (p.c_f32 ? 4 : 2);
-#pragma unroll 1
-          for (int ch = 0; ch < BN / 32; ++ch) {
-            float sum[32];
+          // The contributors' partials of accumulator columns ch*32 .. ch*32+31, in CTA
+          // order, two per round trip.
+          auto sum_chunk = [&](int ch, float (&sum)[32]) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) sum[j] = 0.f;
-            // Contributors in CTA order, two per round trip.
             for (int64_t cc = first; cc <= lastc; cc += 2) {
               const bool two = cc + 1 <= lastc;
               const float4* pa = part_of(cc) + ch * 8 * BM;
@@ -630,10 +663,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
               }
             }
+          };
+#pragma unroll 1
+          for (int ch = 0; ch < OUT_N / 32; ++ch) {
+            float sum[32];
+            sum_chunk(ch, sum);
             uint32_t r[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(sum[j]);
-            if (gm < p.M) store_row_chunk(p, cbase, tn * BN + ch * 32, r);
+            if (DUAL) {
+              float usum[32];
+              sum_chunk(ch + OUT_N / 32, usum);
+              uint32_t u[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) u[j] = __float_as_uint(usum[j]);
+              silu_mul_bf16(r, u);
+            }
+            if (gm < p.M) store_row_chunk(p, cbase, tn * OUT_N + ch * 32, r);
           }
         }
         epi_bar();  // is_last is rewritten only after everyone read it
@@ -646,11 +692,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int32_t y = static_cast<int32_t>(tm * BM + q * 32);
         const int32_t zb = static_cast<int32_t>(b);
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = 0; c < OUT_N / 32; ++c) {
           uint32_t w[32];
           tmem_ld_32x32b_x32(taddr + c * 32, w);
-          tmem_ld_wait();
-          if (c == BN / 32 - 1) {
+          if (DUAL) {
+            uint32_t u[32];
+            tmem_ld_32x32b_x32(taddr + OUT_N + c * 32, u);
+            tmem_ld_wait();
+            silu_mul_bf16(w, u);
+          } else {
+            tmem_ld_wait();
+          }
+          if (c == OUT_N / 32 - 1) {
             // The accumulator is in registers now: hand TMEM back to the MMA issuer.
             tc_fence_before();
             __syncwarp();
@@ -688,7 +741,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            const int32_t x = static_cast<int32_t>(tn * BN + c * 32);
+            const int32_t x = static_cast<int32_t>(tn * OUT_N + c * 32);
             if (y < p.M && x < p.N) {  // skip pieces wholly outside C
               if (RANK3) tma_store_3d(&tmC, buf, x, y, zb);
               else tma_store_2d(&tmC, buf, x, y);
@@ -702,11 +755,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint8_t* cbase = static_cast<uint8_t*>(p.C) +
                          (b * p.strideC + gm * p.ldc) * (p.c_f32 ? 4 : 2);
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = 0; c < OUT_N / 32; ++c) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(taddr + c * 32, r);
-          tmem_ld_wait();
-          if (gm < p.M) store_row_chunk(p, cbase, tn * BN + c * 32, r);
+          if (DUAL) {
+            uint32_t u[32];
+            tmem_ld_32x32b_x32(taddr + OUT_N + c * 32, u);
+            tmem_ld_wait();
+            silu_mul_bf16(r, u);
+          } else {
+            tmem_ld_wait();
+          }
+          if (gm < p.M) store_row_chunk(p, cbase, tn * OUT_N + c * 32, r);
         }
         tc_fence_before();
         __syncwarp();
@@ -814,17 +874,18 @@ EncodeTiledFn get_encode_tiled() {
 }
 
 namespace {
-template <int BN, bool B_KMAJOR, bool RANK3, bool B3D = false, bool PAIR = false>
-cudaError_t launch_tc_variant(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
-                              const TcParams& p, int num_ctas, cudaStream_t s) {
-  auto kern = gemm_tc_kernel<BN, B_KMAJOR, RANK3, B3D, PAIR>;
+template <int BN, bool B_KMAJOR, bool RANK3, bool B3D = false, bool PAIR = false, bool DUAL = false>
+cudaError_t launch_tc_variant(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mb2,
+                              const CUtensorMap& mc, const TcParams& p, int num_ctas,
+                              cudaStream_t s) {
+  auto kern = gemm_tc_kernel<BN, B_KMAJOR, RANK3, B3D, PAIR, DUAL>;
   constexpr uint32_t smem = TcCfg<BN, B_KMAJOR, PAIR>::SMEM_BYTES;
   static_assert(smem <= 232448, "shared memory per CTA");
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = ensure_smem_attr(kern, smem, attr_done);
   if (e != cudaSuccess) return e;
   if (!PAIR)
-    return launch_pdl(kern, dim3(num_ctas), dim3(NUM_THREADS), smem, s, ma, mb, mc, p,
+    return launch_pdl(kern, dim3(num_ctas), dim3(NUM_THREADS), smem, s, ma, mb, mb2, mc, p,
                       g_fault_injection);
   // Clusters of two CTAs, with programmatic stream serialisation as for the other kernels.
   cudaLaunchConfig_t cfg = {};
@@ -841,22 +902,27 @@ cudaError_t launch_tc_variant(const CUtensorMap& ma, const CUtensorMap& mb, cons
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, p, g_fault_injection);
+  return cudaLaunchKernelEx(&cfg, kern, ma, mb, mb2, mc, p, g_fault_injection);
 }
 }  // namespace
 
 cudaError_t launch_gemm_tc(const TcParams& p, int bn, const void* A, int64_t lda, int64_t strideA,
                            const void* B, int64_t ldb, int64_t strideB, bool b_kmajor,
-                           bool pair, int num_ctas, cudaStream_t s) {
-  CUtensorMap ma, mb;
+                           bool pair, int num_ctas, cudaStream_t s, const void* B2,
+                           int64_t ldb2) {
+  CUtensorMap ma, mb, mb2;
   const uint64_t batch = static_cast<uint64_t>(p.batch);
+  const bool dual = B2 != nullptr;
   if (pair && (bn != 256 || batch > 1 || num_ctas % 2 != 0)) return cudaErrorInvalidValue;
-  // B columns one CTA holds (the pair splits the tile's columns between its two CTAs).
-  const int bnc = pair ? bn / 2 : bn;
+  if (dual && (bn != 256 || batch > 1 || b_kmajor)) return cudaErrorInvalidValue;
+  // B columns one tensor map box set covers: the CTA's share of the tile (the pair splits the
+  // tile's columns between its two CTAs; gate/up reads BN / 2 from each of W_g and W_u).
+  const int bnc = dual ? bn / 2 : (pair ? bn / 2 : bn);
   if (!make_bf16_map(&ma, A, p.K, p.M, lda, batch, strideA, BK, BM)) return cudaErrorInvalidValue;
   // N-major B as one 3-D box per stage when the 64-column chunks tile N exactly (so no box
   // reaches past a row) and the tile width is whole chunks.
-  const bool b3d = !b_kmajor && batch <= 1 && p.N % 64 == 0 && bn % 64 == 0 && p.N >= bn;
+  const bool b3d = !b_kmajor && batch <= 1 && p.N % 64 == 0 && bn % 64 == 0 &&
+                   p.N >= (dual ? bn / 2 : bn);
   bool ok_b;
   if (b_kmajor)
     ok_b = make_bf16_map(&mb, B, p.K, p.N, ldb, batch, strideB, BK, bnc);
@@ -867,6 +933,15 @@ cudaError_t launch_gemm_tc(const TcParams& p, int bn, const void* A, int64_t lda
   else
     ok_b = make_bf16_map(&mb, B, p.N, p.K, ldb, batch, strideB, 64, BK);
   if (!ok_b) return cudaErrorInvalidValue;
+  mb2 = mb;
+  if (dual) {
+    const bool ok_b2 =
+        b3d ? make_tile_map(&mb2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B2, 64, p.K, ldb2,
+                            static_cast<uint64_t>(p.N / 64), 64, 64, BK,
+                            CU_TENSOR_MAP_SWIZZLE_128B, static_cast<uint32_t>(bnc / 64))
+            : make_bf16_map(&mb2, B2, p.N, p.K, ldb2, 1, 0, 64, BK);
+    if (!ok_b2) return cudaErrorInvalidValue;
+  }
   CUtensorMap mc;
   std::memset(&mc, 0, sizeof mc);
   TcParams q = p;
@@ -881,19 +956,25 @@ cudaError_t launch_gemm_tc(const TcParams& p, int bn, const void* A, int64_t lda
     if (!ok_c) q.c_tma = 0;  // fall back to direct stores from registers
   }
   const bool rank3 = batch > 1;
+  if (dual) {
+    if (pair && b3d) return launch_tc_variant<256, false, false, true, true, true>(ma, mb, mb2, mc, q, num_ctas, s);
+    if (pair) return launch_tc_variant<256, false, false, false, true, true>(ma, mb, mb2, mc, q, num_ctas, s);
+    if (b3d) return launch_tc_variant<256, false, false, true, false, true>(ma, mb, mb2, mc, q, num_ctas, s);
+    return launch_tc_variant<256, false, false, false, false, true>(ma, mb, mb2, mc, q, num_ctas, s);
+  }
   if (pair) {
-    if (b_kmajor) return launch_tc_variant<256, true, false, false, true>(ma, mb, mc, q, num_ctas, s);
-    if (b3d) return launch_tc_variant<256, false, false, true, true>(ma, mb, mc, q, num_ctas, s);
-    return launch_tc_variant<256, false, false, false, true>(ma, mb, mc, q, num_ctas, s);
+    if (b_kmajor) return launch_tc_variant<256, true, false, false, true>(ma, mb, mb2, mc, q, num_ctas, s);
+    if (b3d) return launch_tc_variant<256, false, false, true, true>(ma, mb, mb2, mc, q, num_ctas, s);
+    return launch_tc_variant<256, false, false, false, true>(ma, mb, mb2, mc, q, num_ctas, s);
   }
   if (b3d) {
-    if (bn == 256) return launch_tc_variant<256, false, false, true>(ma, mb, mc, q, num_ctas, s);
-    if (bn == 192) return launch_tc_variant<192, false, false, true>(ma, mb, mc, q, num_ctas, s);
-    if (bn == 128) return launch_tc_variant<128, false, false, true>(ma, mb, mc, q, num_ctas, s);
+    if (bn == 256) return launch_tc_variant<256, false, false, true>(ma, mb, mb2, mc, q, num_ctas, s);
+    if (bn == 192) return launch_tc_variant<192, false, false, true>(ma, mb, mb2, mc, q, num_ctas, s);
+    if (bn == 128) return launch_tc_variant<128, false, false, true>(ma, mb, mb2, mc, q, num_ctas, s);
   }
 #define DG_TC_CASE(BNV, KM, R3)                                                     \
   if (bn == BNV && b_kmajor == KM && rank3 == R3)                                   \
-    return launch_tc_variant<BNV, KM, R3>(ma, mb, mc, q, num_ctas, s);
+    return launch_tc_variant<BNV, KM, R3>(ma, mb, mb2, mc, q, num_ctas, s);
   DG_TC_CASE(256, false, false)
   DG_TC_CASE(256, false, true)
   DG_TC_CASE(256, true, false)

@@ -117,6 +117,15 @@ def ffn_bf16(M=1024, K=4096, N=12288, W=None) -> dict:
                 ldb=N, C0=None, ldc=N)
 
 
+def ffn_gate_up(M=1024, K=4096, N=12288) -> dict:
+    """FFN gate and up projections: X [M,K] ~ N(0,1), W_g and W_u [K,N] ~ N(0, 1/K), BF16."""
+    s = BASE_SEED + 7
+    X = f32_to_bf16_bits(normal_f32(s, (M, K)))
+    Wg = f32_to_bf16_bits(normal_f32(s + 1, (K, N), std=1.0 / np.sqrt(K)))
+    Wu = f32_to_bf16_bits(normal_f32(s + 2, (K, N), std=1.0 / np.sqrt(K)))
+    return dict(M=M, N=N, K=K, X=X, ldx=K, Wg=Wg, ldwg=N, Wu=Wu, ldwu=N, ldz=N)
+
+
 def bf16_square(n=4096) -> dict:
     """BF16 n^3 GEMM with the FFN operand distributions (the "4096-class" square shape)."""
     s = BASE_SEED + 5

@@ -135,6 +135,26 @@ dg_status gemm_bf16_decode_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
                                    int64_t ldb, float beta, void* C, int64_t ldc, dg_out c_type,
                                    void* stream);
 
+/*
+ * FFN gate and up projections with the activation chain fused into the epilogue
+ * ("Operator & Runtime" section 5.3.1: G = X W_g, U = X W_u, Z = SiLU(G) (.) U, all
+ * [M, N]; section 5.4.3: the FP32 accumulation is rounded to BF16 before the activation,
+ * as the unfused program stores G and U in BF16):
+ *     Z[i][j] = bf16( SiLU(bf16(G[i][j])) * bf16(U[i][j]) ),   SiLU(x) = x / (1 + e^-x),
+ * with the activation and the product in FP32 and every rounding nearest-even.  G and U
+ * never reach memory; only Z (BF16) is written.
+ *   - X is M x K (ldx >= K); W_g and W_u are K x N (ldwg, ldwu >= N), row-major BF16, so
+ *     X W_g is the op(B) = B case of gemm_bf16.  Z is M x N BF16 (ldz >= N).
+ *   - Device pointers owned by the caller; no aliasing between Z and the inputs.
+ *   - Errors as gemm_bf16: negative sizes or short leading dimensions DG_ERR_INVALID_ARG;
+ *     X, W_g, W_u not 16-byte aligned or ldx, ldwg, ldwu not multiples of 8
+ *     DG_ERR_MISALIGNED.  M == 0 or N == 0: nothing; K == 0: Z = 0.
+ *   - Any M uses the tile kernel (CTA pairs from M > 128); there is no decode-shaped form.
+ */
+dg_status gemm_bf16_gate_up_silu(int64_t M, int64_t N, int64_t K, const uint16_t* X, int64_t ldx,
+                                 const uint16_t* Wg, int64_t ldwg, const uint16_t* Wu,
+                                 int64_t ldwu, uint16_t* Z, int64_t ldz, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* dg_status_string(dg_status s);
 

@@ -229,3 +229,50 @@ def check_bf16(C_bits, ref, den):
     ok = bool(np.all(err <= bound) and np.all(np.isfinite(C)))
     ratio = err / bound
     return ok, float(ratio.max()) if ratio.size else 0.0
+
+
+# ---------------------------------------------------------------------------
+# FFN gate/up activation chain ("Operator & Runtime", section 5.3.1: G = X W_g,
+# U = X W_u, Z = SiLU(G) (.) U; section 5.4.3: the FP32 accumulation is rounded
+# to BF16 before the activation, as the unfused program stores G and U as BF16).
+# Steps in the pages' order: the two GEMMs (the oracle's own FP64 GEMM above),
+# round each to BF16, SiLU(x) = x / (1 + e^-x) and the product in FP64.  The
+# result is returned before Z's own rounding to BF16.
+# ---------------------------------------------------------------------------
+SILU_SLOPE_MAX = 1.0999  # >= max |d/dx SiLU(x)| = 1.09984 (at x ~ 2.40), for the error bound
+
+
+def silu(x):
+    """SiLU(x) = x / (1 + e^-x) in float64 (the limit 0 for x -> -inf)."""
+    x = np.asarray(x, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return x / (1.0 + np.exp(-x))
+
+
+def gate_up_silu(M, N, K, X, ldx, Wg, ldwg, Wu, ldwu, nthreads=None):
+    """(z, gb, ub, Dg, Du) for Z = SiLU(bf16(X Wg)) * bf16(X Wu): z before Z's rounding, the
+    BF16-rounded G and U as float64, and the error scales sum_k |x w| of G and U."""
+    G, Dg = gemm(M, N, K, 1.0, X, ldx, Wg, ldwg, absden=True, nthreads=nthreads)
+    U, Du = gemm(M, N, K, 1.0, X, ldx, Wu, ldwu, absden=True, nthreads=nthreads)
+    gb = bf16_to_f64(round_bf16(G[0]))
+    ub = bf16_to_f64(round_bf16(U[0]))
+    return silu(gb) * ub, gb, ub, Dg[0], Du[0]
+
+
+def check_gate_up(Z_bits, z, gb, ub, Dg, Du):
+    """(ok, worst error / bound, fraction bit-equal to bf16(z)) for the GPU's BF16 Z.
+
+    Bound: the GPU's bf16(G) lies within dg = BF16_REL*Dg + ulp_bf16(|G|) of G (the BF16
+    GEMM bound) and the oracle's within half an ulp, so the two differ by at most
+    Dg' = dg + ulp/2 (likewise U).  SiLU is SILU_SLOPE_MAX-Lipschitz, so
+    |z_gpu - z| <= L*Dg'*(|ub| + Du') + |SiLU(gb)|*Du', plus the GPU's FP32 evaluation
+    (a few float32 ulps, 1e-6 relative) and Z's rounding (one BF16 ulp)."""
+    dgp = BF16_REL * Dg + 1.5 * ulp_bf16(np.abs(gb))
+    dup = BF16_REL * Du + 1.5 * ulp_bf16(np.abs(ub))
+    bound = (SILU_SLOPE_MAX * dgp * (np.abs(ub) + dup) + np.abs(silu(gb)) * dup +
+             1e-6 * np.abs(z) + ulp_bf16(np.abs(z)))
+    Zv = bf16_to_f64(Z_bits)
+    err = np.abs(Zv - z)
+    ok = bool(np.all(err <= bound) and np.all(np.isfinite(Zv)))
+    same = float(np.mean(Z_bits == round_bf16(z))) if z.size else 1.0
+    return ok, float((err / bound).max()) if z.size else 0.0, same

@@ -263,3 +263,82 @@ def test_acceptance_checkers():
     bits = oracle.round_bf16(ref)
     ok, worst = oracle.check_bf16(bits, ref, den)
     assert ok and worst == 0.0
+
+
+# --------------------------------------------------------------------------- FFN gate/up
+def test_silu_values_printed_by_the_pages():
+    g, _ = read_golden("silu_chain.txt")
+    assert oracle.silu(0.0) == g["silu_0"]
+    assert round(float(oracle.silu(1.0) + oracle.silu(-1.0)), 4) == g["silu_1_plus_silu_m1"]
+
+
+def test_silu_closed_forms():
+    x = np.random.default_rng(5).normal(0, 6, 1000)
+    # sigma(x) + sigma(-x) = 1  =>  SiLU(x) - SiLU(-x) = x
+    assert np.allclose(oracle.silu(x) - oracle.silu(-x), x, rtol=1e-12, atol=1e-12)
+    assert np.all(oracle.silu(np.array([-1000.0])) == 0.0)           # e^-x overflows: limit 0
+    assert oracle.silu(np.array([1000.0]))[0] == 1000.0
+    assert abs(oracle.silu(1.0) - 1.0 / (1.0 + np.exp(-1.0))) < 1e-15
+    # sigma(ln 3) = 3/4 exactly, so SiLU(ln 3) = (3/4) ln 3
+    assert abs(oracle.silu(np.log(3.0)) - 0.75 * np.log(3.0)) < 1e-15
+    # The checker's Lipschitz constant: the steepest slope of SiLU (near x = 2.4) is just
+    # below SILU_SLOPE_MAX, and nowhere steeper.
+    t = np.linspace(-20, 20, 400001)
+    slope = np.abs(np.diff(oracle.silu(t)) / np.diff(t))
+    assert 1.0995 < slope.max() <= oracle.SILU_SLOPE_MAX
+
+
+def _bits(a):
+    from dense_gemm_sm_gb300 import inputs
+    return inputs.f32_to_bf16_bits(np.asarray(a, np.float32))
+
+
+def test_gate_up_rounds_g_before_the_activation():
+    g, _ = read_golden("silu_chain.txt")
+    X = _bits([[1.0, 1.0]])
+    Wg = _bits([[1.0], [2.0 ** -9]])      # G = 1 + 2^-9, exact in float64, not in BF16
+    Wu = _bits([[1.0], [0.0]])            # U = 1
+    z, gb, ub, _, _ = oracle.gate_up_silu(1, 1, 2, X, 2, Wg, 1, Wu, 1)
+    assert gb[0, 0] == 1.0 and ub[0, 0] == 1.0
+    assert oracle.bf16_to_f64(oracle.round_bf16(z))[0, 0] == g["z_rounded_g"]
+    unrounded = oracle.silu(1.0 + 2.0 ** -9)
+    assert oracle.bf16_to_f64(oracle.round_bf16(np.array([unrounded])))[0] == g["z_unrounded_g"]
+
+
+def test_gate_up_special_cases_and_numpy():
+    rng = np.random.default_rng(6)
+    M, N, K = 5, 7, 11
+    X = _bits(rng.integers(-3, 4, (M, K)))
+    Wg = _bits(rng.integers(-3, 4, (K, N)))
+    Wu = _bits(rng.integers(-3, 4, (K, N)))
+    zero = _bits(np.zeros((K, N)))
+    z, _, _, _, _ = oracle.gate_up_silu(M, N, K, X, K, Wg, N, zero, N)
+    assert np.all(z == 0.0)                                          # U = 0
+    z, _, _, _, _ = oracle.gate_up_silu(M, N, K, X, K, zero, N, Wu, N)
+    assert np.all(z == 0.0)                                          # G = 0, SiLU(0) = 0
+    # Integer data: G and U are small integers, exact in BF16; check against numpy's
+    # float64 matmul and the logistic written out.
+    z, gb, ub, _, _ = oracle.gate_up_silu(M, N, K, X, K, Wg, N, Wu, N)
+    x = oracle.bf16_to_f64(X).reshape(M, K)
+    G = x @ oracle.bf16_to_f64(Wg).reshape(K, N)
+    U = x @ oracle.bf16_to_f64(Wu).reshape(K, N)
+    assert np.array_equal(gb, G) and np.array_equal(ub, U)
+    assert np.allclose(z, G * (1.0 / (1.0 + np.exp(-G))) * U, rtol=1e-14, atol=0)
+
+
+def test_gate_up_check_catches_a_missing_rounding():
+    # The checker must reject a result computed without rounding G and U to BF16 first
+    # (a plausible epilogue mistake): FFN-like data, where the rounding changes most Z.
+    rng = np.random.default_rng(7)
+    M, N, K = 16, 64, 512
+    X = _bits(rng.normal(0, 1, (M, K)))
+    Wg = _bits(rng.normal(0, 1 / 16, (K, N)))
+    Wu = _bits(rng.normal(0, 1 / 16, (K, N)))
+    z, gb, ub, Dg, Du = oracle.gate_up_silu(M, N, K, X, K, Wg, N, Wu, N)
+    ok, _, same = oracle.check_gate_up(oracle.round_bf16(z), z, gb, ub, Dg, Du)
+    assert ok and same == 1.0
+    G = oracle.gemm(M, N, K, 1.0, X, K, Wg, N)[0]
+    U = oracle.gemm(M, N, K, 1.0, X, K, Wu, N)[0]
+    wrong = oracle.round_bf16(oracle.silu(G) * U)
+    _, _, same_wrong = oracle.check_gate_up(wrong, z, gb, ub, Dg, Du)
+    assert same_wrong < 0.95
