@@ -45,14 +45,15 @@ SM_MAX_MHZ_NOMINAL = 2070.0
 # kernel's sources (kernel file, planner, headers) matches the one it was taken with.
 COMMON_SOURCES = ["api.cu", "dg_internal.h", "ptx.cuh", "tile_sched.h"]
 MEASURED_TRAFFIC = {
-    "sgemm_4096": {"bytes_per_launch": 456_453_888, "source_hash": "4ab24ecfcb00ac6d"},
-    "sgemm_ragged": {"bytes_per_launch": 26_131_200, "source_hash": "4ab24ecfcb00ac6d"},
-    "ffn_bf16": {"bytes_per_launch": 164_043_008, "source_hash": "cdf45a12fbe2bbf9"},
-    "bf16_4096": {"bytes_per_launch": 147_007_232, "source_hash": "cdf45a12fbe2bbf9"},
-    "qk_batched": {"bytes_per_launch": 1_078_433_536, "source_hash": "cdf45a12fbe2bbf9"},
-    "decode_m1": {"bytes_per_launch": 105_056_512, "source_hash": "42cf33399a1b7eb4"},
-    "decode_m4": {"bytes_per_launch": 105_287_680, "source_hash": "42cf33399a1b7eb4"},
-    "decode_m16": {"bytes_per_launch": 105_511_680, "source_hash": "42cf33399a1b7eb4"},
+    "sgemm_4096": {"bytes_per_launch": 464_388_096, "source_hash": "cbd90222cbf1f7c5"},
+    "sgemm_ragged": {"bytes_per_launch": 26_063_104, "source_hash": "cbd90222cbf1f7c5"},
+    "ffn_bf16": {"bytes_per_launch": 162_293_248, "source_hash": "ffcd0b77999d56c5"},
+    "ffn_gate_up": {"bytes_per_launch": 234_007_552, "source_hash": "ffcd0b77999d56c5"},
+    "bf16_4096": {"bytes_per_launch": 147_564_544, "source_hash": "ffcd0b77999d56c5"},
+    "qk_batched": {"bytes_per_launch": 1_078_958_592, "source_hash": "ffcd0b77999d56c5"},
+    "decode_m1": {"bytes_per_launch": 105_269_760, "source_hash": "dee96d3fb2bc7307"},
+    "decode_m4": {"bytes_per_launch": 105_322_496, "source_hash": "dee96d3fb2bc7307"},
+    "decode_m16": {"bytes_per_launch": 105_634_560, "source_hash": "dee96d3fb2bc7307"},
 }
 
 

@@ -276,3 +276,101 @@ def check_gate_up(Z_bits, z, gb, ub, Dg, Du):
     ok = bool(np.all(err <= bound) and np.all(np.isfinite(Zv)))
     same = float(np.mean(Z_bits == round_bf16(z))) if z.size else 1.0
     return ok, float((err / bound).max()) if z.size else 0.0, same
+
+
+# ---------------------------------------------------------------------------
+# Attention ("Operator & Runtime", section 5.3.3): S = Q K^T / sqrt(d), P = softmax(S)
+# row by row, O = P V.  The fused method (tiling + online softmax) reaches this same
+# result up to rounding, so the oracle is the definition written out in float64, with
+# numpy's float64 matmul as the product step and the row maximum subtracted before the
+# exponential (which leaves softmax unchanged).  Causal: key j is visible to query i
+# iff j <= i (the pages' causal experiment; queries and keys of one sequence).
+# online_softmax is the pages' block recurrence for one query row, kept beside it.
+# ---------------------------------------------------------------------------
+def attention_f64(Q, K, V, scale, causal=False, rows=None):
+    """One head in float64: Q [Lq, d], K [Lkv, d], V [Lkv, dv] (any float arrays).
+
+    Returns (O, PVabs, Ds) for the query rows `rows` (all by default):
+      O     = softmax(scale * Q K^T) V                   [r, dv]
+      PVabs = P |V|, the error scale of O                [r, dv]
+      Ds    = max_j scale * sum_d |q_id k_jd| over visible keys, the error scale of S   [r]
+    """
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    qi = np.arange(Q.shape[0]) if rows is None else np.asarray(rows, dtype=np.int64)
+    S = float(scale) * (Q[qi] @ K.T)
+    Sabs = abs(float(scale)) * (np.abs(Q[qi]) @ np.abs(K).T)
+    if causal:
+        hidden = np.arange(K.shape[0])[None, :] > qi[:, None]
+        S[hidden] = -np.inf
+        Sabs[hidden] = 0.0
+    m = S.max(axis=1, keepdims=True)
+    E = np.exp(S - m)
+    P = E / E.sum(axis=1, keepdims=True)
+    return P @ V, P @ np.abs(V), Sabs.max(axis=1)
+
+
+def online_softmax(scores, values, block):
+    """The pages' recurrence for one query row, `block` keys at a time:
+    m' = max(m, max s), r = exp(m - m'), p_j = exp(s_j - m'), l' = r l + sum p_j,
+    u' = r u + sum p_j v_j; the output is u / l.  Returns (u / l, [(m, l, u) after each
+    block])."""
+    s = np.asarray(scores, dtype=np.float64)
+    v = np.asarray(values, dtype=np.float64)
+    m, l = -np.inf, 0.0
+    u = np.zeros(v.shape[1:], dtype=np.float64)
+    states = []
+    for b0 in range(0, s.shape[0], block):
+        sb, vb = s[b0:b0 + block], v[b0:b0 + block]
+        m_new = max(m, float(sb.max()))
+        r = np.exp(m - m_new)
+        pj = np.exp(sb - m_new)
+        l = r * l + pj.sum()
+        u = r * u + np.tensordot(pj, vb, axes=(0, 0))
+        m = m_new
+        states.append((m, l, u.copy()))
+    return u / l, states
+
+
+def _bf16_view(bits, batch, L, ld, stride, d):
+    """[batch, L, d] float64 view of a strided BF16 array (elements b*stride + i*ld + c)."""
+    x = bf16_to_f64(np.asarray(bits).reshape(-1))
+    out = np.empty((batch, L, d), dtype=np.float64)
+    for b in range(batch):
+        base = b * stride
+        out[b] = x[base: base + (L - 1) * ld + d].reshape(-1)[
+            (np.arange(L)[:, None] * ld + np.arange(d)[None, :])]
+    return out
+
+
+def attention(batch, Lq, Lkv, d, scale, causal, Q, ldq, sQ, K, ldk, sK, V, ldv, sV,
+              rows=None):
+    """attention_f64 over a strided batch of BF16 (uint16 bit pattern) heads.  `rows`
+    (optional) lists the query rows to compute in every batch.  Returns (O, PVabs, Ds)
+    stacked over the batch."""
+    q = _bf16_view(Q, batch, Lq, ldq, sQ, d)
+    k = _bf16_view(K, batch, Lkv, ldk, sK, d)
+    v = _bf16_view(V, batch, Lkv, ldv, sV, d)
+    res = [attention_f64(q[b], k[b], v[b], scale, causal, rows) for b in range(batch)]
+    return tuple(np.stack([r[i] for r in res]) for i in range(3))
+
+
+# Acceptance bound for BF16 attention output (derived; the pages state none):
+#   |O - O_ref| <= (2^-9 + BF16_REL + 1e-5 + 2 * FP32_REL * Ds) * (P|V|) + ulp_bf16(|O_ref|)
+# 2^-9: P rounded to BF16 before the P V product (relative half-ulp per weight, the
+# normaliser summed from the unrounded weights); BF16_REL: FP32 accumulation of P V and
+# of the normaliser over the keys (the figure of the BF16 GEMM bound); 1e-5: the FP32
+# exponential and its argument; 2 * FP32_REL * Ds: an error e in the scores moves every
+# normalised weight by at most a factor e^(2e); one BF16 ulp for the rounding of O.
+ATTN_P_REL = 2.0 ** -9
+
+
+def check_attention(O_bits, O_ref, PVabs, Ds):
+    """(ok, worst error / bound) for BF16 attention output (uint16 bit patterns)."""
+    O = bf16_to_f64(O_bits)
+    rel = ATTN_P_REL + BF16_REL + 1e-5 + 2.0 * FP32_REL * np.asarray(Ds)[..., None]
+    bound = rel * PVabs + ulp_bf16(np.abs(O_ref))
+    err = np.abs(O - O_ref)
+    ok = bool(np.all(err <= bound) and np.all(np.isfinite(O)))
+    return ok, float((err / bound).max()) if err.size else 0.0

@@ -342,3 +342,113 @@ def test_gate_up_check_catches_a_missing_rounding():
     wrong = oracle.round_bf16(oracle.silu(G) * U)
     _, _, same_wrong = oracle.check_gate_up(wrong, z, gb, ub, Dg, Du)
     assert same_wrong < 0.95
+
+
+# --------------------------------------------------------------------------- attention
+def test_online_softmax_example_5_6():
+    g, _ = read_golden("online_softmax.txt")
+    out, states = oracle.online_softmax([0.0, np.log(2.0)], [[1.0], [3.0]], 1)
+    (m1, l1, u1), (m2, l2, u2) = states
+    assert (m1, l1, u1[0]) == (g["block1_m"], g["block1_l"], g["block1_u"])
+    assert np.isclose(np.exp(m1 - m2), g["block2_r"], rtol=1e-15)
+    assert np.isclose(l2, g["block2_l"], rtol=1e-15) and np.isclose(u2[0], g["block2_u"], rtol=1e-15)
+    assert np.isclose(out[0], g["output"], rtol=1e-15)
+    # The definition gives the same 7/3: one query with q . k_j equal to the scores.
+    O, _, _ = oracle.attention_f64([[1.0]], [[0.0], [np.log(2.0)]], [[1.0], [3.0]], 1.0)
+    assert np.isclose(O[0, 0], g["output"], rtol=1e-15)
+
+
+def test_attention_uniform_scores_closed_forms():
+    # Q = 0: every visible key has the same weight.  Non-causal: O = mean of V; causal:
+    # row i is the mean of V[0..i] (catches a mask that drops or adds the diagonal).
+    rng = np.random.default_rng(21)
+    L, d = 37, 5
+    V = rng.normal(0, 1, (L, d))
+    O, _, _ = oracle.attention_f64(np.zeros((L, d)), rng.normal(0, 1, (L, d)), V, 0.3)
+    assert np.allclose(O, V.mean(axis=0)[None, :], rtol=0, atol=1e-14)
+    O, _, _ = oracle.attention_f64(np.zeros((L, d)), rng.normal(0, 1, (L, d)), V, 0.3, causal=True)
+    prefix = np.cumsum(V, axis=0) / np.arange(1, L + 1)[:, None]
+    assert np.allclose(O, prefix, rtol=0, atol=1e-14)
+    assert np.array_equal(O[0], V[0])
+
+
+def test_attention_dominant_key_and_invariants():
+    rng = np.random.default_rng(22)
+    Lq, Lkv, d = 6, 50, 8
+    Q = rng.normal(0, 1, (Lq, d))
+    K = rng.normal(0, 0.1, (Lkv, d))
+    V = rng.normal(0, 1, (Lkv, d))
+    # One key aligned with every query and far larger: its weight is 1 to within e^-60.
+    K2 = K.copy()
+    K2[17] = 1000.0 * Q.sum(axis=0) / np.linalg.norm(Q.sum(axis=0))
+    Qpos = np.abs(Q) * np.sign(Q.sum(axis=0))   # every query has a positive dot with key 17
+    O, _, _ = oracle.attention_f64(Qpos, K2, V, 1.0)
+    assert np.allclose(O, V[17][None, :], atol=1e-12)
+    # Permuting the keys with their values leaves O unchanged; constant V gives O = V.
+    perm = rng.permutation(Lkv)
+    O1, _, _ = oracle.attention_f64(Q, K, V, 0.7)
+    O2, _, _ = oracle.attention_f64(Q, K[perm], V[perm], 0.7)
+    assert np.allclose(O1, O2, rtol=1e-13, atol=1e-14)
+    O3, _, _ = oracle.attention_f64(Q, K, np.full((Lkv, d), 2.5), 0.7)
+    assert np.allclose(O3, 2.5, rtol=1e-14)
+    # O is a convex combination of the rows of V.
+    assert np.all(O1 <= V.max(axis=0) + 1e-12) and np.all(O1 >= V.min(axis=0) - 1e-12)
+
+
+def test_attention_definition_matches_the_block_recurrence():
+    # The pages' block recurrence (any block size) against the definition, per query row.
+    rng = np.random.default_rng(23)
+    Lq, Lkv, d = 4, 300, 16
+    Q, K, V = rng.normal(0, 2, (Lq, d)), rng.normal(0, 2, (Lkv, d)), rng.normal(0, 1, (Lkv, d))
+    scale = 1.0 / np.sqrt(d)
+    O, _, _ = oracle.attention_f64(Q, K, V, scale)
+    for blk in (1, 7, 128):
+        for i in range(Lq):
+            o, _ = oracle.online_softmax(scale * (K @ Q[i]), V, blk)
+            assert np.allclose(o, O[i], rtol=1e-12, atol=1e-13)
+
+
+def test_attention_strided_bf16_view():
+    # The strided BF16 entry equals attention_f64 on the widened, de-strided heads.
+    from dense_gemm_sm_gb300 import inputs
+    rng = np.random.default_rng(24)
+    batch, L, d, ld = 2, 9, 8, 16
+    stride = L * ld + 8
+    raw = [inputs.f32_to_bf16_bits(rng.normal(0, 1, batch * stride).astype(np.float32))
+           for _ in range(3)]
+    O, PV, Ds = oracle.attention(batch, L, L, d, 0.5, True, raw[0], ld, stride, raw[1], ld, stride,
+                                 raw[2], ld, stride)
+    for b in range(batch):
+        heads = [oracle.bf16_to_f64(r[b * stride: b * stride + L * ld]).reshape(L, ld)[:, :d]
+                 for r in raw]
+        o, pv, ds = oracle.attention_f64(*heads, 0.5, causal=True)
+        assert np.array_equal(O[b], o) and np.array_equal(PV[b], pv) and np.array_equal(Ds[b], ds)
+
+
+def test_attention_check_catches_planted_mistakes():
+    # Each plausible kernel mistake, planted here in oracle-side arithmetic, must fail the
+    # acceptance check: scale 1/d instead of 1/sqrt(d), a causal mask that hides the
+    # diagonal, and blocks combined without rescaling by r.
+    from dense_gemm_sm_gb300 import inputs
+    rng = np.random.default_rng(25)
+    L, d = 256, 128
+    bits = [inputs.f32_to_bf16_bits(rng.normal(0, 1, (L, d)).astype(np.float32)) for _ in range(3)]
+    Q, K, V = (oracle.bf16_to_f64(b) for b in bits)
+    scale = 1.0 / np.sqrt(d)
+    O, PV, Ds = oracle.attention_f64(Q, K, V, scale, causal=True)
+    ok, worst = oracle.check_attention(oracle.round_bf16(O), O, PV, Ds)
+    assert ok and worst <= 0.51
+    wrong_scale, _, _ = oracle.attention_f64(Q, K, V, 1.0 / d, causal=True)
+    assert not oracle.check_attention(oracle.round_bf16(wrong_scale), O, PV, Ds)[0]
+    strict = np.array([oracle.attention_f64(Q[i:i + 1], K[:i], V[:i], scale)[0][0]
+                       if i > 0 else V[0] for i in range(L)])
+    assert not oracle.check_attention(oracle.round_bf16(strict), O, PV, Ds)[0]
+    no_rescale = np.empty_like(O)
+    for i in range(L):
+        s = scale * (K[:i + 1] @ Q[i])
+        l, u = 0.0, np.zeros(d)
+        for b0 in range(0, i + 1, 128):       # per block: own maximum, no r
+            pj = np.exp(s[b0:b0 + 128] - s[b0:b0 + 128].max())
+            l, u = l + pj.sum(), u + pj @ V[b0:b0 + pj.size]
+        no_rescale[i] = u / l
+    assert not oracle.check_attention(oracle.round_bf16(no_rescale), O, PV, Ds)[0]
