@@ -5,7 +5,7 @@ One "step" is one call of the library's public C ABI on one batch of synthetic i
 (resident in HBM).  The default workload is the FP32 SGEMM M = N = K = 4096,
 alpha = 1, beta = 0.5; --workload picks another of the path's configurations
 (ffn_bf16, ffn_gate_up, bf16_4096, decode_m1 / decode_m4 / decode_m16, qk_batched,
-sgemm_ragged, sgemm_256).
+attn_batched, attn_causal_8k, sgemm_ragged, sgemm_256).
 
 Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier and
 torch.cuda.synchronize() on both sides, CUDA events on the launching stream; rotating
@@ -120,6 +120,17 @@ class Workload:
                         sources=["gemm_tc.cu"] + COMMON_SOURCES,
                         desc=f"BF16 FFN gate/up Z=SiLU(XW_g)*(XW_u) M={M} N={N} K={K}, "
                              f"FP32 accumulate, BF16 out")
+        if name in ("attn_batched", "attn_causal_8k"):
+            causal = name == "attn_causal_8k"
+            w = inputs.attention(1, 8192, causal=True) if causal else inputs.attention()
+            b, L, Lkv, d = w["batch"], w["Lq"], w["Lkv"], w["d"]
+            pairs = b * (L * (L + 1) // 2 if causal else L * Lkv)   # (query, visible key) pairs
+            w = dict(w, A=w["Q"], B=w["K"], B2=w["V"])
+            return dict(kind="attn", w=w, batch=b, flops=4.0 * d * pairs,
+                        algo_bytes=2.0 * b * d * (2 * L + 2 * Lkv), bound="tensor", unit="TFLOPS",
+                        kernel="attn_fwd_kernel", sources=["attention.cu"] + COMMON_SOURCES,
+                        desc=f"fused attention O=softmax(QK^T/sqrt(d))V heads={b} L={L} d={d} "
+                             f"{'causal' if causal else 'non-causal'}, BF16 in/out, FP32 accumulate")
         if name == "bf16_4096":
             w = inputs.bf16_square(4096)
             M, N, K = w["M"], w["N"], w["K"]
@@ -165,8 +176,12 @@ class Workload:
                 return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
             for i in range(copies):
                 A, B = bf(w["A"]), bf(w["B"])
-                if self.kind == "gate_up":
-                    B = torch.cat([B.reshape(-1), bf(w["B2"]).reshape(-1)])  # [W_g | W_u]
+                if self.kind in ("gate_up", "attn"):
+                    B = torch.cat([B.reshape(-1), bf(w["B2"]).reshape(-1)])  # [W_g | W_u], [K | V]
+                if self.kind == "attn":
+                    C = torch.empty((w["batch"], w["Lq"], w["d"]), dtype=torch.bfloat16, device="cuda")
+                    self.bufs.append((A, B, C))
+                    continue
                 if self.kind == "bf16b":
                     C = torch.empty((w["batch"], w["M"], w["N"]), dtype=torch.float32, device="cuda")
                 else:
@@ -185,6 +200,11 @@ class Workload:
             kn = w["K"] * w["N"]
             dg.gemm_bf16_gate_up_silu(w["M"], w["N"], w["K"], A, w["lda"], B, w["ldb"],
                                       B.data_ptr() + 2 * kn, w["ldb"], C, w["ldc"], stream=s)
+        elif self.kind == "attn":
+            kv = w["batch"] * w["Lkv"] * w["d"]
+            dg.attention_bf16(w["batch"], w["Lq"], w["Lkv"], w["d"], float(w["scale"]), w["causal"],
+                              A, w["ldq"], w["sQ"], B, w["ldk"], w["sK"], B.data_ptr() + 2 * kv,
+                              w["ldv"], w["sV"], C, w["ldo"], w["sO"], stream=s)
         elif self.kind == "bf16":
             dg.gemm_bf16(w["M"], w["N"], w["K"], float(w["alpha"]), A, w["lda"], B, w["ldb"],
                          float(w["beta"]), C, w["ldc"], dg.DG_OUT_BF16, stream=s)
@@ -412,6 +432,8 @@ def cpu_baseline(wl, budget_s=15.0, nthreads=None):
     import oracle
     w = wl.w
     nthreads = nthreads or os.cpu_count() or 1
+    if wl.kind == "attn":
+        return attn_cpu_baseline(wl, budget_s)
     M, N, K = w["M"], w["N"], w["K"]
     batch = w.get("batch", 1)
     op_b = w.get("op_b", 0)
@@ -442,6 +464,39 @@ def cpu_baseline(wl, budget_s=15.0, nthreads=None):
     return {"value": round(value, 6), "unit": wl.unit, "cores": nthreads, "kind": "oracle",
             "sample": f"rows 0..{rows - 1} of C ({rows}/{M} rows{' of batch 0' if batch > 1 else ''}), "
                       f"FP64 triple loop, {dt:.2f} s"}
+
+
+def attn_cpu_baseline(wl, budget_s):
+    """The attention oracle on the first R query rows of head 0 (numpy float64 matmuls)."""
+    import oracle
+    w = wl.w
+
+    def run(rows):
+        t = time.perf_counter()
+        oracle.attention(1, w["Lq"], w["Lkv"], w["d"], float(w["scale"]), w["causal"], w["Q"],
+                         w["ldq"], w["sQ"], w["K"], w["ldk"], w["sK"], w["V"], w["ldv"], w["sV"],
+                         rows=np.arange(rows))
+        return time.perf_counter() - t
+
+    rows = 64
+    dt = run(rows)
+    target = int(rows * budget_s / max(dt, 1e-6) * 0.8)
+    rows2 = max(rows, min(w["Lq"], target))
+    if rows2 > rows:
+        rows, dt = rows2, run(rows2)
+    pairs = rows * (rows + 1) // 2 if w["causal"] else rows * w["Lkv"]
+    value = 4.0 * w["d"] * pairs / dt / 1e12
+    return {"value": round(value, 6), "unit": wl.unit, "cores": _blas_threads(), "kind": "oracle",
+            "sample": f"query rows 0..{rows - 1} of head 0 ({rows}/{w['Lq']} rows of 1/{w['batch']} "
+                      f"heads), float64 softmax(QK^T)V, {dt:.2f} s"}
+
+
+def _blas_threads():
+    """Threads numpy's BLAS may use (the oracle's matmul steps): the CPU count unless limited."""
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count() or 1
 
 
 def reference_arm(args):
@@ -555,7 +610,8 @@ def main():
     if not args.no_suite:
         suite = {}
         for name in ("ffn_bf16", "ffn_gate_up", "bf16_4096", "decode_m1", "decode_m4",
-                     "decode_m16", "qk_batched", "sgemm_ragged", "sgemm_256"):
+                     "decode_m16", "qk_batched", "attn_batched", "attn_causal_8k", "sgemm_ragged",
+                     "sgemm_256"):
             if name == args.workload:
                 continue
             other = Workload(name, torch, dg, inputs)

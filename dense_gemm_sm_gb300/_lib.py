@@ -25,6 +25,7 @@ EXPORTED = [
     "dg_status_string", "dg_device_status", "dg_release_workspace", "dg_plan_gemm",
     "dg_raster_tile", "dg_streamk_start", "dg_model_traffic_bytes", "dg_model_local_bytes",
     "dg_version", "dg_set_fault_injection", "gemm_bf16_decode_noalloc", "gemm_bf16_gate_up_silu",
+    "attention_bf16",
 ]
 
 
@@ -74,10 +75,12 @@ def load(build_if_missing: bool = True):
     lib.gemm_bf16_strided_batched.argtypes = [i64, i64, i64, f32, vp, i64, i64, vp, i64, i64, i32,
                                               f32, vp, i64, i64, i64, i32, vp]
     lib.gemm_bf16_gate_up_silu.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp]
+    lib.attention_bf16.argtypes = [i64, i64, i64, i64, f32, i32, vp, i64, i64, vp, i64, i64, vp,
+                                   i64, i64, vp, i64, i64, vp]
     lib.gemm_bf16_decode_noalloc.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64,
                                              i32, vp]
     for f in ("gemm_f32", "gemm_f32_strided_batched", "gemm_bf16", "gemm_bf16_strided_batched",
-              "gemm_bf16_decode_noalloc", "gemm_bf16_gate_up_silu"):
+              "gemm_bf16_decode_noalloc", "gemm_bf16_gate_up_silu", "attention_bf16"):
         getattr(lib, f).restype = ctypes.c_int
     lib.dg_status_string.argtypes = [ctypes.c_int]
     lib.dg_status_string.restype = ctypes.c_char_p
@@ -177,6 +180,16 @@ def gemm_bf16_gate_up_silu(M, N, K, X, ldx, Wg, ldwg, Wu, ldwu, Z, ldz, stream=N
     st = lib.gemm_bf16_gate_up_silu(M, N, K, _ptr(X), ldx, _ptr(Wg), ldwg, _ptr(Wu), ldwu,
                                     _ptr(Z), ldz, _stream(stream))
     return _ret(st, "gemm_bf16_gate_up_silu", check)
+
+
+def attention_bf16(batch, Lq, Lkv, d, scale, causal, Q, ldq, strideQ, K, ldk, strideK, V, ldv,
+                   strideV, O, ldo, strideO, stream=None, check=True) -> int:
+    """O = softmax(scale * Q K^T) V per head (fused, online softmax), BF16 in and out."""
+    lib = load()
+    st = lib.attention_bf16(batch, Lq, Lkv, d, scale, 1 if causal else 0, _ptr(Q), ldq, strideQ,
+                            _ptr(K), ldk, strideK, _ptr(V), ldv, strideV, _ptr(O), ldo, strideO,
+                            _stream(stream))
+    return _ret(st, "attention_bf16", check)
 
 
 def status_string(status: int) -> str:

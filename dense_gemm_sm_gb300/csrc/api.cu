@@ -11,6 +11,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
@@ -536,6 +537,48 @@ dg_status gemm_bf16_gate_up_silu(int64_t M, int64_t N, int64_t K, const uint16_t
   const bool c_vec = aligned16(Z) && (ldz * 2) % 16 == 0;
   return run_tile(pl, M, N, K, 1, 1.f, 0.f, X, ldx, 0, Wg, ldwg, 0, DG_OP_N, Z, ldz, 0, false,
                   c_vec, status, dev, s, Wu, ldwu);
+}
+
+dg_status attention_bf16(int64_t batch, int64_t Lq, int64_t Lkv, int64_t d, float scale,
+                         int32_t causal, const uint16_t* Q, int64_t ldq, int64_t strideQ,
+                         const uint16_t* K, int64_t ldk, int64_t strideK, const uint16_t* V,
+                         int64_t ldv, int64_t strideV, uint16_t* O, int64_t ldo, int64_t strideO,
+                         void* stream) {
+  if (batch < 0 || Lq < 0 || Lkv < 0 || d < 0) return DG_ERR_INVALID_ARG;
+  if (batch == 0 || Lq == 0) return DG_OK;
+  if (Lkv == 0 || !(scale > 0.f) || !std::isfinite(scale)) return DG_ERR_INVALID_ARG;
+  if (causal && Lq != Lkv) return DG_ERR_INVALID_ARG;
+  if (ldq < d || ldk < d || ldv < d || ldo < d) return DG_ERR_INVALID_ARG;
+  if (batch > 1 && (strideQ < Lq * ldq || strideK < Lkv * ldk || strideV < Lkv * ldv ||
+                    strideO < Lq * ldo))
+    return DG_ERR_INVALID_ARG;
+  if (!Q || !K || !V || !O) return DG_ERR_INVALID_ARG;
+  if (d != 128 || Lq >= (int64_t(1) << 31) || Lkv >= (int64_t(1) << 31)) return DG_ERR_UNSUPPORTED;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || ldq % 8 || ldk % 8 ||
+      ldv % 8 || ldo % 8 || (batch > 1 && (strideQ % 8 || strideK % 8 || strideV % 8 || strideO % 8)))
+    return DG_ERR_MISALIGNED;
+  const int64_t q_tiles = (Lq + 127) / 128;
+  if (batch * q_tiles > 0x7FFFFFFF) return DG_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int dev = 0;
+  if (current_device(&dev) != cudaSuccess) return DG_ERR_CUDA;
+  uint32_t* status = nullptr;
+  int sms = 0;
+  if (device_info(dev, &status, &sms) != cudaSuccess) return DG_ERR_CUDA;
+  AttnParams p;
+  p.batch = batch;
+  p.Lq = Lq;
+  p.Lkv = Lkv;
+  p.q_tiles = q_tiles;
+  p.c_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);  // log2(e)
+  p.rank3 = batch > 1 ? 1 : 0;
+  p.status = status;
+  if (std::getenv("DG_LOG_PLAN"))
+    std::fprintf(stderr, "[dg] attention_bf16 batch=%lld Lq=%lld Lkv=%lld causal=%d grid=%lld\n",
+                 static_cast<long long>(batch), static_cast<long long>(Lq),
+                 static_cast<long long>(Lkv), causal ? 1 : 0, static_cast<long long>(batch * q_tiles));
+  return from_cuda(launch_attention(p, causal != 0, Q, ldq, strideQ, K, ldk, strideK, V, ldv,
+                                    strideV, O, ldo, strideO, s));
 }
 
 const char* dg_status_string(dg_status s) {

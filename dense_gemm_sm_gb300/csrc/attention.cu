@@ -1,0 +1,433 @@
+// attention.cu -- fused attention forward on the tcgen05 tensor cores:
+//   O = softmax(scale * Q K^T) V  per head, BF16 in, FP32 accumulate, BF16 out, d = 128
+// ("Operator & Runtime", section 5.3.3: tiling with the online softmax, so the score and
+// probability matrices never leave the SM).
+//
+// One CTA computes one 128-row query tile of one head and streams the head's keys and values
+// through shared memory in blocks of 128 rows:
+//   warp 0     TMA producer: the Q tile once, then K_j and V_j into two 2-slot rings;
+//   warp 1     allocates TMEM and issues the MMAs: S_j = Q K_j^T into one of two TMEM score
+//              buffers, O += P_j V_j into the TMEM output accumulator;
+//   warps 2-5  softmax and epilogue, one query row per thread (the TMEM lane of that row):
+//              the running maximum m and sum l in registers, p = 2^(s * scale * log2 e - m)
+//              rounded to BF16 into shared memory as the A operand of the P V product.
+// The recurrence is the pages' (m' = max(m, max s), r = e^(m - m'), l' = r l + sum p,
+// u' = r u + sum p v), with one change that leaves the result unchanged: the reference
+// point m is moved only when the block maximum exceeds it by more than 2^8 in the weights,
+// so the rescale of the TMEM accumulator (a TMEM load/multiply/store of the row) runs only
+// on the few blocks that raise the maximum that much; between moves the weights stay below
+// 2^8, far inside FP32 and BF16 range.  Any common reference point gives the same u / l.
+// Causal attention (key j visible to query i iff j <= i) skips the blocks past the
+// diagonal and masks inside the diagonal block.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "dg_internal.h"
+#include "ptx.cuh"
+
+namespace dg {
+namespace {
+
+constexpr int kBQ = 128, kBKV = 128, kHD = 128;
+constexpr int kThreads = 192;
+constexpr uint32_t kTile = 128 * kHD * 2;  // 128 rows x 128 BF16: two 64-column boxes, 32 KiB
+constexpr uint32_t kHalf = kTile / 2;      // one 128-row x 64-column box (128-byte rows)
+constexpr uint32_t kTmemCols = 512;        // S[0] at 0, S[1] at 128, O at 256
+constexpr uint32_t kOCol = 256;
+constexpr float kMoveLog2 = 8.f;           // move m when the block raises it by > 8 (log2)
+
+// Shared memory: Q | K[2] | V[2] | P[2] (32 KiB each, 1024-byte aligned) | control.
+struct AttnCtl {
+  uint64_t qfull;
+  uint64_t kfull[2], kempty[2], vfull[2], vempty[2];
+  uint64_t sfull[2], pfull[2], odone[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  uint32_t abort;
+};
+static_assert(sizeof(AttnCtl) <= 256, "control block");
+constexpr uint32_t kSmemBytes = 1024 + 7 * kTile + 256;
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// 32 lanes x 32 consecutive 32-bit TMEM columns from registers (thread i -> lane base+i).
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ void load_box(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                         int32_t x, int32_t y, int32_t z, bool rank3) {
+  if (rank3) tma_load_3d(dst, m, bar, x, y, z);
+  else tma_load_2d(dst, m, bar, x, y);
+}
+
+__device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint32_t* status) {
+  uint32_t never = 0;
+  return mbar_wait(bar, parity, &never, status, kDevTimeoutDrain);
+}
+
+// Softmax-warp wait: every lane waits (and acquires), then the warp agrees on the outcome,
+// so the warp-collective TMEM instructions and votes after it never run diverged.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort,
+                                          uint32_t* status) {
+  const bool ok = mbar_wait(bar, parity, abort, status, kDevTimeoutEpilogue);
+  return __all_sync(0xffffffffu, ok);
+}
+
+template <bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    const AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle atoms need 1024-byte alignment
+  const uint32_t sQ = base, sK = base + kTile, sV = base + 3 * kTile, sP = base + 5 * kTile;
+  AttnCtl* ctl = reinterpret_cast<AttnCtl*>(smem_raw + (base - raw) + 7 * kTile);
+  volatile uint32_t* abort = &ctl->abort;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // Work item: causal tiles in decreasing query order, so the longest rows start first.
+  const int64_t id = blockIdx.x;
+  const int64_t qt = p.q_tiles - 1 - id / p.batch;
+  const int64_t b = id % p.batch;
+  const int64_t q0 = qt * kBQ;
+  const int64_t nkv = CAUSAL ? qt + 1 : (p.Lkv + kBKV - 1) / kBKV;
+  const bool rank3 = p.rank3 != 0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&ctl->qfull), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&ctl->kfull[s]), 1);
+      mbar_init(smem_u32(&ctl->kempty[s]), 1);
+      mbar_init(smem_u32(&ctl->vfull[s]), 1);
+      mbar_init(smem_u32(&ctl->vempty[s]), 1);
+      mbar_init(smem_u32(&ctl->sfull[s]), 1);
+      mbar_init(smem_u32(&ctl->pfull[s]), 4);  // one arrival per softmax warp
+      mbar_init(smem_u32(&ctl->odone[s]), 1);
+    }
+    mbar_init(smem_u32(&ctl->drain), 1);
+    ctl->abort = 0;
+    fence_barrier_init();
+    tma_prefetch_map(&tmQ);
+    tma_prefetch_map(&tmK);
+    tma_prefetch_map(&tmV);
+    tma_prefetch_map(&tmO);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  pdl_trigger();
+  pdl_wait();
+
+  const int32_t zb = static_cast<int32_t>(b);
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint32_t qf = smem_u32(&ctl->qfull);
+      mbar_arrive_expect_tx(qf, kTile);
+      load_box(sQ, &tmQ, qf, 0, static_cast<int32_t>(q0), zb, rank3);
+      load_box(sQ + kHalf, &tmQ, qf, 64, static_cast<int32_t>(q0), zb, rank3);
+      int64_t issued = 0;  // blocks whose K and V loads were both issued
+      bool k_only = false; // the last block's K load was issued but not its V load
+      for (int64_t j = 0; j < nkv; ++j) {
+        const uint32_t s = j & 1, ph = (j >> 1) & 1;
+        const int32_t y = static_cast<int32_t>(j * kBKV);
+        if (!mbar_wait(smem_u32(&ctl->kempty[s]), ph ^ 1u, abort, p.status, kDevTimeoutProducer)) break;
+        const uint32_t kf = smem_u32(&ctl->kfull[s]);
+        mbar_arrive_expect_tx(kf, kTile);
+        load_box(sK + s * kTile, &tmK, kf, 0, y, zb, rank3);
+        load_box(sK + s * kTile + kHalf, &tmK, kf, 64, y, zb, rank3);
+        k_only = true;
+        if (!mbar_wait(smem_u32(&ctl->vempty[s]), ph ^ 1u, abort, p.status, kDevTimeoutProducer)) break;
+        const uint32_t vf = smem_u32(&ctl->vfull[s]);
+        mbar_arrive_expect_tx(vf, kTile);
+        load_box(sV + s * kTile, &tmV, vf, 0, y, zb, rank3);
+        load_box(sV + s * kTile + kHalf, &tmV, vf, 64, y, zb, rank3);
+        k_only = false;
+        ++issued;
+      }
+      if (*abort) {
+        // No copy may still be landing in shared memory when the CTA exits: wait for the
+        // last loads issued into each slot (earlier ones were consumed before the reuse).
+        drain_wait(qf, 0, p.status);
+        const int64_t kl = issued + (k_only ? 1 : 0);
+        for (int64_t j = kl > 2 ? kl - 2 : 0; j < kl; ++j)
+          drain_wait(smem_u32(&ctl->kfull[j & 1]), (j >> 1) & 1, p.status);
+        for (int64_t j = issued > 2 ? issued - 2 : 0; j < issued; ++j)
+          drain_wait(smem_u32(&ctl->vfull[j & 1]), (j >> 1) & 1, p.status);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      // S = Q K^T: A = Q and B = K both K-major (d contiguous).  O += P V: A = P K-major
+      // (keys contiguous), B = V N-major (d contiguous, keys along K).
+      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idO = idesc_bf16_f32(128, 128, false, true);
+      bool ok = mbar_wait(smem_u32(&ctl->qfull), 0, abort, p.status, kDevTimeoutMma);
+      auto issue_s = [&](int64_t j) -> bool {
+        const uint32_t s = j & 1, ph = (j >> 1) & 1;
+        if (!mbar_wait(smem_u32(&ctl->kfull[s]), ph, abort, p.status, kDevTimeoutMma)) return false;
+        tc_fence_after();
+        const uint32_t kb = sK + s * kTile;
+#pragma unroll
+        for (int k = 0; k < kHD / 16; ++k) {
+          // 16 columns of d per MMA: 32 bytes inside a 128-byte swizzle row, the second
+          // 64 columns in the second box.
+          const uint32_t off = (k >> 2) * kHalf + (k & 3) * 32;
+          umma_bf16(tmem + s * 128, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                    idS, k > 0 ? 1u : 0u);
+        }
+        umma_commit(smem_u32(&ctl->kempty[s]));
+        umma_commit(smem_u32(&ctl->sfull[s]));
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      if (ok && nkv > 1) ok = issue_s(1);
+      for (int64_t j = 0; ok && j < nkv; ++j) {
+        const uint32_t s = j & 1, ph = (j >> 1) & 1;
+        if (!mbar_wait(smem_u32(&ctl->pfull[s]), ph, abort, p.status, kDevTimeoutMma) ||
+            !mbar_wait(smem_u32(&ctl->vfull[s]), ph, abort, p.status, kDevTimeoutMma)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t pb = sP + s * kTile, vb = sV + s * kTile;
+#pragma unroll
+        for (int k = 0; k < kBKV / 16; ++k) {
+          // P: 16 keys = 32 bytes in the swizzle row (second box for keys 64..127).
+          // V: 16 key rows = 2 KiB; its two 64-column halves of d are one box apart (LBO).
+          const uint64_t adesc = sdesc_sw128(pb + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
+          const uint64_t bdesc = sdesc_sw128(vb + k * 2048, kHalf, 1024);
+          umma_bf16(tmem + kOCol, adesc, bdesc, idO, (j > 0 || k > 0) ? 1u : 0u);
+        }
+        umma_commit(smem_u32(&ctl->vempty[s]));
+        umma_commit(smem_u32(&ctl->odone[s]));
+        if (j + 2 < nkv) ok = issue_s(j + 2);
+      }
+      // Every MMA finished before TMEM is released.
+      umma_commit(smem_u32(&ctl->drain));
+      drain_wait(smem_u32(&ctl->drain), 0, p.status);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int qd = warp & 3;                 // TMEM lane quadrant this warp may access
+    const int row = qd * 32 + lane;          // query row in the tile = TMEM lane
+    const int64_t qrow = q0 + row;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(qd * 32) << 16);
+    const uint32_t swz = static_cast<uint32_t>(row & 7);
+    const uint32_t prow = static_cast<uint32_t>((row >> 3) * 1024 + (row & 7) * 128);
+    const float cl = p.c_log2;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int64_t j = 0; j < nkv; ++j) {
+      const uint32_t s = j & 1, ph = (j >> 1) & 1;
+      if (!warp_wait(smem_u32(&ctl->sfull[s]), ph, abort, p.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sv[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tl + s * 128 + c * 32, sv[c]);
+      tmem_ld_wait();
+      const int64_t kv0 = j * kBKV;
+      if (kv0 + kBKV > p.Lkv || (CAUSAL && j == nkv - 1)) {
+        // Keys at or past `lim` are not visible to this row: weight 0.
+        const int64_t lim = CAUSAL ? (qrow + 1 < p.Lkv ? qrow + 1 : p.Lkv) : p.Lkv;
+        const int64_t nv = lim - kv0;
+        const int nvis = nv < 0 ? 0 : (nv > kBKV ? kBKV : static_cast<int>(nv));
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            if (c * 32 + k >= nvis) sv[c][k] = 0xFF800000u;  // -inf
+      }
+      float mx8[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) mx8[t] = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int k = 0; k < 32; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], __uint_as_float(sv[c][k]));
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const float m_blk = mx * cl;  // the block's maximum in log2 units (scale > 0)
+      float r = 1.f;
+      if (m_blk > m_run + kMoveLog2) {
+        r = ex2(m_run - m_blk);  // 0 on the first block (m_run = -inf)
+        m_run = m_blk;
+      }
+      const bool rescale = j > 0 && __any_sync(0xffffffffu, r != 1.f);
+      const float nb = (m_run == -INFINITY) ? 0.f : -m_run;
+      // P buffer s is free once P V of block j - 2 has completed.
+      if (j >= 2 && !warp_wait(smem_u32(&ctl->odone[s]), ((j - 2) >> 1) & 1, abort, p.status)) {
+        ok = false;
+        break;
+      }
+      float ls8[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) ls8[t] = 0.f;
+      const uint32_t pb = sP + s * kTile + prow;
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i0 = h * 64 + c8 * 8 + 2 * e;
+            const float p0 = ex2(fmaf(__uint_as_float(sv[i0 >> 5][i0 & 31]), cl, nb));
+            const float p1 = ex2(fmaf(__uint_as_float(sv[(i0 + 1) >> 5][(i0 + 1) & 31]), cl, nb));
+            ls8[(c8 & 1) * 4 + e] += p0 + p1;
+            w[e] = pack2(p0, p1);
+          }
+          // Row `row` of the 128B-swizzled K-major tile: 16-byte chunk c8 of box h.
+          st_shared_v4(pb + h * kHalf + ((static_cast<uint32_t>(c8) ^ swz) << 4), w[0], w[1],
+                       w[2], w[3]);
+        }
+      const float lsum = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
+      l_run = l_run * r + lsum;
+      fence_proxy_async_smem();  // P is read by the MMA (async proxy)
+      if (rescale) {
+        // The reference point moved: scale the accumulated row of O by r once P V of block
+        // j - 1 has landed in TMEM (lanes whose point did not move multiply by 1).
+        if (!warp_wait(smem_u32(&ctl->odone[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(tl + kOCol + c * 32, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * r);
+          tmem_st_32x32b_x32(tl + kOCol + c * 32, o);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->pfull[s]));
+    }
+    if (ok) {
+      const int64_t jl = nkv - 1;
+      ok = warp_wait(smem_u32(&ctl->odone[jl & 1]), (jl >> 1) & 1, abort, p.status);
+    }
+    if (ok) {
+      // O = u / l, rounded once to BF16, staged in the (no longer read) Q tile in the
+      // layout of the output tensor map's 128B-swizzled boxes.
+      tc_fence_after();
+      const float inv = 1.f / l_run;
+      const uint32_t ob = sQ + prow;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld_32x32b_x32(tl + kOCol + c * 32, o);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const uint32_t chunk = static_cast<uint32_t>((c & 1) * 4 + q4);
+          const float* f = reinterpret_cast<const float*>(o) + 8 * q4;
+          st_shared_v4(ob + (c >> 1) * kHalf + ((chunk ^ swz) << 4), pack2(f[0] * inv, f[1] * inv),
+                       pack2(f[2] * inv, f[3] * inv), pack2(f[4] * inv, f[5] * inv),
+                       pack2(f[6] * inv, f[7] * inv));
+        }
+      }
+      fence_proxy_async_smem();
+    }
+    softmax_bar();
+    if (warp == 2 && lane == 0 && !*abort) {
+      // Rows past Lq are clipped by the tensor map.
+      if (rank3) {
+        tma_store_3d(&tmO, sQ, 0, static_cast<int32_t>(q0), zb);
+        tma_store_3d(&tmO, sQ + kHalf, 64, static_cast<int32_t>(q0), zb);
+      } else {
+        tma_store_2d(&tmO, sQ, 0, static_cast<int32_t>(q0));
+        tma_store_2d(&tmO, sQ + kHalf, 64, static_cast<int32_t>(q0));
+      }
+      bulk_commit();
+      bulk_wait<0>();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+std::atomic<uint64_t> g_attr_done[2];
+
+template <bool CAUSAL>
+cudaError_t launch_variant(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                           const CUtensorMap& mo, const AttnParams& p, cudaStream_t s) {
+  auto kern = attn_fwd_kernel<CAUSAL>;
+  cudaError_t e = ensure_smem_attr(kern, static_cast<int>(kSmemBytes), g_attr_done[CAUSAL ? 1 : 0]);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(static_cast<unsigned>(p.batch * p.q_tiles));
+  return launch_pdl(kern, grid, dim3(kThreads), kSmemBytes, s, mq, mk, mv, mo, p);
+}
+
+}  // namespace
+
+cudaError_t launch_attention(const AttnParams& p, bool causal, const void* Q, int64_t ldq,
+                             int64_t sQ, const void* K, int64_t ldk, int64_t sK, const void* V,
+                             int64_t ldv, int64_t sV, void* O, int64_t ldo, int64_t sO,
+                             cudaStream_t s) {
+  const uint64_t batch = static_cast<uint64_t>(p.batch);
+  CUtensorMap mq, mk, mv, mo;
+  // Every operand is a (batch x) rows x 128 row-major BF16 view read or written in boxes of
+  // 128 rows x 64 columns (128-byte rows, 128-byte swizzle).
+  auto map = [&](CUtensorMap* m, const void* ptr, int64_t rows, int64_t ld, int64_t stride) {
+    return make_tile_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, kHD,
+                         static_cast<uint64_t>(rows), static_cast<uint64_t>(ld), batch,
+                         static_cast<uint64_t>(stride), 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, 1);
+  };
+  if (!map(&mq, Q, p.Lq, ldq, sQ) || !map(&mk, K, p.Lkv, ldk, sK) || !map(&mv, V, p.Lkv, ldv, sV) ||
+      !map(&mo, O, p.Lq, ldo, sO))
+    return cudaErrorInvalidValue;
+  return causal ? launch_variant<true>(mq, mk, mv, mo, p, s)
+                : launch_variant<false>(mq, mk, mv, mo, p, s);
+}
+
+}  // namespace dg

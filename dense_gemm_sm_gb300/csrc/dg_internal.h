@@ -1,5 +1,6 @@
 // dg_internal.h -- declarations shared by the C-ABI layer and the kernel translation units.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -95,6 +96,26 @@ cudaError_t launch_gemm_thin(const ThinParams& p, int ntok, const void* X, int64
                              const void* W, int64_t ldw, bool w_kmajor, cudaStream_t s);
 constexpr int kThinBN = 128, kThinBK = 64;
 inline int64_t thin_ws_floats(int64_t ctas, int ntok) { return ctas * 2 * ntok * 128; }
+
+// ------------------------------------------------------------------ fused attention
+struct AttnParams {
+  int64_t batch, Lq, Lkv;
+  int64_t q_tiles;     // ceil(Lq / 128)
+  float c_log2;        // scale * log2(e)
+  int32_t rank3;       // batch > 1: 3-D tensor maps
+  uint32_t* status;
+};
+// Q, O: [batch][Lq][ld] bf16; K, V: [batch][Lkv][ld] bf16 (d = 128 contiguous columns).
+cudaError_t launch_attention(const AttnParams& p, bool causal, const void* Q, int64_t ldq,
+                             int64_t sQ, const void* K, int64_t ldk, int64_t sK, const void* V,
+                             int64_t ldv, int64_t sV, void* O, int64_t ldo, int64_t sO,
+                             cudaStream_t s);
+
+// Tensor map over a (batch x) outer x inner row-major view (cached by address, shape, box).
+bool make_tile_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t esz, const void* base,
+                   uint64_t inner, uint64_t outer, uint64_t ld, uint64_t batch, uint64_t stride,
+                   uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle,
+                   uint32_t box_batch);
 
 // ------------------------------------------------------------------ misc
 // C = beta * C over a (batch, M, N) strided view (K == 0 or alpha == 0).

@@ -15,6 +15,10 @@ Workloads (shapes and distributions from the FFN running example of
   decode_bf16    X[M,4096] ~ N(0,1), same W, M in {1,4,16}
   bf16_square    BF16 4096^3 with the same operand distributions
   qk_batched     64 x (Q[2048,128] . K[2048,128]^T), alpha=fp32(1/sqrt(128)), FP32 out
+  ffn_gate_up    X[1024,4096] ~ N(0,1), W_g, W_u [4096,12288] ~ N(0,1/4096), BF16
+  attention      Q, K, V [batch, L, 128] ~ N(0,1) BF16, scale fp32(1/sqrt(128)); the batched
+                 shape (64 heads x 2048) and one causal head of 8192 ("Operator & Runtime",
+                 section 5.3.3)
 """
 from __future__ import annotations
 
@@ -151,3 +155,15 @@ def qk_batched(batch=64, S=2048, D=128) -> dict:
     return dict(M=S, N=S, K=D, batch=batch, alpha=np.float32(1.0 / np.sqrt(np.float32(D))),
                 beta=np.float32(0.0), A=Q, lda=D, strideA=S * D, B=Kt, ldb=D, strideB=S * D,
                 op_b=1, C0=None, ldc=S, strideC=S * S)
+
+
+def attention(batch=64, L=2048, d=128, causal=False, Lkv=None, std_q=1.0) -> dict:
+    """Q [batch, L, d], K and V [batch, Lkv, d] ~ N(0,1) BF16 (Q scaled by std_q), contiguous."""
+    s = BASE_SEED + 8 + (1 if causal else 0)
+    Lkv = L if Lkv is None else Lkv
+    Q = f32_to_bf16_bits(normal_f32(s, (batch, L, d), std=std_q))
+    K = f32_to_bf16_bits(normal_f32(s + 100, (batch, Lkv, d)))
+    V = f32_to_bf16_bits(normal_f32(s + 200, (batch, Lkv, d)))
+    return dict(batch=batch, Lq=L, Lkv=Lkv, d=d, causal=causal,
+                scale=np.float32(1.0 / np.sqrt(np.float32(d))), Q=Q, ldq=d, sQ=L * d, K=K, ldk=d,
+                sK=Lkv * d, V=V, ldv=d, sV=Lkv * d, ldo=d, sO=L * d)

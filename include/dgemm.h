@@ -155,6 +155,36 @@ dg_status gemm_bf16_gate_up_silu(int64_t M, int64_t N, int64_t K, const uint16_t
                                  const uint16_t* Wg, int64_t ldwg, const uint16_t* Wu,
                                  int64_t ldwu, uint16_t* Z, int64_t ldz, void* stream);
 
+/*
+ * Fused attention forward ("Operator & Runtime" section 5.3.3: S = Q K^T / sqrt(d),
+ * P = softmax(S) row by row, O = P V, computed block by block with the online softmax so
+ * that S and P never reach memory), over a strided batch of heads:
+ *     O[b][i][:] = sum_j softmax_j(scale * Q[b][i][:] . K[b][j][:]) V[b][j][:]
+ * for b < batch, i < Lq, over the keys j < Lkv visible to query i (all of them, or j <= i
+ * when `causal` is non-zero).  BF16 inputs, FP32 scores, weights and accumulation, the
+ * weights rounded to BF16 for the P V product, O rounded once to BF16 (nearest-even).
+ *   - Layout: row-major, element (b, i, c) of Q at Q[b * strideQ + i * ldq + c], likewise
+ *     K, V (Lkv rows) and O (Lq rows); c < d.  Only d = 128 is implemented.
+ *   - scale: the factor applied to the scores (1/sqrt(d) for the standard form); must be
+ *     finite and > 0.
+ *   - causal requires Lq == Lkv (queries and keys of one sequence).
+ *   - Device pointers owned by the caller; O must not alias the inputs, and the batch
+ *     entries of O must not overlap (strideO >= Lq * ldo when batch > 1; likewise the
+ *     strides of the inputs are at least L * ld).
+ *   - Errors: negative sizes, Lkv == 0 (softmax over no keys), ld < d, overlapping batch
+ *     strides, causal with Lq != Lkv, or a scale that is not finite and positive:
+ *     DG_ERR_INVALID_ARG.  d != 128, or Lq, Lkv >= 2^31: DG_ERR_UNSUPPORTED.  Base
+ *     pointers not 16-byte aligned, or ld / strides not multiples of 8 elements:
+ *     DG_ERR_MISALIGNED.  batch == 0 or Lq == 0: nothing.  Nothing is enqueued on an error.
+ *   - Enqueued on `stream`; allocates nothing.  A kernel that gives up a bounded wait
+ *     reports DG_ERR_TIMEOUT through dg_device_status.
+ */
+dg_status attention_bf16(int64_t batch, int64_t Lq, int64_t Lkv, int64_t d, float scale,
+                         int32_t causal, const uint16_t* Q, int64_t ldq, int64_t strideQ,
+                         const uint16_t* K, int64_t ldk, int64_t strideK, const uint16_t* V,
+                         int64_t ldv, int64_t strideV, uint16_t* O, int64_t ldo, int64_t strideO,
+                         void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* dg_status_string(dg_status s);
 
