@@ -5,7 +5,7 @@ One "step" is one call of the library's public C ABI on one batch of synthetic i
 (resident in HBM).  The default workload is the FP32 SGEMM M = N = K = 4096,
 alpha = 1, beta = 0.5; --workload picks another of the path's configurations
 (ffn_bf16, ffn_gate_up, bf16_4096, decode_m1 / decode_m4 / decode_m16, qk_batched,
-attn_batched, attn_causal_8k, sgemm_ragged, sgemm_256).
+attn_batched, attn_causal_8k, fp8_ffn, fp8_quant_gemm, sgemm_ragged, sgemm_256).
 
 Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier and
 torch.cuda.synchronize() on both sides, CUDA events on the launching stream; rotating
@@ -131,6 +131,20 @@ class Workload:
                         kernel="attn_fwd_kernel", sources=["attention.cu"] + COMMON_SOURCES,
                         desc=f"fused attention O=softmax(QK^T/sqrt(d))V heads={b} L={L} d={d} "
                              f"{'causal' if causal else 'non-causal'}, BF16 in/out, FP32 accumulate")
+        if name in ("fp8_ffn", "fp8_quant_gemm"):
+            # fp8_ffn: the FFN shape on resident E4M3 codes; fp8_quant_gemm: the pages' FP8
+            # example (A BF16 [4096, 4096] quantised per row each step, then the GEMM with
+            # resident E4M3 weights [1536, 4096]); both BF16 out.
+            w = inputs.fp8_gemm() if name == "fp8_ffn" else inputs.fp8_gemm(4096, 1536, 4096)
+            M, N, K = w["M"], w["N"], w["K"]
+            quant = name == "fp8_quant_gemm"
+            return dict(kind="fp8", w=dict(w, quant=quant), batch=1, flops=2.0 * M * N * K,
+                        algo_bytes=(M * K + K * N + 2.0 * M * N + (3.0 * M * K if quant else 0.0)),
+                        bound="tensor8", unit="TFLOPS", kernel="gemm_tc_kernel",
+                        sources=["gemm_tc.cu", "quant.cu"] + COMMON_SOURCES,
+                        desc=(f"FP8 E4M3 GEMM C=diag(sa)(A B^T)diag(sb) M={M} N={N} K={K}, "
+                              f"FP32 accumulate, BF16 out"
+                              + (", per-row quantisation of BF16 A inside each step" if quant else "")))
         if name == "bf16_4096":
             w = inputs.bf16_square(4096)
             M, N, K = w["M"], w["N"], w["K"]
@@ -164,6 +178,24 @@ class Workload:
             copies = min(copies, 8)
         self.copies = copies
         self.bufs = []
+        if self.kind == "fp8":
+            # Resident codes and scales, made by the library's own quantiser (setup, untimed).
+            M, N, K = w["M"], w["N"], w["K"]
+            dev = lambda bits: torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+            for i in range(copies):
+                X, Wt = dev(w["X"]), dev(w["W"])
+                A = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+                SA = torch.empty((M,), dtype=torch.float32, device="cuda")
+                B = torch.empty((N, K), dtype=torch.uint8, device="cuda")
+                SB = torch.empty((N,), dtype=torch.float32, device="cuda")
+                self.dg.quantize_rows_e4m3(M, K, X, K, A, K, SA)
+                self.dg.quantize_rows_e4m3(N, K, Wt, K, B, K, SB)
+                del Wt
+                C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+                self.bufs.append(((A, SA, X), (B, SB), C))
+            torch.cuda.synchronize()
+            self.stream = torch.cuda.current_stream().cuda_stream
+            return
         if self.kind == "f32":
             for i in range(copies):
                 A = torch.from_numpy(w["A"]).cuda()
@@ -200,6 +232,12 @@ class Workload:
             kn = w["K"] * w["N"]
             dg.gemm_bf16_gate_up_silu(w["M"], w["N"], w["K"], A, w["lda"], B, w["ldb"],
                                       B.data_ptr() + 2 * kn, w["ldb"], C, w["ldc"], stream=s)
+        elif self.kind == "fp8":
+            (qa, sa, X), (qb, sb) = A, B
+            M, N, K = w["M"], w["N"], w["K"]
+            if w["quant"]:
+                dg.quantize_rows_e4m3(M, K, X, K, qa, K, sa, stream=s)
+            dg.gemm_fp8_e4m3(M, N, K, qa, K, sa, qb, K, sb, C, N, dg.DG_OUT_BF16, stream=s)
         elif self.kind == "attn":
             kv = w["batch"] * w["Lkv"] * w["d"]
             dg.attention_bf16(w["batch"], w["Lq"], w["Lkv"], w["d"], float(w["scale"]), w["causal"],
@@ -226,6 +264,12 @@ class Workload:
             unit = "TFLOP/s"
             note = (f"FP32 CUDA-core peak = {SM_COUNT_NOMINAL} SMs x {FP32_LANES_PER_SM} FMA/clk x 2 "
                     f"x {peaks['sm_max_mhz']:.0f} MHz")
+        elif self.bound == "tensor8":
+            peak = 2.0 * peaks["bf16_sustained"]
+            achieved = self.flops / sec_per_launch / 1e12
+            unit = "TFLOP/s"
+            note = (f"fp8 dense = 2 x the bf16 sustained cuBLAS figure of {peaks['source']} peaks "
+                    f"(nominal fp8 / bf16 ratio 4.5 / 2.25)")
         elif self.bound == "tensor":
             peak = peaks["bf16_sustained"]
             achieved = self.flops / sec_per_launch / 1e12
@@ -240,7 +284,8 @@ class Workload:
         t = MEASURED_TRAFFIC.get(self.name)
         if t and t["source_hash"] == kernel_source_hash(self.sources):
             traffic = t["bytes_per_launch"]
-        return {"bound": self.bound, "achieved": round(achieved, 3), "peak": round(peak, 1),
+        return {"bound": "tensor" if self.bound == "tensor8" else self.bound,
+                "achieved": round(achieved, 3), "peak": round(peak, 1),
                 "unit": unit, "frac": round(achieved / peak, 4), "traffic": traffic,
                 "kernel": self.kernel, "algorithmic": {"flops": self.flops, "bytes": self.algo_bytes},
                 "peak_note": note}
@@ -391,6 +436,8 @@ def time_e2e(torch, wl, steps, warmup):
     """Same workload through the public API with host inputs: each step copies that step's
     inputs from pinned host memory, calls the library and reads the result back."""
     w = wl.w
+    if wl.kind == "fp8":
+        return None  # the FP8 lines are suite entries: device-resident codes only
     A0, B0, C0 = wl.bufs[0]
     hA = A0.cpu().pin_memory()
     hB = B0.cpu().pin_memory()
@@ -596,7 +643,7 @@ def main():
         "metric": METRIC, "value": round(value, 3), "unit": wl.unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32" if wl.kind == "f32" else "bf16",
+        "dtype": {"f32": "f32", "fp8": "e4m3"}.get(wl.kind, "bf16"),
         "data": "synthetic (seeded PCG64; shapes and distributions of the pages' workloads)",
         "config": {"workload": args.workload, "desc": wl.desc,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -610,8 +657,8 @@ def main():
     if not args.no_suite:
         suite = {}
         for name in ("ffn_bf16", "ffn_gate_up", "bf16_4096", "decode_m1", "decode_m4",
-                     "decode_m16", "qk_batched", "attn_batched", "attn_causal_8k", "sgemm_ragged",
-                     "sgemm_256"):
+                     "decode_m16", "qk_batched", "attn_batched", "attn_causal_8k", "fp8_ffn",
+                     "fp8_quant_gemm", "sgemm_ragged", "sgemm_256"):
             if name == args.workload:
                 continue
             other = Workload(name, torch, dg, inputs)

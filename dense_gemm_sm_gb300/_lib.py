@@ -25,7 +25,7 @@ EXPORTED = [
     "dg_status_string", "dg_device_status", "dg_release_workspace", "dg_plan_gemm",
     "dg_raster_tile", "dg_streamk_start", "dg_model_traffic_bytes", "dg_model_local_bytes",
     "dg_version", "dg_set_fault_injection", "gemm_bf16_decode_noalloc", "gemm_bf16_gate_up_silu",
-    "attention_bf16",
+    "attention_bf16", "quantize_rows_e4m3", "gemm_fp8_e4m3", "dg_model_quant_traffic_bytes",
 ]
 
 
@@ -75,12 +75,15 @@ def load(build_if_missing: bool = True):
     lib.gemm_bf16_strided_batched.argtypes = [i64, i64, i64, f32, vp, i64, i64, vp, i64, i64, i32,
                                               f32, vp, i64, i64, i64, i32, vp]
     lib.gemm_bf16_gate_up_silu.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp]
+    lib.quantize_rows_e4m3.argtypes = [i64, i64, vp, i64, vp, i64, vp, vp]
+    lib.gemm_fp8_e4m3.argtypes = [i64, i64, i64, vp, i64, vp, vp, i64, vp, vp, i64, i32, vp]
     lib.attention_bf16.argtypes = [i64, i64, i64, i64, f32, i32, vp, i64, i64, vp, i64, i64, vp,
                                    i64, i64, vp, i64, i64, vp]
     lib.gemm_bf16_decode_noalloc.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64,
                                              i32, vp]
     for f in ("gemm_f32", "gemm_f32_strided_batched", "gemm_bf16", "gemm_bf16_strided_batched",
-              "gemm_bf16_decode_noalloc", "gemm_bf16_gate_up_silu", "attention_bf16"):
+              "gemm_bf16_decode_noalloc", "gemm_bf16_gate_up_silu", "attention_bf16",
+              "quantize_rows_e4m3", "gemm_fp8_e4m3"):
         getattr(lib, f).restype = ctypes.c_int
     lib.dg_status_string.argtypes = [ctypes.c_int]
     lib.dg_status_string.restype = ctypes.c_char_p
@@ -99,6 +102,8 @@ def load(build_if_missing: bool = True):
     lib.dg_model_traffic_bytes.restype = ctypes.c_double
     lib.dg_model_local_bytes.argtypes = [i64, i64, i64, i32]
     lib.dg_model_local_bytes.restype = i64
+    lib.dg_model_quant_traffic_bytes.argtypes = [i64, i64, i64, i64, i64, i32, i32, i32, i32]
+    lib.dg_model_quant_traffic_bytes.restype = ctypes.c_double
     lib.dg_version.argtypes = []
     lib.dg_version.restype = ctypes.c_char_p
     lib.dg_set_fault_injection.argtypes = [i32]
@@ -182,6 +187,23 @@ def gemm_bf16_gate_up_silu(M, N, K, X, ldx, Wg, ldwg, Wu, ldwu, Z, ldz, stream=N
     return _ret(st, "gemm_bf16_gate_up_silu", check)
 
 
+def quantize_rows_e4m3(rows, cols, X, ldx, Q, ldq, scales, stream=None, check=True) -> int:
+    """Per-row FP8 E4M3 quantisation of BF16 X: codes Q and float32 scales (amax / 448)."""
+    lib = load()
+    st = lib.quantize_rows_e4m3(rows, cols, _ptr(X), ldx, _ptr(Q), ldq, _ptr(scales),
+                                _stream(stream))
+    return _ret(st, "quantize_rows_e4m3", check)
+
+
+def gemm_fp8_e4m3(M, N, K, A, lda, scale_a, B, ldb, scale_b, C, ldc, c_type=DG_OUT_BF16,
+                  stream=None, check=True) -> int:
+    """C = diag(scale_a) (A B^T) diag(scale_b) for E4M3 codes A [M, K] and B [N, K]."""
+    lib = load()
+    st = lib.gemm_fp8_e4m3(M, N, K, _ptr(A), lda, _ptr(scale_a), _ptr(B), ldb, _ptr(scale_b),
+                           _ptr(C), ldc, c_type, _stream(stream))
+    return _ret(st, "gemm_fp8_e4m3", check)
+
+
 def attention_bf16(batch, Lq, Lkv, d, scale, causal, Q, ldq, strideQ, K, ldk, strideK, V, ldv,
                    strideV, O, ldo, strideO, stream=None, check=True) -> int:
     """O = softmax(scale * Q K^T) V per head (fused, online softmax), BF16 in and out."""
@@ -231,6 +253,12 @@ def dg_model_traffic_bytes(M, N, K, tile_m, tile_n, elem_bytes=2, out_bytes=2) -
 
 def dg_model_local_bytes(tile_m, tile_n, tile_k, elem_bytes=2) -> int:
     return load().dg_model_local_bytes(tile_m, tile_n, tile_k, elem_bytes)
+
+
+def dg_model_quant_traffic_bytes(M, K, N, tile_m, tile_n, in_bytes=2, q_bytes=1, out_bytes=2,
+                                 fused=False) -> float:
+    return load().dg_model_quant_traffic_bytes(M, K, N, tile_m, tile_n, in_bytes, q_bytes,
+                                               out_bytes, 1 if fused else 0)
 
 
 def dg_version() -> str:

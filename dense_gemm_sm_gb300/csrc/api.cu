@@ -162,8 +162,8 @@ void plan_f32(int64_t M, int64_t N, int64_t K, int64_t batch, int64_t resident, 
 // dual: the FFN gate/up form, planned as one GEMM over [W_g | W_u] (N = 2 x the output
 // columns): always the tile kernel, 256-column tiles (128 output columns).
 void plan_bf16(int64_t M, int64_t N, int64_t K, int64_t batch, int sms, dg_plan* pl,
-               bool dual = false) {
-  if (!dual && batch == 1 && M <= kThinMaxM) {
+               bool dual = false, bool fp8 = false) {
+  if (!dual && !fp8 && batch == 1 && M <= kThinMaxM) {
     pl->kernel = DG_KERNEL_THIN_BF16;
     pl->ntok = M <= 16 ? 16 : 32;
     pl->tile_m = pl->ntok;
@@ -185,7 +185,7 @@ void plan_bf16(int64_t M, int64_t N, int64_t K, int64_t batch, int sms, dg_plan*
   // costs more than the better wave fill they buy), so 128 is used only when N <= 128.
   int bn = N <= 128 && !dual ? 128 : 256;
   // Tuning override (bench and sweeps): DG_TC_BN=256|224|192|128 forces the tile width.
-  if (const char* e = dual ? nullptr : std::getenv("DG_TC_BN")) {
+  if (const char* e = (dual || fp8) ? nullptr : std::getenv("DG_TC_BN")) {
     const int f = std::atoi(e);
     if (f == 256 || f == 224 || f == 192 || f == 128) bn = f;
   }
@@ -196,7 +196,9 @@ void plan_bf16(int64_t M, int64_t N, int64_t K, int64_t batch, int sms, dg_plan*
   pl->group = kRasterGroup;
   pl->tiles = batch * cdiv(M, kTcBM) * cdiv(N, bn);
   pl->grid = pl->tiles < sms ? pl->tiles : sms;
-  pl->kblocks = cdiv(K, kTcBK);
+  // A stage row is 128 bytes: 64 BF16 or 128 FP8 elements of K.
+  pl->tile_k = fp8 ? 2 * kTcBK : kTcBK;
+  pl->kblocks = cdiv(K, pl->tile_k);
   // CTA pairs (tcgen05 cta_group::2, 256 x 256 tiles) for one problem with at least two
   // 128-row tile rows: each SM then moves half the B bytes per FLOP through its shared
   // memory, which bounds the single-CTA tile.  DG_TC_PAIR=0 keeps single CTAs (sweeps).
@@ -348,7 +350,8 @@ dg_status run_tile(const dg_plan& pl, int64_t M, int64_t N, int64_t K, int64_t b
                    float beta, const uint16_t* A, int64_t lda, int64_t sA, const uint16_t* B,
                    int64_t ldb, int64_t sB, dg_op op_b, void* C, int64_t ldc, int64_t sC,
                    bool c_f32, bool c_vec, uint32_t* status, int dev, cudaStream_t s,
-                   const uint16_t* B2, int64_t ldb2) {
+                   const uint16_t* B2, int64_t ldb2, const float* scale_a = nullptr,
+                   const float* scale_b = nullptr) {
   dg_status st = DG_OK;
   TcParams p;
   p.M = M; p.N = N; p.K = K;
@@ -370,6 +373,8 @@ dg_status run_tile(const dg_plan& pl, int64_t M, int64_t N, int64_t K, int64_t b
   p.sk_ctas = pl.tail_tiles > 0 ? pl.splits : 0;
   p.ws = nullptr;
   p.counters = nullptr;
+  p.scale_a = scale_a;
+  p.scale_b = scale_b;
   if (p.sk_tiles > 0) {
     Workspace w;
     const int64_t per = pair ? 2 : 1;
@@ -381,7 +386,7 @@ dg_status run_tile(const dg_plan& pl, int64_t M, int64_t N, int64_t K, int64_t b
   }
   return from_cuda(launch_gemm_tc(p, pl.tile_n, A, lda, batch > 1 ? sA : 0, B, ldb,
                                   batch > 1 ? sB : 0, op_b == DG_OP_T, pair,
-                                  static_cast<int>(pl.grid), s, B2, ldb2));
+                                  static_cast<int>(pl.grid), s, B2, ldb2, scale_a != nullptr));
 }
 
 
@@ -539,6 +544,49 @@ dg_status gemm_bf16_gate_up_silu(int64_t M, int64_t N, int64_t K, const uint16_t
                   c_vec, status, dev, s, Wu, ldwu);
 }
 
+dg_status quantize_rows_e4m3(int64_t rows, int64_t cols, const uint16_t* X, int64_t ldx,
+                             uint8_t* Q, int64_t ldq, float* scales, void* stream) {
+  if (rows < 0 || cols < 0) return DG_ERR_INVALID_ARG;
+  if (rows == 0) return DG_OK;
+  if (ldx < cols || ldq < cols || !scales || (cols > 0 && (!X || !Q))) return DG_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int dev = 0;
+  if (current_device(&dev) != cudaSuccess) return DG_ERR_CUDA;
+  uint32_t* status = nullptr;
+  int sms = 0;
+  if (device_info(dev, &status, &sms) != cudaSuccess) return DG_ERR_CUDA;
+  const bool vec = aligned16(X) && aligned16(Q) && ldx % 8 == 0 && ldq % 16 == 0;
+  return from_cuda(launch_quantize_rows(rows, cols, X, ldx, Q, ldq, scales, vec, sms, s));
+}
+
+dg_status gemm_fp8_e4m3(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda,
+                        const float* scale_a, const uint8_t* B, int64_t ldb, const float* scale_b,
+                        void* C, int64_t ldc, dg_out c_type, void* stream) {
+  if (M < 0 || N < 0 || K < 0) return DG_ERR_INVALID_ARG;
+  if (c_type != DG_OUT_BF16 && c_type != DG_OUT_F32) return DG_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return DG_OK;
+  if (ldc < N || !C || (K > 0 && (lda < K || ldb < K || !A || !B || !scale_a || !scale_b)))
+    return DG_ERR_INVALID_ARG;
+  const bool c_f32 = c_type == DG_OUT_F32;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int dev = 0;
+  if (current_device(&dev) != cudaSuccess) return DG_ERR_CUDA;
+  uint32_t* status = nullptr;
+  int sms = 0;
+  if (device_info(dev, &status, &sms) != cudaSuccess) return DG_ERR_CUDA;
+  if (K == 0) return run_scale(C, c_f32, M, N, ldc, 0, 1, 0.f, s);  // empty sums: C = 0
+  if (!aligned16(A) || !aligned16(B) || lda % 16 != 0 || ldb % 16 != 0 || !aligned16(scale_b) ||
+      (reinterpret_cast<uintptr_t>(scale_a) & 3u) != 0)
+    return DG_ERR_MISALIGNED;
+  dg_plan pl;
+  plan_bf16(M, N, K, 1, sms, &pl, false, true);
+  log_plan("gemm_fp8_e4m3", M, N, K, 1, pl);
+  const bool c_vec = aligned16(C) && (ldc * (c_f32 ? 4 : 2)) % 16 == 0;
+  return run_tile(pl, M, N, K, 1, 1.f, 0.f, reinterpret_cast<const uint16_t*>(A), lda, 0,
+                  reinterpret_cast<const uint16_t*>(B), ldb, 0, DG_OP_T, C, ldc, 0, c_f32, c_vec,
+                  status, dev, s, nullptr, 0, scale_a, scale_b);
+}
+
 dg_status attention_bf16(int64_t batch, int64_t Lq, int64_t Lkv, int64_t d, float scale,
                          int32_t causal, const uint16_t* Q, int64_t ldq, int64_t strideQ,
                          const uint16_t* K, int64_t ldk, int64_t strideK, const uint16_t* V,
@@ -665,6 +713,18 @@ double dg_model_traffic_bytes(int64_t M, int64_t N, int64_t K, int64_t tile_m, i
                               int32_t elem_bytes, int32_t out_bytes) {
   const double e = elem_bytes, Md = M, Nd = N, Kd = K;
   return e * Md * Kd * (Nd / tile_n) + e * Kd * Nd * (Md / tile_m) + out_bytes * Md * Nd;
+}
+
+double dg_model_quant_traffic_bytes(int64_t M, int64_t K, int64_t N, int64_t tile_m,
+                                    int64_t tile_n, int32_t in_bytes, int32_t q_bytes,
+                                    int32_t out_bytes, int32_t fused) {
+  const double Md = M, Kd = K, Nd = N;
+  const double col_blocks = Nd / tile_n, row_blocks = Md / tile_m;
+  // Both schedules read the input once for the row maxima; then either write the codes and
+  // let every column block read them, or let every column block re-read the input.
+  const double input = fused ? in_bytes * Md * Kd + col_blocks * in_bytes * Md * Kd
+                             : in_bytes * Md * Kd + q_bytes * Md * Kd + col_blocks * q_bytes * Md * Kd;
+  return input + row_blocks * q_bytes * Kd * Nd + out_bytes * Md * Nd;
 }
 
 int64_t dg_model_local_bytes(int64_t tile_m, int64_t tile_n, int64_t tile_k, int32_t elem_bytes) {

@@ -64,6 +64,9 @@ struct TcParams {
   int32_t sk_ctas;
   float* ws;
   uint32_t* counters;
+  // FP8 (E4M3) operands: C = acc * scale_a[row] * scale_b[column] (null otherwise).
+  const float* scale_a;
+  const float* scale_b;
 };
 inline int64_t tc_ws_floats(int64_t sk_ctas, int bn) { return sk_ctas * 2 * 128 * bn; }
 // A: [batch][M][lda] bf16 (K contiguous).  B: op N -> [batch][K][ldb] (N contiguous),
@@ -72,10 +75,12 @@ inline int64_t tc_ws_floats(int64_t sk_ctas, int bn) { return sk_ctas * 2 * 128 
 // batch 1, num_ctas even; p.tiles_m then counts 256-row tile rows).
 // B2 non-null: the FFN gate/up form -- B = W_g, B2 = W_u (both K x N, N-major, batch 1),
 // bn = 256 covers 128 output columns of each, and C = SiLU(bf16(X W_g)) * bf16(X W_u).
+// fp8: A [M][lda] and B [N][ldb] are E4M3 codes (bytes, K contiguous; b_kmajor), batch 1, and
+// p.scale_a / p.scale_b scale the rows and columns of the FP32 accumulator.
 cudaError_t launch_gemm_tc(const TcParams& p, int bn, const void* A, int64_t lda, int64_t strideA,
                            const void* B, int64_t ldb, int64_t strideB, bool b_kmajor,
                            bool pair, int num_ctas, cudaStream_t s, const void* B2 = nullptr,
-                           int64_t ldb2 = 0);
+                           int64_t ldb2 = 0, bool fp8 = false);
 constexpr int kTcBM = 128, kTcBK = 64;
 
 // ------------------------------------------------------------------ BF16 thin (decode) path
@@ -96,6 +101,12 @@ cudaError_t launch_gemm_thin(const ThinParams& p, int ntok, const void* X, int64
                              const void* W, int64_t ldw, bool w_kmajor, cudaStream_t s);
 constexpr int kThinBN = 128, kThinBK = 64;
 inline int64_t thin_ws_floats(int64_t ctas, int ntok) { return ctas * 2 * ntok * 128; }
+
+// ------------------------------------------------------------------ FP8 row quantiser
+// Q[i][:] = E4M3(X[i][:] * (448 / amax_i)), scales[i] = amax_i / 448 (X BF16, Q bytes).
+// vec: rows 16-byte aligned (X ld % 8 == 0, Q ld % 16 == 0, bases aligned).
+cudaError_t launch_quantize_rows(int64_t rows, int64_t cols, const void* X, int64_t ldx, void* Q,
+                                 int64_t ldq, float* scales, bool vec, int sms, cudaStream_t s);
 
 // ------------------------------------------------------------------ fused attention
 struct AttnParams {

@@ -239,6 +239,55 @@ __device__ __forceinline__ void umma2_commit(uint32_t bar) {
                : "memory");
 }
 
+// FP8 (E4M3 x E4M3 -> FP32) forms: kind::f8f6f4, K = 32 per instruction (32 bytes of K, as
+// for BF16), so the shared-memory descriptors and their K steps are the BF16 ones.
+__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma2_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Instruction descriptor for kind::f8f6f4 with E4M3 A and B (format code 0) and FP32 D;
+// the other fields as idesc_bf16_f32.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t m, uint32_t n, bool a_mn_major,
+                                                      bool b_mn_major) {
+  return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+
+// FP8 epilogue: acc[i][j] * scale_a[i] * scale_b[j] for the 32 columns gn0 .. gn0+31 of row
+// gm (columns past N get scale 0; they are not stored).
+__device__ __forceinline__ void fp8_scale(uint32_t (&r)[32], const TcParams& p, int64_t gm,
+                                          int64_t gn0) {
+  const float sa = gm < p.M ? __ldg(p.scale_a + gm) : 0.f;
+  float sb[32];
+  if (gn0 + 32 <= p.N) {
+    const float4* s4 = reinterpret_cast<const float4*>(p.scale_b + gn0);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 v = __ldg(s4 + q);
+      sb[4 * q] = v.x; sb[4 * q + 1] = v.y; sb[4 * q + 2] = v.z; sb[4 * q + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) sb[j] = gn0 + j < p.N ? __ldg(p.scale_b + gn0 + j) : 0.f;
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) r[j] = __float_as_uint((__uint_as_float(r[j]) * sa) * sb[j]);
+}
+
 __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint32_t* status) {
   uint32_t never = 0;
   return mbar_wait(bar, parity, &never, status, kDevTimeoutDrain);
@@ -340,7 +389,11 @@ __device__ __forceinline__ void store_row_chunk(const TcParams& p, void* crow_v,
 // DUAL (FFN gate and up projections): B is [W_g tile | W_u tile], BN / 2 columns each, so the
 // accumulator holds G and U side by side; the epilogue writes z = SiLU(bf16(G)) * bf16(U),
 // BN / 2 output columns per tile.  Pair: rank 0 holds the W_g tile and rank 1 the W_u tile.
-template <int BN, bool B_KMAJOR, bool RANK3, bool B3D, bool PAIR, bool DUAL>
+//
+// FP8: A and B are E4M3 codes (K-major, 128 codes = 128 bytes per stage row, so a stage holds
+// 128 K elements), the MMA is kind::f8f6f4, and the epilogue scales the accumulator by the
+// per-row scale of A and the per-column scale of op(B) (alpha = 1, beta = 0).
+template <int BN, bool B_KMAJOR, bool RANK3, bool B3D, bool PAIR, bool DUAL, bool FP8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC,
@@ -348,6 +401,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   using Cfg = TcCfg<BN, B_KMAJOR, PAIR>;
   static_assert(!PAIR || (BN == 256 && !RANK3), "pair tiles are 256 x 256, one problem");
   static_assert(!DUAL || (BN == 256 && !B_KMAJOR && !RANK3), "gate/up: 2 x 128 columns, N-major");
+  static_assert(!FP8 || (B_KMAJOR && !RANK3 && !DUAL), "FP8: one problem, K-major B");
+  constexpr int BK_ELEMS = FP8 ? 128 : BK;  // K elements per stage (128 bytes per row)
   constexpr int OUT_N = DUAL ? BN / 2 : BN;  // output columns per tile
   constexpr int STAGES = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -431,7 +486,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = false;
             break;
           }
-          const int32_t kx = kb * BK;
+          const int32_t kx = kb * BK_ELEMS;
           const uint32_t adst = a_ring + s * A_BYTES, bdst = b_ring + s * Cfg::B_BYTES;
           if (PAIR) {
             // Both CTAs' loads of stage s count on rank 0's full[s]; rank 0 posts the bytes
@@ -500,7 +555,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && (!PAIR || rank == 0)) {
-      constexpr uint32_t idesc = idesc_bf16_f32(PAIR ? 2 * BM : BM, BN, false, !B_KMAJOR);
+      constexpr uint32_t idesc = FP8 ? idesc_e4m3_f32(PAIR ? 2 * BM : BM, BN, false, !B_KMAJOR)
+                                     : idesc_bf16_f32(PAIR ? 2 * BM : BM, BN, false, !B_KMAJOR);
       uint32_t it = 0, lt = 0;
       bool ok = true;
       TcWalk walk(p, cid, ncl);
@@ -535,8 +591,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint64_t bdesc = B_KMAJOR ? sdesc_sw128(b0 + k * 32, 16, 1024)
                                             : sdesc_sw128(b0 + k * 2048, 8192, 1024);
             const uint32_t accum = (kb > item.kbeg || k > 0) ? 1u : 0u;
-            if (PAIR) umma2_bf16(d, adesc, bdesc, idesc, accum);
-            else umma_bf16(d, adesc, bdesc, idesc, accum);
+            if (FP8) {
+              if (PAIR) umma2_f8(d, adesc, bdesc, idesc, accum);
+              else umma_f8(d, adesc, bdesc, idesc, accum);
+            } else {
+              if (PAIR) umma2_bf16(d, adesc, bdesc, idesc, accum);
+              else umma_bf16(d, adesc, bdesc, idesc, accum);
+            }
           }
           if (fault != 1) {
             if (PAIR) umma2_commit_both(smem_u32(&ctl->empty[s]));
@@ -679,6 +740,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               for (int j = 0; j < 32; ++j) u[j] = __float_as_uint(usum[j]);
               silu_mul_bf16(r, u);
             }
+            if (FP8) fp8_scale(r, p, gm, tn * OUT_N + ch * 32);
             if (gm < p.M) store_row_chunk(p, cbase, tn * OUT_N + ch * 32, r);
           }
         }
@@ -703,6 +765,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           } else {
             tmem_ld_wait();
           }
+          if (FP8) fp8_scale(w, p, tm * BM + row, tn * OUT_N + c * 32);
           if (c == OUT_N / 32 - 1) {
             // The accumulator is in registers now: hand TMEM back to the MMA issuer.
             tc_fence_before();
@@ -766,6 +829,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           } else {
             tmem_ld_wait();
           }
+          if (FP8) fp8_scale(r, p, gm, tn * OUT_N + c * 32);
           if (gm < p.M) store_row_chunk(p, cbase, tn * OUT_N + c * 32, r);
         }
         tc_fence_before();
@@ -874,11 +938,12 @@ EncodeTiledFn get_encode_tiled() {
 }
 
 namespace {
-template <int BN, bool B_KMAJOR, bool RANK3, bool B3D = false, bool PAIR = false, bool DUAL = false>
+template <int BN, bool B_KMAJOR, bool RANK3, bool B3D = false, bool PAIR = false, bool DUAL = false,
+          bool FP8 = false>
 cudaError_t launch_tc_variant(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mb2,
                               const CUtensorMap& mc, const TcParams& p, int num_ctas,
                               cudaStream_t s) {
-  auto kern = gemm_tc_kernel<BN, B_KMAJOR, RANK3, B3D, PAIR, DUAL>;
+  auto kern = gemm_tc_kernel<BN, B_KMAJOR, RANK3, B3D, PAIR, DUAL, FP8>;
   constexpr uint32_t smem = TcCfg<BN, B_KMAJOR, PAIR>::SMEM_BYTES;
   static_assert(smem <= 232448, "shared memory per CTA");
   static std::atomic<uint64_t> attr_done{0};
@@ -909,7 +974,7 @@ cudaError_t launch_tc_variant(const CUtensorMap& ma, const CUtensorMap& mb, cons
 cudaError_t launch_gemm_tc(const TcParams& p, int bn, const void* A, int64_t lda, int64_t strideA,
                            const void* B, int64_t ldb, int64_t strideB, bool b_kmajor,
                            bool pair, int num_ctas, cudaStream_t s, const void* B2,
-                           int64_t ldb2) {
+                           int64_t ldb2, bool fp8) {
   CUtensorMap ma, mb, mb2;
   const uint64_t batch = static_cast<uint64_t>(p.batch);
   const bool dual = B2 != nullptr;
@@ -918,13 +983,21 @@ cudaError_t launch_gemm_tc(const TcParams& p, int bn, const void* A, int64_t lda
   // B columns one tensor map box set covers: the CTA's share of the tile (the pair splits the
   // tile's columns between its two CTAs; gate/up reads BN / 2 from each of W_g and W_u).
   const int bnc = dual ? bn / 2 : (pair ? bn / 2 : bn);
-  if (!make_bf16_map(&ma, A, p.K, p.M, lda, batch, strideA, BK, BM)) return cudaErrorInvalidValue;
+  if (fp8 && (!b_kmajor || dual || batch > 1)) return cudaErrorInvalidValue;
+  // FP8: E4M3 codes as bytes, boxes of 128 codes (128-byte rows) along K.
+  if (fp8 ? !make_tile_map(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, p.K, p.M, lda, 1, 0, 128, BM,
+                           CU_TENSOR_MAP_SWIZZLE_128B, 1)
+          : !make_bf16_map(&ma, A, p.K, p.M, lda, batch, strideA, BK, BM))
+    return cudaErrorInvalidValue;
   // N-major B as one 3-D box per stage when the 64-column chunks tile N exactly (so no box
   // reaches past a row) and the tile width is whole chunks.
-  const bool b3d = !b_kmajor && batch <= 1 && p.N % 64 == 0 && bn % 64 == 0 &&
+  const bool b3d = !fp8 && !b_kmajor && batch <= 1 && p.N % 64 == 0 && bn % 64 == 0 &&
                    p.N >= (dual ? bn / 2 : bn);
   bool ok_b;
-  if (b_kmajor)
+  if (fp8)
+    ok_b = make_tile_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, p.K, p.N, ldb, 1, 0, 128,
+                         static_cast<uint32_t>(bnc), CU_TENSOR_MAP_SWIZZLE_128B, 1);
+  else if (b_kmajor)
     ok_b = make_bf16_map(&mb, B, p.K, p.N, ldb, batch, strideB, BK, bnc);
   else if (b3d)
     ok_b = make_tile_map(&mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, 64, p.K, ldb,
@@ -956,6 +1029,12 @@ cudaError_t launch_gemm_tc(const TcParams& p, int bn, const void* A, int64_t lda
     if (!ok_c) q.c_tma = 0;  // fall back to direct stores from registers
   }
   const bool rank3 = batch > 1;
+  if (fp8) {
+    if (pair) return launch_tc_variant<256, true, false, false, true, false, true>(ma, mb, mb2, mc, q, num_ctas, s);
+    if (bn == 256) return launch_tc_variant<256, true, false, false, false, false, true>(ma, mb, mb2, mc, q, num_ctas, s);
+    if (bn == 128) return launch_tc_variant<128, true, false, false, false, false, true>(ma, mb, mb2, mc, q, num_ctas, s);
+    return cudaErrorInvalidValue;
+  }
   if (dual) {
     if (pair && b3d) return launch_tc_variant<256, false, false, true, true, true>(ma, mb, mb2, mc, q, num_ctas, s);
     if (pair) return launch_tc_variant<256, false, false, false, true, true>(ma, mb, mb2, mc, q, num_ctas, s);

@@ -167,3 +167,12 @@ def attention(batch=64, L=2048, d=128, causal=False, Lkv=None, std_q=1.0) -> dic
     return dict(batch=batch, Lq=L, Lkv=Lkv, d=d, causal=causal,
                 scale=np.float32(1.0 / np.sqrt(np.float32(d))), Q=Q, ldq=d, sQ=L * d, K=K, ldk=d,
                 sK=Lkv * d, V=V, ldv=d, sV=Lkv * d, ldo=d, sO=L * d)
+
+
+def fp8_gemm(M=1024, N=12288, K=4096) -> dict:
+    """BF16 activations X [M, K] ~ N(0,1) and weights W [N, K] ~ N(0, 1/K) (stored by output
+    column), to be quantised per row to FP8 E4M3."""
+    s = BASE_SEED + 10
+    X = f32_to_bf16_bits(normal_f32(s, (M, K)))
+    W = f32_to_bf16_bits(normal_f32(s + 1, (N, K), std=1.0 / np.sqrt(K)))
+    return dict(M=M, N=N, K=K, X=X, W=W)

@@ -156,6 +156,46 @@ dg_status gemm_bf16_gate_up_silu(int64_t M, int64_t N, int64_t K, const uint16_t
                                  int64_t ldwu, uint16_t* Z, int64_t ldz, void* stream);
 
 /*
+ * FP8 E4M3 quantisation of a BF16 matrix, one scale per row ("Operator & Runtime" section
+ * 5.4.3, Example 5-7: the scale comes from the absolute maximum of the whole row, so the
+ * row is read in full before any element is quantised):
+ *     amax_i = max_k |X[i][k]|,   Q[i][k] = E4M3(X[i][k] * (448 / amax_i)),
+ *     scales[i] = amax_i / 448,   so X[i][k] ~ Q[i][k] * scales[i].
+ * E4M3 is the E4M3FN format (1 sign, 4 exponent, 3 mantissa bits, largest finite 448).  The
+ * two divisions and the product are IEEE float32 operations, the conversion rounds to
+ * nearest-even and saturates to +-448.  A row of zeros gets codes 0 and scale 0.  X must be
+ * finite (a row holding Inf or NaN gets unspecified codes).
+ *   - X: rows x cols BF16, row stride ldx >= cols.  Q: rows x cols E4M3 codes (bytes), row
+ *     stride ldq >= cols.  scales: rows float32.  Device pointers owned by the caller.
+ *   - Activations are quantised this way for gemm_fp8_e4m3; so are weights stored [N][K],
+ *     whose row scales are then the per-output-column scales of the product.
+ *   - Errors: negative sizes, short leading dimensions or null pointers DG_ERR_INVALID_ARG;
+ *     rows == 0: nothing.  Any alignment is accepted (16-byte rows take the vector path).
+ */
+dg_status quantize_rows_e4m3(int64_t rows, int64_t cols, const uint16_t* X, int64_t ldx,
+                             uint8_t* Q, int64_t ldq, float* scales, void* stream);
+
+/*
+ * FP8 E4M3 GEMM with per-row scales (tcgen05 kind::f8f6f4, FP32 accumulate):
+ *     C[i][j] = scale_a[i] * scale_b[j] * sum_k A[i][k] * B[j][k]
+ * with A and B E4M3 codes as written by quantize_rows_e4m3: A is M x K (activations, one
+ * scale per row), B is N x K (weights stored by output column, one scale per output
+ * column), both K contiguous.  The accumulation is FP32 over the exact code products; the
+ * scales are applied to the finished sum (two FP32 multiplications) and C is rounded once
+ * to BF16 (nearest-even) or kept FP32 (c_type).
+ *   - C is M x N row-major, ldc >= N.  Device pointers owned by the caller; C must not alias
+ *     the inputs.
+ *   - Errors: negative sizes, short leading dimensions, null pointers or another c_type
+ *     DG_ERR_INVALID_ARG; A, B or scale_b not 16-byte aligned, lda or ldb not multiples of
+ *     16, or scale_a not 4-byte aligned DG_ERR_MISALIGNED.  M == 0 or N == 0: nothing;
+ *     K == 0: C = 0.
+ *   - The tile kernel of gemm_bf16 (CTA pairs from M > 128), 128 K elements per stage.
+ */
+dg_status gemm_fp8_e4m3(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda,
+                        const float* scale_a, const uint8_t* B, int64_t ldb, const float* scale_b,
+                        void* C, int64_t ldc, dg_out c_type, void* stream);
+
+/*
  * Fused attention forward ("Operator & Runtime" section 5.3.3: S = Q K^T / sqrt(d),
  * P = softmax(S) row by row, O = P V, computed block by block with the online softmax so
  * that S and P never reach memory), over a strided batch of heads:
@@ -254,6 +294,17 @@ int64_t dg_streamk_start(int64_t c, int64_t units, int64_t ctas);
 double dg_model_traffic_bytes(int64_t M, int64_t N, int64_t K, int64_t tile_m, int64_t tile_n,
                               int32_t elem_bytes, int32_t out_bytes);
 int64_t dg_model_local_bytes(int64_t tile_m, int64_t tile_n, int64_t tile_k, int32_t elem_bytes);
+/*
+ * Traffic model of an FP8 GEMM whose input A (M x K, in_bytes per element) is quantised
+ * per row ("Operator & Runtime" section 5.4.4, Example 5-8), output tiles tile_m x tile_n,
+ * every tile reading what it needs: fused == 0 quantises once (read A for the maxima and
+ * codes, write the q_bytes codes, every column block reads the codes); fused != 0 lets
+ * every column block re-read A and quantise locally.  Plus, for both, every row block reads
+ * the q_bytes weights (K x N) and the output is written once (out_bytes).
+ */
+double dg_model_quant_traffic_bytes(int64_t M, int64_t K, int64_t N, int64_t tile_m,
+                                    int64_t tile_n, int32_t in_bytes, int32_t q_bytes,
+                                    int32_t out_bytes, int32_t fused);
 
 /* Library version string. */
 const char* dg_version(void);

@@ -374,3 +374,86 @@ def check_attention(O_bits, O_ref, PVabs, Ds):
     err = np.abs(O - O_ref)
     ok = bool(np.all(err <= bound) and np.all(np.isfinite(O)))
     return ok, float((err / bound).max()) if err.size else 0.0
+
+
+# ---------------------------------------------------------------------------
+# FP8 E4M3 with per-row scales ("Operator & Runtime", section 5.4.3, Example 5-7, and
+# section 5.4.4, Example 5-8).  E4M3FN: 1 sign, 4 exponent (bias 7) and 3 mantissa bits,
+# no infinities, largest finite value 448.  A row is quantised with the scale of its
+# absolute maximum over the whole row: x -> round(x * 448 / amax), dequantised as
+# q * amax / 448.  The quantised code is an integer decided by floating point, so the
+# oracle takes that decision in the kernel's precision: amax, 448 / amax and the product
+# x * (448 / amax) in IEEE float32, then round-to-nearest-even of that float32 value to
+# E4M3, values beyond 448 saturating to +-448.  The GEMM on the codes is the definition
+# C[i, j] = s_a[i] * s_b[j] * sum_k qa[i, k] qb[j, k] in float64 (B stored [N, K], so the
+# per-output-column scale of B is the scale of its row).
+# ---------------------------------------------------------------------------
+E4M3_MAX = 448.0
+
+
+def e4m3_values() -> np.ndarray:
+    """Value of every E4M3FN code 0..255 (NaN for the two NaN codes), from the format."""
+    vals = np.empty(256, dtype=np.float64)
+    for code in range(256):
+        sign = -1.0 if code & 0x80 else 1.0
+        e, m = (code >> 3) & 0xF, code & 0x7
+        if e == 0xF and m == 0x7:
+            vals[code] = np.nan
+        elif e == 0:
+            vals[code] = sign * (m / 8.0) * 2.0 ** -6          # subnormal
+        else:
+            vals[code] = sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+    return vals
+
+
+_E4M3 = None
+
+
+def e4m3_to_f64(codes) -> np.ndarray:
+    global _E4M3
+    if _E4M3 is None:
+        _E4M3 = e4m3_values()
+    return _E4M3[np.asarray(codes, dtype=np.uint8)]
+
+
+def round_e4m3(y) -> np.ndarray:
+    """Round-to-nearest-even of (float32-valued) y to E4M3FN codes, saturating to +-448;
+    NaN gives the NaN code 0x7F."""
+    y = np.asarray(y, dtype=np.float64)
+    pos = e4m3_values()[:127]                 # codes 0..126: 0 .. 448, increasing
+    a = np.minimum(np.abs(y), E4M3_MAX)
+    hi = np.clip(np.searchsorted(pos, a, side="left"), 0, 126)
+    lo = np.clip(hi - 1, 0, 126)
+    d_lo, d_hi = a - pos[lo], pos[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))   # ties: even mantissa
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    code = np.where(a == pos[hi], hi, code).astype(np.uint8)     # exact values
+    code = np.where((y < 0) & (code != 0), code | 0x80, code).astype(np.uint8)
+    code = np.where(np.signbit(y) & (code == 0), np.uint8(0x80), code).astype(np.uint8)
+    return np.where(np.isnan(y), np.uint8(0x7F), code).astype(np.uint8)
+
+
+def quantize_rows_e4m3(rows, cols, X, ldx):
+    """(codes [rows, cols] uint8, scales [rows] float32) of BF16 (bits) or float32 X.
+    Per row: amax = max |x|, multiplier 448 / amax and scale amax / 448 in float32; an
+    all-zero row has codes 0 and scale 0."""
+    X = np.asarray(X).reshape(-1)
+    x = (bf16_to_f64(X) if X.dtype == np.uint16 else X.astype(np.float64)).astype(np.float32)
+    idx = np.arange(rows)[:, None] * ldx + np.arange(cols)[None, :]
+    xr = x[idx]
+    amax = np.abs(xr).max(axis=1).astype(np.float32) if cols > 0 else np.zeros(rows, np.float32)
+    with np.errstate(divide="ignore"):
+        mult = np.where(amax > 0, np.float32(E4M3_MAX) / amax, np.float32(0)).astype(np.float32)
+    y = (xr * mult[:, None]).astype(np.float32)                   # float32 product (RNE)
+    scale = (amax / np.float32(E4M3_MAX)).astype(np.float32)
+    return round_e4m3(y), scale
+
+
+def gemm_fp8(M, N, K, QA, lda, sa, QB, ldb, sb):
+    """(C, D): C[i, j] = sa[i] * sb[j] * sum_k qa[i, k] qb[j, k] and its error scale
+    D = |sa[i] sb[j]| sum_k |qa qb|, float64, for E4M3 codes QA [M, lda] and QB [N, ldb]."""
+    a = e4m3_to_f64(np.asarray(QA).reshape(-1))
+    b = e4m3_to_f64(np.asarray(QB).reshape(-1))
+    P, D = gemm(M, N, K, 1.0, a, lda, b, ldb, op_b=1, absden=True)
+    s = np.asarray(sa, np.float64)[:, None] * np.asarray(sb, np.float64)[None, :]
+    return P[0] * s, D[0] * np.abs(s)

@@ -131,3 +131,21 @@ def test_ffn_counts_from_chapter_intro():
     # 128 MiB once-through bytes = the traffic model with one tile covering everything.
     v = dg.dg_model_traffic_bytes(1024, 12288, 4096, 1024, 12288, 2, 2)
     assert v == 128 * 2 ** 20
+
+
+def test_quant_traffic_model_reproduces_example_5_8():
+    from .test_oracle_pins import read_golden
+    # "Operator & Runtime" section 5.4.4, Example 5-8: A FP16 [4096, 4096], FP8 weights
+    # [4096, 1536], FP16 output, 128 x 128 tiles: 444 MiB with separate quantisation, 620 MiB
+    # fused into the GEMM (tests/golden/fp8_e4m3.txt).
+    g, _ = read_golden("fp8_e4m3.txt")
+    MiB = 2.0 ** 20
+    sep = dg.dg_model_quant_traffic_bytes(4096, 4096, 1536, 128, 128, 2, 1, 2, fused=False)
+    fus = dg.dg_model_quant_traffic_bytes(4096, 4096, 1536, 128, 128, 2, 1, 2, fused=True)
+    assert sep / MiB == g["total_separate_mib"] and fus / MiB == g["total_fused_mib"]
+    wo = dg.dg_model_quant_traffic_bytes(4096, 0, 1536, 128, 128, 2, 1, 2) / MiB     # output only
+    assert wo == 12
+    # weights + output = 204 MiB in both; the input side 240 vs 416 MiB
+    w_out = 32 * 6 + 12
+    assert w_out == g["weights_output_mib"]
+    assert sep / MiB - w_out == g["input_separate_mib"] and fus / MiB - w_out == g["input_fused_mib"]

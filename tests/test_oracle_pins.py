@@ -452,3 +452,92 @@ def test_attention_check_catches_planted_mistakes():
             l, u = l + pj.sum(), u + pj @ V[b0:b0 + pj.size]
         no_rescale[i] = u / l
     assert not oracle.check_attention(oracle.round_bf16(no_rescale), O, PV, Ds)[0]
+
+
+# --------------------------------------------------------------------------- FP8 E4M3
+def test_e4m3_format_values():
+    g, _ = read_golden("fp8_e4m3.txt")
+    v = oracle.e4m3_values()
+    pos = v[:127]
+    assert pos[126] == g["e4m3_max"] and np.all(np.diff(pos) > 0)         # 0 .. 448, increasing
+    assert pos[1] == 2.0 ** -9 and pos[8] == 2.0 ** -6                    # subnormal, normal
+    assert np.isnan(v[0x7F]) and np.isnan(v[0xFF])
+    assert np.array_equal(v[128:255], -pos) and np.signbit(v[128])
+    # Spacing: 3 mantissa bits, so 8 values per binade from 2^-6 up.
+    assert pos[120] == 256.0 and pos[121] == 288.0 and pos[112] == 128.0
+
+
+def test_e4m3_rounding_ties_and_saturation():
+    r = oracle.round_e4m3
+    assert oracle.e4m3_to_f64(r([17.0, 19.0, 2.0 ** -10, 3 * 2.0 ** -11, 460.0, 470.0, 1e9]))\
+        .tolist() == [16.0, 20.0, 0.0, 2.0 ** -9, 448.0, 448.0, 448.0]
+    assert r([-44.8])[0] == (r([44.8])[0] | 0x80) and r([np.nan])[0] == 0x7F
+
+
+def test_e4m3_rounding_matches_torch():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("no float8_e4m3fn in this torch")
+    x = np.random.default_rng(41).normal(0, 60, 200000).astype(np.float32)
+    x = np.concatenate([np.clip(x, -448, 448), np.float32(2.0) ** np.arange(-12, 9, 0.25).astype(np.float32)])
+    t = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.round_e4m3(x), t)
+
+
+def test_quantize_example_5_7():
+    g, _ = read_golden("fp8_e4m3.txt")
+    row = np.zeros(256, np.float32)
+    row[0], row[128] = 1.0, 10.0
+    q, s = oracle.quantize_rows_e4m3(1, 256, row, 256)
+    assert np.isclose(np.float32(448) / np.float32(10), g["scaled_first"], rtol=1e-7)
+    assert oracle.e4m3_to_f64(q[0, 0]) == g["rounded_first"]
+    # Dequantised exactly (q * amax / 448) the code gives 55/56; the stored float32 scale is
+    # amax / 448 rounded once.
+    assert oracle.e4m3_to_f64(q[0, 0]) * 10.0 / 448.0 == g["dequant_row_scale"]
+    assert s[0] == np.float32(10.0) / np.float32(448.0)
+    assert np.isclose(oracle.e4m3_to_f64(q[0, 0]) * float(s[0]), g["dequant_row_scale"], rtol=1e-7)
+    qb, sb = oracle.quantize_rows_e4m3(1, 128, row, 128)              # first block alone
+    assert oracle.e4m3_to_f64(qb[0, 0]) == g["e4m3_max"]
+    assert oracle.e4m3_to_f64(qb[0, 0]) * 1.0 / 448.0 == g["dequant_block_scale"]
+    assert np.isclose(g["dequant_block_scale"] - g["dequant_row_scale"], g["difference"], rtol=1e-12)
+    assert oracle.e4m3_to_f64(q[0, 128]) == 448.0                        # the maximum maps to 448
+
+
+def test_quantize_rows_special_cases():
+    from dense_gemm_sm_gb300 import inputs
+    rng = np.random.default_rng(42)
+    X = rng.normal(0, 3, (5, 40)).astype(np.float32)
+    X[2] = 0.0
+    bits = inputs.f32_to_bf16_bits(X)
+    q, s = oracle.quantize_rows_e4m3(5, 40, bits, 40)
+    assert np.all(q[2] == 0) and s[2] == 0.0                              # all-zero row
+    xb = oracle.bf16_to_f64(bits)
+    for i in (0, 1, 3, 4):
+        j = np.argmax(np.abs(xb[i]))
+        assert oracle.e4m3_to_f64(q[i, j]) == 448.0 * np.sign(xb[i, j])   # the maximum maps to 448
+        assert s[i] == np.float32(np.abs(xb[i]).max()) / np.float32(448)
+    qn, sn = oracle.quantize_rows_e4m3(5, 40, inputs.f32_to_bf16_bits(-X), 40)
+    assert np.array_equal(qn[[0, 1, 3, 4]], q[[0, 1, 3, 4]] ^ 0x80) and np.array_equal(sn, s)
+    # Dequantised values are within half an E4M3 spacing (relative 1/16) of the input.
+    deq = oracle.e4m3_to_f64(q) * s[:, None].astype(np.float64)
+    big = np.abs(xb) >= 2.0 ** -6 * s[:, None]
+    assert np.all(np.abs(deq - xb)[big] <= np.abs(xb)[big] / 16 + 1e-12)
+
+
+def test_gemm_fp8_closed_forms():
+    # Codes of small integers (exact in E4M3) with unit scales: the integer matmul; then
+    # row and column scales multiply the rows and columns.
+    rng = np.random.default_rng(43)
+    M, N, K = 7, 5, 33
+    A = rng.integers(-8, 9, (M, K)).astype(np.float32)
+    B = rng.integers(-8, 9, (N, K)).astype(np.float32)
+    qa, qb = oracle.round_e4m3(A), oracle.round_e4m3(B)
+    assert np.array_equal(oracle.e4m3_to_f64(qa), A)
+    C, D = oracle.gemm_fp8(M, N, K, qa, K, np.ones(M, np.float32), qb, K, np.ones(N, np.float32))
+    assert np.array_equal(C, A.astype(np.float64) @ B.T.astype(np.float64))
+    assert np.array_equal(D, np.abs(A).astype(np.float64) @ np.abs(B).T.astype(np.float64))
+    sa = np.float32(2.0) ** rng.integers(-3, 4, M).astype(np.float32)
+    sb = rng.uniform(0.1, 2.0, N).astype(np.float32)
+    C2, _ = oracle.gemm_fp8(M, N, K, qa, K, sa, qb, K, sb)
+    assert np.allclose(C2, C * sa[:, None].astype(np.float64) * sb[None, :].astype(np.float64),
+                       rtol=1e-15, atol=0)
