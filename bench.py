@@ -4,7 +4,8 @@
 One "step" is one call of the library's public C ABI on one batch of synthetic input
 (resident in HBM).  The default workload is the FP32 SGEMM M = N = K = 4096,
 alpha = 1, beta = 0.5; --workload picks another of the path's configurations
-(ffn_bf16, ffn_gate_up, bf16_4096, decode_m1 / decode_m4 / decode_m16, qk_batched,
+(ffn_bf16, ffn_gate_up, bf16_4096, decode_m1 / decode_m4 / decode_m16,
+decode_chain_m1 / decode_chain_m16, qk_batched,
 attn_batched, attn_causal_8k, fp8_ffn, fp8_quant_gemm, sgemm_ragged, sgemm_256).
 
 Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier and
@@ -145,6 +146,18 @@ class Workload:
                         desc=(f"FP8 E4M3 GEMM C=diag(sa)(A B^T)diag(sb) M={M} N={N} K={K}, "
                               f"FP32 accumulate, BF16 out"
                               + (", per-row quantisation of BF16 A inside each step" if quant else "")))
+        if name.startswith("decode_chain_m"):
+            m = int(name[len("decode_chain_m"):])
+            w = inputs.decode_chain(m)
+            dims = w["dims"]
+            L = len(dims) - 1
+            byts = sum(2.0 * (m * dims[l] + dims[l] * dims[l + 1] + m * dims[l + 1]) for l in range(L))
+            fl = sum(2.0 * m * dims[l] * dims[l + 1] for l in range(L))
+            return dict(kind="chain", w=w, batch=1, flops=fl, algo_bytes=byts, bound="hbm",
+                        unit="GB/s", kernel="gemm_chain_kernel",
+                        sources=["gemm_chain.cu"] + COMMON_SOURCES,
+                        desc=f"persistent decode chain of {L} BF16 GEMMs, M={m}, widths "
+                             f"{'-'.join(str(d) for d in dims)}, one launch, BF16 out")
         if name == "bf16_4096":
             w = inputs.bf16_square(4096)
             M, N, K = w["M"], w["N"], w["K"]
@@ -178,6 +191,18 @@ class Workload:
             copies = min(copies, 8)
         self.copies = copies
         self.bufs = []
+        if self.kind == "chain":
+            dev = lambda bits: torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+            dims = w["dims"]
+            for i in range(copies):
+                X = dev(w["X"])
+                Ws = [dev(W) for W in w["Ws"]]
+                Ys = [torch.empty(w["M"] * dims[l + 1], dtype=torch.bfloat16, device="cuda")
+                      for l in range(len(Ws))]
+                self.bufs.append((X, Ws, Ys))
+            torch.cuda.synchronize()
+            self.stream = torch.cuda.current_stream().cuda_stream
+            return
         if self.kind == "fp8":
             # Resident codes and scales, made by the library's own quantiser (setup, untimed).
             M, N, K = w["M"], w["N"], w["K"]
@@ -232,6 +257,9 @@ class Workload:
             kn = w["K"] * w["N"]
             dg.gemm_bf16_gate_up_silu(w["M"], w["N"], w["K"], A, w["lda"], B, w["ldb"],
                                       B.data_ptr() + 2 * kn, w["ldb"], C, w["ldc"], stream=s)
+        elif self.kind == "chain":
+            dims = w["dims"]
+            dg.gemm_bf16_decode_chain(w["M"], dims, A, dims[0], B, dims[1:], C, stream=s)
         elif self.kind == "fp8":
             (qa, sa, X), (qb, sb) = A, B
             M, N, K = w["M"], w["N"], w["K"]
@@ -417,7 +445,8 @@ def time_graph(torch, wl, steps, warmup):
 
 
 # Short kernels also timed as a CUDA-graph replay (launch and submission cost removed).
-GRAPH_WORKLOADS = ("sgemm_256", "ffn_bf16", "ffn_gate_up", "decode_m1", "decode_m4", "decode_m16")
+GRAPH_WORKLOADS = ("sgemm_256", "ffn_bf16", "ffn_gate_up", "decode_m1", "decode_m4", "decode_m16",
+                   "decode_chain_m1")
 
 
 def aggregate_ranks(ms_local, metric_of_seconds, world, dist, device):
@@ -436,8 +465,8 @@ def time_e2e(torch, wl, steps, warmup):
     """Same workload through the public API with host inputs: each step copies that step's
     inputs from pinned host memory, calls the library and reads the result back."""
     w = wl.w
-    if wl.kind == "fp8":
-        return None  # the FP8 lines are suite entries: device-resident codes only
+    if wl.kind in ("fp8", "chain"):
+        return None  # suite entries on device-resident inputs only
     A0, B0, C0 = wl.bufs[0]
     hA = A0.cpu().pin_memory()
     hB = B0.cpu().pin_memory()
@@ -481,6 +510,24 @@ def cpu_baseline(wl, budget_s=15.0, nthreads=None):
     nthreads = nthreads or os.cpu_count() or 1
     if wl.kind == "attn":
         return attn_cpu_baseline(wl, budget_s)
+    if wl.kind == "chain":
+        t = time.perf_counter()
+        oracle.decode_chain(w["M"], w["dims"], w["X"], w["dims"][0], w["Ws"], w["dims"][1:],
+                            nthreads=nthreads)
+        dt = time.perf_counter() - t
+        return {"value": round(wl.algo_bytes / dt / 1e9, 6), "unit": wl.unit, "cores": nthreads,
+                "kind": "oracle", "sample": f"the whole chain ({len(w['Ws'])} layers), FP64, {dt:.2f} s"}
+    if wl.kind == "fp8":
+        M, N, K = w["M"], w["N"], w["K"]
+        rows = min(M, 64)
+        t = time.perf_counter()
+        qa, sa = oracle.quantize_rows_e4m3(rows, K, w["X"], K)
+        qb, sb = oracle.quantize_rows_e4m3(N, K, w["W"], K)
+        oracle.gemm_fp8(rows, N, K, qa, K, sa, qb, K, sb)
+        dt = time.perf_counter() - t
+        return {"value": round(2.0 * rows * N * K / dt / 1e12, 6), "unit": wl.unit, "cores": nthreads,
+                "kind": "oracle", "sample": f"rows 0..{rows - 1} of C ({rows}/{M}), quantisation of "
+                                            f"those rows and of all of B, FP64 GEMM, {dt:.2f} s"}
     M, N, K = w["M"], w["N"], w["K"]
     batch = w.get("batch", 1)
     op_b = w.get("op_b", 0)
@@ -657,8 +704,9 @@ def main():
     if not args.no_suite:
         suite = {}
         for name in ("ffn_bf16", "ffn_gate_up", "bf16_4096", "decode_m1", "decode_m4",
-                     "decode_m16", "qk_batched", "attn_batched", "attn_causal_8k", "fp8_ffn",
-                     "fp8_quant_gemm", "sgemm_ragged", "sgemm_256"):
+                     "decode_m16", "decode_chain_m1", "decode_chain_m16", "qk_batched",
+                     "attn_batched", "attn_causal_8k", "fp8_ffn", "fp8_quant_gemm", "sgemm_ragged",
+                     "sgemm_256"):
             if name == args.workload:
                 continue
             other = Workload(name, torch, dg, inputs)

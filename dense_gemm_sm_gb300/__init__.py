@@ -11,6 +11,6 @@ from ._lib import (  # noqa: F401
     DG_KERNEL_TC_BF16, DG_KERNEL_TC2_BF16, DG_OK, DG_OP_N, DG_OP_T, DG_OUT_BF16, DG_OUT_F32, EXPORTED, DgError,
     dg_device_status, dg_model_local_bytes, dg_model_quant_traffic_bytes, dg_model_traffic_bytes, dg_plan_gemm, dg_raster_tile,
     dg_release_workspace, dg_set_fault_injection, dg_status_string, dg_streamk_start, dg_version,
-    attention_bf16, gemm_bf16, gemm_bf16_decode_noalloc, gemm_bf16_gate_up_silu, gemm_bf16_strided_batched, gemm_f32, gemm_fp8_e4m3, quantize_rows_e4m3, gemm_f32_strided_batched, library_path, load,
+    attention_bf16, gemm_bf16, gemm_bf16_decode_chain, gemm_bf16_decode_noalloc, gemm_bf16_gate_up_silu, gemm_bf16_strided_batched, gemm_f32, gemm_fp8_e4m3, quantize_rows_e4m3, gemm_f32_strided_batched, library_path, load,
     status_string,
 )

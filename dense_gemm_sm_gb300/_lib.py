@@ -26,6 +26,7 @@ EXPORTED = [
     "dg_raster_tile", "dg_streamk_start", "dg_model_traffic_bytes", "dg_model_local_bytes",
     "dg_version", "dg_set_fault_injection", "gemm_bf16_decode_noalloc", "gemm_bf16_gate_up_silu",
     "attention_bf16", "quantize_rows_e4m3", "gemm_fp8_e4m3", "dg_model_quant_traffic_bytes",
+    "gemm_bf16_decode_chain",
 ]
 
 
@@ -75,6 +76,7 @@ def load(build_if_missing: bool = True):
     lib.gemm_bf16_strided_batched.argtypes = [i64, i64, i64, f32, vp, i64, i64, vp, i64, i64, i32,
                                               f32, vp, i64, i64, i64, i32, vp]
     lib.gemm_bf16_gate_up_silu.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp]
+    lib.gemm_bf16_decode_chain.argtypes = [i32, i64, vp, vp, i64, vp, vp, vp, vp]
     lib.quantize_rows_e4m3.argtypes = [i64, i64, vp, i64, vp, i64, vp, vp]
     lib.gemm_fp8_e4m3.argtypes = [i64, i64, i64, vp, i64, vp, vp, i64, vp, vp, i64, i32, vp]
     lib.attention_bf16.argtypes = [i64, i64, i64, i64, f32, i32, vp, i64, i64, vp, i64, i64, vp,
@@ -83,7 +85,7 @@ def load(build_if_missing: bool = True):
                                              i32, vp]
     for f in ("gemm_f32", "gemm_f32_strided_batched", "gemm_bf16", "gemm_bf16_strided_batched",
               "gemm_bf16_decode_noalloc", "gemm_bf16_gate_up_silu", "attention_bf16",
-              "quantize_rows_e4m3", "gemm_fp8_e4m3"):
+              "quantize_rows_e4m3", "gemm_fp8_e4m3", "gemm_bf16_decode_chain"):
         getattr(lib, f).restype = ctypes.c_int
     lib.dg_status_string.argtypes = [ctypes.c_int]
     lib.dg_status_string.restype = ctypes.c_char_p
@@ -185,6 +187,20 @@ def gemm_bf16_gate_up_silu(M, N, K, X, ldx, Wg, ldwg, Wu, ldwu, Z, ldz, stream=N
     st = lib.gemm_bf16_gate_up_silu(M, N, K, _ptr(X), ldx, _ptr(Wg), ldwg, _ptr(Wu), ldwu,
                                     _ptr(Z), ldz, _stream(stream))
     return _ret(st, "gemm_bf16_gate_up_silu", check)
+
+
+def gemm_bf16_decode_chain(M, dims, X, ldx, Ws, ldws, Ys, stream=None, check=True) -> int:
+    """Y[0] = bf16(X W[0]), Y[l] = bf16(Y[l-1] W[l]): `len(Ws)` decode GEMMs in one launch."""
+    lib = load()
+    layers = len(Ws)
+    dims_a = (ctypes.c_int64 * (layers + 1))(*[int(d) for d in dims])
+    ldw_a = (ctypes.c_int64 * layers)(*[int(v) for v in ldws])
+    w_a = (ctypes.c_void_p * layers)(*[_ptr(w) for w in Ws])
+    y_a = (ctypes.c_void_p * layers)(*[_ptr(y) for y in Ys])
+    st = lib.gemm_bf16_decode_chain(layers, M, ctypes.cast(dims_a, ctypes.c_void_p), _ptr(X), ldx,
+                                    ctypes.cast(w_a, ctypes.c_void_p), ctypes.cast(ldw_a, ctypes.c_void_p),
+                                    ctypes.cast(y_a, ctypes.c_void_p), _stream(stream))
+    return _ret(st, "gemm_bf16_decode_chain", check)
 
 
 def quantize_rows_e4m3(rows, cols, X, ldx, Q, ldq, scales, stream=None, check=True) -> int:

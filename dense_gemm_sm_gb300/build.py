@@ -23,7 +23,7 @@ LIB_NAME = "libdgemm_sm103a.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 
 SOURCES = ["api.cu", "sgemm_simt.cu", "gemm_tc.cu", "gemm_thin.cu", "gemm_thin_noalloc.cu",
-           "attention.cu", "quant.cu"]
+           "attention.cu", "quant.cu", "gemm_chain.cu"]
 HEADERS = ["dg_internal.h", "ptx.cuh", "tile_sched.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -15,6 +15,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
+#include <cstring>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -47,6 +48,17 @@ struct Workspace {
   size_t n_counters = 0;
 };
 std::map<std::pair<int, cudaStream_t>, Workspace> g_workspaces;
+
+// State of the persistent decode chain, per (device, stream), never shared with the other
+// kernels: partials, and a word array [done, tiles_done[8], tickets[cap]] zeroed when
+// allocated; the kernel leaves every word zero again at the end of a call.
+struct ChainState {
+  float* ws = nullptr;
+  size_t ws_floats = 0;
+  uint32_t* words = nullptr;
+  size_t cap = 0;
+};
+std::map<std::pair<int, cudaStream_t>, ChainState> g_chain_states;
 
 bool log_enabled() {
   static const bool on = [] {
@@ -587,6 +599,108 @@ dg_status gemm_fp8_e4m3(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64
                   status, dev, s, nullptr, 0, scale_a, scale_b);
 }
 
+dg_status gemm_bf16_decode_chain(int32_t layers, int64_t M, const int64_t* dims, const uint16_t* X,
+                                 int64_t ldx, const uint16_t* const* W, const int64_t* ldw,
+                                 uint16_t* const* Y, void* stream) {
+  if (layers < 1 || layers > kChainMax || M < 0 || !dims || !W || !ldw || !Y) return DG_ERR_INVALID_ARG;
+  if (M == 0) return DG_OK;
+  if (M > 16) return DG_ERR_UNSUPPORTED;
+  for (int l = 0; l <= layers; ++l)
+    if (dims[l] <= 0) return DG_ERR_INVALID_ARG;
+  if (!X || ldx < dims[0]) return DG_ERR_INVALID_ARG;
+  for (int l = 0; l < layers; ++l)
+    if (!W[l] || !Y[l] || ldw[l] < dims[l + 1]) return DG_ERR_INVALID_ARG;
+  if (!aligned16(X) || ldx % 8 != 0) return DG_ERR_MISALIGNED;
+  for (int l = 0; l < layers; ++l)
+    if (!aligned16(W[l]) || ldw[l] % 8 != 0 || !aligned16(Y[l]) ||
+        (l + 1 < layers && dims[l + 1] % 8 != 0))
+      return DG_ERR_MISALIGNED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int dev = 0;
+  if (current_device(&dev) != cudaSuccess) return DG_ERR_CUDA;
+  uint32_t* status = nullptr;
+  int sms = 0;
+  if (device_info(dev, &status, &sms) != cudaSuccess) return DG_ERR_CUDA;
+  ChainParams p;
+  std::memset(&p, 0, sizeof p);
+  p.layers = layers;
+  p.M = M;
+  p.ctas = static_cast<uint32_t>(sms);
+  p.status = status;
+  size_t tiles = 0;
+  for (int l = 0; l < layers; ++l) {
+    const int64_t n_tiles = cdiv(dims[l + 1], kThinBN), kb = cdiv(dims[l], kThinBK);
+    if (!sk_fits_u32(n_tiles * kb, sms)) return DG_ERR_UNSUPPORTED;
+    tiles += static_cast<size_t>(n_tiles);
+  }
+  const size_t per_layer = static_cast<size_t>(thin_ws_floats(sms, 16));
+  ChainState st;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    ChainState& cs = g_chain_states[{dev, s}];
+    if (cs.ws_floats < per_layer * layers || cs.cap < tiles) {
+      if (cs.ws || cs.words) {
+        if (cudaStreamSynchronize(s) != cudaSuccess) return DG_ERR_CUDA;
+        cudaFree(cs.ws);
+        cudaFree(cs.words);
+        cs = ChainState{};
+      }
+      size_t cap = 4096;
+      while (cap < tiles) cap *= 2;
+      const size_t nf = per_layer * kChainMax;
+      if (cudaMalloc(&cs.ws, nf * sizeof(float)) != cudaSuccess) {
+        cs = ChainState{};
+        return DG_ERR_NO_MEMORY;
+      }
+      if (cudaMalloc(&cs.words, (1 + kChainMax + cap) * sizeof(uint32_t)) != cudaSuccess) {
+        cudaFree(cs.ws);
+        cs = ChainState{};
+        return DG_ERR_NO_MEMORY;
+      }
+      if (cudaMemsetAsync(cs.words, 0, (1 + kChainMax + cap) * sizeof(uint32_t), s) != cudaSuccess)
+        return DG_ERR_CUDA;
+      cs.ws_floats = nf;
+      cs.cap = cap;
+    }
+    st = cs;
+  }
+  p.done = st.words;
+  size_t off = 0;
+  for (int l = 0; l < layers; ++l) {
+    ChainLayer& L = p.L[l];
+    L.N = dims[l + 1];
+    L.K = dims[l];
+    L.n_tiles = static_cast<uint32_t>(cdiv(L.N, kThinBN));
+    L.kblocks = static_cast<uint32_t>(cdiv(L.K, kThinBK));
+    L.units = L.n_tiles * L.kblocks;
+    L.ctas = L.units < static_cast<uint32_t>(sms) ? L.units : static_cast<uint32_t>(sms);
+    L.C = Y[l];
+    L.ldc = dims[l + 1];
+    L.ws = st.ws + per_layer * l;
+    L.counters = st.words + 1 + kChainMax + off;
+    L.tiles_done = st.words + 1 + l;
+    off += L.n_tiles;
+  }
+  if (log_enabled())
+    std::fprintf(stderr, "[dg] gemm_bf16_decode_chain layers=%d M=%lld grid=%d\n", layers,
+                 static_cast<long long>(M), sms);
+  // Tuning knobs (sweeps): DG_CHAIN_PREFETCH (W blocks per CTA asked of L2 at a layer
+  // boundary), DG_CHAIN_POLL_NS (sleep between polls of a layer's tile count),
+  // DG_CHAIN_PDL=0 (no programmatic overlap with the previous kernel), DG_CHAIN_COOP=0 (no
+  // cooperative attribute; co-residency then rests on the grid of one CTA per SM).
+  p.prefetch = 0;
+  if (const char* e = std::getenv("DG_CHAIN_PREFETCH")) p.prefetch = static_cast<uint32_t>(std::atoi(e));
+  p.poll_ns = 64;
+  if (const char* e = std::getenv("DG_CHAIN_POLL_NS")) p.poll_ns = static_cast<uint32_t>(std::atoi(e));
+  const char* pe = std::getenv("DG_CHAIN_PDL");
+  const bool pdl = !(pe && pe[0] == '0');
+  const char* ce = std::getenv("DG_CHAIN_COOP");
+  const bool coop = !(ce && ce[0] == '0');
+  const void* wp[kChainMax];
+  for (int l = 0; l < layers; ++l) wp[l] = W[l];
+  return from_cuda(launch_gemm_chain(p, X, ldx, wp, ldw, s, pdl, coop));
+}
+
 dg_status attention_bf16(int64_t batch, int64_t Lq, int64_t Lkv, int64_t d, float scale,
                          int32_t causal, const uint16_t* Q, int64_t ldq, int64_t strideQ,
                          const uint16_t* K, int64_t ldk, int64_t strideK, const uint16_t* V,
@@ -670,7 +784,7 @@ dg_status dg_device_status(void* stream) {
 
 dg_status dg_release_workspace(void) {
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_workspaces.empty()) return DG_OK;
+  if (g_workspaces.empty() && g_chain_states.empty()) return DG_OK;
   if (cudaDeviceSynchronize() != cudaSuccess) return DG_ERR_CUDA;
   int cur = 0;
   cudaGetDevice(&cur);
@@ -679,8 +793,14 @@ dg_status dg_release_workspace(void) {
     cudaFree(kv.second.ws);
     cudaFree(kv.second.counters);
   }
+  for (auto& kv : g_chain_states) {
+    cudaSetDevice(kv.first.first);
+    cudaFree(kv.second.ws);
+    cudaFree(kv.second.words);
+  }
   cudaSetDevice(cur);
   g_workspaces.clear();
+  g_chain_states.clear();
   return DG_OK;
 }
 

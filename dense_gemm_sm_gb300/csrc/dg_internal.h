@@ -102,6 +102,35 @@ cudaError_t launch_gemm_thin(const ThinParams& p, int ntok, const void* X, int64
 constexpr int kThinBN = 128, kThinBK = 64;
 inline int64_t thin_ws_floats(int64_t ctas, int ntok) { return ctas * 2 * ntok * 128; }
 
+// ------------------------------------------------------------------ persistent decode chain
+// y_{l+1} = bf16(y_l W_l) for l < layers (y_0 = X, M <= 16 rows), one cooperative launch of
+// `ctas` CTAs; every layer is split stream-K over the same CTAs as gemm_thin_kernel splits
+// one call; a layer's X loads wait for the previous layer's last output tile.
+constexpr int kChainMax = 8;
+struct ChainLayer {
+  int64_t N, K;
+  uint32_t n_tiles, kblocks, units;  // ceil(N / 128), ceil(K / 64), n_tiles * kblocks
+  uint32_t ctas;                     // CTAs sharing the layer: min(units, grid), as one call
+  void* C; int64_t ldc;              // the layer's BF16 output [M][ldc]
+  float* ws;                         // partials: [ctas][2][4][128] float4
+  uint32_t* counters;                // [n_tiles] split-K tickets, zero between calls
+  uint32_t* tiles_done;              // output tiles written so far, zero between calls
+};
+struct ChainParams {
+  int32_t layers;
+  int64_t M;
+  uint32_t ctas;
+  uint32_t prefetch;  // W blocks of a later layer's range asked of L2 at the layer boundary
+  uint32_t poll_ns;   // sleep between polls of the previous layer's tile count
+  ChainLayer L[kChainMax];
+  uint32_t* done;   // CTAs finished in this call, zero between calls
+  uint32_t* status;
+};
+// W_l [K_l][ldw_l] N-major BF16; X [M][ldx].
+cudaError_t launch_gemm_chain(const ChainParams& p, const void* X, int64_t ldx,
+                              const void* const* W, const int64_t* ldw, cudaStream_t s,
+                              bool pdl, bool coop);
+
 // ------------------------------------------------------------------ FP8 row quantiser
 // Q[i][:] = E4M3(X[i][:] * (448 / amax_i)), scales[i] = amax_i / 448 (X BF16, Q bytes).
 // vec: rows 16-byte aligned (X ld % 8 == 0, Q ld % 16 == 0, bases aligned).

@@ -176,3 +176,13 @@ def fp8_gemm(M=1024, N=12288, K=4096) -> dict:
     X = f32_to_bf16_bits(normal_f32(s, (M, K)))
     W = f32_to_bf16_bits(normal_f32(s + 1, (N, K), std=1.0 / np.sqrt(K)))
     return dict(M=M, N=N, K=K, X=X, W=W)
+
+
+def decode_chain(M=1, dims=(4096, 12288, 4096, 12288, 4096)) -> dict:
+    """X [M, dims[0]] ~ N(0,1) and layer weights W_l [dims[l], dims[l+1]] ~ N(0, 1/dims[l])
+    (so activations keep unit scale), BF16: FFN-shaped up/down layers."""
+    s = BASE_SEED + 11
+    X = f32_to_bf16_bits(normal_f32(s + M, (M, dims[0])))
+    Ws = [f32_to_bf16_bits(normal_f32(s + 100 + l, (dims[l], dims[l + 1]), std=1.0 / np.sqrt(dims[l])))
+          for l in range(len(dims) - 1)]
+    return dict(M=M, dims=list(dims), X=X, Ws=Ws)

@@ -156,6 +156,35 @@ dg_status gemm_bf16_gate_up_silu(int64_t M, int64_t N, int64_t K, const uint16_t
                                  int64_t ldwu, uint16_t* Z, int64_t ldz, void* stream);
 
 /*
+ * A chain of decode GEMMs in one persistent launch ("Operator & Runtime" sections 5.5.2 and
+ * 5.5.4: one submission instead of one per layer, and a dependent layer starts on each block
+ * of its input as soon as that block is written):
+ *     Y[0] = bf16(X W[0]),  Y[l] = bf16(Y[l-1] W[l])  for 0 < l < layers,
+ * each layer FP32-accumulated and rounded once to BF16 (nearest-even), exactly what
+ * `layers` calls of gemm_bf16 (alpha = 1, beta = 0, op N) compute -- and with the same
+ * stream-K partition and combine order as those calls when a layer has at least as many
+ * (128-column, 64-row) W blocks as the GPU has SMs, so bit for bit the same result.
+ *   - dims[0 .. layers]: dims[0] = columns of X, dims[l+1] = columns of Y[l] (= rows of
+ *     W[l]).  X is M x dims[0] (ldx); W[l] is dims[l] x dims[l+1] row-major (ldw[l] >=
+ *     dims[l+1]); Y[l] is M x dims[l+1] with row stride dims[l+1].  dims, W, ldw and Y are
+ *     host arrays (of device pointers for W and Y).  1 <= layers <= 8, M <= 16.
+ *   - Device buffers owned by the caller; every Y[l] is written, Y buffers must not alias
+ *     each other or the inputs.  The library keeps per-stream scratch for the chain
+ *     (partials and per-tile flags), allocated on first use (cudaMalloc) and freed by
+ *     dg_release_workspace.
+ *   - Launched cooperatively, one CTA per SM (all resident at once): the call fails with
+ *     DG_ERR_CUDA when the GPU cannot hold that grid.  Waits are bounded (DG_ERR_TIMEOUT via
+ *     dg_device_status).
+ *   - Errors: layers outside 1..8, non-positive dims, short leading dimensions or null
+ *     pointers DG_ERR_INVALID_ARG; M > 16 DG_ERR_UNSUPPORTED; M == 0: nothing; X, W[l] or
+ *     Y[l] not 16-byte aligned, ldx or ldw[l] not multiples of 8, or an intermediate width
+ *     dims[l] (0 < l < layers) not a multiple of 8 DG_ERR_MISALIGNED.
+ */
+dg_status gemm_bf16_decode_chain(int32_t layers, int64_t M, const int64_t* dims, const uint16_t* X,
+                                 int64_t ldx, const uint16_t* const* W, const int64_t* ldw,
+                                 uint16_t* const* Y, void* stream);
+
+/*
  * FP8 E4M3 quantisation of a BF16 matrix, one scale per row ("Operator & Runtime" section
  * 5.4.3, Example 5-7: the scale comes from the absolute maximum of the whole row, so the
  * row is read in full before any element is quantised):

@@ -457,3 +457,38 @@ def gemm_fp8(M, N, K, QA, lda, sa, QB, ldb, sb):
     P, D = gemm(M, N, K, 1.0, a, lda, b, ldb, op_b=1, absden=True)
     s = np.asarray(sa, np.float64)[:, None] * np.asarray(sb, np.float64)[None, :]
     return P[0] * s, D[0] * np.abs(s)
+
+
+# ---------------------------------------------------------------------------
+# A chain of decode GEMMs ("Operator & Runtime", sections 5.5.2 and 5.5.4): y_0 = X,
+# y_{l+1} = bf16(y_l W_l) -- each layer the BF16 GEMM above, its output rounded once and
+# fed to the next.  The acceptance bound of layer l adds to the BF16 GEMM bound the effect
+# of the input's difference: the GPU's input (its rounded y_l) and the oracle's (its own
+# rounded y_l) differ by at most b_{l-1} + ulp/2 <= 2 b_{l-1} elementwise, which moves
+# each output by at most (2 b_{l-1}) |W_l|.
+# ---------------------------------------------------------------------------
+def decode_chain(M, dims, X, ldx, Ws, ldws, nthreads=None):
+    """[(y_l float64 before rounding, y_l BF16 bits, bound_l)] for layers l = 0 .. L-1."""
+    out = []
+    x, ld, b_prev = X, ldx, None
+    for l, (W, ldw) in enumerate(zip(Ws, ldws)):
+        K, N = dims[l], dims[l + 1]
+        y, D = gemm(M, N, K, 1.0, x, ld, W, ldw, absden=True, nthreads=nthreads)
+        y, D = y[0], D[0]
+        bound = BF16_REL * D + ulp_bf16(np.abs(y))
+        if b_prev is not None:
+            w = np.abs(bf16_to_f64(np.asarray(W).reshape(-1)[: (K - 1) * ldw + N]))
+            wk = w[(np.arange(K)[:, None] * ldw + np.arange(N)[None, :])]
+            bound = bound + (2.0 * b_prev) @ wk
+        bits = round_bf16(y)
+        out.append((y, bits, bound))
+        x, ld, b_prev = bits, N, bound
+    return out
+
+
+def check_chain_layer(Y_bits, y, bound):
+    """(ok, worst error / bound) of one layer's BF16 output."""
+    Yv = bf16_to_f64(Y_bits)
+    err = np.abs(Yv - y)
+    ok = bool(np.all(err <= bound) and np.all(np.isfinite(Yv)))
+    return ok, float((err / bound).max()) if err.size else 0.0

@@ -541,3 +541,46 @@ def test_gemm_fp8_closed_forms():
     C2, _ = oracle.gemm_fp8(M, N, K, qa, K, sa, qb, K, sb)
     assert np.allclose(C2, C * sa[:, None].astype(np.float64) * sb[None, :].astype(np.float64),
                        rtol=1e-15, atol=0)
+
+
+# --------------------------------------------------------------------------- decode chain
+def test_decode_chain_structure():
+    from dense_gemm_sm_gb300 import inputs
+    rng = np.random.default_rng(61)
+    M, d = 3, 24
+    X = inputs.f32_to_bf16_bits(rng.normal(0, 1, (M, d)).astype(np.float32))
+    eye = inputs.f32_to_bf16_bits(np.eye(d, dtype=np.float32))
+    perm = rng.permutation(d)
+    P = inputs.f32_to_bf16_bits(np.eye(d, dtype=np.float32)[:, perm])
+    # Identity and permutation layers move values exactly.
+    res = oracle.decode_chain(M, [d, d, d], X, d, [eye, P], [d, d])
+    assert np.array_equal(res[0][1], X.reshape(M, d))
+    assert np.array_equal(res[1][1], X.reshape(M, d)[:, perm])
+    # One layer is the BF16 GEMM rounded once; layer 2 takes layer 1's rounded output.
+    W1 = inputs.f32_to_bf16_bits(rng.normal(0, 0.3, (d, 40)).astype(np.float32))
+    W2 = inputs.f32_to_bf16_bits(rng.normal(0, 0.3, (40, 16)).astype(np.float32))
+    res = oracle.decode_chain(M, [d, 40, 16], X, d, [W1, W2], [40, 16])
+    x = oracle.bf16_to_f64(X).reshape(M, d)
+    y1 = x @ oracle.bf16_to_f64(W1).reshape(d, 40)
+    assert np.allclose(res[0][0], y1, rtol=1e-14, atol=1e-14)
+    y2 = oracle.bf16_to_f64(oracle.round_bf16(y1)) @ oracle.bf16_to_f64(W2).reshape(40, 16)
+    assert np.allclose(res[1][0], y2, rtol=1e-14, atol=1e-14)
+    # The second layer's bound includes the propagated first-layer bound.
+    assert np.all(res[1][2] > oracle.BF16_REL * 0 + oracle.ulp_bf16(np.abs(res[1][0])))
+
+
+def test_decode_chain_check_catches_a_dropped_k_block():
+    # A layer that drops its last 64 K rows (a plausible split-K mistake) fails the check.
+    from dense_gemm_sm_gb300 import inputs
+    rng = np.random.default_rng(62)
+    M, dims = 4, [256, 384, 256]
+    X = inputs.f32_to_bf16_bits(rng.normal(0, 1, (M, 256)).astype(np.float32))
+    Ws = [inputs.f32_to_bf16_bits(rng.normal(0, 1 / 16, (dims[l], dims[l + 1])).astype(np.float32))
+          for l in range(2)]
+    res = oracle.decode_chain(M, dims, X, 256, Ws, [384, 256])
+    ok, _ = oracle.check_chain_layer(res[0][1], res[0][0], res[0][2])
+    assert ok
+    x = oracle.bf16_to_f64(X).reshape(M, 256)
+    w = oracle.bf16_to_f64(Ws[0]).reshape(256, 384)
+    wrong = oracle.round_bf16(x[:, :192] @ w[:192])
+    assert not oracle.check_chain_layer(wrong, res[0][0], res[0][2])[0]
