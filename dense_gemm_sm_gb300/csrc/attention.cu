@@ -26,6 +26,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 
 #include "dg_internal.h"
 #include "ptx.cuh"
@@ -37,11 +38,13 @@ constexpr int kBQ = 128, kBKV = 128, kHD = 128;
 constexpr int kThreads = 192;
 constexpr uint32_t kTile = 128 * kHD * 2;  // 128 rows x 128 BF16: two 64-column boxes, 32 KiB
 constexpr uint32_t kHalf = kTile / 2;      // one 128-row x 64-column box (128-byte rows)
-constexpr uint32_t kTmemCols = 512;        // S[0] at 0, S[1] at 128, O at 256
+constexpr uint32_t kTmemCols = 512;        // S[0] at 0, S[1] at 128, O at 256, P[0..1] at 384
 constexpr uint32_t kOCol = 256;
+constexpr uint32_t kPCol = 384;            // P in TMEM: 64 columns (128 BF16 pairs) per buffer
 constexpr float kMoveLog2 = 8.f;           // move m when the block raises it by > 8 (log2)
 
-// Shared memory: Q | K[2] | V[2] | P[2] (32 KiB each, 1024-byte aligned) | control.
+// Shared memory: Q | K[2] | V[2] | P[2] (32 KiB each, 1024-byte aligned) | control; with P in
+// TMEM the P tiles are not allocated.
 struct AttnCtl {
   uint64_t qfull;
   uint64_t kfull[2], kempty[2], vfull[2], vempty[2];
@@ -51,7 +54,7 @@ struct AttnCtl {
   uint32_t abort;
 };
 static_assert(sizeof(AttnCtl) <= 256, "control block");
-constexpr uint32_t kSmemBytes = 1024 + 7 * kTile + 256;
+constexpr uint32_t smem_bytes(bool p_tmem) { return 1024 + (p_tmem ? 5 : 7) * kTile + 256; }
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -77,6 +80,18 @@ __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_
       "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem desc] (the A operand read from tensor memory: row m in lane
+// m, K elements packed two BF16 per 32-bit column, low half first).
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -102,7 +117,9 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __all_sync(0xffffffffu, ok);
 }
 
-template <bool CAUSAL>
+// P_TMEM: the softmax writes P into TMEM (tcgen05.st) and the P V MMA reads its A operand
+// from there, so only V passes through shared memory for that product.
+template <bool CAUSAL, bool P_TMEM>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -111,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle atoms need 1024-byte alignment
   const uint32_t sQ = base, sK = base + kTile, sV = base + 3 * kTile, sP = base + 5 * kTile;
-  AttnCtl* ctl = reinterpret_cast<AttnCtl*>(smem_raw + (base - raw) + 7 * kTile);
+  AttnCtl* ctl = reinterpret_cast<AttnCtl*>(smem_raw + (base - raw) + (P_TMEM ? 5 : 7) * kTile);
   volatile uint32_t* abort = &ctl->abort;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -232,9 +249,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < kBKV / 16; ++k) {
           // P: 16 keys = 32 bytes in the swizzle row (second box for keys 64..127).
           // V: 16 key rows = 2 KiB; its two 64-column halves of d are one box apart (LBO).
-          const uint64_t adesc = sdesc_sw128(pb + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
           const uint64_t bdesc = sdesc_sw128(vb + k * 2048, kHalf, 1024);
-          umma_bf16(tmem + kOCol, adesc, bdesc, idO, (j > 0 || k > 0) ? 1u : 0u);
+          if (P_TMEM) {
+            // 16 keys of P = 8 packed columns of the TMEM P buffer.
+            umma_bf16_ts(tmem + kOCol, tmem + kPCol + s * 64 + k * 8, bdesc, idO, (j > 0 || k > 0) ? 1u : 0u);
+          } else {
+            const uint64_t adesc = sdesc_sw128(pb + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
+            umma_bf16(tmem + kOCol, adesc, bdesc, idO, (j > 0 || k > 0) ? 1u : 0u);
+          }
         }
         umma_commit(smem_u32(&ctl->vempty[s]));
         umma_commit(smem_u32(&ctl->odone[s]));
@@ -304,6 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int t = 0; t < 8; ++t) ls8[t] = 0.f;
       const uint32_t pb = sP + s * kTile + prow;
+      uint32_t pw[2][32];  // P_TMEM: the row's 128 weights as 64 packed BF16 pairs
 #pragma unroll
       for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -316,14 +339,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float p1 = ex2(fmaf(__uint_as_float(sv[(i0 + 1) >> 5][(i0 + 1) & 31]), cl, nb));
             ls8[(c8 & 1) * 4 + e] += p0 + p1;
             w[e] = pack2(p0, p1);
+            pw[h][c8 * 4 + e] = w[e];
           }
           // Row `row` of the 128B-swizzled K-major tile: 16-byte chunk c8 of box h.
-          st_shared_v4(pb + h * kHalf + ((static_cast<uint32_t>(c8) ^ swz) << 4), w[0], w[1],
-                       w[2], w[3]);
+          if (!P_TMEM)
+            st_shared_v4(pb + h * kHalf + ((static_cast<uint32_t>(c8) ^ swz) << 4), w[0], w[1],
+                         w[2], w[3]);
         }
       const float lsum = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
       l_run = l_run * r + lsum;
-      fence_proxy_async_smem();  // P is read by the MMA (async proxy)
+      if (P_TMEM) {
+        tmem_st_32x32b_x32(tl + kPCol + s * 64, pw[0]);
+        tmem_st_32x32b_x32(tl + kPCol + s * 64 + 32, pw[1]);
+        tmem_st_wait();
+      } else {
+        fence_proxy_async_smem();  // P is read by the MMA (async proxy)
+      }
       if (rescale) {
         // The reference point moved: scale the accumulated row of O by r once P V of block
         // j - 1 has landed in TMEM (lanes whose point did not move multiply by 1).
@@ -396,16 +427,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-std::atomic<uint64_t> g_attr_done[2];
+std::atomic<uint64_t> g_attr_done[4];
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool P_TMEM>
 cudaError_t launch_variant(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                            const CUtensorMap& mo, const AttnParams& p, cudaStream_t s) {
-  auto kern = attn_fwd_kernel<CAUSAL>;
-  cudaError_t e = ensure_smem_attr(kern, static_cast<int>(kSmemBytes), g_attr_done[CAUSAL ? 1 : 0]);
+  auto kern = attn_fwd_kernel<CAUSAL, P_TMEM>;
+  constexpr uint32_t smem = smem_bytes(P_TMEM);
+  cudaError_t e = ensure_smem_attr(kern, static_cast<int>(smem), g_attr_done[(CAUSAL ? 1 : 0) + (P_TMEM ? 2 : 0)]);
   if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>(p.batch * p.q_tiles));
-  return launch_pdl(kern, grid, dim3(kThreads), kSmemBytes, s, mq, mk, mv, mo, p);
+  return launch_pdl(kern, grid, dim3(kThreads), smem, s, mq, mk, mv, mo, p);
 }
 
 }  // namespace
@@ -426,8 +458,14 @@ cudaError_t launch_attention(const AttnParams& p, bool causal, const void* Q, in
   if (!map(&mq, Q, p.Lq, ldq, sQ) || !map(&mk, K, p.Lkv, ldk, sK) || !map(&mv, V, p.Lkv, ldv, sV) ||
       !map(&mo, O, p.Lq, ldo, sO))
     return cudaErrorInvalidValue;
-  return causal ? launch_variant<true>(mq, mk, mv, mo, p, s)
-                : launch_variant<false>(mq, mk, mv, mo, p, s);
+  // P in TMEM unless DG_ATTN_P_SMEM=1 (the shared-memory P tile, kept for comparison).
+  const char* e = std::getenv("DG_ATTN_P_SMEM");
+  const bool p_smem = e && e[0] == '1';
+  if (p_smem)
+    return causal ? launch_variant<true, false>(mq, mk, mv, mo, p, s)
+                  : launch_variant<false, false>(mq, mk, mv, mo, p, s);
+  return causal ? launch_variant<true, true>(mq, mk, mv, mo, p, s)
+                : launch_variant<false, true>(mq, mk, mv, mo, p, s);
 }
 
 }  // namespace dg

@@ -27,6 +27,16 @@ def torch():
     return t
 
 
+@pytest.fixture(params=["p_tmem", "p_smem"])
+def p_mode(request, monkeypatch):
+    # P (the BF16 weights) in tensor memory, or in a swizzled shared-memory tile.
+    if request.param == "p_smem":
+        monkeypatch.setenv("DG_ATTN_P_SMEM", "1")
+    else:
+        monkeypatch.delenv("DG_ATTN_P_SMEM", raising=False)
+    return request.param
+
+
 def run(torch, w, O_fill=float("nan")):
     b, Lq = w["batch"], w["Lq"]
     n_out = (b - 1) * w["sO"] + (Lq - 1) * w["ldo"] + w["d"] if b > 0 and Lq > 0 else 1
@@ -64,7 +74,7 @@ def check(Ob, w, rows=None, what=""):
     (2, 128, 1, False),       # one key: O = V[0]
     (1, 64, 1000, False),     # one partial query tile, eight key blocks
 ])
-def test_attention_parity(torch, batch, L, Lkv, causal):
+def test_attention_parity(torch, p_mode, batch, L, Lkv, causal):
     w = inputs.attention(batch, L, causal=causal, Lkv=Lkv)
     Ob = run(torch, w)
     check(Ob, w, what=f"attention b={batch} L={L} Lkv={Lkv} causal={causal}")
@@ -72,7 +82,7 @@ def test_attention_parity(torch, batch, L, Lkv, causal):
         assert np.array_equal(gather(Ob, w)[:, :, :], np.broadcast_to(w["V"][:, :1, :], (batch, L, 128)))
 
 
-def test_attention_large_score_spread(torch):
+def test_attention_large_score_spread(torch, p_mode):
     # Q scaled by 8: scores spread over ~+-90, so the reference maximum moves on many
     # blocks and the TMEM rescale of O runs; causal and non-causal.
     for causal in (False, True):
@@ -98,7 +108,7 @@ def test_attention_padded_strides(torch):
     assert np.all((Ob[~written] & 0x7FFF) > 0x7F80), "padding of O was written"
 
 
-def test_attention_batched_full_size_sampled(torch):
+def test_attention_batched_full_size_sampled(torch, p_mode):
     # The batched shape (64 heads x 2048 x 128, non-causal), 48 sampled query rows per head
     # including the first and last of each 128-row tile edge.
     w = inputs.attention()
