@@ -732,13 +732,54 @@ dg_status attention_bf16(int64_t batch, int64_t Lq, int64_t Lkv, int64_t d, floa
   p.Lq = Lq;
   p.Lkv = Lkv;
   p.q_tiles = q_tiles;
+  p.kv_blocks = cdiv(Lkv, 128);
+  // Split over keys when the query tiles alone do not fill the GPU: chunks of `chunk` key
+  // blocks, the smallest chunk for which the chunks still fit in one wave.
+  p.chunk = 0;
+  p.ws = nullptr;
+  p.counters = nullptr;
+  int64_t items = batch * q_tiles;
+  {
+    auto nk = [&](int64_t t) { return causal ? t + 1 : p.kv_blocks; };
+    const int64_t max_nk = causal ? q_tiles : p.kv_blocks;
+    const char* se = std::getenv("DG_ATTN_SPLIT");
+    const bool allow = !(se && se[0] == '0');
+    if (allow && items < sms && max_nk > 1) {
+      int64_t total = 0;
+      for (int64_t t = 0; t < q_tiles; ++t) total += nk(t);
+      total *= batch;
+      int64_t C = cdiv(total, sms);
+      if (C < 1) C = 1;
+      for (;; ++C) {
+        int64_t cnt = 0;
+        for (int64_t t = 0; t < q_tiles; ++t) cnt += cdiv(nk(t), C);
+        if (cnt * batch <= sms || C >= max_nk) {
+          items = cnt * batch;
+          break;
+        }
+      }
+      if (C < max_nk) p.chunk = C;
+      else items = batch * q_tiles;
+    }
+  }
+  if (p.chunk > 0) {
+    Workspace w;
+    const dg_status ws_st =
+        get_workspace(dev, static_cast<cudaStream_t>(stream), static_cast<size_t>(items * kAttnPartFloats),
+                      static_cast<size_t>(batch * q_tiles), &w);
+    if (ws_st != DG_OK) return ws_st;
+    p.ws = w.ws;
+    p.counters = w.counters;
+  }
+  p.items = items;
   p.c_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);  // log2(e)
   p.rank3 = batch > 1 ? 1 : 0;
   p.status = status;
   if (std::getenv("DG_LOG_PLAN"))
-    std::fprintf(stderr, "[dg] attention_bf16 batch=%lld Lq=%lld Lkv=%lld causal=%d grid=%lld\n",
+    std::fprintf(stderr, "[dg] attention_bf16 batch=%lld Lq=%lld Lkv=%lld causal=%d grid=%lld chunk=%lld\n",
                  static_cast<long long>(batch), static_cast<long long>(Lq),
-                 static_cast<long long>(Lkv), causal ? 1 : 0, static_cast<long long>(batch * q_tiles));
+                 static_cast<long long>(Lkv), causal ? 1 : 0, static_cast<long long>(items),
+                 static_cast<long long>(p.chunk));
   return from_cuda(launch_attention(p, causal != 0, Q, ldq, strideQ, K, ldk, strideK, V, ldv,
                                     strideV, O, ldo, strideO, s));
 }

@@ -35,7 +35,14 @@ namespace dg {
 namespace {
 
 constexpr int kBQ = 128, kBKV = 128, kHD = 128;
-constexpr int kThreads = 192;
+// Softmax warps per 128 rows: 4 (one row per thread, all 128 keys of a block) or 8 (two
+// warps per row quadrant, 64 keys each).  Measured: 4 is faster (1007 vs 900 TFLOPS on 64
+// heads x 2048): with 8 every row's maximum is taken twice and the exponential / conversion
+// pipe, not latency, bounds the softmax.
+constexpr int kSoftWarps = 4;
+constexpr int kHalves = kSoftWarps / 4;       // key / column parts per row
+constexpr int kKeysPer = kBKV / kHalves;      // keys of a block per thread
+constexpr int kThreads = 64 + 32 * kSoftWarps;
 constexpr uint32_t kTile = 128 * kHD * 2;  // 128 rows x 128 BF16: two 64-column boxes, 32 KiB
 constexpr uint32_t kHalf = kTile / 2;      // one 128-row x 64-column box (128-byte rows)
 constexpr uint32_t kTmemCols = 512;        // S[0] at 0, S[1] at 128, O at 256, P[0..1] at 384
@@ -43,8 +50,7 @@ constexpr uint32_t kOCol = 256;
 constexpr uint32_t kPCol = 384;            // P in TMEM: 64 columns (128 BF16 pairs) per buffer
 constexpr float kMoveLog2 = 8.f;           // move m when the block raises it by > 8 (log2)
 
-// Shared memory: Q | K[2] | V[2] | P[2] (32 KiB each, 1024-byte aligned) | control; with P in
-// TMEM the P tiles are not allocated.
+// Shared memory: Q | K[2] | V[2] (32 KiB each, 1024-byte aligned) | control | l exchange.
 struct AttnCtl {
   uint64_t qfull;
   uint64_t kfull[2], kempty[2], vfull[2], vempty[2];
@@ -52,9 +58,12 @@ struct AttnCtl {
   uint64_t drain;
   uint32_t tmem_base;
   uint32_t abort;
+  uint32_t is_last;  // split over keys: this CTA merges the tile's chunks
+  uint32_t epi_ok;   // the softmax warps' common verdict before the epilogue
 };
 static_assert(sizeof(AttnCtl) <= 256, "control block");
-constexpr uint32_t smem_bytes(bool p_tmem) { return 1024 + (p_tmem ? 5 : 7) * kTile + 256; }
+// Q | K[2] | V[2] (32 KiB each) | control (256 B) | the halves' l exchange (1 KiB).
+constexpr uint32_t kSmemBytes = 1024 + 5 * kTile + 256 + 1024;
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -96,7 +105,13 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void softmax_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * kSoftWarps) : "memory");
+}
+
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
 
 __device__ __forceinline__ void load_box(uint32_t dst, const CUtensorMap* m, uint32_t bar,
                                          int32_t x, int32_t y, int32_t z, bool rank3) {
@@ -117,9 +132,9 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __all_sync(0xffffffffu, ok);
 }
 
-// P_TMEM: the softmax writes P into TMEM (tcgen05.st) and the P V MMA reads its A operand
-// from there, so only V passes through shared memory for that product.
-template <bool CAUSAL, bool P_TMEM>
+// The softmax writes P into TMEM (tcgen05.st) and the P V MMA reads its A operand from there,
+// so only V passes through shared memory for that product.
+template <bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -127,18 +142,43 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle atoms need 1024-byte alignment
-  const uint32_t sQ = base, sK = base + kTile, sV = base + 3 * kTile, sP = base + 5 * kTile;
-  AttnCtl* ctl = reinterpret_cast<AttnCtl*>(smem_raw + (base - raw) + (P_TMEM ? 5 : 7) * kTile);
+  const uint32_t sQ = base, sK = base + kTile, sV = base + 3 * kTile;
+  AttnCtl* ctl = reinterpret_cast<AttnCtl*>(smem_raw + (base - raw) + 5 * kTile);
+  float* xl = reinterpret_cast<float*>(smem_raw + (base - raw) + 5 * kTile + 256);  // [2][128]
   volatile uint32_t* abort = &ctl->abort;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Work item: causal tiles in decreasing query order, so the longest rows start first.
-  const int64_t id = blockIdx.x;
-  const int64_t qt = p.q_tiles - 1 - id / p.batch;
-  const int64_t b = id % p.batch;
+  // Work item: query tiles in decreasing order (causal: the longest rows start first); with
+  // a split over keys, the tile's chunk `kc` of nch covers its key blocks j0 .. j0 + nkv - 1.
+  int64_t qt, b, j0 = 0, kc = 0, nch = 1, nkv;
+  {
+    int64_t id = blockIdx.x;
+    if (p.chunk > 0) {
+      qt = 0;
+      b = 0;
+      nkv = 0;
+      for (int64_t t = p.q_tiles - 1; t >= 0; --t) {
+        const int64_t nk = CAUSAL ? t + 1 : p.kv_blocks;
+        const int64_t ch = (nk + p.chunk - 1) / p.chunk;
+        if (id < ch * p.batch) {
+          qt = t;
+          b = id % p.batch;
+          kc = id / p.batch;
+          nch = ch;
+          j0 = kc * p.chunk;
+          nkv = (nk - j0 < p.chunk ? nk - j0 : p.chunk);
+          break;
+        }
+        id -= ch * p.batch;
+      }
+    } else {
+      qt = p.q_tiles - 1 - id / p.batch;
+      b = id % p.batch;
+      nkv = CAUSAL ? qt + 1 : p.kv_blocks;
+    }
+  }
   const int64_t q0 = qt * kBQ;
-  const int64_t nkv = CAUSAL ? qt + 1 : (p.Lkv + kBKV - 1) / kBKV;
   const bool rank3 = p.rank3 != 0;
 
   if (threadIdx.x == 0) {
@@ -149,11 +189,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&ctl->vfull[s]), 1);
       mbar_init(smem_u32(&ctl->vempty[s]), 1);
       mbar_init(smem_u32(&ctl->sfull[s]), 1);
-      mbar_init(smem_u32(&ctl->pfull[s]), 4);  // one arrival per softmax warp
+      mbar_init(smem_u32(&ctl->pfull[s]), kSoftWarps);  // one arrival per softmax warp
       mbar_init(smem_u32(&ctl->odone[s]), 1);
     }
     mbar_init(smem_u32(&ctl->drain), 1);
     ctl->abort = 0;
+    ctl->is_last = 1;
     fence_barrier_init();
     tma_prefetch_map(&tmQ);
     tma_prefetch_map(&tmK);
@@ -183,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool k_only = false; // the last block's K load was issued but not its V load
       for (int64_t j = 0; j < nkv; ++j) {
         const uint32_t s = j & 1, ph = (j >> 1) & 1;
-        const int32_t y = static_cast<int32_t>(j * kBKV);
+        const int32_t y = static_cast<int32_t>((j0 + j) * kBKV);
         if (!mbar_wait(smem_u32(&ctl->kempty[s]), ph ^ 1u, abort, p.status, kDevTimeoutProducer)) break;
         const uint32_t kf = smem_u32(&ctl->kfull[s]);
         mbar_arrive_expect_tx(kf, kTile);
@@ -244,19 +285,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t pb = sP + s * kTile, vb = sV + s * kTile;
+        const uint32_t vb = sV + s * kTile;
 #pragma unroll
         for (int k = 0; k < kBKV / 16; ++k) {
           // P: 16 keys = 32 bytes in the swizzle row (second box for keys 64..127).
           // V: 16 key rows = 2 KiB; its two 64-column halves of d are one box apart (LBO).
           const uint64_t bdesc = sdesc_sw128(vb + k * 2048, kHalf, 1024);
-          if (P_TMEM) {
-            // 16 keys of P = 8 packed columns of the TMEM P buffer.
-            umma_bf16_ts(tmem + kOCol, tmem + kPCol + s * 64 + k * 8, bdesc, idO, (j > 0 || k > 0) ? 1u : 0u);
-          } else {
-            const uint64_t adesc = sdesc_sw128(pb + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
-            umma_bf16(tmem + kOCol, adesc, bdesc, idO, (j > 0 || k > 0) ? 1u : 0u);
-          }
+          // 16 keys of P = 8 packed columns of the TMEM P buffer.
+          umma_bf16_ts(tmem + kOCol, tmem + kPCol + s * 64 + k * 8, bdesc, idO, (j > 0 || k > 0) ? 1u : 0u);
         }
         umma_commit(smem_u32(&ctl->vempty[s]));
         umma_commit(smem_u32(&ctl->odone[s]));
@@ -268,7 +304,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
+    // One query row per thread (the TMEM lane of warp w % 4's quadrant).  With 8 warps, warps
+    // w and w + 4 split each block's keys and the row's columns of O in halves; both read the
+    // whole row of scores for its maximum, so both take the same reference point without
+    // exchanging anything, and their parts of l are added at the end.
     const int qd = warp & 3;                 // TMEM lane quadrant this warp may access
+    const int half = kHalves == 1 ? 0 : (warp - 2) >> 2;  // which keys of a block / columns of O
     const int row = qd * 32 + lane;          // query row in the tile = TMEM lane
     const int64_t qrow = q0 + row;
     const uint32_t tl = tmem + (static_cast<uint32_t>(qd * 32) << 16);
@@ -288,8 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tl + s * 128 + c * 32, sv[c]);
       tmem_ld_wait();
-      const int64_t kv0 = j * kBKV;
-      if (kv0 + kBKV > p.Lkv || (CAUSAL && j == nkv - 1)) {
+      const int64_t kv0 = (j0 + j) * kBKV;
+      if (kv0 + kBKV > p.Lkv || (CAUSAL && j0 + j == qt)) {
         // Keys at or past `lim` are not visible to this row: weight 0.
         const int64_t lim = CAUSAL ? (qrow + 1 < p.Lkv ? qrow + 1 : p.Lkv) : p.Lkv;
         const int64_t nv = lim - kv0;
@@ -325,52 +366,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       float ls8[8];
 #pragma unroll
       for (int t = 0; t < 8; ++t) ls8[t] = 0.f;
-      const uint32_t pb = sP + s * kTile + prow;
-      uint32_t pw[2][32];  // P_TMEM: the row's 128 weights as 64 packed BF16 pairs
+      uint32_t pw[kKeysPer / 64][32];  // this thread's weights as packed BF16 pairs
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
+      for (int c = 0; c < kKeysPer / 32; ++c)
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i0 = h * 64 + c8 * 8 + 2 * e;
-            const float p0 = ex2(fmaf(__uint_as_float(sv[i0 >> 5][i0 & 31]), cl, nb));
-            const float p1 = ex2(fmaf(__uint_as_float(sv[(i0 + 1) >> 5][(i0 + 1) & 31]), cl, nb));
-            ls8[(c8 & 1) * 4 + e] += p0 + p1;
-            w[e] = pack2(p0, p1);
-            pw[h][c8 * 4 + e] = w[e];
-          }
-          // Row `row` of the 128B-swizzled K-major tile: 16-byte chunk c8 of box h.
-          if (!P_TMEM)
-            st_shared_v4(pb + h * kHalf + ((static_cast<uint32_t>(c8) ^ swz) << 4), w[0], w[1],
-                         w[2], w[3]);
+        for (int k = 0; k < 16; ++k) {
+          const int cc = half * (kKeysPer / 32) + c;  // 32-key chunk of the block
+          const float p0 = ex2(fmaf(__uint_as_float(sv[cc][2 * k]), cl, nb));
+          const float p1 = ex2(fmaf(__uint_as_float(sv[cc][2 * k + 1]), cl, nb));
+          ls8[k & 7] += p0 + p1;
+          pw[c >> 1][(c & 1) * 16 + k] = pack2(p0, p1);
         }
       const float lsum = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
       l_run = l_run * r + lsum;
-      if (P_TMEM) {
-        tmem_st_32x32b_x32(tl + kPCol + s * 64, pw[0]);
-        tmem_st_32x32b_x32(tl + kPCol + s * 64 + 32, pw[1]);
-        tmem_st_wait();
-      } else {
-        fence_proxy_async_smem();  // P is read by the MMA (async proxy)
-      }
+#pragma unroll
+      for (int c = 0; c < kKeysPer / 64; ++c)
+        tmem_st_32x32b_x32(tl + kPCol + s * 64 + half * (kKeysPer / 2) + c * 32, pw[c]);
+      tmem_st_wait();
       if (rescale) {
-        // The reference point moved: scale the accumulated row of O by r once P V of block
-        // j - 1 has landed in TMEM (lanes whose point did not move multiply by 1).
+        // The reference point moved: scale this half's 64 columns of the row of O by r once
+        // P V of block j - 1 has landed in TMEM (lanes whose point did not move multiply by 1).
         if (!warp_wait(smem_u32(&ctl->odone[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 4 / kHalves; ++c) {
           uint32_t o[32];
-          tmem_ld_32x32b_x32(tl + kOCol + c * 32, o);
+          tmem_ld_32x32b_x32(tl + kOCol + half * (128 / kHalves) + c * 32, o);
           tmem_ld_wait();
 #pragma unroll
           for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * r);
-          tmem_st_32x32b_x32(tl + kOCol + c * 32, o);
+          tmem_st_32x32b_x32(tl + kOCol + half * (128 / kHalves) + c * 32, o);
         }
         tmem_st_wait();
       }
@@ -382,30 +410,120 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t jl = nkv - 1;
       ok = warp_wait(smem_u32(&ctl->odone[jl & 1]), (jl >> 1) & 1, abort, p.status);
     }
-    if (ok) {
-      // O = u / l, rounded once to BF16, staged in the (no longer read) Q tile in the
-      // layout of the output tensor map's 128B-swizzled boxes.
-      tc_fence_after();
-      const float inv = 1.f / l_run;
-      const uint32_t ob = sQ + prow;
+    // Writes 32 values of this row's O (columns 32c .. 32c+31, already divided by l) as BF16
+    // into the (no longer read) Q tile, in the layout of the output map's 128B-swizzled boxes.
+    const uint32_t ob = sQ + prow;
+    auto stage = [&](int c, const float (&f)[32]) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const uint32_t chunk = static_cast<uint32_t>((c & 1) * 4 + q4);
+        st_shared_v4(ob + (c >> 1) * kHalf + ((chunk ^ swz) << 4), pack2(f[8 * q4], f[8 * q4 + 1]),
+                     pack2(f[8 * q4 + 2], f[8 * q4 + 3]), pack2(f[8 * q4 + 4], f[8 * q4 + 5]),
+                     pack2(f[8 * q4 + 6], f[8 * q4 + 7]));
+      }
+    };
+    // The eight softmax warps take one decision (the split path below has group barriers):
+    // any failed wait has set the abort flag before this barrier.  The row's l is the sum
+    // of the two halves' parts, half 0's first.
+    xl[half * 128 + row] = l_run;
+    softmax_bar();
+    if (threadIdx.x == 64) ctl->epi_ok = (ok && !*abort) ? 1u : 0u;
+    softmax_bar();
+    ok = ctl->epi_ok != 0;
+    const float l_tot = kHalves == 1 ? l_run : xl[row] + xl[128 + row];
+    constexpr int kCols = 4 / kHalves;  // 32-column chunks of O per thread
+    if (ok && nch == 1) {
+      // O = u / l, rounded once to BF16.
+      tc_fence_after();
+      const float inv = 1.f / l_tot;
+#pragma unroll
+      for (int c = kCols * half; c < kCols * half + kCols; ++c) {
         uint32_t o[32];
         tmem_ld_32x32b_x32(tl + kOCol + c * 32, o);
         tmem_ld_wait();
+        float f[32];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const uint32_t chunk = static_cast<uint32_t>((c & 1) * 4 + q4);
-          const float* f = reinterpret_cast<const float*>(o) + 8 * q4;
-          st_shared_v4(ob + (c >> 1) * kHalf + ((chunk ^ swz) << 4), pack2(f[0] * inv, f[1] * inv),
-                       pack2(f[2] * inv, f[3] * inv), pack2(f[4] * inv, f[5] * inv),
-                       pack2(f[6] * inv, f[7] * inv));
-        }
+        for (int k = 0; k < 32; ++k) f[k] = __uint_as_float(o[k]) * inv;
+        stage(c, f);
       }
       fence_proxy_async_smem();
+    } else if (ok) {
+      // Split over keys: publish this chunk's state (u unnormalised in FP32, m and l per row),
+      // take a ticket; the chunk that takes the last merges all chunks in chunk order with
+      // the pages' recurrence: m* = max m_k, l* = sum 2^(m_k - m*) l_k,
+      // u* = sum 2^(m_k - m*) u_k, O = u* / l*.
+      tc_fence_after();
+      float* mine = p.ws + static_cast<int64_t>(blockIdx.x) * kAttnPartFloats;
+      {
+        float4* u4 = reinterpret_cast<float4*>(mine);
+#pragma unroll
+        for (int c = kCols * half; c < kCols * half + kCols; ++c) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(tl + kOCol + c * 32, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int g = 0; g < 8; ++g)
+            __stcg(u4 + (c * 8 + g) * 128 + row,
+                   make_float4(__uint_as_float(o[4 * g]), __uint_as_float(o[4 * g + 1]),
+                               __uint_as_float(o[4 * g + 2]), __uint_as_float(o[4 * g + 3])));
+        }
+        if (half == 0) {
+          __stcg(mine + 128 * 128 + row, m_run);
+          __stcg(mine + 128 * 128 + 128 + row, l_tot);
+        }
+      }
+      softmax_bar();
+      uint32_t* counter = &p.counters[b * p.q_tiles + qt];
+      if (threadIdx.x == 64) {
+        fence_acq_rel_gpu();  // cumulative: the 128 threads' stores, ordered by the barrier
+        const uint32_t prev = atomicAdd(counter, 1u);
+        const bool last = prev + 1u == static_cast<uint32_t>(nch);
+        if (last) {
+          fence_acq_rel_gpu();
+          *counter = 0u;  // every chunk holds its ticket: ready for the next call
+        }
+        ctl->is_last = last ? 1u : 0u;
+      }
+      softmax_bar();
+      if (ctl->is_last) {
+        // The tile's chunks are the items blockIdx.x + (k - kc) * batch, k < nch.
+        const float* first = mine - kc * p.batch * kAttnPartFloats;
+        auto part = [&](int64_t k) { return first + k * p.batch * kAttnPartFloats; };
+        float ms = -INFINITY;
+        for (int64_t k = 0; k < nch; ++k) ms = fmaxf(ms, __ldcg(part(k) + 128 * 128 + row));
+        float ls = 0.f;
+        for (int64_t k = 0; k < nch; ++k)
+          ls += ex2(__ldcg(part(k) + 128 * 128 + row) - ms) * __ldcg(part(k) + 128 * 128 + 128 + row);
+        const float inv = 1.f / ls;
+#pragma unroll 1
+        for (int c = kCols * half; c < kCols * half + kCols; ++c) {
+          float f[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) f[k] = 0.f;
+          for (int64_t k = 0; k < nch; ++k) {
+            const float* pk = part(k);
+            const float w = ex2(__ldcg(pk + 128 * 128 + row) - ms);
+            const float4* u4 = reinterpret_cast<const float4*>(pk) + c * 8 * 128 + row;
+            float4 v[8];
+#pragma unroll
+            for (int g = 0; g < 8; ++g) v[g] = __ldcg(u4 + g * 128);
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+              f[4 * g] = fmaf(w, v[g].x, f[4 * g]);
+              f[4 * g + 1] = fmaf(w, v[g].y, f[4 * g + 1]);
+              f[4 * g + 2] = fmaf(w, v[g].z, f[4 * g + 2]);
+              f[4 * g + 3] = fmaf(w, v[g].w, f[4 * g + 3]);
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < 32; ++k) f[k] *= inv;
+          stage(c, f);
+        }
+        fence_proxy_async_smem();
+      }
     }
     softmax_bar();
-    if (warp == 2 && lane == 0 && !*abort) {
+    if (warp == 2 && lane == 0 && !*abort && ctl->is_last) {
       // Rows past Lq are clipped by the tensor map.
       if (rank3) {
         tma_store_3d(&tmO, sQ, 0, static_cast<int32_t>(q0), zb);
@@ -427,16 +545,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-std::atomic<uint64_t> g_attr_done[4];
+std::atomic<uint64_t> g_attr_done[2];
 
-template <bool CAUSAL, bool P_TMEM>
+template <bool CAUSAL>
 cudaError_t launch_variant(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                            const CUtensorMap& mo, const AttnParams& p, cudaStream_t s) {
-  auto kern = attn_fwd_kernel<CAUSAL, P_TMEM>;
-  constexpr uint32_t smem = smem_bytes(P_TMEM);
-  cudaError_t e = ensure_smem_attr(kern, static_cast<int>(smem), g_attr_done[(CAUSAL ? 1 : 0) + (P_TMEM ? 2 : 0)]);
+  auto kern = attn_fwd_kernel<CAUSAL>;
+  constexpr uint32_t smem = kSmemBytes;
+  cudaError_t e = ensure_smem_attr(kern, static_cast<int>(smem), g_attr_done[CAUSAL ? 1 : 0]);
   if (e != cudaSuccess) return e;
-  const dim3 grid(static_cast<unsigned>(p.batch * p.q_tiles));
+  const dim3 grid(static_cast<unsigned>(p.items));
   return launch_pdl(kern, grid, dim3(kThreads), smem, s, mq, mk, mv, mo, p);
 }
 
@@ -458,14 +576,8 @@ cudaError_t launch_attention(const AttnParams& p, bool causal, const void* Q, in
   if (!map(&mq, Q, p.Lq, ldq, sQ) || !map(&mk, K, p.Lkv, ldk, sK) || !map(&mv, V, p.Lkv, ldv, sV) ||
       !map(&mo, O, p.Lq, ldo, sO))
     return cudaErrorInvalidValue;
-  // P in TMEM unless DG_ATTN_P_SMEM=1 (the shared-memory P tile, kept for comparison).
-  const char* e = std::getenv("DG_ATTN_P_SMEM");
-  const bool p_smem = e && e[0] == '1';
-  if (p_smem)
-    return causal ? launch_variant<true, false>(mq, mk, mv, mo, p, s)
-                  : launch_variant<false, false>(mq, mk, mv, mo, p, s);
-  return causal ? launch_variant<true, true>(mq, mk, mv, mo, p, s)
-                : launch_variant<false, true>(mq, mk, mv, mo, p, s);
+  return causal ? launch_variant<true>(mq, mk, mv, mo, p, s)
+                : launch_variant<false>(mq, mk, mv, mo, p, s);
 }
 
 }  // namespace dg

@@ -141,10 +141,21 @@ cudaError_t launch_quantize_rows(int64_t rows, int64_t cols, const void* X, int6
 struct AttnParams {
   int64_t batch, Lq, Lkv;
   int64_t q_tiles;     // ceil(Lq / 128)
+  int64_t kv_blocks;   // ceil(Lkv / 128)
   float c_log2;        // scale * log2(e)
   int32_t rank3;       // batch > 1: 3-D tensor maps
+  // Split over keys (0: none): a query tile's key blocks are cut into chunks of `chunk`
+  // blocks, one CTA each; the chunks' (m, l, u) go to ws, [item][32 column groups][128
+  // rows] float4 then m[128], l[128], and the last chunk to finish (counters[b * q_tiles +
+  // tile], zero between calls) merges them in chunk order.
+  int64_t chunk;
+  int64_t items;       // grid size: work items (query tiles, or their key chunks)
+  float* ws;
+  uint32_t* counters;
   uint32_t* status;
 };
+// Floats of one split-key partial: u (128 x 128) and the row statistics m, l.
+constexpr int64_t kAttnPartFloats = 128 * 128 + 2 * 128;
 // Q, O: [batch][Lq][ld] bf16; K, V: [batch][Lkv][ld] bf16 (d = 128 contiguous columns).
 cudaError_t launch_attention(const AttnParams& p, bool causal, const void* Q, int64_t ldq,
                              int64_t sQ, const void* K, int64_t ldk, int64_t sK, const void* V,

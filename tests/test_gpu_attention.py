@@ -27,13 +27,14 @@ def torch():
     return t
 
 
-@pytest.fixture(params=["p_tmem", "p_smem"])
-def p_mode(request, monkeypatch):
-    # P (the BF16 weights) in tensor memory, or in a swizzled shared-memory tile.
-    if request.param == "p_smem":
-        monkeypatch.setenv("DG_ATTN_P_SMEM", "1")
+@pytest.fixture(params=["split", "nosplit"])
+def split_mode(request, monkeypatch):
+    # Key blocks split over CTAs (merged with the recurrence) when the query tiles do not
+    # fill the GPU, or one CTA per query tile.
+    if request.param == "nosplit":
+        monkeypatch.setenv("DG_ATTN_SPLIT", "0")
     else:
-        monkeypatch.delenv("DG_ATTN_P_SMEM", raising=False)
+        monkeypatch.delenv("DG_ATTN_SPLIT", raising=False)
     return request.param
 
 
@@ -74,7 +75,7 @@ def check(Ob, w, rows=None, what=""):
     (2, 128, 1, False),       # one key: O = V[0]
     (1, 64, 1000, False),     # one partial query tile, eight key blocks
 ])
-def test_attention_parity(torch, p_mode, batch, L, Lkv, causal):
+def test_attention_parity(torch, split_mode, batch, L, Lkv, causal):
     w = inputs.attention(batch, L, causal=causal, Lkv=Lkv)
     Ob = run(torch, w)
     check(Ob, w, what=f"attention b={batch} L={L} Lkv={Lkv} causal={causal}")
@@ -82,7 +83,7 @@ def test_attention_parity(torch, p_mode, batch, L, Lkv, causal):
         assert np.array_equal(gather(Ob, w)[:, :, :], np.broadcast_to(w["V"][:, :1, :], (batch, L, 128)))
 
 
-def test_attention_large_score_spread(torch, p_mode):
+def test_attention_large_score_spread(torch, split_mode):
     # Q scaled by 8: scores spread over ~+-90, so the reference maximum moves on many
     # blocks and the TMEM rescale of O runs; causal and non-causal.
     for causal in (False, True):
@@ -108,7 +109,7 @@ def test_attention_padded_strides(torch):
     assert np.all((Ob[~written] & 0x7FFF) > 0x7F80), "padding of O was written"
 
 
-def test_attention_batched_full_size_sampled(torch, p_mode):
+def test_attention_batched_full_size_sampled(torch):
     # The batched shape (64 heads x 2048 x 128, non-causal), 48 sampled query rows per head
     # including the first and last of each 128-row tile edge.
     w = inputs.attention()
@@ -117,7 +118,7 @@ def test_attention_batched_full_size_sampled(torch, p_mode):
     check(run(torch, w), w, rows=rows, what="attention 64x2048")
 
 
-def test_attention_causal_8k_sampled(torch):
+def test_attention_causal_8k_sampled(torch, split_mode):
     # One causal head of 8192 tokens (the pages' experiment), sampled rows across the sequence.
     w = inputs.attention(1, 8192, causal=True)
     rows = np.unique(np.concatenate([[0, 1, 127, 128, 8191],
@@ -125,7 +126,7 @@ def test_attention_causal_8k_sampled(torch):
     check(run(torch, w), w, rows=rows, what="attention causal 8192")
 
 
-def test_attention_deterministic(torch):
+def test_attention_deterministic(torch, split_mode):
     w = inputs.attention(4, 512, causal=True)
     outs = [run(torch, w) for _ in range(3)]
     assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
