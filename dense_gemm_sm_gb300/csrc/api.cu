@@ -772,6 +772,7 @@ dg_status attention_bf16(int64_t batch, int64_t Lq, int64_t Lkv, int64_t d, floa
     p.counters = w.counters;
   }
   p.items = items;
+  p.sms = sms;
   p.c_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);  // log2(e)
   p.rank3 = batch > 1 ? 1 : 0;
   p.status = status;

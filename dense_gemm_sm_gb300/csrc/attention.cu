@@ -545,6 +545,332 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------------------
+// Two query tiles per CTA (non-causal attention with enough tiles to fill the GPU; opt-in,
+// see launch_attention).  The
+// tiles A and B share every K and V block; each has its own softmax group of four warps
+// (warps 2-5: A, 6-9: B) and its own S and O in TMEM (S_A 0, O_A 128, S_B 256, O_B 384; the
+// weights P are written over the first 64 columns of their S after S has been read).  While
+// one group exponentiates, the tensor core runs the other group's P V and S products, so
+// the two groups' softmax latencies and the MMAs overlap.  The MMA issuer waits for P V of
+// block j to complete before it overwrites that tile's S (and P) with block j + 1.
+constexpr uint32_t kPairSmemBytes = 1024 + 6 * kTile + 256;  // Q_A, Q_B, K[2], V[2], control
+constexpr int kPairThreads = 320;
+
+struct PairCtl {
+  uint64_t qfull;
+  uint64_t kfull[2], kempty[2], vfull[2], vempty[2];
+  uint64_t sfull[2], pfull[2], odone[2];  // per tile (A, B)
+  uint64_t drain;
+  uint32_t tmem_base;
+  uint32_t abort;
+};
+static_assert(sizeof(PairCtl) <= 256, "control block");
+
+__device__ __forceinline__ void group_bar(int g) {
+  // Named barriers 2 and 3: the four warps of softmax group g.
+  asm volatile("bar.sync %0, 128;" ::"r"(2 + g) : "memory");
+}
+
+__global__ void __launch_bounds__(kPairThreads, 1)
+    attn_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                     const AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  const uint32_t sQ = base, sK = base + 2 * kTile, sV = base + 4 * kTile;  // Q_A, Q_B, K[2], V[2]
+  PairCtl* ctl = reinterpret_cast<PairCtl*>(smem_raw + (base - raw) + 6 * kTile);
+  volatile uint32_t* abort = &ctl->abort;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const int64_t pairs = (p.q_tiles + 1) / 2;
+  const int64_t pi = static_cast<int64_t>(blockIdx.x) / p.batch;
+  const int64_t b = static_cast<int64_t>(blockIdx.x) % p.batch;
+  const int64_t qtA = 2 * pi;
+  const bool hasB = qtA + 1 < p.q_tiles;
+  const int64_t nkv = p.kv_blocks;
+  const bool rank3 = p.rank3 != 0;
+  (void)pairs;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&ctl->qfull), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&ctl->kfull[s]), 1);
+      mbar_init(smem_u32(&ctl->kempty[s]), 1);
+      mbar_init(smem_u32(&ctl->vfull[s]), 1);
+      mbar_init(smem_u32(&ctl->vempty[s]), 1);
+      mbar_init(smem_u32(&ctl->sfull[s]), 1);
+      mbar_init(smem_u32(&ctl->pfull[s]), 4);
+      mbar_init(smem_u32(&ctl->odone[s]), 1);
+    }
+    mbar_init(smem_u32(&ctl->drain), 1);
+    ctl->abort = 0;
+    fence_barrier_init();
+    tma_prefetch_map(&tmQ);
+    tma_prefetch_map(&tmK);
+    tma_prefetch_map(&tmV);
+    tma_prefetch_map(&tmO);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  pdl_trigger();
+  pdl_wait();
+
+  const int32_t zb = static_cast<int32_t>(b);
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint32_t qf = smem_u32(&ctl->qfull);
+      mbar_arrive_expect_tx(qf, hasB ? 2 * kTile : kTile);
+      for (int t = 0; t < (hasB ? 2 : 1); ++t) {
+        const int32_t y = static_cast<int32_t>((qtA + t) * kBQ);
+        load_box(sQ + t * kTile, &tmQ, qf, 0, y, zb, rank3);
+        load_box(sQ + t * kTile + kHalf, &tmQ, qf, 64, y, zb, rank3);
+      }
+      int64_t issued = 0;
+      bool k_only = false;
+      for (int64_t j = 0; j < nkv; ++j) {
+        const uint32_t s = j & 1, ph = (j >> 1) & 1;
+        const int32_t y = static_cast<int32_t>(j * kBKV);
+        if (!mbar_wait(smem_u32(&ctl->kempty[s]), ph ^ 1u, abort, p.status, kDevTimeoutProducer)) break;
+        const uint32_t kf = smem_u32(&ctl->kfull[s]);
+        mbar_arrive_expect_tx(kf, kTile);
+        load_box(sK + s * kTile, &tmK, kf, 0, y, zb, rank3);
+        load_box(sK + s * kTile + kHalf, &tmK, kf, 64, y, zb, rank3);
+        k_only = true;
+        if (!mbar_wait(smem_u32(&ctl->vempty[s]), ph ^ 1u, abort, p.status, kDevTimeoutProducer)) break;
+        const uint32_t vf = smem_u32(&ctl->vfull[s]);
+        mbar_arrive_expect_tx(vf, kTile);
+        load_box(sV + s * kTile, &tmV, vf, 0, y, zb, rank3);
+        load_box(sV + s * kTile + kHalf, &tmV, vf, 64, y, zb, rank3);
+        k_only = false;
+        ++issued;
+      }
+      if (*abort) {
+        drain_wait(qf, 0, p.status);
+        const int64_t kl = issued + (k_only ? 1 : 0);
+        for (int64_t j = kl > 2 ? kl - 2 : 0; j < kl; ++j)
+          drain_wait(smem_u32(&ctl->kfull[j & 1]), (j >> 1) & 1, p.status);
+        for (int64_t j = issued > 2 ? issued - 2 : 0; j < issued; ++j)
+          drain_wait(smem_u32(&ctl->vfull[j & 1]), (j >> 1) & 1, p.status);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idO = idesc_bf16_f32(128, 128, false, true);
+      const int nt = hasB ? 2 : 1;
+      bool ok = mbar_wait(smem_u32(&ctl->qfull), 0, abort, p.status, kDevTimeoutMma);
+      // S_t = Q_t K_j^T into tile t's S columns.
+      auto issue_s = [&](int t, uint32_t kb) {
+        const uint32_t qb = sQ + t * kTile;
+#pragma unroll
+        for (int k = 0; k < kHD / 16; ++k) {
+          const uint32_t off = (k >> 2) * kHalf + (k & 3) * 32;
+          umma_bf16(tmem + t * 256, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                    idS, k > 0 ? 1u : 0u);
+        }
+        umma_commit(smem_u32(&ctl->sfull[t]));
+      };
+      if (ok) ok = mbar_wait(smem_u32(&ctl->kfull[0]), 0, abort, p.status, kDevTimeoutMma);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < nt; ++t) issue_s(t, sK);
+        umma_commit(smem_u32(&ctl->kempty[0]));
+      }
+      for (int64_t j = 0; ok && j < nkv; ++j) {
+        const uint32_t s = j & 1, ph = (j >> 1) & 1, jp = j & 1;
+        if (!mbar_wait(smem_u32(&ctl->vfull[s]), ph, abort, p.status, kDevTimeoutMma)) {
+          ok = false;
+          break;
+        }
+        const uint32_t vb = sV + s * kTile;
+        for (int t = 0; t < nt; ++t) {
+          if (!mbar_wait(smem_u32(&ctl->pfull[t]), jp, abort, p.status, kDevTimeoutMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < kBKV / 16; ++k)
+            umma_bf16_ts(tmem + t * 256 + 128, tmem + t * 256 + k * 8, sdesc_sw128(vb + k * 2048, kHalf, 1024),
+                         idO, (j > 0 || k > 0) ? 1u : 0u);
+          umma_commit(smem_u32(&ctl->odone[t]));
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(&ctl->vempty[s]));
+        if (j + 1 < nkv) {
+          const uint32_t s1 = (j + 1) & 1, ph1 = ((j + 1) >> 1) & 1;
+          if (!mbar_wait(smem_u32(&ctl->kfull[s1]), ph1, abort, p.status, kDevTimeoutMma)) {
+            ok = false;
+            break;
+          }
+          for (int t = 0; t < nt; ++t) {
+            // Tile t's S columns hold P of block j until its P V has run.
+            if (!mbar_wait(smem_u32(&ctl->odone[t]), jp, abort, p.status, kDevTimeoutMma)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(t, sK + s1 * kTile);
+          }
+          if (!ok) break;
+          umma_commit(smem_u32(&ctl->kempty[s1]));
+        }
+      }
+      umma_commit(smem_u32(&ctl->drain));
+      drain_wait(smem_u32(&ctl->drain), 0, p.status);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue, per tile
+    const int g = (warp - 2) >> 2;  // tile: 0 = A, 1 = B
+    const int qd = warp & 3;
+    const int row = qd * 32 + lane;
+    const bool active = g == 0 || hasB;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(qd * 32) << 16) + g * 256;
+    const uint32_t swz = static_cast<uint32_t>(row & 7);
+    const uint32_t prow = static_cast<uint32_t>((row >> 3) * 1024 + (row & 7) * 128);
+    const float cl = p.c_log2;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = active;
+    for (int64_t j = 0; ok && j < nkv; ++j) {
+      const uint32_t jp = j & 1;
+      if (!warp_wait(smem_u32(&ctl->sfull[g]), jp, abort, p.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sv[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tl + c * 32, sv[c]);
+      tmem_ld_wait();
+      const int64_t kv0 = j * kBKV;
+      if (kv0 + kBKV > p.Lkv) {
+        const int64_t nv = p.Lkv - kv0;
+        const int nvis = nv > kBKV ? kBKV : static_cast<int>(nv);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            if (c * 32 + k >= nvis) sv[c][k] = 0xFF800000u;
+      }
+      float mx8[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) mx8[t] = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int k = 0; k < 32; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], __uint_as_float(sv[c][k]));
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const float m_blk = mx * cl;
+      float r = 1.f;
+      if (m_blk > m_run + kMoveLog2) {
+        r = ex2(m_run - m_blk);
+        m_run = m_blk;
+      }
+      const bool rescale = j > 0 && __any_sync(0xffffffffu, r != 1.f);
+      const float nb = (m_run == -INFINITY) ? 0.f : -m_run;
+      float ls8[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) ls8[t] = 0.f;
+      uint32_t pw[2][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float p0 = ex2(fmaf(__uint_as_float(sv[c][2 * k]), cl, nb));
+          const float p1 = ex2(fmaf(__uint_as_float(sv[c][2 * k + 1]), cl, nb));
+          ls8[k & 7] += p0 + p1;
+          pw[c >> 1][(c & 1) * 16 + k] = pack2(p0, p1);
+        }
+      const float lsum = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
+      l_run = l_run * r + lsum;
+      // P over the first 64 columns of this tile's S (already read into registers).
+      tmem_st_32x32b_x32(tl, pw[0]);
+      tmem_st_32x32b_x32(tl + 32, pw[1]);
+      tmem_st_wait();
+      if (rescale) {
+        // P V of block j - 1 has completed: the MMA issuer waited for it before computing S
+        // of block j into these columns.
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(tl + 128 + c * 32, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * r);
+          tmem_st_32x32b_x32(tl + 128 + c * 32, o);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->pfull[g]));
+    }
+    if (ok) {
+      const int64_t jl = nkv - 1;
+      ok = warp_wait(smem_u32(&ctl->odone[g]), jl & 1, abort, p.status);
+    }
+    // The group's four warps agree, then write O = u / l through the tile's Q buffer.
+    group_bar(g);
+    const bool store = active && !*abort;
+    group_bar(g);
+    if (store && ok) {
+      tc_fence_after();
+      const float inv = 1.f / l_run;
+      const uint32_t ob = sQ + g * kTile + prow;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld_32x32b_x32(tl + 128 + c * 32, o);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const uint32_t chunk = static_cast<uint32_t>((c & 1) * 4 + q4);
+          const float* f = reinterpret_cast<const float*>(o) + 8 * q4;
+          st_shared_v4(ob + (c >> 1) * kHalf + ((chunk ^ swz) << 4), pack2(f[0] * inv, f[1] * inv),
+                       pack2(f[2] * inv, f[3] * inv), pack2(f[4] * inv, f[5] * inv),
+                       pack2(f[6] * inv, f[7] * inv));
+        }
+      }
+      fence_proxy_async_smem();
+    }
+    group_bar(g);
+    if (store && (warp & 3) == 2 && lane == 0 && !*abort) {
+      const int32_t y = static_cast<int32_t>((qtA + g) * kBQ);
+      const uint32_t src = sQ + g * kTile;
+      if (rank3) {
+        tma_store_3d(&tmO, src, 0, y, zb);
+        tma_store_3d(&tmO, src + kHalf, 64, y, zb);
+      } else {
+        tma_store_2d(&tmO, src, 0, y);
+        tma_store_2d(&tmO, src + kHalf, 64, y);
+      }
+      bulk_commit();
+      bulk_wait<0>();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+std::atomic<uint64_t> g_pair_attr{0};
+
 std::atomic<uint64_t> g_attr_done[2];
 
 template <bool CAUSAL>
@@ -576,6 +902,19 @@ cudaError_t launch_attention(const AttnParams& p, bool causal, const void* Q, in
   if (!map(&mq, Q, p.Lq, ldq, sQ) || !map(&mk, K, p.Lkv, ldk, sK) || !map(&mv, V, p.Lkv, ldv, sV) ||
       !map(&mo, O, p.Lq, ldo, sO))
     return cudaErrorInvalidValue;
+  // DG_ATTN_PAIR=1: non-causal attention with at least one pair of query tiles per SM takes
+  // the two-tile kernel.  Measured slower (890 vs 1004 TFLOPS on 64 heads x 2048): each
+  // tile's chain softmax -> P V -> (wait) -> next S serialises, and two softmax groups per
+  // SM sub-partition slow each other down more than their overlap gains; so one tile per CTA
+  // is the default.
+  const char* pe = std::getenv("DG_ATTN_PAIR");
+  if (!causal && p.chunk == 0 && pe && pe[0] == '1' &&
+      p.batch * ((p.q_tiles + 1) / 2) >= static_cast<int64_t>(p.sms)) {
+    cudaError_t e = ensure_smem_attr(attn_pair_kernel, static_cast<int>(kPairSmemBytes), g_pair_attr);
+    if (e != cudaSuccess) return e;
+    const dim3 grid(static_cast<unsigned>(p.batch * ((p.q_tiles + 1) / 2)));
+    return launch_pdl(attn_pair_kernel, grid, dim3(kPairThreads), kPairSmemBytes, s, mq, mk, mv, mo, p);
+  }
   return causal ? launch_variant<true>(mq, mk, mv, mo, p, s)
                 : launch_variant<false>(mq, mk, mv, mo, p, s);
 }

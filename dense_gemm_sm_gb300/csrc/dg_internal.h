@@ -150,6 +150,7 @@ struct AttnParams {
   // tile], zero between calls) merges them in chunk order.
   int64_t chunk;
   int64_t items;       // grid size: work items (query tiles, or their key chunks)
+  int32_t sms;         // SMs of the device
   float* ws;
   uint32_t* counters;
   uint32_t* status;

@@ -151,3 +151,21 @@ def test_attention_errors(torch):
     assert a(1, 128, 128, 128, s, 0, t, 132, 0, t, 128, 0, t, 128, 0, t, 128, 0) == dg.DG_ERR_MISALIGNED
     assert a(1, 128, 128, 128, s, 0, t.data_ptr() + 2, 128, 0, t, 128, 0, t, 128, 0, t, 128,
              0) == dg.DG_ERR_MISALIGNED
+
+
+@pytest.mark.parametrize("batch,L,Lkv", [(152, 256, 256), (160, 300, 200), (100, 512, 1000)])
+def test_attention_two_tile_kernel(torch, batch, L, Lkv):
+    # The opt-in two-tile kernel (DG_ATTN_PAIR=1) with enough query tiles that each CTA takes
+    # a pair: ragged query and key lengths, a last pair with only one tile; compared in
+    # full, and bit for bit with the default one-tile kernel (the same operations per row in
+    # the same order).
+    import os
+    w = inputs.attention(batch, L, Lkv=Lkv)
+    os.environ["DG_ATTN_PAIR"] = "1"
+    try:
+        Ob = run(torch, w)
+    finally:
+        del os.environ["DG_ATTN_PAIR"]
+    check(Ob, w, what=f"attention two-tile b={batch} L={L} Lkv={Lkv}")
+    Ob1 = run(torch, w)
+    assert np.array_equal(Ob, Ob1)
