@@ -153,8 +153,14 @@ void plan_f32(int64_t M, int64_t N, int64_t K, int64_t batch, int64_t resident, 
   int best_s = 1;
   if (tail > 0) {
     double best = 1.0;  // tail time (in tile times) without splitting
-    const int64_t min_chunk = cdiv(256, kSimtBK);  // K tiles in 256 of K
-    for (int64_t S = 2; S <= KT / min_chunk && tail * S <= 3 * G; ++S) {
+    // At least 256 of K per chunk, so a chunk outweighs its partial tile -- unless the tiles
+    // fill under a quarter of the resident CTA slots (e.g. 256^3: 4 tiles for 304 slots),
+    // where one tile's whole K on one SM is the call's time: then chunks down to one K tile.
+    // (At most 16 chunks then: the last chunk of a tile adds every chunk's partial tile.)
+    const bool few = 4 * T <= G;
+    const int64_t min_chunk = few ? 1 : cdiv(256, kSimtBK);
+    const int64_t max_s = few ? 16 : KT;
+    for (int64_t S = 2; S <= KT / min_chunk && S <= max_s && tail * S <= 3 * G; ++S) {
       const double t = static_cast<double>(cdiv(tail * S, G)) / static_cast<double>(S);
       if (t < best - 1e-9) {
         best = t;

@@ -149,3 +149,15 @@ def test_quant_traffic_model_reproduces_example_5_8():
     w_out = 32 * 6 + 12
     assert w_out == g["weights_output_mib"]
     assert sep / MiB - w_out == g["input_separate_mib"] and fus / MiB - w_out == g["input_fused_mib"]
+
+
+def test_fp32_plan_splits_k_when_tiles_are_few():
+    # 256^3: 4 tiles for 2 x 152 resident CTAs -- K is cut into 8 chunks of 32 (one K tile);
+    # with a quarter of the slots or more filled, chunks keep at least 256 of K.
+    p = dg.dg_plan_gemm(0, 256, 256, 256, num_sms=152)
+    assert (p["tiles"], p["splits"], p["tail_tiles"], p["grid"]) == (4, 8, 4, 32)
+    p = dg.dg_plan_gemm(0, 200, 136, 1000, num_sms=152)
+    assert p["splits"] == 16 and p["grid"] == 64                      # at most 16 chunks
+    p = dg.dg_plan_gemm(0, 1000, 3000, 777, num_sms=152)
+    assert (p["tiles"], p["splits"]) == (192, 3)                        # 777 / 3 >= 256 of K
+    assert dg.dg_plan_gemm(0, 7, 9, 5, num_sms=152)["splits"] == 1      # one K tile: no split
