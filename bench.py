@@ -46,15 +46,18 @@ SM_MAX_MHZ_NOMINAL = 2070.0
 # kernel's sources (kernel file, planner, headers) matches the one it was taken with.
 COMMON_SOURCES = ["api.cu", "dg_internal.h", "ptx.cuh", "tile_sched.h"]
 MEASURED_TRAFFIC = {
-    "sgemm_4096": {"bytes_per_launch": 464_388_096, "source_hash": "cbd90222cbf1f7c5"},
-    "sgemm_ragged": {"bytes_per_launch": 26_063_104, "source_hash": "cbd90222cbf1f7c5"},
-    "ffn_bf16": {"bytes_per_launch": 162_293_248, "source_hash": "ffcd0b77999d56c5"},
-    "ffn_gate_up": {"bytes_per_launch": 234_007_552, "source_hash": "ffcd0b77999d56c5"},
-    "bf16_4096": {"bytes_per_launch": 147_564_544, "source_hash": "ffcd0b77999d56c5"},
-    "qk_batched": {"bytes_per_launch": 1_078_958_592, "source_hash": "ffcd0b77999d56c5"},
-    "decode_m1": {"bytes_per_launch": 105_269_760, "source_hash": "dee96d3fb2bc7307"},
-    "decode_m4": {"bytes_per_launch": 105_322_496, "source_hash": "dee96d3fb2bc7307"},
-    "decode_m16": {"bytes_per_launch": 105_634_560, "source_hash": "dee96d3fb2bc7307"},
+    "sgemm_4096": {"bytes_per_launch": 420_676_608, "source_hash": "6e112f0fcfd6e801"},
+    "sgemm_ragged": {"bytes_per_launch": 25_740_800, "source_hash": "6e112f0fcfd6e801"},
+    "ffn_bf16": {"bytes_per_launch": 163_070_976, "source_hash": "c05f3fffc086cae9"},
+    "ffn_gate_up": {"bytes_per_launch": 234_515_712, "source_hash": "c05f3fffc086cae9"},
+    "bf16_4096": {"bytes_per_launch": 147_407_104, "source_hash": "c05f3fffc086cae9"},
+    "qk_batched": {"bytes_per_launch": 1_078_260_736, "source_hash": "c05f3fffc086cae9"},
+    "decode_m1": {"bytes_per_launch": 105_299_968, "source_hash": "ad1077b61e2d3563"},
+    "decode_m4": {"bytes_per_launch": 105_382_144, "source_hash": "ad1077b61e2d3563"},
+    "decode_m16": {"bytes_per_launch": 105_478_144, "source_hash": "ad1077b61e2d3563"},
+    "attn_batched": {"bytes_per_launch": 322_631_424, "source_hash": "ac6d72f45ae4e393"},
+    "fp8_ffn": {"bytes_per_launch": 57_459_712, "source_hash": "889bba971476a4ad"},
+    "decode_chain_m1": {"bytes_per_launch": 408_375_552, "source_hash": "fb5e7a4e36218aea"},
 }
 
 
@@ -187,8 +190,10 @@ class Workload:
         w = self.w
         per_copy = self.algo_bytes
         if copies is None:
+            # Enough rotating copies that the inputs of the steps between two uses of a copy
+            # exceed twice the L2 (small workloads get many small copies).
             copies = max(2, int(np.ceil(2.0 * L2_BYTES / per_copy)) + 1)
-            copies = min(copies, 8)
+            copies = min(copies, 512)
         self.copies = copies
         self.bufs = []
         if self.kind == "chain":
