@@ -1,8 +1,8 @@
 // quant.cu -- per-row FP8 E4M3 quantisation of BF16 activations for the FP8 GEMM
 // ("Operator & Runtime", section 5.4.3, Example 5-7, and section 5.4.4, Example 5-8):
 //   amax_i = max_k |x_ik|,  q_ik = E4M3(x_ik * (448 / amax_i)),  s_i = amax_i / 448,
-// so that x_ik ~ q_ik * s_i.  The scale comes from the whole row, so the row is read twice:
-// once for its maximum, once to quantise (the second read hits L1/L2).  The quantised codes
+// so that x_ik ~ q_ik * s_i.  The scale comes from the whole row, so the whole row is read
+// before any element is quantised (from registers, or a second read hitting L1/L2).  The codes
 // are written once; the GEMM then reads one byte per element instead of two (the separate
 // quantisation the pages find cheaper than quantising inside every column block).
 //
@@ -11,8 +11,9 @@
 // float32 multiplication, then round-to-nearest-even to E4M3 with saturation to +-448
 // (cvt.rn.satfinite.e4m3x2.f32).  A row of zeros gets codes 0 and scale 0.
 //
-// HBM-bound: 2 bytes read and 1 byte written per element (plus 4 bytes per row).  A CTA of
-// 256 threads takes one row at a time, 8 elements (16 bytes) per thread per step.
+// HBM-bound: 2 bytes read and 1 byte written per element (plus 4 bytes per row).  One warp
+// takes one row: rows of up to 4096 elements stay in the warp's registers between the two
+// passes (one HBM read), the maximum is a warp shuffle reduction (no CTA barrier).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -39,65 +40,73 @@ __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-template <bool VEC>
-__global__ void __launch_bounds__(kQThreads, 1)
+// One warp per row.  R > 0: the row (cols <= 256 R, 16-byte aligned) is held in registers,
+// R 16-byte chunks per lane, so it is read from HBM once and quantised from registers.
+// R == 0: two passes over the row (the second from L1/L2), 16-byte chunks when VEC.
+template <int R, bool VEC>
+__global__ void __launch_bounds__(kQThreads)
     quantize_rows_kernel(int64_t rows, int64_t cols, const uint16_t* __restrict__ X, int64_t ldx,
                          uint8_t* __restrict__ Q, int64_t ldq, float* __restrict__ scales) {
-  __shared__ float red[kQThreads / 32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (kQThreads / 32);
   pdl_trigger();
   pdl_wait();  // launched with programmatic serialisation: X may come from the previous kernel
-  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * (kQThreads / 32) + (threadIdx.x >> 5); r < rows;
+       r += warps) {
     const uint16_t* x = X + r * ldx;
     uint8_t* q = Q + r * ldq;
-    // Pass 1: the row's absolute maximum.
+    const int64_t n8 = VEC ? cols / 8 : 0;  // whole 16-byte chunks
+    uint4 v[R > 0 ? R : 1];
     float m = 0.f;
-    if (VEC) {
-      const int64_t n8 = cols / 8;
-      for (int64_t i = tid; i < n8; i += kQThreads) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(x) + i);
-        m = fmaxf(m, fmaxf(fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))),
-                           fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y)))));
-        m = fmaxf(m, fmaxf(fmaxf(fabsf(bf16_lo(v.z)), fabsf(bf16_hi(v.z))),
-                           fmaxf(fabsf(bf16_lo(v.w)), fabsf(bf16_hi(v.w)))));
+    // Pass 1: the row's absolute maximum.
+    if (R > 0) {
+#pragma unroll
+      for (int i = 0; i < R; ++i) {
+        const int64_t c = lane + 32 * i;
+        v[i] = c < n8 ? __ldcs(reinterpret_cast<const uint4*>(x) + c) : make_uint4(0u, 0u, 0u, 0u);
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(bf16_lo(v[i].x)), fabsf(bf16_hi(v[i].x))),
+                           fmaxf(fabsf(bf16_lo(v[i].y)), fabsf(bf16_hi(v[i].y)))));
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(bf16_lo(v[i].z)), fabsf(bf16_hi(v[i].z))),
+                           fmaxf(fabsf(bf16_lo(v[i].w)), fabsf(bf16_hi(v[i].w)))));
       }
-      for (int64_t i = n8 * 8 + tid; i < cols; i += kQThreads)
-        m = fmaxf(m, fabsf(__uint_as_float(static_cast<uint32_t>(x[i]) << 16)));
-    } else {
-      for (int64_t i = tid; i < cols; i += kQThreads)
-        m = fmaxf(m, fabsf(__uint_as_float(static_cast<uint32_t>(x[i]) << 16)));
+    } else if (VEC) {
+      for (int64_t c = lane; c < n8; c += 32) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4*>(x) + c);
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(bf16_lo(u.x)), fabsf(bf16_hi(u.x))),
+                           fmaxf(fabsf(bf16_lo(u.y)), fabsf(bf16_hi(u.y)))));
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(bf16_lo(u.z)), fabsf(bf16_hi(u.z))),
+                           fmaxf(fabsf(bf16_lo(u.w)), fabsf(bf16_hi(u.w)))));
+      }
     }
+    for (int64_t i = n8 * 8 + lane; i < cols; i += 32)
+      m = fmaxf(m, fabsf(__uint_as_float(static_cast<uint32_t>(x[i]) << 16)));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0) red[warp] = m;
-    __syncthreads();
-    float amax = red[0];
-#pragma unroll
-    for (int w = 1; w < kQThreads / 32; ++w) amax = fmaxf(amax, red[w]);
-    __syncthreads();  // red is rewritten for the next row
+    const float amax = m;
     const float inv = amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f;
-    if (tid == 0) scales[r] = __fdiv_rn(amax, 448.f);
-    // Pass 2: quantise.
-    if (VEC) {
-      const int64_t n8 = cols / 8;
-      for (int64_t i = tid; i < n8; i += kQThreads) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(x) + i);
-        uint2 o;
-        o.x = static_cast<uint32_t>(e4m3x2(__fmul_rn(bf16_lo(v.x), inv), __fmul_rn(bf16_hi(v.x), inv))) |
-              (static_cast<uint32_t>(e4m3x2(__fmul_rn(bf16_lo(v.y), inv), __fmul_rn(bf16_hi(v.y), inv))) << 16);
-        o.y = static_cast<uint32_t>(e4m3x2(__fmul_rn(bf16_lo(v.z), inv), __fmul_rn(bf16_hi(v.z), inv))) |
-              (static_cast<uint32_t>(e4m3x2(__fmul_rn(bf16_lo(v.w), inv), __fmul_rn(bf16_hi(v.w), inv))) << 16);
-        reinterpret_cast<uint2*>(q)[i] = o;
+    if (lane == 0) scales[r] = __fdiv_rn(amax, 448.f);
+    // Pass 2: quantise, 8 codes (8 bytes) per 16-byte chunk.
+    auto codes8 = [&](const uint4& u) {
+      uint2 o;
+      o.x = static_cast<uint32_t>(e4m3x2(__fmul_rn(bf16_lo(u.x), inv), __fmul_rn(bf16_hi(u.x), inv))) |
+            (static_cast<uint32_t>(e4m3x2(__fmul_rn(bf16_lo(u.y), inv), __fmul_rn(bf16_hi(u.y), inv))) << 16);
+      o.y = static_cast<uint32_t>(e4m3x2(__fmul_rn(bf16_lo(u.z), inv), __fmul_rn(bf16_hi(u.z), inv))) |
+            (static_cast<uint32_t>(e4m3x2(__fmul_rn(bf16_lo(u.w), inv), __fmul_rn(bf16_hi(u.w), inv))) << 16);
+      return o;
+    };
+    if (R > 0) {
+#pragma unroll
+      for (int i = 0; i < R; ++i) {
+        const int64_t c = lane + 32 * i;
+        if (c < n8) reinterpret_cast<uint2*>(q)[c] = codes8(v[i]);
       }
-      for (int64_t i = n8 * 8 + tid; i < cols; i += kQThreads) {
-        const float y = __fmul_rn(__uint_as_float(static_cast<uint32_t>(x[i]) << 16), inv);
-        q[i] = static_cast<uint8_t>(e4m3x2(y, 0.f) & 0xFFu);
-      }
-    } else {
-      for (int64_t i = tid; i < cols; i += kQThreads) {
-        const float y = __fmul_rn(__uint_as_float(static_cast<uint32_t>(x[i]) << 16), inv);
-        q[i] = static_cast<uint8_t>(e4m3x2(y, 0.f) & 0xFFu);
-      }
+    } else if (VEC) {
+      for (int64_t c = lane; c < n8; c += 32)
+        reinterpret_cast<uint2*>(q)[c] = codes8(__ldg(reinterpret_cast<const uint4*>(x) + c));
+    }
+    for (int64_t i = n8 * 8 + lane; i < cols; i += 32) {
+      const float y = __fmul_rn(__uint_as_float(static_cast<uint32_t>(x[i]) << 16), inv);
+      q[i] = static_cast<uint8_t>(e4m3x2(y, 0.f) & 0xFFu);
     }
   }
 }
@@ -106,15 +115,18 @@ __global__ void __launch_bounds__(kQThreads, 1)
 
 cudaError_t launch_quantize_rows(int64_t rows, int64_t cols, const void* X, int64_t ldx, void* Q,
                                  int64_t ldq, float* scales, bool vec, int sms, cudaStream_t s) {
-  int64_t grid = static_cast<int64_t>(sms > 0 ? sms : 1) * 8;
-  if (grid > rows) grid = rows;
+  // One warp per row, up to 8 resident CTAs of 8 warps per SM.
+  int64_t grid = (rows + kQThreads / 32 - 1) / (kQThreads / 32);
+  const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 1) * 8;
+  if (grid > cap) grid = cap;
   const auto* x = static_cast<const uint16_t*>(X);
   auto* q = static_cast<uint8_t*>(Q);
-  if (vec)
-    return launch_pdl(quantize_rows_kernel<true>, dim3(static_cast<unsigned>(grid)), dim3(kQThreads),
-                      0, s, rows, cols, x, ldx, q, ldq, scales);
-  return launch_pdl(quantize_rows_kernel<false>, dim3(static_cast<unsigned>(grid)), dim3(kQThreads), 0,
-                    s, rows, cols, x, ldx, q, ldq, scales);
+  const dim3 g(static_cast<unsigned>(grid)), b(kQThreads);
+  const int64_t chunks = vec ? (cols / 8 + 31) / 32 : 0;  // 16-byte chunks per lane
+  if (vec && chunks <= 4) return launch_pdl(quantize_rows_kernel<4, true>, g, b, 0, s, rows, cols, x, ldx, q, ldq, scales);
+  if (vec && chunks <= 16) return launch_pdl(quantize_rows_kernel<16, true>, g, b, 0, s, rows, cols, x, ldx, q, ldq, scales);
+  if (vec) return launch_pdl(quantize_rows_kernel<0, true>, g, b, 0, s, rows, cols, x, ldx, q, ldq, scales);
+  return launch_pdl(quantize_rows_kernel<0, false>, g, b, 0, s, rows, cols, x, ldx, q, ldq, scales);
 }
 
 }  // namespace dg
