@@ -52,9 +52,9 @@ MEASURED_TRAFFIC = {
     "ffn_gate_up": {"bytes_per_launch": 234_515_712, "source_hash": "c05f3fffc086cae9"},
     "bf16_4096": {"bytes_per_launch": 147_407_104, "source_hash": "c05f3fffc086cae9"},
     "qk_batched": {"bytes_per_launch": 1_078_260_736, "source_hash": "c05f3fffc086cae9"},
-    "decode_m1": {"bytes_per_launch": 105_299_968, "source_hash": "ad1077b61e2d3563"},
-    "decode_m4": {"bytes_per_launch": 105_382_144, "source_hash": "ad1077b61e2d3563"},
-    "decode_m16": {"bytes_per_launch": 105_478_144, "source_hash": "ad1077b61e2d3563"},
+    "decode_m1": {"bytes_per_launch": 105_169_920, "source_hash": "84a3cfbbf06296db"},
+    "decode_m4": {"bytes_per_launch": 105_385_728, "source_hash": "84a3cfbbf06296db"},
+    "decode_m16": {"bytes_per_launch": 105_748_480, "source_hash": "84a3cfbbf06296db"},
     "attn_batched": {"bytes_per_launch": 322_631_424, "source_hash": "ac6d72f45ae4e393"},
     "fp8_ffn": {"bytes_per_launch": 57_459_712, "source_hash": "889bba971476a4ad"},
     "decode_chain_m1": {"bytes_per_launch": 408_375_552, "source_hash": "fb5e7a4e36218aea"},

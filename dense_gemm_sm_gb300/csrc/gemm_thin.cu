@@ -245,9 +245,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem_base = ctl->tmem_base;
   // Everything above touches only shared memory, TMEM and kernel parameters; it may overlap
   // the previous kernel of the stream.  The producer and the epilogue wait for the previous
-  // grid (pdl_wait) before their first global access; the MMA issuer reads only shared
-  // memory and TMEM that the producer fills, so it needs no wait.
-  pdl_trigger();
+  // grid (pdl_wait) before their first global access; the MMA issuer waits too, so that its
+  // bounded waits start only once this grid's data can arrive.  The next grid is released
+  // (pdl_trigger) by the producer once it has issued its last load: one CTA per SM fits, so
+  // the next grid's CTAs take an SM only as this grid's leave it, and an earlier release
+  // measured 1-1.5% slower.
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -297,6 +299,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ++it;
         }
       }
+      pdl_trigger();
       if (!ok) {
         const uint32_t first = it > static_cast<uint32_t>(STAGES) ? it - STAGES : 0u;
         uint32_t never = 0;
@@ -314,6 +317,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       Segment<IDX> sg;
       uint32_t it = 0, lt = 0;
       bool ok = true;
+      pdl_wait();
       while (ok && walk.next(&sg)) {
         const uint32_t acc = lt & 1u, aph = (lt >> 1) & 1u;
         if (!mbar_wait(smem_u32(&ctl->tempty[acc]), aph ^ 1u, abort, p.status, kDevTimeoutMma)) {
