@@ -46,18 +46,18 @@ SM_MAX_MHZ_NOMINAL = 2070.0
 # kernel's sources (kernel file, planner, headers) matches the one it was taken with.
 COMMON_SOURCES = ["api.cu", "dg_internal.h", "ptx.cuh", "tile_sched.h"]
 MEASURED_TRAFFIC = {
-    "sgemm_4096": {"bytes_per_launch": 420_676_608, "source_hash": "6e112f0fcfd6e801"},
-    "sgemm_ragged": {"bytes_per_launch": 25_740_800, "source_hash": "6e112f0fcfd6e801"},
-    "ffn_bf16": {"bytes_per_launch": 163_070_976, "source_hash": "c05f3fffc086cae9"},
-    "ffn_gate_up": {"bytes_per_launch": 234_515_712, "source_hash": "c05f3fffc086cae9"},
-    "bf16_4096": {"bytes_per_launch": 147_407_104, "source_hash": "c05f3fffc086cae9"},
-    "qk_batched": {"bytes_per_launch": 1_078_260_736, "source_hash": "c05f3fffc086cae9"},
-    "decode_m1": {"bytes_per_launch": 105_169_920, "source_hash": "84a3cfbbf06296db"},
-    "decode_m4": {"bytes_per_launch": 105_385_728, "source_hash": "84a3cfbbf06296db"},
-    "decode_m16": {"bytes_per_launch": 105_748_480, "source_hash": "84a3cfbbf06296db"},
-    "attn_batched": {"bytes_per_launch": 322_631_424, "source_hash": "ac6d72f45ae4e393"},
-    "fp8_ffn": {"bytes_per_launch": 57_459_712, "source_hash": "889bba971476a4ad"},
-    "decode_chain_m1": {"bytes_per_launch": 408_375_552, "source_hash": "fb5e7a4e36218aea"},
+    "sgemm_4096": {"bytes_per_launch": 464_847_872, "source_hash": "a93b4b847359fd31"},
+    "sgemm_ragged": {"bytes_per_launch": 26_462_464, "source_hash": "a93b4b847359fd31"},
+    "ffn_bf16": {"bytes_per_launch": 163_321_088, "source_hash": "3198cecd1ee343c5"},
+    "ffn_gate_up": {"bytes_per_launch": 234_397_184, "source_hash": "3198cecd1ee343c5"},
+    "bf16_4096": {"bytes_per_launch": 147_519_488, "source_hash": "3198cecd1ee343c5"},
+    "qk_batched": {"bytes_per_launch": 1_078_651_904, "source_hash": "3198cecd1ee343c5"},
+    "decode_m1": {"bytes_per_launch": 105_342_208, "source_hash": "36ed44c05924eb42"},
+    "decode_m4": {"bytes_per_launch": 105_141_248, "source_hash": "36ed44c05924eb42"},
+    "decode_m16": {"bytes_per_launch": 105_492_736, "source_hash": "36ed44c05924eb42"},
+    "attn_batched": {"bytes_per_launch": 267_400_448, "source_hash": "49821aa59b33e504"},
+    "fp8_ffn": {"bytes_per_launch": 57_830_912, "source_hash": "910aedba867a0f09"},
+    "decode_chain_m1": {"bytes_per_launch": 408_459_520, "source_hash": "6056eb10f7537d26"},
 }
 
 

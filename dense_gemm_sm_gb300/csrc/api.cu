@@ -226,6 +226,17 @@ void plan_bf16(int64_t M, int64_t N, int64_t K, int64_t batch, int sms, dg_plan*
   if (pair) {
     pl->kernel = DG_KERNEL_TC2_BF16;
     pl->tile_m = 2 * kTcBM;
+    // FP8 pairs also come 224 columns wide (112 B rows per CTA).  The width with the smaller
+    // tile-waves x width wins, 256 on a tie: on the FFN shape 4 x 55 tiles of 224 fill 3
+    // waves of 76 pairs to 96% where 4 x 48 tiles of 256 fill them to 84%.
+    if (fp8) {
+      const int64_t G2 = sms / 2, tm2 = cdiv(cdiv(M, kTcBM), 2);
+      const int64_t w256 = cdiv(tm2 * cdiv(N, 256), G2) * 256, w224 = cdiv(tm2 * cdiv(N, 224), G2) * 224;
+      if (w224 < w256) {
+        bn = 224;
+        pl->tile_n = bn;
+      }
+    }
     pl->stages = 6;
     pl->group = kRasterGroup / 2;  // in 256-row tile rows: the same 8 rows of 128
     pl->tiles = cdiv(cdiv(M, kTcBM), 2) * cdiv(N, bn);
@@ -270,7 +281,7 @@ dg_status plan(int32_t dtype, int64_t M, int64_t N, int64_t K, int64_t batch, fl
     plan_f32(M, N, K, batch, static_cast<int64_t>(sms) * kSimtCtasPerSmPlan, pl, &dp, &sk,
              &splits);
   } else {
-    plan_bf16(M, N, K, batch, sms, pl);
+    plan_bf16(M, N, K, batch, sms, pl, false, dtype == 2);
   }
   return DG_OK;
 }
@@ -854,7 +865,7 @@ dg_status dg_release_workspace(void) {
 
 dg_status dg_plan_gemm(int32_t dtype, int64_t M, int64_t N, int64_t K, int64_t batch, dg_op op_b,
                        dg_out c_type, int32_t num_sms, dg_plan* out) {
-  if (!out || (dtype != 0 && dtype != 1)) return DG_ERR_INVALID_ARG;
+  if (!out || dtype < 0 || dtype > 2 || (dtype == 2 && batch > 1)) return DG_ERR_INVALID_ARG;
   if (M < 0 || N < 0 || K < 0 || batch < 0) return DG_ERR_INVALID_ARG;
   if (op_b != DG_OP_N && op_b != DG_OP_T) return DG_ERR_INVALID_ARG;
   if (c_type != DG_OUT_BF16 && c_type != DG_OUT_F32) return DG_ERR_INVALID_ARG;

@@ -71,8 +71,8 @@ struct TcParams {
 inline int64_t tc_ws_floats(int64_t sk_ctas, int bn) { return sk_ctas * 2 * 128 * bn; }
 // A: [batch][M][lda] bf16 (K contiguous).  B: op N -> [batch][K][ldb] (N contiguous),
 // op T -> [batch][N][ldb] (K contiguous).
-// pair: launch clusters of two CTAs that each compute half of a 256 x bn tile (bn = 256,
-// batch 1, num_ctas even; p.tiles_m then counts 256-row tile rows).
+// pair: launch clusters of two CTAs that each compute half of a 256 x bn tile (bn = 256, or
+// 224 for FP8; batch 1, num_ctas even; p.tiles_m then counts 256-row tile rows).
 // B2 non-null: the FFN gate/up form -- B = W_g, B2 = W_u (both K x N, N-major, batch 1),
 // bn = 256 covers 128 output columns of each, and C = SiLU(bf16(X W_g)) * bf16(X W_u).
 // fp8: A [M][lda] and B [N][ldb] are E4M3 codes (bytes, K contiguous; b_kmajor), batch 1, and

@@ -399,7 +399,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                    const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC,
                    const TcParams p, const int fault) {
   using Cfg = TcCfg<BN, B_KMAJOR, PAIR>;
-  static_assert(!PAIR || (BN == 256 && !RANK3), "pair tiles are 256 x 256, one problem");
+  static_assert(!PAIR || ((BN == 256 || (BN == 224 && FP8)) && !RANK3),
+                "pair tiles are 256 x 256 (FP8 also 256 x 224), one problem");
   static_assert(!DUAL || (BN == 256 && !B_KMAJOR && !RANK3), "gate/up: 2 x 128 columns, N-major");
   static_assert(!FP8 || (B_KMAJOR && !RANK3 && !DUAL), "FP8: one problem, K-major B");
   constexpr int BK_ELEMS = FP8 ? 128 : BK;  // K elements per stage (128 bytes per row)
@@ -978,7 +979,8 @@ cudaError_t launch_gemm_tc(const TcParams& p, int bn, const void* A, int64_t lda
   CUtensorMap ma, mb, mb2;
   const uint64_t batch = static_cast<uint64_t>(p.batch);
   const bool dual = B2 != nullptr;
-  if (pair && (bn != 256 || batch > 1 || num_ctas % 2 != 0)) return cudaErrorInvalidValue;
+  if (pair && ((bn != 256 && !(fp8 && bn == 224)) || batch > 1 || num_ctas % 2 != 0))
+    return cudaErrorInvalidValue;
   if (dual && (bn != 256 || batch > 1 || b_kmajor)) return cudaErrorInvalidValue;
   // B columns one tensor map box set covers: the CTA's share of the tile (the pair splits the
   // tile's columns between its two CTAs; gate/up reads BN / 2 from each of W_g and W_u).
@@ -1030,6 +1032,7 @@ cudaError_t launch_gemm_tc(const TcParams& p, int bn, const void* A, int64_t lda
   }
   const bool rank3 = batch > 1;
   if (fp8) {
+    if (pair && bn == 224) return launch_tc_variant<224, true, false, false, true, false, true>(ma, mb, mb2, mc, q, num_ctas, s);
     if (pair) return launch_tc_variant<256, true, false, false, true, false, true>(ma, mb, mb2, mc, q, num_ctas, s);
     if (bn == 256) return launch_tc_variant<256, true, false, false, false, false, true>(ma, mb, mb2, mc, q, num_ctas, s);
     if (bn == 128) return launch_tc_variant<128, true, false, false, false, false, true>(ma, mb, mb2, mc, q, num_ctas, s);

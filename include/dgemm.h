@@ -300,7 +300,8 @@ typedef struct {
 
 /*
  * The kernel choice and launch shape for a problem, without running it.
- * dtype: 0 = FP32 path, 1 = BF16 path.  num_sms <= 0 queries the current
+ * dtype: 0 = FP32 path, 1 = BF16 path, 2 = FP8 E4M3 path (gemm_fp8_e4m3: batch
+ * at most 1, B K-major whatever op_b says).  num_sms <= 0 queries the current
  * device (needs a GPU); pass the SM count explicitly to plan on a CPU.
  * Pointer alignment is not considered (vec assumes aligned rows).
  */

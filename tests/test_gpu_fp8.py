@@ -96,9 +96,11 @@ def run_fp8(torch, M, N, K, A, lda, sa, B, ldb, sb, ldc, c_type):
 
 @pytest.mark.parametrize("M,N,K,lda,ldb", [(512, 2048, 1024, 1024, 1024), (300, 1000, 1000, 1008, 1024),
                                            (128, 128, 256, 256, 256), (1280, 2048, 6144, 6144, 6144),
-                                           (256, 520, 200, 208, 224)])
+                                           (256, 520, 200, 208, 224), (512, 8960, 256, 256, 256)])
 @pytest.mark.parametrize("c_type", [dg.DG_OUT_BF16, dg.DG_OUT_F32])
 def test_fp8_gemm_parity(torch, tile_mode, M, N, K, lda, ldb, c_type):
+    # Pairs take 224-column tiles on every shape here but 512 x 8960 x 256, whose 2 x 35
+    # tiles of 256 fill one wave where 2 x 40 tiles of 224 would need two.
     A, sa, B, sb = quantized_operands(M, N, K, lda, ldb, seed=M + N + K)
     ldc = N + 3 if M == 300 else N   # one case with unaligned C rows (direct stores)
     C = run_fp8(torch, M, N, K, A, lda, sa, B, ldb, sb, ldc, c_type)
@@ -144,6 +146,39 @@ def test_fp8_ffn_full_size_sampled(torch):
     D = np.einsum("ik,ik->i", np.abs(a[rows]), np.abs(b[cols])) * np.abs(sa_ref[rows] * sb_ref[cols]).astype(np.float64)
     ok, worst = oracle.check_bf16(C[rows, cols], ref, D)
     assert ok, f"fp8 FFN sampled: {worst:.3g} of the bound"
+
+
+def test_fp8_pair224_streamk_sampled(torch):
+    # 224-column pair tiles with a stream-K tail: FFN widths with K = 6144 give 4 x 55 tiles,
+    # 2 whole waves of 76 pairs and 68 tail tiles spread over the pairs.  Random codes (no
+    # NaN codes) and scales; FP32 output on sampled entries against the oracle, and a repeat
+    # bit for bit (the tail tiles' parts are added in a fixed order).
+    M, N, K = 1024, 12288, 6144
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    plan = dg.dg_plan_gemm(2, M, N, K, num_sms=sms)
+    if sms == 152:
+        assert plan["tile_n"] == 224 and plan["tail_tiles"] == 68
+    rng = np.random.default_rng(61)
+
+    def codes(r, c):
+        q = rng.integers(0, 256, (r, c), dtype=np.uint8)
+        q[(q & 0x7F) == 0x7F] = 0
+        return q
+
+    A, B = codes(M, K), codes(N, K)
+    sa = (rng.uniform(0.5, 2.0, M) / 448).astype(np.float32)
+    sb = (rng.uniform(0.5, 2.0, N) / 448).astype(np.float32)
+    C = run_fp8(torch, M, N, K, A, K, sa, B, K, sb, N, dg.DG_OUT_F32)
+    again = run_fp8(torch, M, N, K, A, K, sa, B, K, sb, N, dg.DG_OUT_F32)
+    assert np.array_equal(C.view(np.uint32), again.view(np.uint32))
+    rows, cols = sample_indices(62, 3000, M, N)
+    a = oracle.e4m3_to_f64(np.ascontiguousarray(A[rows])).reshape(len(rows), K)
+    b = oracle.e4m3_to_f64(np.ascontiguousarray(B[cols])).reshape(len(cols), K)
+    s = sa[rows].astype(np.float64) * sb[cols].astype(np.float64)
+    ref = np.einsum("ik,ik->i", a, b) * s
+    D = np.einsum("ik,ik->i", np.abs(a), np.abs(b)) * np.abs(s)
+    ok, worst = oracle.check_f32(C[rows, cols], ref, D)
+    assert ok, f"fp8 224-wide pairs with stream-K: {worst:.3g} of the bound"
 
 
 def test_fp8_deterministic(torch):

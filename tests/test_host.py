@@ -64,6 +64,27 @@ def test_plan_dispatch_table():
     assert dg.dg_plan_gemm(1, 0, 10, 10, num_sms=152)["kernel"] == dg.DG_KERNEL_NONE
 
 
+def test_plan_fp8_pair_width():
+    # FP8 pairs take the width (256 or 224) with the smaller tile-waves x width, 256 on a tie.
+    # FFN shape: 4 x 48 tiles of 256 = 3 waves of 76 pairs (768) vs 4 x 55 of 224 (672).
+    ffn = dg.dg_plan_gemm(2, 1024, 12288, 4096, num_sms=152)
+    assert ffn["kernel"] == dg.DG_KERNEL_TC2_BF16 and ffn["tile_n"] == 224 and ffn["tiles"] == 220
+    assert ffn["tile_k"] == 128 and ffn["kblocks"] == 32 and ffn["tail_tiles"] == 0
+    # Example 5-8 GEMM: 16 x 6 tiles (2 waves, 512) vs 16 x 7 (2 waves, 448).
+    assert dg.dg_plan_gemm(2, 4096, 1536, 4096, num_sms=152)["tile_n"] == 224
+    # 2 x 35 tiles of 256 fit one wave; 2 x 40 of 224 would need two.
+    assert dg.dg_plan_gemm(2, 512, 8960, 4096, num_sms=152)["tile_n"] == 256
+    # K = 6144 gives the 224-wide tiles a stream-K tail: 220 = 2 x 76 + 68.
+    sk = dg.dg_plan_gemm(2, 1024, 12288, 6144, num_sms=152)
+    assert sk["tile_n"] == 224 and sk["tail_tiles"] == 68 and sk["splits"] == 76
+    assert sk["workspace_bytes"] == 2 * 76 * 2 * 128 * 224 * 4 + 2 * 68 * 4
+    # The BF16 path keeps 256 on pairs; one 128-row tile row keeps single CTAs.
+    assert dg.dg_plan_gemm(1, 1024, 12288, 4096, num_sms=152)["tile_n"] == 256
+    assert dg.dg_plan_gemm(2, 128, 12288, 4096, num_sms=152)["kernel"] == dg.DG_KERNEL_TC_BF16
+    with pytest.raises(RuntimeError):
+        dg.dg_plan_gemm(2, 1024, 1024, 1024, batch=2, num_sms=152)
+
+
 def test_tile_width_choice():
     # 256-wide tiles except for narrow problems (measured sweep; see the planner's comment)
     for M, N, batch in [(1024, 12288, 1), (4096, 4096, 1), (2048, 2048, 64), (300, 1000, 1),
