@@ -218,7 +218,8 @@ dg_status quantize_rows_e4m3(int64_t rows, int64_t cols, const uint16_t* X, int6
  *     DG_ERR_INVALID_ARG; A, B or scale_b not 16-byte aligned, lda or ldb not multiples of
  *     16, or scale_a not 4-byte aligned DG_ERR_MISALIGNED.  M == 0 or N == 0: nothing;
  *     K == 0: C = 0.
- *   - The tile kernel of gemm_bf16 (CTA pairs from M > 128), 128 K elements per stage.
+ *   - The tile kernel of gemm_bf16 (CTA pairs from M > 128), 128 K elements per stage; pair
+ *     tiles are 256 x 256 or 256 x 224, whichever fills the waves of CTA pairs better.
  */
 dg_status gemm_fp8_e4m3(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda,
                         const float* scale_a, const uint8_t* B, int64_t ldb, const float* scale_b,
@@ -278,7 +279,8 @@ typedef enum {
   DG_KERNEL_SIMT_F32 = 2,  /* FP32 CUDA-core SGEMM */
   DG_KERNEL_TC_BF16 = 3,   /* tcgen05 tile kernel (persistent, TMA ring, TMEM accumulators) */
   DG_KERNEL_THIN_BF16 = 4, /* tcgen05 stream-K decode kernel (M <= 32) */
-  DG_KERNEL_TC2_BF16 = 5   /* tile kernel on CTA pairs (cta_group::2, 256 x 256 tiles) */
+  DG_KERNEL_TC2_BF16 = 5   /* tile kernel on CTA pairs (cta_group::2, 256 x 256 tiles;
+                              FP8 also 256 x 224) */
 } dg_kernel;
 
 typedef struct {
