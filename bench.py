@@ -466,6 +466,18 @@ def aggregate_ranks(ms_local, metric_of_seconds, world, dist, device):
     return ms, metric_of_seconds(ms / 1e3) * world
 
 
+def aggregate_e2e(e2e, metric_of_seconds, world, dist, device):
+    """The e2e object for the whole job, like `value`: the slowest rank's step time, and the
+    work and the copies of all ranks (e2e["_ms"] is this rank's unrounded step time)."""
+    if e2e is None:
+        return None
+    ms, value = aggregate_ranks(e2e.pop("_ms"), metric_of_seconds, world, dist, device)
+    e2e.update(value=round(value, 3), ms_per_step=round(ms, 4),
+               h2d_bytes_per_step=e2e["h2d_bytes_per_step"] * world,
+               d2h_bytes_per_step=e2e["d2h_bytes_per_step"] * world)
+    return e2e
+
+
 def time_e2e(torch, wl, steps, warmup):
     """Same workload through the public API with host inputs.  Every step copies that step's
     inputs from pinned host memory, calls the library and reads the result back into pinned
@@ -545,7 +557,7 @@ def time_e2e(torch, wl, steps, warmup):
     sec = start.elapsed_time(end) / 1e3 / steps
     same = all(torch.equal(outs[(steps - 1 - j) % nbuf], ref) for j in range(min(nbuf, steps)))
     return {"value": round(wl.metric_value(sec), 3), "unit": wl.unit, "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "ms_per_step": round(sec * 1e3, 4),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": round(sec * 1e3, 4), "_ms": sec * 1e3,
             "overlap": f"copies on two copy streams, {nbuf} device buffer sets",
             "result_equals_serial_call": bool(same)}
 
@@ -726,6 +738,7 @@ def main():
     launch_ms = float(np.mean(per_launch))
 
     e2e = None if args.no_e2e else time_e2e(torch, wl, max(3, min(args.steps, 20)), 2)
+    e2e = aggregate_e2e(e2e, wl.metric_value, world, dist, torch.device("cuda"))
 
     if rank != 0:
         if dist is not None:
