@@ -415,6 +415,43 @@ def test_bf16_square_4096_sampled(torch):
     assert_bf16_close(C[rows, cols], ref, den, "BF16 4096^3 (sampled)")
 
 
+@pytest.mark.parametrize("path", ["f32", "bf16"])
+def test_outputs_past_2_31_elements(torch, path):
+    # C of 65536 x 32800 = 2,149,580,800 elements (> 2^31): the element and byte offsets of
+    # the last rows overflow 32-bit integers, so every index on the store path must be 64-bit.
+    # N leaves a 32-column last tile; K = 64 keeps the call short.  Sampled entries, the
+    # corners and the last row's tail are gathered on the device and checked against the
+    # oracle's single entries.
+    M, N, K = 65536, 32800, 64
+    assert M * N > 2 ** 31
+    rows, cols = sample_indices(71, 2000, M, N)
+    tail = np.arange(N - 80, N)
+    rows = np.concatenate([rows, np.full(tail.size, M - 1), np.full(tail.size, M - 129)])
+    cols = np.concatenate([cols, tail, tail])
+    ri = torch.from_numpy(rows).cuda()
+    ci = torch.from_numpy(cols).cuda()
+    if path == "f32":
+        A = inputs.uniform_f32(72, (M, K))
+        B = inputs.uniform_f32(73, (K, N))
+        dC = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        dg.gemm_f32(M, N, K, 1.0, dev_f32(A), K, dev_f32(B), N, 0.0, dC, N)
+        sync(torch)
+        got = host_f32(dC[ri, ci])
+        ref, den = oracle.gemm_entries(M, N, K, 1.0, A, K, B, N, 0.0, None, N, rows, cols)
+        assert_f32_close(got, ref, den, "FP32 C past 2^31 elements (sampled)")
+    else:
+        A = inputs.f32_to_bf16_bits(inputs.normal_f32(74, (M, K)))
+        B = inputs.f32_to_bf16_bits(inputs.normal_f32(75, (K, N), 0.125))
+        dC = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        dg.gemm_bf16(M, N, K, 1.0, dev_bf16(A), K, dev_bf16(B), N, 0.0, dC, N)
+        sync(torch)
+        got = host_bf16_bits(dC[ri, ci])
+        ref, den = oracle.gemm_entries(M, N, K, 1.0, A, K, B, N, 0.0, None, N, rows, cols)
+        assert_bf16_close(got, ref, den, "BF16 C past 2^31 elements (sampled)")
+    del dC
+    torch.cuda.empty_cache()
+
+
 def run_qk(torch, w):
     batch, S, D = w["batch"], w["M"], w["K"]
     dQ, dK = dev_bf16(w["A"]), dev_bf16(w["B"])
