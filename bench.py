@@ -665,7 +665,8 @@ def reference_arm(args):
 
     wl = W()
     wl.__dict__.update(spec)
-    per_step = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    # About 150 s of oracle work for the whole run (steps + warm-up), at least 0.5 s a step.
+    per_step = max(0.5, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         cpu_baseline(wl, budget_s=per_step)
     vals = [cpu_baseline(wl, budget_s=per_step) for _ in range(args.steps)]
