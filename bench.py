@@ -797,6 +797,9 @@ def main():
         line["suite"] = suite
     if not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(wl)
+        # The same oracle on one host thread, beside the all-cores figure.
+        one = cpu_baseline(wl, budget_s=5.0, nthreads=1)
+        line["cpu_baseline"]["single_thread"] = {"value": one["value"], "sample": one["sample"]}
     print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()
