@@ -760,7 +760,9 @@ def main():
                          f"({wl.copies * wl.algo_bytes / 2 ** 20:.0f} MiB) > L2 between steps"},
         "roofline": wl.roofline(launch_ms / 1e3, peaks, clocks and clocks["sm_mhz"]),
         "clocks": clocks,
-        "gpu_launches": args.steps,
+        # One library kernel a step; the FP8 workload that quantises inside each step adds the
+        # quantiser's.
+        "gpu_launches": args.steps * (2 if wl.kind == "fp8" and wl.w.get("quant") else 1),
         "e2e": e2e,
     }
     if not args.no_suite:
