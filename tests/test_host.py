@@ -182,3 +182,74 @@ def test_fp32_plan_splits_k_when_tiles_are_few():
     p = dg.dg_plan_gemm(0, 1000, 3000, 777, num_sms=152)
     assert (p["tiles"], p["splits"]) == (192, 3)                        # 777 / 3 >= 256 of K
     assert dg.dg_plan_gemm(0, 7, 9, 5, num_sms=152)["splits"] == 1      # one K tile: no split
+
+
+def _cdiv(a, b):
+    return -(-a // b)
+
+
+def test_plan_properties_on_random_shapes():
+    # Invariants of the planner over seeded random shapes, recomputed here from the tile
+    # sizes: tile counts, grids, the FP32 tail split, the decode stream-K grid, CTA pairs and
+    # their widths, stream-K tails and workspace sizes.
+    rng = np.random.default_rng(20261202)
+    sms = 152
+    for _ in range(1500):
+        M = int(rng.choice([rng.integers(1, 40), rng.integers(1, 5000), rng.integers(1, 70000)]))
+        N = int(rng.choice([rng.integers(1, 300), rng.integers(1, 20000)]))
+        K = int(rng.choice([rng.integers(1, 200), rng.integers(1, 9000)]))
+        batch = int(rng.choice([1, 1, 1, rng.integers(2, 70)]))
+        # FP32
+        p = dg.dg_plan_gemm(0, M, N, K, batch=batch, num_sms=sms)
+        assert p["kernel"] == dg.DG_KERNEL_SIMT_F32
+        tiles = batch * _cdiv(M, 128) * _cdiv(N, 128)
+        assert p["tiles"] == tiles and p["kblocks"] == _cdiv(K, p["tile_k"])
+        assert p["splits"] >= 1 and 0 <= p["tail_tiles"] <= tiles
+        assert p["grid"] == tiles - p["tail_tiles"] + p["tail_tiles"] * p["splits"]
+        if p["splits"] > 1:
+            # Chunks of at least 256 of K (8 K tiles), at most 3 waves of chunk CTAs on the
+            # 2 x 152 resident slots; when the tiles fill under a quarter of the slots, chunks
+            # go down to one K tile, at most 16.
+            G = 2 * sms
+            few = 4 * tiles <= G
+            assert p["tail_tiles"] > 0 and p["tail_tiles"] * p["splits"] <= 3 * G
+            assert p["splits"] <= (min(16, p["kblocks"]) if few else p["kblocks"] // 8)
+            assert p["workspace_bytes"] > 0
+        else:
+            assert p["tail_tiles"] == 0 and p["workspace_bytes"] == 0
+        # BF16 and FP8 (FP8 is planned for one problem only)
+        for dtype in (1, 2) if batch == 1 else (1,):
+            q = dg.dg_plan_gemm(dtype, M, N, K, batch=batch, num_sms=sms)
+            if dtype == 1 and batch == 1 and M <= 32:
+                assert q["kernel"] == dg.DG_KERNEL_THIN_BF16
+                assert q["ntok"] == (16 if M <= 16 else 32)
+                units = _cdiv(N, 128) * _cdiv(K, 64)
+                assert q["tiles"] == _cdiv(N, 128) and q["grid"] == min(units, sms)
+                continue
+            tk = 128 if dtype == 2 else 64
+            assert q["tile_k"] == tk and q["kblocks"] == _cdiv(K, tk)
+            bn = q["tile_n"]
+            if q["kernel"] == dg.DG_KERNEL_TC2_BF16:
+                assert batch == 1 and _cdiv(M, 128) >= 2 and q["tile_m"] == 256
+                tm2 = _cdiv(_cdiv(M, 128), 2)
+                assert q["tiles"] == tm2 * _cdiv(N, bn)
+                assert q["grid"] % 2 == 0 and q["grid"] // 2 == min(q["tiles"], sms // 2)
+                if dtype == 2:
+                    w256 = _cdiv(tm2 * _cdiv(N, 256), sms // 2) * 256
+                    w224 = _cdiv(tm2 * _cdiv(N, 224), sms // 2) * 224
+                    assert bn == (224 if w224 < w256 else 256)
+                else:
+                    assert bn == 256
+                G = q["grid"] // 2
+            else:
+                assert q["kernel"] == dg.DG_KERNEL_TC_BF16 and q["tile_m"] == 128
+                assert q["tiles"] == batch * _cdiv(M, 128) * _cdiv(N, bn)
+                assert q["grid"] == min(q["tiles"], sms)
+                G = q["grid"]
+            if q["tail_tiles"]:
+                assert q["tiles"] > G and q["tail_tiles"] == q["tiles"] % G
+                assert q["kblocks"] >= 16 and (q["tiles"] // G) * q["kblocks"] >= 96
+                assert 1 <= q["splits"] <= min(4 * q["tail_tiles"], G)
+                assert q["workspace_bytes"] > 0
+            else:
+                assert q["splits"] == 1
