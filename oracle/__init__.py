@@ -449,12 +449,26 @@ def quantize_rows_e4m3(rows, cols, X, ldx):
     return round_e4m3(y), scale
 
 
-def gemm_fp8(M, N, K, QA, lda, sa, QB, ldb, sb):
+def quantize_rows_e4m3_f64(rows, cols, X, ldx):
+    """The same per-row quantisation with every decision in float64: amax, y = x * 448 / amax
+    and the scale amax / 448 in double, then round-to-nearest-even of y to E4M3.  Kept beside
+    the float32 form above to show how many codes depend on the precision of the decision."""
+    X = np.asarray(X).reshape(-1)
+    x = bf16_to_f64(X) if X.dtype == np.uint16 else X.astype(np.float64)
+    idx = np.arange(rows)[:, None] * ldx + np.arange(cols)[None, :]
+    xr = x[idx]
+    amax = np.abs(xr).max(axis=1) if cols > 0 else np.zeros(rows)
+    safe = np.where(amax > 0, amax, 1.0)
+    y = np.where(amax[:, None] > 0, xr * E4M3_MAX / safe[:, None], 0.0)
+    return round_e4m3(y), amax / E4M3_MAX
+
+
+def gemm_fp8(M, N, K, QA, lda, sa, QB, ldb, sb, nthreads=None):
     """(C, D): C[i, j] = sa[i] * sb[j] * sum_k qa[i, k] qb[j, k] and its error scale
     D = |sa[i] sb[j]| sum_k |qa qb|, float64, for E4M3 codes QA [M, lda] and QB [N, ldb]."""
     a = e4m3_to_f64(np.asarray(QA).reshape(-1))
     b = e4m3_to_f64(np.asarray(QB).reshape(-1))
-    P, D = gemm(M, N, K, 1.0, a, lda, b, ldb, op_b=1, absden=True)
+    P, D = gemm(M, N, K, 1.0, a, lda, b, ldb, op_b=1, absden=True, nthreads=nthreads)
     s = np.asarray(sa, np.float64)[:, None] * np.asarray(sb, np.float64)[None, :]
     return P[0] * s, D[0] * np.abs(s)
 

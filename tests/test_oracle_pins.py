@@ -265,6 +265,53 @@ def test_acceptance_checkers():
     assert ok and worst == 0.0
 
 
+# BF16 output bound |C - C_ref| <= 2e-4 * D + ulp_bf16(|C_ref|): GPU values are BF16 numbers,
+# so each case fixes a BF16 value c and puts the reference just inside (0.99 x the bound) or
+# just outside (1.01 x) of it, in three binades whose ulps differ (2^-7 at 1.5, 2 at 384 and
+# 2^-14 at 3 * 2^-8) and with D chosen so that both terms matter (2e-4 * D is 20% to 50% of the
+# bound).  The references stay in c's binade, so the ulp term is that binade's spacing.  A
+# relative figure typed as 2e-3, a doubled or dropped ulp term, or an error measured from the
+# wrong operand moves at least one case to the other side.
+BF16_BOUND_CASES = [  # (c, D, ulp of the binade)
+    (1.5, 10.0, 2.0 ** -7),
+    (384.0, 1000.0, 2.0),
+    (3.0 * 2.0 ** -8, 0.1, 2.0 ** -14),
+]
+
+
+@pytest.mark.parametrize("c,D,ulp", BF16_BOUND_CASES)
+@pytest.mark.parametrize("side", [-1.0, 1.0])
+def test_check_bf16_accepts_inside_and_rejects_outside_the_bound(c, D, ulp, side):
+    bound = 2e-4 * D + ulp
+    bits = oracle.round_bf16(np.array([c]))
+    assert oracle.bf16_to_f64(bits)[0] == c                      # c is a BF16 number
+    for factor, expect in ((0.99, True), (1.01, False)):
+        ref = np.array([c - side * factor * bound])
+        assert oracle.ulp_bf16(np.abs(ref))[0] == ulp            # same binade as c
+        ok, worst = oracle.check_bf16(bits, ref, np.array([D]))
+        assert ok == expect, (c, D, factor, side)
+        assert abs(worst - factor) < 1e-9
+
+
+def test_check_bf16_needs_every_element_and_finite_values():
+    c = np.array([1.5, 384.0])
+    bits = oracle.round_bf16(c)
+    den = np.array([10.0, 1000.0])
+    inside = c - 0.99 * (2e-4 * den + np.array([2.0 ** -7, 2.0]))
+    ok, _ = oracle.check_bf16(bits, inside, den)
+    assert ok
+    one_out = inside.copy()
+    one_out[1] = 384.0 - 1.01 * (2e-4 * 1000.0 + 2.0)            # only the second one fails
+    ok, worst = oracle.check_bf16(bits, one_out, den)
+    assert not ok and abs(worst - 1.01) < 1e-9
+    nan_bits = bits.copy()
+    nan_bits[0] = 0x7FC0                                          # a NaN output never passes
+    assert not oracle.check_bf16(nan_bits, c, den)[0]
+    inf_bits = bits.copy()
+    inf_bits[1] = 0x7F80                                          # nor does an infinity
+    assert not oracle.check_bf16(inf_bits, c, den)[0]
+
+
 # --------------------------------------------------------------------------- FFN gate/up
 def test_silu_values_printed_by_the_pages():
     g, _ = read_golden("silu_chain.txt")
@@ -482,6 +529,32 @@ def test_e4m3_rounding_matches_torch():
     x = np.concatenate([np.clip(x, -448, 448), np.float32(2.0) ** np.arange(-12, 9, 0.25).astype(np.float32)])
     t = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     assert np.array_equal(oracle.round_e4m3(x), t)
+
+
+def test_quantize_decision_precision_float32_against_float64():
+    # The codes are integers decided by floating point; the oracle takes the decision in
+    # float32 (the kernel's precision).  The float64 decision is kept beside it: on the FFN
+    # activations X [1024, 4096] and the first 1024 rows of W [12288, 4096] (stored [N, K]),
+    # the two agree except where y = x * 448 / amax lies within float32 rounding of a
+    # midpoint between two E4M3 values; there they differ by one code step, the scales by at
+    # most one float32 rounding.  The counts are stated in the design notes.
+    w = inputs.fp8_gemm()
+    K = w["K"]
+    for name, X, rows in (("X", w["X"], 1024), ("W", w["W"], 1024)):
+        q32, s32 = oracle.quantize_rows_e4m3(rows, K, X, K)
+        q64, s64 = oracle.quantize_rows_e4m3_f64(rows, K, X, K)
+        diff = q32 != q64
+        n = int(diff.sum())
+        assert n <= rows * K // 2000, (name, n)
+        v32 = oracle.e4m3_to_f64(q32[diff])
+        v64 = oracle.e4m3_to_f64(q64[diff])
+        # one code step apart: no E4M3 value strictly between the two
+        pos = oracle.e4m3_values()[:127]
+        lo, hi = np.minimum(np.abs(v32), np.abs(v64)), np.maximum(np.abs(v32), np.abs(v64))
+        between = np.searchsorted(pos, hi, side="left") - np.searchsorted(pos, lo, side="right")
+        assert np.all(between == 0) and np.all(np.sign(v32) == np.sign(v64))
+        assert np.all(np.abs(s32.astype(np.float64) - s64) <= np.abs(s64) * 2.0 ** -24)
+        print(f"{name}: {n} of {rows * K} codes differ between float32 and float64 decisions")
 
 
 def test_quantize_example_5_7():
