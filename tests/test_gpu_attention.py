@@ -4,7 +4,8 @@ O = softmax(scale * Q K^T) V per head, optionally causal.
 Acceptance (oracle.check_attention): every element of O within
 (2^-9 + 2e-4 + 1e-5 + 2e-5 * Ds) * (P|V|) + ulp_bf16(|O_ref|), the bound derived from the
 BF16 rounding of the weights, FP32 accumulation and the score error.  Small problems are
-compared in full; the full-size ones on sampled query rows of every head.
+compared in full; at full size every row of four heads of the batched shape and of the
+causal 8192-token head, plus sampled query rows of every head.
 """
 import numpy as np
 import pytest
@@ -109,21 +110,40 @@ def test_attention_padded_strides(torch):
     assert np.all((Ob[~written] & 0x7FFF) > 0x7F80), "padding of O was written"
 
 
-def test_attention_batched_full_size_sampled(torch):
-    # The batched shape (64 heads x 2048 x 128, non-causal), 48 sampled query rows per head
-    # including the first and last of each 128-row tile edge.
+def head_view(w, h):
+    """The single-head problem of head h of a strided batch (flat slices of Q, K and V)."""
+    sl = lambda x, st: np.asarray(x).reshape(-1)[h * st: h * st + st] if st else x
+    return dict(w, batch=1, Q=sl(w["Q"], w["sQ"]), K=sl(w["K"], w["sK"]), V=sl(w["V"], w["sV"]),
+                sQ=0, sK=0, sV=0, sO=0)
+
+
+def check_whole_head(Ob, w, h, what, rows_per_chunk=1024):
+    """Every query row of head h against the oracle, in chunks of rows."""
+    wh = head_view(w, h)
+    Oh = Ob[h * w["sO"]: h * w["sO"] + (w["Lq"] - 1) * w["ldo"] + w["d"]] if w["sO"] else Ob
+    for r0 in range(0, w["Lq"], rows_per_chunk):
+        rows = np.arange(r0, min(w["Lq"], r0 + rows_per_chunk))
+        check(Oh, wh, rows=rows, what=f"{what}, head {h}, rows {r0}..{rows[-1]}")
+
+
+def test_attention_batched_full_size(torch):
+    # The batched shape (64 heads x 2048 x 128, non-causal): every row of heads 0, 1, 32 and
+    # 63 (the first and last head of each sequence's block of 32), and 48 sampled query rows
+    # of every head, including the first and last of each 128-row tile edge.
     w = inputs.attention()
+    Ob = run(torch, w)
+    for h in (0, 1, 32, 63):
+        check_whole_head(Ob, w, h, "attention 64x2048")
     rows = np.unique(np.concatenate([[0, 127, 128, 1023, 2047],
                                      np.random.default_rng(32).integers(0, 2048, 43)]))
-    check(run(torch, w), w, rows=rows, what="attention 64x2048")
+    check(Ob, w, rows=rows, what="attention 64x2048 (sampled rows)")
 
 
-def test_attention_causal_8k_sampled(torch, split_mode):
-    # One causal head of 8192 tokens (the pages' experiment), sampled rows across the sequence.
+def test_attention_causal_8k_whole(torch, split_mode):
+    # One causal head of 8192 tokens (the pages' experiment), every query row, with and
+    # without the split over keys.
     w = inputs.attention(1, 8192, causal=True)
-    rows = np.unique(np.concatenate([[0, 1, 127, 128, 8191],
-                                     np.random.default_rng(33).integers(0, 8192, 59)]))
-    check(run(torch, w), w, rows=rows, what="attention causal 8192")
+    check_whole_head(run(torch, w), w, 0, "attention causal 8192")
 
 
 def test_attention_deterministic(torch, split_mode):
