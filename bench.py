@@ -38,9 +38,8 @@ if ROOT not in sys.path:
 
 METRIC = "GEMM TFLOPS (2MNK/s) and % of GB300 BF16/FP32 roofline; GB/s at M=1..16"
 L2_BYTES = 126.5 * 2 ** 20
-SM_COUNT_NOMINAL = 152
 FP32_LANES_PER_SM = 128          # FP32 FMA units per SM (4 partitions x 32)
-SM_MAX_MHZ_NOMINAL = 2070.0
+SM_MAX_MHZ_NOMINAL = 2070.0      # only if MEASURED_PEAKS.json gives no maximum SM clock
 
 # ncu DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum, one capture of
 # the workload's kernel), keyed by workload; an entry is used only while the hash of the
@@ -292,23 +291,29 @@ class Workload:
         return self.flops / seconds_per_step / 1e12
 
     def roofline(self, sec_per_launch, peaks, sm_mhz):
+        """Roofline object of the workload's kernel.  Every kernel here is timed in
+        isolation (back-to-back calls over a region of milliseconds, not inside a
+        seconds-long step), so the tensor peaks are the burst figures of the measured
+        peaks; the FP32 CUDA-core peak comes from this device's SM count and the maximum
+        SM clock."""
         if self.bound == "alu":
-            peak = SM_COUNT_NOMINAL * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+            sms = self.torch.cuda.get_device_properties(self.torch.cuda.current_device()).multi_processor_count
+            peak = sms * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
             achieved = self.flops / sec_per_launch / 1e12
             unit = "TFLOP/s"
-            note = (f"FP32 CUDA-core peak = {SM_COUNT_NOMINAL} SMs x {FP32_LANES_PER_SM} FMA/clk x 2 "
-                    f"x {peaks['sm_max_mhz']:.0f} MHz")
+            note = (f"FP32 CUDA-core peak = {sms} SMs (this device) x {FP32_LANES_PER_SM} FMA/clk x 2 "
+                    f"x {peaks['sm_max_mhz']:.0f} MHz (maximum SM clock)")
         elif self.bound == "tensor8":
-            peak = 2.0 * peaks["bf16_sustained"]
+            peak = 2.0 * peaks["bf16"]
             achieved = self.flops / sec_per_launch / 1e12
             unit = "TFLOP/s"
-            note = (f"fp8 dense = 2 x the bf16 sustained cuBLAS figure of {peaks['source']} peaks "
-                    f"(nominal fp8 / bf16 ratio 4.5 / 2.25)")
+            note = (f"fp8 dense = 2 x the bf16 burst cuBLAS figure of {peaks['source']} peaks "
+                    f"(nominal fp8 / bf16 ratio 4.5 / 2.25); kernel timed in isolation")
         elif self.bound == "tensor":
-            peak = peaks["bf16_sustained"]
+            peak = peaks["bf16"]
             achieved = self.flops / sec_per_launch / 1e12
             unit = "TFLOP/s"
-            note = f"bf16 dense, sustained cuBLAS figure of {peaks['source']} peaks"
+            note = f"bf16 dense, burst cuBLAS figure of {peaks['source']} peaks; kernel timed in isolation"
         else:
             peak = peaks["hbm_gbs"]
             achieved = self.algo_bytes / sec_per_launch / 1e9
@@ -563,14 +568,38 @@ def time_e2e(torch, wl, steps, warmup):
             "result_equals_serial_call": bool(same)}
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def cpu_baseline(wl, budget_s=15.0, nthreads=None):
-    """The oracle, as it stands, on a bounded sample (the first R rows of C) of the workload."""
+    """The oracle, as it stands, on a bounded sample (the first R rows of C) of the workload.
+    `nthreads` is the number of host threads the oracle's loops use (all cores by default);
+    the returned `cores` is the number it actually used."""
     import oracle
     w = wl.w
     nthreads = nthreads or os.cpu_count() or 1
     if wl.kind == "attn":
-        return attn_cpu_baseline(wl, budget_s)
+        return attn_cpu_baseline(wl, budget_s, nthreads)
     if wl.kind == "chain":
+        # The whole chain: four layers of M x 4096 x 12288 are a few seconds of FP64 work at
+        # M <= 16, inside any budget used here.
         t = time.perf_counter()
         oracle.decode_chain(w["M"], w["dims"], w["X"], w["dims"][0], w["Ws"], w["dims"][1:],
                             nthreads=nthreads)
@@ -583,7 +612,7 @@ def cpu_baseline(wl, budget_s=15.0, nthreads=None):
         t = time.perf_counter()
         qa, sa = oracle.quantize_rows_e4m3(rows, K, w["X"], K)
         qb, sb = oracle.quantize_rows_e4m3(N, K, w["W"], K)
-        oracle.gemm_fp8(rows, N, K, qa, K, sa, qb, K, sb)
+        oracle.gemm_fp8(rows, N, K, qa, K, sa, qb, K, sb, nthreads=nthreads)
         dt = time.perf_counter() - t
         return {"value": round(2.0 * rows * N * K / dt / 1e12, 6), "unit": wl.unit, "cores": nthreads,
                 "kind": "oracle", "sample": f"rows 0..{rows - 1} of C ({rows}/{M}), quantisation of "
@@ -620,10 +649,22 @@ def cpu_baseline(wl, budget_s=15.0, nthreads=None):
                       f"FP64 triple loop, {dt:.2f} s"}
 
 
-def attn_cpu_baseline(wl, budget_s):
-    """The attention oracle on the first R query rows of head 0 (numpy float64 matmuls)."""
+def attn_cpu_baseline(wl, budget_s, nthreads=None):
+    """The attention oracle on the first R query rows of head 0 (numpy float64 matmuls).
+    Its matmul steps run on numpy's BLAS threads; a single-thread run limits them with
+    threadpoolctl, and returns None where that package is missing (the thread count of a
+    BLAS already loaded cannot be changed otherwise)."""
     import oracle
     w = wl.w
+    limit = None
+    cores = _blas_threads()
+    if nthreads is not None and nthreads < cores:
+        try:
+            from threadpoolctl import threadpool_limits
+        except ImportError:
+            return None
+        limit = threadpool_limits(limits=nthreads, user_api="blas")
+        cores = nthreads
 
     def run(rows):
         t = time.perf_counter()
@@ -632,15 +673,19 @@ def attn_cpu_baseline(wl, budget_s):
                          rows=np.arange(rows))
         return time.perf_counter() - t
 
-    rows = 64
-    dt = run(rows)
-    target = int(rows * budget_s / max(dt, 1e-6) * 0.8)
-    rows2 = max(rows, min(w["Lq"], target))
-    if rows2 > rows:
-        rows, dt = rows2, run(rows2)
+    try:
+        rows = 64
+        dt = run(rows)
+        target = int(rows * budget_s / max(dt, 1e-6) * 0.8)
+        rows2 = max(rows, min(w["Lq"], target))
+        if rows2 > rows:
+            rows, dt = rows2, run(rows2)
+    finally:
+        if limit is not None:
+            limit.restore_original_limits()
     pairs = rows * (rows + 1) // 2 if w["causal"] else rows * w["Lkv"]
     value = 4.0 * w["d"] * pairs / dt / 1e12
-    return {"value": round(value, 6), "unit": wl.unit, "cores": _blas_threads(), "kind": "oracle",
+    return {"value": round(value, 6), "unit": wl.unit, "cores": cores, "kind": "oracle",
             "sample": f"query rows 0..{rows - 1} of head 0 ({rows}/{w['Lq']} rows of 1/{w['batch']} "
                       f"heads), float64 softmax(QK^T)V, {dt:.2f} s"}
 
@@ -674,6 +719,7 @@ def reference_arm(args):
     value = float(np.median([v["value"] for v in vals]))
     cb = dict(vals[-1])
     cb["value"] = round(value, 6)
+    cb["cpu_model"] = cpu_model()
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": wl.unit,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -799,9 +845,13 @@ def main():
         line["suite"] = suite
     if not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(wl)
-        # The same oracle on one host thread, beside the all-cores figure.
+        line["cpu_baseline"]["cpu_model"] = cpu_model()
+        # The same oracle on one host thread, beside the all-cores figure (left out where the
+        # oracle's threads cannot be limited to one).
         one = cpu_baseline(wl, budget_s=5.0, nthreads=1)
-        line["cpu_baseline"]["single_thread"] = {"value": one["value"], "sample": one["sample"]}
+        if one is not None:
+            line["cpu_baseline"]["single_thread"] = {"value": one["value"], "cores": one["cores"],
+                                                     "sample": one["sample"]}
     print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()

@@ -498,8 +498,17 @@ cudaError_t device_status_word(int dev, uint32_t** status, int* sms) {
 cudaError_t launch_scale(void* C, bool c_f32, int64_t M, int64_t N, int64_t ldc, int64_t strideC,
                          int64_t batch, float beta, cudaStream_t s) {
   const int64_t total = batch * M * N;
+  // A grid-stride loop over at most 32 blocks of 256 threads per SM of this device.
+  int dev = 0;
+  cudaError_t e = current_device(&dev);
+  if (e != cudaSuccess) return e;
+  uint32_t* status = nullptr;
+  int sms = 0;
+  e = device_info(dev, &status, &sms);
+  if (e != cudaSuccess) return e;
   int64_t blocks = (total + 255) / 256;
-  if (blocks > 152 * 32) blocks = 152 * 32;
+  const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 1) * 32;
+  if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   if (c_f32)
     scale_kernel<float><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
@@ -837,6 +846,7 @@ dg_status dg_device_status(void* stream) {
       if (kv.first.first == dev && kv.second.counters)
         cudaMemset(kv.second.counters, 0, kv.second.n_counters * sizeof(uint32_t));
   }
+  if (noalloc_reset_counters(dev) != cudaSuccess) return DG_ERR_CUDA;
   if (cudaDeviceSynchronize() != cudaSuccess) return DG_ERR_CUDA;
   return DG_ERR_TIMEOUT;
 }

@@ -56,3 +56,39 @@ def test_batched_qk_counts():
     w = bench.Workload.__new__(bench.Workload)
     w.__dict__.update(s)
     assert w.metric_value(1e-3) == pytest.approx(68.719476736)
+
+
+class _FakeCuda:
+    """Stands in for torch.cuda in the roofline's SM-count query (no GPU here)."""
+
+    def __init__(self, sms):
+        self.sms = sms
+
+    def current_device(self):
+        return 0
+
+    def get_device_properties(self, dev):
+        return type("Props", (), {"multi_processor_count": self.sms})()
+
+
+@pytest.mark.parametrize("sms", [152, 148])
+def test_roofline_peaks(sms):
+    # Kernels are timed in isolation, so tensor work is measured against the burst BF16
+    # figure (FP8: twice it); the FP32 CUDA-core peak uses the device's own SM count.
+    peaks = dict(hbm_gbs=6698.5, bf16=1929.9, bf16_sustained=1761.4, sm_max_mhz=2070.0,
+                 source="measured")
+    fake_torch = type("T", (), {"cuda": _FakeCuda(sms)})()
+
+    def wl(name):
+        w = bench.Workload.__new__(bench.Workload)
+        w.__dict__.update(spec(name), name=name, torch=fake_torch)
+        return w
+
+    r = wl("sgemm_4096").roofline(2.0e-3, peaks, None)
+    assert r["bound"] == "alu"
+    assert r["peak"] == pytest.approx(sms * 128 * 2 * 2070e6 / 1e12, abs=0.05)
+    assert r["frac"] == pytest.approx((2 * 4096 ** 3 / 2.0e-3 / 1e12) / r["peak"], rel=1e-3)
+    assert wl("ffn_bf16").roofline(60e-6, peaks, None)["peak"] == pytest.approx(1929.9)
+    assert wl("fp8_ffn").roofline(40e-6, peaks, None)["peak"] == pytest.approx(2 * 1929.9)
+    d = wl("decode_m1").roofline(19e-6, peaks, None)
+    assert d["bound"] == "hbm" and d["peak"] == pytest.approx(6698.5)
