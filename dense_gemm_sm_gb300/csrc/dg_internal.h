@@ -102,6 +102,10 @@ cudaError_t launch_gemm_thin(const ThinParams& p, int ntok, const void* X, int64
 constexpr int kThinBN = 128, kThinBK = 64;
 inline int64_t thin_ws_floats(int64_t ctas, int ntok) { return ctas * 2 * ntok * 128; }
 
+// Zeroes the arrival counters of the no-allocation decode entry point's fixed scratch on
+// `dev` (after a bounded wait gave up); a no-op where that entry point never ran.
+cudaError_t noalloc_reset_counters(int dev);
+
 // ------------------------------------------------------------------ persistent decode chain
 // y_{l+1} = bf16(y_l W_l) for l < layers (y_0 = X, M <= 16 rows), one cooperative launch of
 // `ctas` CTAs; every layer is split stream-K over the same CTAs as gemm_thin_kernel splits

@@ -11,7 +11,9 @@
 // Limits: M <= 16 rows of X, N <= 1,048,576 columns, at most 160 CTAs; 2.5 MiB of partials
 // plus 32 KiB of counters.  Every call shares the array: calls whose kernels overlap on the
 // GPU (on different streams, or the same call issued from two threads) race on it and give
-// wrong results; serialise them, e.g. on one stream.
+// wrong results; serialise them, e.g. on one stream.  Between calls the counters are zero
+// (the kernel resets each one as it combines its tile), so a call enqueues only its kernel,
+// which keeps back-to-back calls overlapping through programmatic dependent launch.
 #include <cstdint>
 #include <mutex>
 
@@ -41,12 +43,17 @@ unsigned char* g_na_addr[kNaMaxDevices] = {};
 
 // Device address of the scratch array on `dev` (the current device).  In host code the
 // array's name is only a host-side stand-in, so the address is taken once per device with
-// cudaGetSymbolAddress and cached.
-cudaError_t scratch_address(int dev, unsigned char** out) {
+// cudaGetSymbolAddress and cached.  The array starts zeroed (module load), and the kernel
+// leaves every arrival counter at zero when it finishes, so calls need no memset; the first
+// call on a device still zeroes the counters on its stream once, and a call that gave up on
+// a bounded wait is cleaned up by dg_device_status (noalloc_reset_counters below).
+cudaError_t scratch_address(int dev, cudaStream_t s, unsigned char** out) {
   std::lock_guard<std::mutex> lock(g_na_mu);
   if (!g_na_addr[dev]) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    e = cudaMemsetAsync(static_cast<unsigned char*>(p) + kNaPartialBytes, 0, kNaCounterBytes, s);
     if (e != cudaSuccess) return e;
     g_na_addr[dev] = static_cast<unsigned char*>(p);
   }
@@ -57,6 +64,16 @@ cudaError_t scratch_address(int dev, unsigned char** out) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
+
+// Re-zeroes the arrival counters of `dev` (the current device) after a call gave up on a
+// bounded wait and may have left some non-zero; synchronous (dg_device_status already
+// synchronised the stream).  Nothing to do on a device that never ran this entry point.
+cudaError_t noalloc_reset_counters(int dev) {
+  std::lock_guard<std::mutex> lock(g_na_mu);
+  if (dev < 0 || dev >= kNaMaxDevices || !g_na_addr[dev]) return cudaSuccess;
+  return cudaMemset(g_na_addr[dev] + kNaPartialBytes, 0, kNaCounterBytes);
+}
+
 }  // namespace dg
 
 using namespace dg;
@@ -85,7 +102,7 @@ extern "C" dg_status gemm_bf16_decode_noalloc(int64_t M, int64_t N, int64_t K, f
   int sms = 0;
   if (device_status_word(dev, &status, &sms) != cudaSuccess) return DG_ERR_CUDA;
   unsigned char* scratch = nullptr;
-  if (scratch_address(dev, &scratch) != cudaSuccess) return DG_ERR_CUDA;
+  if (scratch_address(dev, s, &scratch) != cudaSuccess) return DG_ERR_CUDA;
 
   ThinParams p;
   p.M = M; p.N = N; p.K = K;
@@ -101,9 +118,8 @@ extern "C" dg_status gemm_bf16_decode_noalloc(int64_t M, int64_t N, int64_t K, f
   p.ws = reinterpret_cast<float*>(scratch);
   p.counters = reinterpret_cast<uint32_t*>(scratch + kNaPartialBytes);
   p.status = status;
-  // The arrival counters must start at zero; the partials are always written before read.
-  if (cudaMemsetAsync(p.counters, 0, static_cast<size_t>(p.n_tiles) * 4, s) != cudaSuccess)
-    return DG_ERR_CUDA;
+  // The arrival counters are zero between calls (the kernel resets each one when it combines
+  // the tile); the partials are always written before they are read.
   return launch_gemm_thin(p, kNaNtok, A, lda, B, ldb, false, s) == cudaSuccess ? DG_OK
                                                                               : DG_ERR_CUDA;
 }

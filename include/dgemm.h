@@ -123,12 +123,15 @@ dg_status gemm_bf16_strided_batched(int64_t M, int64_t N, int64_t K, float alpha
  *     M <= 16 and N <= 1,048,576; larger sizes return DG_ERR_UNSUPPORTED and enqueue
  *     nothing.  Alignment rules as gemm_bf16 (DG_ERR_MISALIGNED).
  *   - Calls no cudaMalloc, cudaFree or other allocating routine.  The first call on a
- *     device looks up the array's device address (cudaGetSymbolAddress) for that device;
- *     make that first call before any stream capture.
- *   - Every call shares the one array and leaves its contents behind; each call zeroes the
- *     counters it uses (cudaMemsetAsync on `stream`) before its kernel.  Calls whose work
- *     overlaps on the GPU (other streams, other host threads) race on the array and give
- *     wrong results: serialise them.
+ *     device does that device's set-up: it looks up the array's device address
+ *     (cudaGetSymbolAddress) and zeroes the arrival counters once (cudaMemsetAsync on
+ *     `stream`); make that first call before any stream capture.  The address is cached
+ *     for the life of the process and does not survive cudaDeviceReset on that device.
+ *   - Every call shares the one array and leaves its contents behind.  The kernel leaves
+ *     every arrival counter at zero when it finishes, so later calls enqueue only the
+ *     kernel; after a bounded wait gave up (dg_device_status returns DG_ERR_TIMEOUT) that
+ *     call re-zeroes the counters.  Calls whose work overlaps on the GPU (other streams,
+ *     other host threads) race on the array and give wrong results: serialise them.
  */
 dg_status gemm_bf16_decode_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
                                    const uint16_t* A, int64_t lda, const uint16_t* B,
