@@ -307,8 +307,13 @@ def test_bf16_decode_full_size(torch, M):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 8, 8), (3, 136, 200), (16, 1000, 4104), (5, 128, 64),
-                                   (9, 4096, 64), (32, 264, 2056)])
+                                   (9, 4096, 64), (32, 264, 2056), (16, 19456, 64),
+                                   (7, 19400, 128), (32, 12200, 136), (2, 3000, 4096)])
 def test_bf16_thin_ragged(torch, M, N, K):
+    # On 152 SMs: (16, 19456, 64) and (7, 19400, 128) give every CTA one whole tile of one
+    # or two K blocks; (32, 12200, 136) three K blocks per tile (a ragged last one) shared by
+    # neighbouring CTAs; (2, 3000, 4096) ranges shorter than a tile, so some tiles hold the
+    # ends of two ranges.
     lda = ((K + 7) // 8) * 8
     ldb = ((N + 7) // 8) * 8
     A = inputs.pad_rows(inputs.f32_to_bf16_bits(inputs.normal_f32(K + M, (M, K))), lda, 0)
