@@ -362,6 +362,7 @@ dg_status f32_impl(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
   p.sk_splits = splits;
   p.ws = nullptr;
   p.counters = nullptr;
+  p.status = status;
   if (sk > 0) {
     Workspace w;
     st = get_workspace(dev, s, static_cast<size_t>(simt_ws_floats(sk * splits)),

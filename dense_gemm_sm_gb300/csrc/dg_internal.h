@@ -27,8 +27,10 @@ struct SimtParams {
   int32_t sk_splits;
   float* ws;           // split-K partials: [sk_tiles][sk_splits][16][256] float4
   uint32_t* counters;  // [sk_tiles], zero between calls
+  uint32_t* status;    // device status word (bounded-wait expiry)
 };
-// vec: all rows 16-byte aligned (bases aligned, ld % 4 == 0) so 16-byte copies are legal.
+// vec: all rows 16-byte aligned (bases aligned, ld % 4 == 0): TMA-staged kernel; otherwise
+// the cp.async kernel with 4-byte copies.
 cudaError_t launch_sgemm_simt(const SimtParams& p, bool trans_b, bool vec, cudaStream_t s);
 // CTAs of the SIMT kernel that fit on one SM at once (occupancy query, cached).
 int sgemm_simt_ctas_per_sm(bool trans_b, bool vec);

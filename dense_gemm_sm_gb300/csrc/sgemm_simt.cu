@@ -4,15 +4,20 @@
 // steps: block tiling in shared memory along K (section 4), a register-blocked outer
 // product per thread (section 5), a 4 x 8 lane arrangement per warp (section 6), 16-byte
 // vector accesses (section 7), a bank-conflict-free shared layout (section 8) and
-// asynchronous multistage copies (sections 9-10).  This kernel keeps those ideas and sets
+// asynchronous multistage copies (sections 9-10).  These kernels keep those ideas and set
 // them for this GPU:
 //   * 128 x 128 block tile, BK = 32, 256 threads, an 8 x 8 FP32 accumulator per thread
-//     (4 x 8 lanes per warp, warp tile 32 x 64);
-//   * a 2-stage cp.async ring (global -> shared without registers), zero-filled edges;
-//   * A is kept K-contiguous in shared memory (row stride BK + 4 floats).  Each thread reads
-//     4 K-steps of one A row with one 16-byte load; the 4 distinct rows a warp reads
-//     fall in 4 different bank quads, and the 8 lanes of a quarter-warp share a row, so
-//     the reads are conflict-free without the register transpose of the tutorial;
+//     (4 x 8 lanes per warp, warp tile 32 x 64), 2 CTAs per SM;
+//   * operands staged by the tensor memory accelerator when every row is 16-byte aligned
+//     (sgemm_tma_kernel): a 3-stage ring whose stages one thread fills with two bulk tensor
+//     copies, completion counted in bytes on a per-stage mbarrier; the last warp to finish
+//     reading a stage refills it, so no thread waits at a CTA barrier and no thread spends
+//     issue slots on per-element copies;
+//   * otherwise (unaligned rows) a 2-stage cp.async ring with zero-filled edges
+//     (sgemm_simt_kernel);
+//   * A stays K-contiguous in shared memory with a 36-float row stride: a thread reads 4
+//     K-steps of one A row with one 16-byte load, and the 4 rows a warp reads at once fall
+//     in 4 different bank quads (conflict-free without the tutorial's register transpose);
 //   * B rows are read as two 16-byte vectors per K-step, 8 lanes covering 128 contiguous
 //     bytes (conflict-free);
 //   * thread rows are interleaved (row = base + 4*i) so C rows are written by 8 lanes
@@ -121,6 +126,104 @@ __device__ __forceinline__ void ffma2(float& d0, float& d1, float a, float b0, f
   d0 = fmaf(a, b0, d0);
   d1 = fmaf(a, b1, d1);
 #endif
+}
+
+// The end of one work item: a tail chunk publishes its partial accumulator and the last
+// chunk of the tile to arrive sums all chunks in chunk (= K) order; then C = alpha*acc +
+// beta*C_old with one FP32 rounding per operation, masked at the edges.  Called by every
+// thread of the CTA.
+template <bool TRANS_B, bool VEC>
+__device__ __forceinline__ void simt_finish(const SimtParams& p, float (&acc)[8][8], int64_t b,
+                                            int64_t m0, int64_t n0, int64_t tile, int chunk,
+                                            uint32_t* s_is_last) {
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int wm = warp >> 1, wn = warp & 1;
+  const int lm = lane >> 3, ln = lane & 7;
+  const int row_base = wm * 32 + lm;          // thread rows: row_base + 4*i
+  const int col_base_n = wn * 64 + ln * 4;    // N layout: cols col_base_n + {0..3}, +32
+  const int col_base_t = wn * 64 + ln;        // T layout: cols col_base_t + 8*j
+  float* C = p.C + b * p.strideC;
+
+  if (chunk >= 0) {
+    // One of the sk_splits K chunks of a tail tile: publish the partial accumulator; the last
+    // chunk to arrive sums all chunks in chunk (= K) order -- a fixed order -- and writes C.
+    const int64_t sk_tile = tile - p.dp_tiles;
+    const int S = p.sk_splits;
+    float4* mine = reinterpret_cast<float4*>(p.ws) + ((sk_tile * S + chunk) * 16) * NT + tid;
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+      mine[q * NT] = make_float4(acc[q >> 1][4 * (q & 1)], acc[q >> 1][4 * (q & 1) + 1],
+                                 acc[q >> 1][4 * (q & 1) + 2], acc[q >> 1][4 * (q & 1) + 3]);
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      const uint32_t prev = atomicAdd(&p.counters[sk_tile], 1u);
+      const bool last = prev + 1u == static_cast<uint32_t>(S);
+      if (last) __threadfence();
+      *s_is_last = last ? 1u : 0u;
+    }
+    __syncthreads();
+    if (!*s_is_last) return;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    for (int cc = 0; cc < S; ++cc) {
+      const float4* src = reinterpret_cast<const float4*>(p.ws) + ((sk_tile * S + cc) * 16) * NT + tid;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {  // 8 independent 16-byte loads in flight
+        float4 part[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) part[q] = __ldcg(src + (8 * half + q) * NT);
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8) {
+          const int q = 8 * half + q8;
+          acc[q >> 1][4 * (q & 1)] += part[q8].x;
+          acc[q >> 1][4 * (q & 1) + 1] += part[q8].y;
+          acc[q >> 1][4 * (q & 1) + 2] += part[q8].z;
+          acc[q >> 1][4 * (q & 1) + 3] += part[q8].w;
+        }
+      }
+    }
+    if (tid == 0) p.counters[sk_tile] = 0u;  // ready for the next call
+  }
+
+  // Epilogue: C = alpha*acc + beta*C_old, one FP32 rounding per operation.
+  const float alpha = p.alpha, beta = p.beta;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int64_t gm = m0 + row_base + 4 * i;
+    if (gm >= p.M) continue;
+    float* crow = C + gm * p.ldc;
+    if (TRANS_B) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int64_t gn = n0 + col_base_t + 8 * j;
+        if (gn < p.N)
+          crow[gn] = beta != 0.f ? fmaf(alpha, acc[i][j], beta * crow[gn]) : alpha * acc[i][j];
+      }
+    } else {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t gn = n0 + col_base_n + 32 * h;
+        const float* a4 = &acc[i][4 * h];
+        if (VEC && gn + 3 < p.N) {
+          float4* dst = reinterpret_cast<float4*>(crow + gn);
+          float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (beta != 0.f) o = *dst;
+          *dst = make_float4(fmaf(alpha, a4[0], beta * o.x), fmaf(alpha, a4[1], beta * o.y),
+                             fmaf(alpha, a4[2], beta * o.z), fmaf(alpha, a4[3], beta * o.w));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (gn + j < p.N)
+              crow[gn + j] = beta != 0.f ? fmaf(alpha, a4[j], beta * crow[gn + j]) : alpha * a4[j];
+          }
+        }
+      }
+    }
+  }
 }
 
 // One work item: the K tiles [kbeg, kend) of output tile `tile`.  sk_cta < 0 marks a
@@ -260,89 +363,7 @@ __device__ __forceinline__ void simt_item(const SimtParams& p, float* As, float*
     stage = stage + 1 == STAGES ? 0 : stage + 1;
   }
   cp_async_wait<0>();
-  {
-  float* C = p.C + b * p.strideC;
-
-  if (chunk >= 0) {
-    // One of the sk_splits K chunks of a tail tile: publish the partial accumulator; the last
-    // chunk to arrive sums all chunks in chunk (= K) order -- a fixed order -- and writes C.
-    const int64_t sk_tile = tile - p.dp_tiles;
-    const int S = p.sk_splits;
-    float4* mine = reinterpret_cast<float4*>(p.ws) + ((sk_tile * S + chunk) * 16) * NT + tid;
-#pragma unroll
-    for (int q = 0; q < 16; ++q)
-      mine[q * NT] = make_float4(acc[q >> 1][4 * (q & 1)], acc[q >> 1][4 * (q & 1) + 1],
-                                 acc[q >> 1][4 * (q & 1) + 2], acc[q >> 1][4 * (q & 1) + 3]);
-    __syncthreads();
-    if (tid == 0) {
-      __threadfence();
-      const uint32_t prev = atomicAdd(&p.counters[sk_tile], 1u);
-      const bool last = prev + 1u == static_cast<uint32_t>(S);
-      if (last) __threadfence();
-      *s_is_last = last ? 1u : 0u;
-    }
-    __syncthreads();
-    if (!*s_is_last) return;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-      for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-    for (int cc = 0; cc < S; ++cc) {
-      const float4* src = reinterpret_cast<const float4*>(p.ws) + ((sk_tile * S + cc) * 16) * NT + tid;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {  // 8 independent 16-byte loads in flight
-        float4 part[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) part[q] = __ldcg(src + (8 * half + q) * NT);
-#pragma unroll
-        for (int q8 = 0; q8 < 8; ++q8) {
-          const int q = 8 * half + q8;
-          acc[q >> 1][4 * (q & 1)] += part[q8].x;
-          acc[q >> 1][4 * (q & 1) + 1] += part[q8].y;
-          acc[q >> 1][4 * (q & 1) + 2] += part[q8].z;
-          acc[q >> 1][4 * (q & 1) + 3] += part[q8].w;
-        }
-      }
-    }
-    if (tid == 0) p.counters[sk_tile] = 0u;  // ready for the next call
-  }
-
-  // Epilogue: C = alpha*acc + beta*C_old, one FP32 rounding per operation.
-  const float alpha = p.alpha, beta = p.beta;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int64_t gm = m0 + row_base + 4 * i;
-    if (gm >= p.M) continue;
-    float* crow = C + gm * p.ldc;
-    if (TRANS_B) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int64_t gn = n0 + col_base_t + 8 * j;
-        if (gn < p.N)
-          crow[gn] = beta != 0.f ? fmaf(alpha, acc[i][j], beta * crow[gn]) : alpha * acc[i][j];
-      }
-    } else {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int64_t gn = n0 + col_base_n + 32 * h;
-        const float* a4 = &acc[i][4 * h];
-        if (VEC && gn + 3 < p.N) {
-          float4* dst = reinterpret_cast<float4*>(crow + gn);
-          float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (beta != 0.f) o = *dst;
-          *dst = make_float4(fmaf(alpha, a4[0], beta * o.x), fmaf(alpha, a4[1], beta * o.y),
-                             fmaf(alpha, a4[2], beta * o.z), fmaf(alpha, a4[3], beta * o.w));
-        } else {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (gn + j < p.N)
-              crow[gn + j] = beta != 0.f ? fmaf(alpha, a4[j], beta * crow[gn + j]) : alpha * a4[j];
-          }
-        }
-      }
-    }
-  }
-  }
+  simt_finish<TRANS_B, VEC>(p, acc, b, m0, n0, tile, chunk, s_is_last);
 }
 
 template <bool TRANS_B, bool VEC>
@@ -370,6 +391,260 @@ __global__ void __launch_bounds__(NT, DG_SIMT_MIN_BLOCKS) sgemm_simt_kernel(cons
   const int kbeg = static_cast<int>(static_cast<int64_t>(chunk) * KT / S);
   const int kend = static_cast<int>(static_cast<int64_t>(chunk + 1) * KT / S);
   simt_item<TRANS_B, VEC>(p, As, Bs, p.dp_tiles + j / S, kbeg, kend, chunk, &s_is_last);
+}
+
+// ------------------------------------------------------------------ TMA-staged kernel
+// Work item of CTA `cta`: the first dp_tiles CTAs take one whole tile each; CTA
+// dp_tiles + j takes K chunk j % S (of S equal chunks) of tail tile dp_tiles + j / S.
+struct SimtItem {
+  int64_t tile, b, m0, n0;
+  int kbeg, kend, chunk;  // chunk -1: a whole tile
+};
+__device__ __forceinline__ SimtItem simt_item_of(const SimtParams& p, int64_t cta) {
+  SimtItem it;
+  const int KT = static_cast<int>((p.K + BK - 1) / BK);
+  if (cta < p.dp_tiles) {
+    it.tile = cta; it.kbeg = 0; it.kend = KT; it.chunk = -1;
+  } else {
+    const int64_t j = cta - p.dp_tiles;
+    const int S = p.sk_splits;
+    it.chunk = static_cast<int>(j % S);
+    it.kbeg = static_cast<int>(static_cast<int64_t>(it.chunk) * KT / S);
+    it.kend = static_cast<int>(static_cast<int64_t>(it.chunk + 1) * KT / S);
+    it.tile = p.dp_tiles + j / S;
+  }
+  int64_t tm, tn;
+  raster_tile(it.tile, p.tiles_m, p.tiles_n, p.group, &it.b, &tm, &tn);
+  it.m0 = tm * BM;
+  it.n0 = tn * BN;
+  return it;
+}
+
+// A (and B^T) arrive as boxes of 128 rows x LDS_K = 36 floats: the copy carries 4 columns
+// of the next K tile (or zeros past K) that are never read, and in exchange the rows land
+// with the padded 144-byte pitch, so the 4 rows a warp reads at once fall in 4 different bank
+// quads and every shared address is a register plus an immediate offset.  B [K][N] arrives
+// as dense [32][128] rows.
+constexpr int T_STAGES = 3;
+constexpr uint32_t T_A_BYTES = BM * LDS_K * 4;                     // 18 KiB
+template <bool TRANS_B>
+struct TmaCfg {
+  static constexpr uint32_t B_BYTES = TRANS_B ? BN * LDS_K * 4 : BK * BN * 4;  // 18 / 16 KiB
+  static constexpr uint32_t STAGE_BYTES = T_A_BYTES + B_BYTES;
+  static constexpr int SMEM_BYTES = 1024 + T_STAGES * STAGE_BYTES + 128;
+};
+constexpr int T_WARPS = NT / 32;
+
+
+// Bounded wait for a stage (mbar_wait with the abort flag addressed in the shared window,
+// so that few registers stay live in the main loop).
+__device__ __forceinline__ bool stage_wait(uint32_t bar, uint32_t parity, uint32_t abort_s,
+                                           const SimtParams& p) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 31u) == 0) {
+      uint32_t ab;
+      asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(ab) : "r"(abort_s) : "memory");
+      if (ab) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        asm volatile("st.volatile.shared.u32 [%0], 1;" ::"r"(abort_s) : "memory");
+        atomicCAS(p.status, 0u, static_cast<uint32_t>(kDevTimeoutMma));
+        return false;
+      }
+    }
+  }
+}
+
+struct TmaCtl {
+  int32_t coord[4];         // the copies' coordinates: first K column, row, column, batch
+  int64_t tile;             // the work item's tile and K chunk (-1: whole tile)
+  int32_t chunk;
+  uint64_t full[T_STAGES];  // stage s holds K tile i (bytes counted by the copies)
+  uint32_t done[T_STAGES];  // warps that have finished reading stage s, over all its uses
+  uint32_t abort;
+  uint32_t is_last;
+};
+
+// Shared-memory add with acquire and release at CTA scope: the warps' reads of a stage are
+// ordered before the count that tells the last of them to refill it.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_cta(uint32_t addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+  return old;
+}
+
+// One work item (tile `tile`, K tiles [kbeg, kend), chunk as in sgemm_simt_kernel), operands
+// staged by TMA.  Every thread waits on the stage's barrier (bounded); after reading a
+// stage, each warp counts itself done, and the warp completing the count issues the copies
+// of the K tile that goes to that stage next.
+template <bool TRANS_B, bool RANK3>
+__global__ void __launch_bounds__(NT, DG_SIMT_MIN_BLOCKS)
+    sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const SimtParams p) {
+  using Cfg = TmaCfg<TRANS_B>;
+  constexpr uint32_t T_STAGE_BYTES = Cfg::STAGE_BYTES;
+  extern __shared__ __align__(16) float smem_f[];
+  const uint32_t raw = smem_u32(smem_f);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  float* const stages = smem_f + (base - raw) / 4;
+  TmaCtl* ctl = reinterpret_cast<TmaCtl*>(stages + T_STAGES * T_STAGE_BYTES / 4);
+
+  // Launched with programmatic serialisation: wait for the previous kernel before the first
+  // global access, and let the next one launch early.
+  pdl_trigger();
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  // Only the K-tile count stays in a register through the main loop; the copy issue reads
+  // its coordinates from shared memory and the epilogue recomputes the work item.
+  int n_k;
+  {
+    const SimtItem it = simt_item_of(p, blockIdx.x);
+    n_k = it.kend - it.kbeg;
+    if (tid == 0) {
+      ctl->coord[0] = it.kbeg * BK;
+      ctl->coord[1] = static_cast<int32_t>(it.m0);
+      ctl->coord[2] = static_cast<int32_t>(it.n0);
+      ctl->coord[3] = static_cast<int32_t>(it.b);
+      ctl->tile = it.tile;
+      ctl->chunk = it.chunk;
+    }
+  }
+
+  if (tid == 0) {
+    for (int s = 0; s < T_STAGES; ++s) {
+      mbar_init(smem_u32(&ctl->full[s]), 1);
+      ctl->done[s] = 0;
+    }
+    ctl->abort = 0;
+    ctl->is_last = 0;
+    fence_barrier_init();
+    tma_prefetch_map(&tmA);
+    tma_prefetch_map(&tmB);
+  }
+  __syncthreads();
+  pdl_wait();
+
+  // Copies of relative K tile i into its stage, by one thread.
+  auto issue = [&](int i) {
+    const int4 c = *reinterpret_cast<const int4*>(ctl->coord);
+    const int32_t x_m = c.y, x_n = c.z, x_b = c.w;
+    const int s = i % T_STAGES;
+    const uint32_t fb = smem_u32(&ctl->full[s]);
+    const uint32_t dst = base + s * T_STAGE_BYTES;
+    static_assert(T_STAGE_BYTES % 128 == 0 && T_A_BYTES % 128 == 0, "TMA destinations");
+    const int32_t kx = c.x + i * BK;
+    fence_proxy_async_smem();  // earlier reads of the stage come before the async writes
+    mbar_arrive_expect_tx(fb, T_STAGE_BYTES);
+    if (RANK3) {
+      tma_load_3d(dst, &tmA, fb, kx, x_m, x_b);
+      if (TRANS_B)
+        tma_load_3d(dst + T_A_BYTES, &tmB, fb, kx, x_n, x_b);
+      else
+        tma_load_3d(dst + T_A_BYTES, &tmB, fb, x_n, kx, x_b);
+    } else {
+      tma_load_2d(dst, &tmA, fb, kx, x_m);
+      if (TRANS_B)
+        tma_load_2d(dst + T_A_BYTES, &tmB, fb, kx, x_n);
+      else
+        tma_load_2d(dst + T_A_BYTES, &tmB, fb, x_n, kx);
+    }
+  };
+  if (tid == 0)
+    for (int i = 0; i < T_STAGES && i < n_k; ++i) issue(i);
+
+  const int wm = warp >> 1, wn = warp & 1;
+  const int lm = lane >> 3, ln = lane & 7;
+  const int row_base = wm * 32 + lm;          // thread rows: row_base + 4*i
+  const int col_base_n = wn * 64 + ln * 4;    // N layout: cols col_base_n + {0..3}, +32
+  const int col_base_t = wn * 64 + ln;        // T layout: cols col_base_t + 8*j
+
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+  int consumed = 0;
+  for (int i = 0; i < n_k; ++i) {
+    const int s = i % T_STAGES;
+    if (!stage_wait(smem_u32(&ctl->full[s]), static_cast<uint32_t>(i / T_STAGES) & 1u,
+                    smem_u32(&ctl->abort), p))
+      break;
+    const float* as = stages + s * (T_STAGE_BYTES / 4);
+    const float* bs = as + T_A_BYTES / 4;
+#pragma unroll
+    for (int kk = 0; kk < BK / 4; ++kk) {
+      float4 a[8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+        a[r] = *reinterpret_cast<const float4*>(as + (row_base + 4 * r) * LDS_K + kk * 4);
+      if (TRANS_B) {
+        float4 bt[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          bt[j] = *reinterpret_cast<const float4*>(bs + (col_base_t + 8 * j) * LDS_K + kk * 4);
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4)
+#pragma unroll
+          for (int r = 0; r < 8; ++r)
+#pragma unroll
+            for (int j = 0; j < 8; j += 2)
+              ffma2(acc[r][j], acc[r][j + 1], f4get(a[r], k4), f4get(bt[j], k4), f4get(bt[j + 1], k4));
+      } else {
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const int k = kk * 4 + k4;
+          const float4 b0 = *reinterpret_cast<const float4*>(bs + k * BN + col_base_n);
+          const float4 b1 = *reinterpret_cast<const float4*>(bs + k * BN + col_base_n + 32);
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            const float av = f4get(a[r], k4);
+            ffma2(acc[r][0], acc[r][1], av, b0.x, b0.y);
+            ffma2(acc[r][2], acc[r][3], av, b0.z, b0.w);
+            ffma2(acc[r][4], acc[r][5], av, b1.x, b1.y);
+            ffma2(acc[r][6], acc[r][7], av, b1.z, b1.w);
+          }
+        }
+      }
+    }
+    consumed = i + 1;
+    // This warp is done with the stage; the warp that completes its count refills it.
+    __syncwarp();
+    if (lane == 0) {
+      const uint32_t prev = atom_add_acq_rel_cta(smem_u32(&ctl->done[s]), 1u);
+      if (prev + 1u == static_cast<uint32_t>(T_WARPS * (i / T_STAGES + 1)) && i + T_STAGES < n_k)
+        issue(i + T_STAGES);
+    }
+  }
+  __syncthreads();
+  if (*reinterpret_cast<volatile uint32_t*>(&ctl->abort)) {
+    // A wait gave up: no copy may still be landing in shared memory when the CTA exits.
+    if (tid == 0) {
+      uint32_t never = 0;
+      const int issued_end = consumed + T_STAGES < n_k ? consumed + T_STAGES : n_k;
+      for (int i = consumed; i < issued_end; ++i)
+        mbar_wait(smem_u32(&ctl->full[i % T_STAGES]), static_cast<uint32_t>(i / T_STAGES) & 1u,
+                  &never, p.status, kDevTimeoutDrain);
+    }
+    return;
+  }
+  simt_finish<TRANS_B, true>(p, acc, ctl->coord[3], ctl->coord[1], ctl->coord[2], ctl->tile,
+                             ctl->chunk, &ctl->is_last);
+}
+
+template <bool TRANS_B, bool RANK3>
+cudaError_t launch_tma_variant(const CUtensorMap& ma, const CUtensorMap& mb, const SimtParams& p,
+                               cudaStream_t s) {
+  auto kern = sgemm_tma_kernel<TRANS_B, RANK3>;
+  constexpr int smem = TmaCfg<TRANS_B>::SMEM_BYTES;
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t e = ensure_smem_attr(kern, smem, attr_done);
+  if (e != cudaSuccess) return e;
+  const int64_t grid = p.dp_tiles + p.sk_tiles * p.sk_splits;
+  return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(NT), smem, s, ma, mb, p);
 }
 
 template <bool TRANS_B, bool VEC>
@@ -400,16 +675,50 @@ int ctas_per_sm_variant() {
   cached.store(n, std::memory_order_relaxed);
   return n;
 }
+template <bool TRANS_B>
+int ctas_per_sm_tma() {
+  static std::atomic<int> cached{0};
+  int n = cached.load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  auto kern = sgemm_tma_kernel<TRANS_B, false>;
+  constexpr int smem = TmaCfg<TRANS_B>::SMEM_BYTES;
+  static std::atomic<uint64_t> attr_done{0};
+  n = 0;
+  if (ensure_smem_attr(kern, smem, attr_done) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, NT, smem) != cudaSuccess ||
+      n < 1)
+    n = 1;
+  cached.store(n, std::memory_order_relaxed);
+  return n;
+}
 }  // namespace
 
 int sgemm_simt_ctas_per_sm(bool trans_b, bool vec) {
-  if (trans_b) return vec ? ctas_per_sm_variant<true, true>() : ctas_per_sm_variant<true, false>();
-  return vec ? ctas_per_sm_variant<false, true>() : ctas_per_sm_variant<false, false>();
+  if (vec) return trans_b ? ctas_per_sm_tma<true>() : ctas_per_sm_tma<false>();
+  return trans_b ? ctas_per_sm_variant<true, false>() : ctas_per_sm_variant<false, false>();
 }
 
 cudaError_t launch_sgemm_simt(const SimtParams& p, bool trans_b, bool vec, cudaStream_t s) {
-  if (trans_b) return vec ? launch_variant<true, true>(p, s) : launch_variant<true, false>(p, s);
-  return vec ? launch_variant<false, true>(p, s) : launch_variant<false, false>(p, s);
+  if (vec) {
+    // Tensor maps over A [batch][M][lda] (box 36 K x 128 rows) and B: [K][ldb] (box 128 N x
+    // 32 K rows) or, transposed, [N][ldb] (box 36 K x 128 rows); no swizzle.
+    const uint64_t batch = p.batch > 1 ? static_cast<uint64_t>(p.batch) : 1;
+    CUtensorMap ma, mb;
+    if (!make_tile_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.A, p.K, p.M, p.lda, batch,
+                       p.strideA, LDS_K, BM, CU_TENSOR_MAP_SWIZZLE_NONE, 1))
+      return cudaErrorInvalidValue;
+    const bool okb = trans_b ? make_tile_map(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.B, p.K, p.N,
+                                             p.ldb, batch, p.strideB, LDS_K, BN,
+                                             CU_TENSOR_MAP_SWIZZLE_NONE, 1)
+                             : make_tile_map(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.B, p.N, p.K,
+                                             p.ldb, batch, p.strideB, BN, BK,
+                                             CU_TENSOR_MAP_SWIZZLE_NONE, 1);
+    if (!okb) return cudaErrorInvalidValue;
+    if (batch > 1)
+      return trans_b ? launch_tma_variant<true, true>(ma, mb, p, s) : launch_tma_variant<false, true>(ma, mb, p, s);
+    return trans_b ? launch_tma_variant<true, false>(ma, mb, p, s) : launch_tma_variant<false, false>(ma, mb, p, s);
+  }
+  return trans_b ? launch_variant<true, false>(p, s) : launch_variant<false, false>(p, s);
 }
 
 }  // namespace dg
