@@ -25,10 +25,16 @@ struct SimtParams {
   // (tail) tiles.  Grid = dp_tiles + sk_tiles * sk_splits.
   int64_t dp_tiles, sk_tiles;
   int32_t sk_splits;
-  float* ws;           // split-K partials: [sk_tiles][sk_splits][16][256] float4
-  uint32_t* counters;  // [sk_tiles], zero between calls
+  // Stream-K schedule instead (TMA kernel, sk_ctas > 0): CTA c computes the units
+  // [c*U/G, (c+1)*U/G) of the U = sk_units (tile, K tile) pairs, G = sk_ctas = grid; a tile
+  // shared by several CTAs is finished by the last of them, adding their parts in CTA order.
+  int64_t sk_units, sk_ctas;
+  float* ws;           // partials: [sk_tiles][sk_splits] or, stream-K, [sk_ctas][2], x [16][256] float4
+  uint32_t* counters;  // [sk_tiles] or, stream-K, [tiles]; zero between calls
   uint32_t* status;    // device status word (bounded-wait expiry)
 };
+// Stream-K SIMT ranges span at most this many segments (whole tiles or pieces of tiles).
+constexpr int kSimtMaxSegments = 10;
 // vec: all rows 16-byte aligned (bases aligned, ld % 4 == 0): TMA-staged kernel; otherwise
 // the cp.async kernel with 4-byte copies.
 cudaError_t launch_sgemm_simt(const SimtParams& p, bool trans_b, bool vec, cudaStream_t s);

@@ -457,10 +457,21 @@ __device__ __forceinline__ bool stage_wait(uint32_t bar, uint32_t parity, uint32
   }
 }
 
+// A CTA's work in (tile, K tile) units is one contiguous range, cut into segments at tile
+// boundaries: one segment (a whole tile or one K chunk of a tail tile) in the data-parallel
+// schedule, a few in the stream-K schedule.  The segment table is built once per CTA.
+constexpr int T_MAX_SEG = kSimtMaxSegments;
+struct SegInfo {
+  int64_t tile;
+  int32_t start, len;       // relative unit index of the first K tile, number of K tiles
+  int32_t kbeg, kend;       // K tiles of the tile
+  int32_t kx0, x_m, x_n, x_b;  // copy coordinates of the first K tile
+};
+
 struct TmaCtl {
-  int32_t coord[4];         // the copies' coordinates: first K column, row, column, batch
-  int64_t tile;             // the work item's tile and K chunk (-1: whole tile)
-  int32_t chunk;
+  SegInfo seg[T_MAX_SEG];
+  int32_t nseg, total;      // segments, K tiles over all of them
+  int32_t chunk;            // data-parallel schedule: the K chunk (-1: whole tile)
   uint64_t full[T_STAGES];  // stage s holds K tile i (bytes counted by the copies)
   uint32_t done[T_STAGES];  // warps that have finished reading stage s, over all its uses
   uint32_t abort;
@@ -475,11 +486,69 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_cta(uint32_t addr, uint32_t
   return old;
 }
 
-// One work item (tile `tile`, K tiles [kbeg, kend), chunk as in sgemm_simt_kernel), operands
-// staged by TMA.  Every thread waits on the stage's barrier (bounded); after reading a
-// stage, each warp counts itself done, and the warp completing the count issues the copies
-// of the K tile that goes to that stage next.
-template <bool TRANS_B, bool RANK3>
+// Global add with acquire and release at GPU scope (the stream-K ticket).
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* a, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(a), "r"(v) : "memory");
+  return old;
+}
+
+// Stream-K end of a segment that covers only part of its tile's K range: the CTA publishes
+// its partial accumulator (slot 0 for its range's first segment, 1 for its last) and takes a
+// ticket; the last contributor to take one adds every contributor's part in CTA (= K) order
+// -- a fixed order, so results repeat bit for bit whoever is last -- and writes C.
+template <bool TRANS_B>
+__device__ __forceinline__ void sk_segment_finish(const SimtParams& p, float (&acc)[8][8],
+                                                  const SegInfo& sg, int slot, uint32_t* s_is_last) {
+  const int tid = threadIdx.x;
+  const int64_t KT = (p.K + BK - 1) / BK, U = p.sk_units, G = p.sk_ctas;
+  const int64_t c = blockIdx.x;
+  const int64_t first = sk_cta_of<int64_t>(sg.tile * KT, U, G);
+  const int64_t last = sk_cta_of<int64_t>((sg.tile + 1) * KT - 1, U, G);
+  float4* mine = reinterpret_cast<float4*>(p.ws) + ((c * 2 + slot) * 16) * NT + tid;
+#pragma unroll
+  for (int q = 0; q < 16; ++q)
+    __stcg(mine + q * NT, make_float4(acc[q >> 1][4 * (q & 1)], acc[q >> 1][4 * (q & 1) + 1],
+                                      acc[q >> 1][4 * (q & 1) + 2], acc[q >> 1][4 * (q & 1) + 3]));
+  __syncthreads();
+  if (tid == 0) {
+    const uint32_t prev = atom_add_acq_rel_gpu(&p.counters[sg.tile], 1u);
+    const bool is_last = prev + 1u == static_cast<uint32_t>(last - first + 1);
+    if (is_last) p.counters[sg.tile] = 0u;  // ready for the next call
+    *s_is_last = is_last ? 1u : 0u;
+  }
+  __syncthreads();
+  if (!*s_is_last) return;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+  for (int64_t cc = first; cc <= last; ++cc) {
+    const int sl = sk_start<int64_t>(cc, U, G) >= sg.tile * KT ? 0 : 1;
+    const float4* src = reinterpret_cast<const float4*>(p.ws) + ((cc * 2 + sl) * 16) * NT + tid;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {  // 8 independent 16-byte loads in flight
+      float4 part[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) part[q] = __ldcg(src + (8 * half + q) * NT);
+#pragma unroll
+      for (int q8 = 0; q8 < 8; ++q8) {
+        const int q = 8 * half + q8;
+        acc[q >> 1][4 * (q & 1)] += part[q8].x;
+        acc[q >> 1][4 * (q & 1) + 1] += part[q8].y;
+        acc[q >> 1][4 * (q & 1) + 2] += part[q8].z;
+        acc[q >> 1][4 * (q & 1) + 3] += part[q8].w;
+      }
+    }
+  }
+  simt_finish<TRANS_B, true>(p, acc, sg.x_b, sg.x_m, sg.x_n, sg.tile, -1, s_is_last);
+}
+
+// One CTA's range of (tile, K tile) units, operands staged by TMA.  Every thread waits on the
+// stage's barrier (bounded); after reading a stage, each warp counts itself done, and the warp
+// completing the count issues the copies of the K tile that goes to that stage next -- across
+// segment boundaries too, so the next tile's operands stream in during an epilogue.
+template <bool TRANS_B, bool RANK3, bool STREAMK>
 __global__ void __launch_bounds__(NT, DG_SIMT_MIN_BLOCKS)
     sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const SimtParams p) {
@@ -497,23 +566,40 @@ __global__ void __launch_bounds__(NT, DG_SIMT_MIN_BLOCKS)
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  // Only the K-tile count stays in a register through the main loop; the copy issue reads
-  // its coordinates from shared memory and the epilogue recomputes the work item.
-  int n_k;
-  {
-    const SimtItem it = simt_item_of(p, blockIdx.x);
-    n_k = it.kend - it.kbeg;
-    if (tid == 0) {
-      ctl->coord[0] = it.kbeg * BK;
-      ctl->coord[1] = static_cast<int32_t>(it.m0);
-      ctl->coord[2] = static_cast<int32_t>(it.n0);
-      ctl->coord[3] = static_cast<int32_t>(it.b);
-      ctl->tile = it.tile;
+  if (tid == 0) {
+    // The segment table (64-bit index arithmetic here, once; the main loop reads the table).
+    const int64_t KT = (p.K + BK - 1) / BK;
+    int64_t u, u1;
+    ctl->chunk = -1;
+    if (STREAMK) {
+      u = sk_start<int64_t>(blockIdx.x, p.sk_units, p.sk_ctas);
+      u1 = sk_start<int64_t>(blockIdx.x + 1, p.sk_units, p.sk_ctas);
+    } else {
+      const SimtItem it = simt_item_of(p, blockIdx.x);
+      u = it.tile * KT + it.kbeg;
+      u1 = it.tile * KT + it.kend;
       ctl->chunk = it.chunk;
     }
-  }
-
-  if (tid == 0) {
+    int n = 0, start = 0;
+    while (u < u1 && n < T_MAX_SEG) {
+      SegInfo& sg = ctl->seg[n];
+      sg.tile = u / KT;
+      sg.kbeg = static_cast<int32_t>(u - sg.tile * KT);
+      sg.kend = static_cast<int32_t>(u1 - sg.tile * KT < KT ? u1 - sg.tile * KT : KT);
+      sg.start = start;
+      sg.len = sg.kend - sg.kbeg;
+      int64_t b, tm, tn;
+      raster_tile(sg.tile, p.tiles_m, p.tiles_n, p.group, &b, &tm, &tn);
+      sg.kx0 = sg.kbeg * BK;
+      sg.x_m = static_cast<int32_t>(tm * BM);
+      sg.x_n = static_cast<int32_t>(tn * BN);
+      sg.x_b = static_cast<int32_t>(b);
+      start += sg.len;
+      u += sg.len;
+      ++n;
+    }
+    ctl->nseg = n;
+    ctl->total = start;
     for (int s = 0; s < T_STAGES; ++s) {
       mbar_init(smem_u32(&ctl->full[s]), 1);
       ctl->done[s] = 0;
@@ -526,16 +612,20 @@ __global__ void __launch_bounds__(NT, DG_SIMT_MIN_BLOCKS)
   }
   __syncthreads();
   pdl_wait();
+  const int total = ctl->total;
 
   // Copies of relative K tile i into its stage, by one thread.
   auto issue = [&](int i) {
-    const int4 c = *reinterpret_cast<const int4*>(ctl->coord);
-    const int32_t x_m = c.y, x_n = c.z, x_b = c.w;
+    int g = 0;
+    if (STREAMK)
+      while (g + 1 < ctl->nseg && ctl->seg[g + 1].start <= i) ++g;
+    const SegInfo& sg = ctl->seg[g];
+    const int32_t x_m = sg.x_m, x_n = sg.x_n, x_b = sg.x_b;
+    const int32_t kx = sg.kx0 + (i - sg.start) * BK;
     const int s = i % T_STAGES;
     const uint32_t fb = smem_u32(&ctl->full[s]);
     const uint32_t dst = base + s * T_STAGE_BYTES;
     static_assert(T_STAGE_BYTES % 128 == 0 && T_A_BYTES % 128 == 0, "TMA destinations");
-    const int32_t kx = c.x + i * BK;
     fence_proxy_async_smem();  // earlier reads of the stage come before the async writes
     mbar_arrive_expect_tx(fb, T_STAGE_BYTES);
     if (RANK3) {
@@ -553,7 +643,7 @@ __global__ void __launch_bounds__(NT, DG_SIMT_MIN_BLOCKS)
     }
   };
   if (tid == 0)
-    for (int i = 0; i < T_STAGES && i < n_k; ++i) issue(i);
+    for (int i = 0; i < T_STAGES && i < total; ++i) issue(i);
 
   const int wm = warp >> 1, wn = warp & 1;
   const int lm = lane >> 3, ln = lane & 7;
@@ -561,89 +651,102 @@ __global__ void __launch_bounds__(NT, DG_SIMT_MIN_BLOCKS)
   const int col_base_n = wn * 64 + ln * 4;    // N layout: cols col_base_n + {0..3}, +32
   const int col_base_t = wn * 64 + ln;        // T layout: cols col_base_t + 8*j
 
-  float acc[8][8];
+  int i = 0;  // relative K tile across the range
+  bool failed = false;
+  const int nseg = STREAMK ? ctl->nseg : 1;
+  for (int g = 0; g < nseg && !failed; ++g) {
+    const int seg_end = STREAMK ? ctl->seg[g].start + ctl->seg[g].len : total;
+    float acc[8][8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
+    for (int r = 0; r < 8; ++r)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-
-  int consumed = 0;
-  for (int i = 0; i < n_k; ++i) {
-    const int s = i % T_STAGES;
-    if (!stage_wait(smem_u32(&ctl->full[s]), static_cast<uint32_t>(i / T_STAGES) & 1u,
-                    smem_u32(&ctl->abort), p))
-      break;
-    const float* as = stages + s * (T_STAGE_BYTES / 4);
-    const float* bs = as + T_A_BYTES / 4;
+      for (int j = 0; j < 8; ++j) acc[r][j] = 0.f;
+    for (; i < seg_end; ++i) {
+      const int s = i % T_STAGES;
+      if (!stage_wait(smem_u32(&ctl->full[s]), static_cast<uint32_t>(i / T_STAGES) & 1u,
+                      smem_u32(&ctl->abort), p)) {
+        failed = true;
+        break;
+      }
+      const float* as = stages + s * (T_STAGE_BYTES / 4);
+      const float* bs = as + T_A_BYTES / 4;
 #pragma unroll
-    for (int kk = 0; kk < BK / 4; ++kk) {
-      float4 a[8];
+      for (int kk = 0; kk < BK / 4; ++kk) {
+        float4 a[8];
 #pragma unroll
-      for (int r = 0; r < 8; ++r)
-        a[r] = *reinterpret_cast<const float4*>(as + (row_base + 4 * r) * LDS_K + kk * 4);
-      if (TRANS_B) {
-        float4 bt[8];
+        for (int r = 0; r < 8; ++r)
+          a[r] = *reinterpret_cast<const float4*>(as + (row_base + 4 * r) * LDS_K + kk * 4);
+        if (TRANS_B) {
+          float4 bt[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          bt[j] = *reinterpret_cast<const float4*>(bs + (col_base_t + 8 * j) * LDS_K + kk * 4);
+          for (int j = 0; j < 8; ++j)
+            bt[j] = *reinterpret_cast<const float4*>(bs + (col_base_t + 8 * j) * LDS_K + kk * 4);
 #pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4)
+          for (int k4 = 0; k4 < 4; ++k4)
 #pragma unroll
-          for (int r = 0; r < 8; ++r)
+            for (int r = 0; r < 8; ++r)
 #pragma unroll
-            for (int j = 0; j < 8; j += 2)
-              ffma2(acc[r][j], acc[r][j + 1], f4get(a[r], k4), f4get(bt[j], k4), f4get(bt[j + 1], k4));
-      } else {
+              for (int j = 0; j < 8; j += 2)
+                ffma2(acc[r][j], acc[r][j + 1], f4get(a[r], k4), f4get(bt[j], k4), f4get(bt[j + 1], k4));
+        } else {
 #pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-          const int k = kk * 4 + k4;
-          const float4 b0 = *reinterpret_cast<const float4*>(bs + k * BN + col_base_n);
-          const float4 b1 = *reinterpret_cast<const float4*>(bs + k * BN + col_base_n + 32);
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const int k = kk * 4 + k4;
+            const float4 b0 = *reinterpret_cast<const float4*>(bs + k * BN + col_base_n);
+            const float4 b1 = *reinterpret_cast<const float4*>(bs + k * BN + col_base_n + 32);
 #pragma unroll
-          for (int r = 0; r < 8; ++r) {
-            const float av = f4get(a[r], k4);
-            ffma2(acc[r][0], acc[r][1], av, b0.x, b0.y);
-            ffma2(acc[r][2], acc[r][3], av, b0.z, b0.w);
-            ffma2(acc[r][4], acc[r][5], av, b1.x, b1.y);
-            ffma2(acc[r][6], acc[r][7], av, b1.z, b1.w);
+            for (int r = 0; r < 8; ++r) {
+              const float av = f4get(a[r], k4);
+              ffma2(acc[r][0], acc[r][1], av, b0.x, b0.y);
+              ffma2(acc[r][2], acc[r][3], av, b0.z, b0.w);
+              ffma2(acc[r][4], acc[r][5], av, b1.x, b1.y);
+              ffma2(acc[r][6], acc[r][7], av, b1.z, b1.w);
+            }
           }
         }
       }
+      // This warp is done with the stage; the warp that completes its count refills it.
+      __syncwarp();
+      if (lane == 0) {
+        const uint32_t prev = atom_add_acq_rel_cta(smem_u32(&ctl->done[s]), 1u);
+        if (prev + 1u == static_cast<uint32_t>(T_WARPS * (i / T_STAGES + 1)) && i + T_STAGES < total)
+          issue(i + T_STAGES);
+      }
     }
-    consumed = i + 1;
-    // This warp is done with the stage; the warp that completes its count refills it.
-    __syncwarp();
-    if (lane == 0) {
-      const uint32_t prev = atom_add_acq_rel_cta(smem_u32(&ctl->done[s]), 1u);
-      if (prev + 1u == static_cast<uint32_t>(T_WARPS * (i / T_STAGES + 1)) && i + T_STAGES < n_k)
-        issue(i + T_STAGES);
+    // Every thread leaves the K loop at the same K tile (a stage whose copies never land
+    // times all of them out), so the barriers of the segment's end are reached by all.
+    __syncthreads();
+    if (failed || *reinterpret_cast<volatile uint32_t*>(&ctl->abort)) {
+      failed = true;
+      break;
     }
+    const SegInfo& sg = ctl->seg[g];
+    if (STREAMK && sg.len < static_cast<int32_t>((p.K + BK - 1) / BK))
+      sk_segment_finish<TRANS_B>(p, acc, sg, g == 0 ? 0 : 1, &ctl->is_last);
+    else
+      simt_finish<TRANS_B, true>(p, acc, sg.x_b, sg.x_m, sg.x_n, sg.tile,
+                                 STREAMK ? -1 : ctl->chunk, &ctl->is_last);
+    if (STREAMK) __syncthreads();  // is_last is rewritten by the next segment's end
   }
-  __syncthreads();
-  if (*reinterpret_cast<volatile uint32_t*>(&ctl->abort)) {
+  if (failed && tid == 0) {
     // A wait gave up: no copy may still be landing in shared memory when the CTA exits.
-    if (tid == 0) {
-      uint32_t never = 0;
-      const int issued_end = consumed + T_STAGES < n_k ? consumed + T_STAGES : n_k;
-      for (int i = consumed; i < issued_end; ++i)
-        mbar_wait(smem_u32(&ctl->full[i % T_STAGES]), static_cast<uint32_t>(i / T_STAGES) & 1u,
-                  &never, p.status, kDevTimeoutDrain);
-    }
-    return;
+    uint32_t never = 0;
+    const int issued_end = i + T_STAGES < total ? i + T_STAGES : total;
+    for (int j = i; j < issued_end; ++j)
+      mbar_wait(smem_u32(&ctl->full[j % T_STAGES]), static_cast<uint32_t>(j / T_STAGES) & 1u,
+                &never, p.status, kDevTimeoutDrain);
   }
-  simt_finish<TRANS_B, true>(p, acc, ctl->coord[3], ctl->coord[1], ctl->coord[2], ctl->tile,
-                             ctl->chunk, &ctl->is_last);
 }
 
-template <bool TRANS_B, bool RANK3>
+template <bool TRANS_B, bool RANK3, bool STREAMK>
 cudaError_t launch_tma_variant(const CUtensorMap& ma, const CUtensorMap& mb, const SimtParams& p,
                                cudaStream_t s) {
-  auto kern = sgemm_tma_kernel<TRANS_B, RANK3>;
+  auto kern = sgemm_tma_kernel<TRANS_B, RANK3, STREAMK>;
   constexpr int smem = TmaCfg<TRANS_B>::SMEM_BYTES;
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = ensure_smem_attr(kern, smem, attr_done);
   if (e != cudaSuccess) return e;
-  const int64_t grid = p.dp_tiles + p.sk_tiles * p.sk_splits;
+  const int64_t grid = p.sk_ctas > 0 ? p.sk_ctas : p.dp_tiles + p.sk_tiles * p.sk_splits;
   return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(NT), smem, s, ma, mb, p);
 }
 
@@ -680,7 +783,7 @@ int ctas_per_sm_tma() {
   static std::atomic<int> cached{0};
   int n = cached.load(std::memory_order_relaxed);
   if (n > 0) return n;
-  auto kern = sgemm_tma_kernel<TRANS_B, false>;
+  auto kern = sgemm_tma_kernel<TRANS_B, false, false>;
   constexpr int smem = TmaCfg<TRANS_B>::SMEM_BYTES;
   static std::atomic<uint64_t> attr_done{0};
   n = 0;
@@ -714,9 +817,19 @@ cudaError_t launch_sgemm_simt(const SimtParams& p, bool trans_b, bool vec, cudaS
                                              p.ldb, batch, p.strideB, BN, BK,
                                              CU_TENSOR_MAP_SWIZZLE_NONE, 1);
     if (!okb) return cudaErrorInvalidValue;
-    if (batch > 1)
-      return trans_b ? launch_tma_variant<true, true>(ma, mb, p, s) : launch_tma_variant<false, true>(ma, mb, p, s);
-    return trans_b ? launch_tma_variant<true, false>(ma, mb, p, s) : launch_tma_variant<false, false>(ma, mb, p, s);
+    const bool sk = p.sk_ctas > 0;
+#define DG_TMA_CASE(TB, R3, SK) \
+    if (trans_b == TB && (batch > 1) == R3 && sk == SK) return launch_tma_variant<TB, R3, SK>(ma, mb, p, s);
+    DG_TMA_CASE(false, false, false)
+    DG_TMA_CASE(true, false, false)
+    DG_TMA_CASE(false, true, false)
+    DG_TMA_CASE(true, true, false)
+    DG_TMA_CASE(false, false, true)
+    DG_TMA_CASE(true, false, true)
+    DG_TMA_CASE(false, true, true)
+    DG_TMA_CASE(true, true, true)
+#undef DG_TMA_CASE
+    return cudaErrorInvalidValue;
   }
   return trans_b ? launch_variant<true, false>(p, s) : launch_variant<false, false>(p, s);
 }

@@ -179,9 +179,13 @@ def test_fp32_plan_splits_k_when_tiles_are_few():
     assert (p["tiles"], p["splits"], p["tail_tiles"], p["grid"]) == (4, 8, 4, 32)
     p = dg.dg_plan_gemm(0, 200, 136, 1000, num_sms=152)
     assert p["splits"] == 16 and p["grid"] == 64                      # at most 16 chunks
-    p = dg.dg_plan_gemm(0, 1000, 3000, 777, num_sms=152)
-    assert (p["tiles"], p["splits"]) == (192, 3)                        # 777 / 3 >= 256 of K
     assert dg.dg_plan_gemm(0, 7, 9, 5, num_sms=152)["splits"] == 1      # one K tile: no split
+    # 1000 x 3000 x 777: 192 tiles x 25 K tiles for 304 resident CTAs -- stream-K, 15.8 K
+    # tiles per CTA (splits 0); 4096^3 keeps whole-tile waves and a split tail.
+    p = dg.dg_plan_gemm(0, 1000, 3000, 777, num_sms=152)
+    assert (p["tiles"], p["splits"], p["grid"], p["tail_tiles"]) == (192, 0, 304, 192)
+    p = dg.dg_plan_gemm(0, 4096, 4096, 4096, num_sms=152)
+    assert (p["tiles"], p["splits"], p["tail_tiles"]) == (1024, 8, 112)
 
 
 def _cdiv(a, b):
@@ -204,19 +208,28 @@ def test_plan_properties_on_random_shapes():
         assert p["kernel"] == dg.DG_KERNEL_SIMT_F32
         tiles = batch * _cdiv(M, 128) * _cdiv(N, 128)
         assert p["tiles"] == tiles and p["kblocks"] == _cdiv(K, p["tile_k"])
-        assert p["splits"] >= 1 and 0 <= p["tail_tiles"] <= tiles
-        assert p["grid"] == tiles - p["tail_tiles"] + p["tail_tiles"] * p["splits"]
-        if p["splits"] > 1:
-            # Chunks of at least 256 of K (8 K tiles), at most 3 waves of chunk CTAs on the
-            # 2 x 152 resident slots; when the tiles fill under a quarter of the slots, chunks
-            # go down to one K tile, at most 16.
-            G = 2 * sms
-            few = 4 * tiles <= G
-            assert p["tail_tiles"] > 0 and p["tail_tiles"] * p["splits"] <= 3 * G
-            assert p["splits"] <= (min(16, p["kblocks"]) if few else p["kblocks"] // 8)
-            assert p["workspace_bytes"] > 0
+        G, KT = 2 * sms, p["kblocks"]
+        streamk = (tiles < G and tiles * KT >= 4 * G and 4 * tiles > G
+                   and _cdiv(tiles * KT, G) <= 7 * KT)
+        if streamk:
+            # Stream-K: tiles for between a quarter and one wave, at least 4 K tiles per
+            # resident CTA, ranges of at most 7 tiles' K (so at most 8 segments); one wave of
+            # CTAs over all tiles.
+            assert p["splits"] == 0 and p["grid"] == G and p["tail_tiles"] == tiles
+            assert p["workspace_bytes"] == 2 * G * 16 * 256 * 16 + tiles * 4
         else:
-            assert p["tail_tiles"] == 0 and p["workspace_bytes"] == 0
+            assert p["splits"] >= 1 and 0 <= p["tail_tiles"] <= tiles
+            assert p["grid"] == tiles - p["tail_tiles"] + p["tail_tiles"] * p["splits"]
+            if p["splits"] > 1:
+                # Chunks of at least 256 of K (8 K tiles), at most 3 waves of chunk CTAs on the
+                # 2 x 152 resident slots; when the tiles fill under a quarter of the slots,
+                # chunks go down to one K tile, at most 16.
+                few = 4 * tiles <= G
+                assert p["tail_tiles"] > 0 and p["tail_tiles"] * p["splits"] <= 3 * G
+                assert p["splits"] <= (min(16, p["kblocks"]) if few else p["kblocks"] // 8)
+                assert p["workspace_bytes"] > 0
+            else:
+                assert p["tail_tiles"] == 0 and p["workspace_bytes"] == 0
         # BF16 and FP8 (FP8 is planned for one problem only)
         for dtype in (1, 2) if batch == 1 else (1,):
             q = dg.dg_plan_gemm(dtype, M, N, K, batch=batch, num_sms=sms)
