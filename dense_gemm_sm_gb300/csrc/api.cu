@@ -140,6 +140,41 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 void plan_f32(int64_t M, int64_t N, int64_t K, int64_t batch, int64_t resident, dg_plan* pl,
               int64_t* dp_tiles, int64_t* sk_tiles, int* sk_splits, bool vec = true) {
   pl->kernel = DG_KERNEL_SIMT_F32;
+  {
+    // Small problems (128 x 128 tiles for under a quarter of the resident slots): 32 x 32
+    // tiles, K in chunks of at least 4 pieces of 128 over at most as many CTAs as are
+    // resident (at most 16 chunks).  tile_k reports the staged K piece.
+    const int64_t T128 = batch * cdiv(M, kSimtBM) * cdiv(N, kSimtBN);
+    const int64_t G = resident > 0 ? resident : 1;
+    if (4 * T128 <= G) {
+      const int64_t T = batch * cdiv(M, kSimtSmallT) * cdiv(N, kSimtSmallT);
+      const int64_t pieces = cdiv(K, kSimtSmallKP);
+      int64_t S = G / T;
+      if (S > cdiv(pieces, 4)) S = cdiv(pieces, 4);
+      if (S > 16) S = 16;
+      if (S < 1) S = 1;
+      if (const char* f = std::getenv("DG_SIMT_SPLITS")) {  // tuning override (sweeps)
+        const int64_t v = std::atoi(f);
+        if (v >= 1) S = v < pieces ? v : pieces;
+      }
+      pl->tile_m = kSimtSmallT;
+      pl->tile_n = kSimtSmallT;
+      pl->tile_k = kSimtSmallKP;
+      pl->stages = 2;
+      pl->group = 1;
+      pl->tiles = T;
+      pl->kblocks = pieces;
+      pl->vec = 1;
+      pl->splits = static_cast<int32_t>(S);
+      pl->tail_tiles = S > 1 ? T : 0;
+      pl->grid = T * S;
+      pl->workspace_bytes = S > 1 ? T * S * kSimtSmallT * kSimtSmallT * 4 + T * 4 : 0;
+      *sk_splits = static_cast<int>(S);
+      *sk_tiles = S > 1 ? T : 0;
+      *dp_tiles = -1;  // marks the small-tile kernel
+      return;
+    }
+  }
   pl->tile_m = kSimtBM;
   pl->tile_n = kSimtBN;
   pl->tile_k = kSimtBK;
@@ -158,14 +193,9 @@ void plan_f32(int64_t M, int64_t N, int64_t K, int64_t batch, int64_t resident, 
     best_s = static_cast<int>(forced < KT ? forced : KT);
   } else if (tail > 0) {
     double best = 1.0;  // tail time (in tile times) without splitting
-    // At least 256 of K per chunk, so a chunk outweighs its partial tile -- unless the tiles
-    // fill under a quarter of the resident CTA slots (e.g. 256^3: 4 tiles for 304 slots),
-    // where one tile's whole K on one SM is the call's time: then chunks down to one K tile.
-    // (At most 16 chunks then: the last chunk of a tile adds every chunk's partial tile.)
-    const bool few = 4 * T <= G;
-    const int64_t min_chunk = few ? 1 : cdiv(256, kSimtBK);
-    const int64_t max_s = few ? 16 : KT;
-    for (int64_t S = 2; S <= KT / min_chunk && S <= max_s && tail * S <= 3 * G; ++S) {
+    // At least 256 of K per chunk, so a chunk outweighs its partial tile.
+    const int64_t min_chunk = cdiv(256, kSimtBK);
+    for (int64_t S = 2; S <= KT / min_chunk && tail * S <= 3 * G; ++S) {
       const double t = static_cast<double>(cdiv(tail * S, G)) / static_cast<double>(S);
       if (t < best - 1e-9) {
         best = t;
@@ -189,7 +219,7 @@ void plan_f32(int64_t M, int64_t N, int64_t K, int64_t batch, int64_t resident, 
   // most kSimtMaxSegments segments.  DG_SIMT_STREAMK=0/1 forces it off or on (sweeps).
   const int64_t U = T * KT;
   const char* fsk = std::getenv("DG_SIMT_STREAMK");
-  bool sk = vec && T < G && U >= 4 * G && !(4 * T <= G);
+  bool sk = vec && T < G && U >= 4 * G;
   if (fsk) sk = vec && fsk[0] == '1' && U >= G;
   if (sk && cdiv(U, G) + 2 * KT > static_cast<int64_t>(kSimtMaxSegments - 1) * KT) sk = false;
   if (sk) {
@@ -372,7 +402,7 @@ dg_status f32_impl(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
   int splits = 1;
   plan_f32(M, N, K, batch, resident, &pl, &dp, &sk, &splits, vec);
   log_plan("gemm_f32", M, N, K, batch, pl);
-  if (pl.tiles > INT32_MAX) return DG_ERR_UNSUPPORTED;
+  if (pl.tiles > INT32_MAX || pl.grid > INT32_MAX) return DG_ERR_UNSUPPORTED;
   SimtParams p;
   p.M = M; p.N = N; p.K = K;
   p.alpha = alpha; p.beta = beta;
@@ -391,6 +421,22 @@ dg_status f32_impl(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
   p.status = status;
   p.sk_units = 0;
   p.sk_ctas = 0;
+  if (dp < 0) {  // small problem: 32 x 32 tiles
+    p.tiles_m = cdiv(M, kSimtSmallT);
+    p.tiles_n = cdiv(N, kSimtSmallT);
+    p.dp_tiles = 0;
+    p.sk_tiles = sk;
+    p.sk_splits = splits;
+    if (splits > 1) {
+      Workspace w;
+      st = get_workspace(dev, s, static_cast<size_t>(pl.tiles * splits * kSimtSmallT * kSimtSmallT),
+                         static_cast<size_t>(pl.tiles), &w);
+      if (st != DG_OK) return st;
+      p.ws = w.ws;
+      p.counters = w.counters;
+    }
+    return from_cuda(launch_sgemm_simt_small(p, trans_b, vec, s));
+  }
   if (splits == 0) {  // stream-K over all tiles
     p.sk_units = pl.tiles * pl.kblocks;
     p.sk_ctas = pl.grid;

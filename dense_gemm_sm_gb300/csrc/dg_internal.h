@@ -38,6 +38,10 @@ constexpr int kSimtMaxSegments = 10;
 // vec: all rows 16-byte aligned (bases aligned, ld % 4 == 0): TMA-staged kernel; otherwise
 // the cp.async kernel with 4-byte copies.
 cudaError_t launch_sgemm_simt(const SimtParams& p, bool trans_b, bool vec, cudaStream_t s);
+// Small problems: 32 x 32 tiles (p.tiles_m, p.tiles_n count them), K cut into p.sk_splits
+// chunks; partials [tiles][splits][1024] floats and counters [tiles] when splits > 1.
+cudaError_t launch_sgemm_simt_small(const SimtParams& p, bool trans_b, bool vec, cudaStream_t s);
+constexpr int kSimtSmallT = 32, kSimtSmallKP = 128;
 // CTAs of the SIMT kernel that fit on one SM at once (occupancy query, cached).
 int sgemm_simt_ctas_per_sm(bool trans_b, bool vec);
 inline int64_t simt_ws_floats(int64_t partial_tiles) { return partial_tiles * 16 * 256 * 4; }

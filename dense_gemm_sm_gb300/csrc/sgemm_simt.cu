@@ -778,6 +778,252 @@ int ctas_per_sm_variant() {
   cached.store(n, std::memory_order_relaxed);
   return n;
 }
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
+// ------------------------------------------------------------------ small problems
+// When the 128 x 128 tiles would fill under a quarter of the resident CTA slots (256^3: 4
+// tiles), one tile's whole K on one SM is the call's time, and splitting K over CTAs in
+// 128 x 128 pieces leaves the last CTA adding eight 64 KiB partial tiles.  Here a CTA
+// computes a 32 x 32 tile instead: its 8 warps split each staged K piece 8 ways (16 K-steps
+// each, a 4 x 8 register tile per lane), then add their 8 partial tiles through shared
+// memory in warp order.  K may also be cut into S chunks over CTAs (partials of 4 KiB,
+// added in chunk order by the last chunk to arrive).
+constexpr int SM_T = 32, SM_KP = 128, SM_STAGES = 2;
+constexpr int SM_LDA = SM_KP + 4;   // K-contiguous rows (A, and B^T): 132 floats
+constexpr int SM_LDB = SM_T + 4;    // B rows [k][36]
+constexpr int SM_A_FLOATS = SM_T * SM_LDA;                    // 4224
+constexpr int SM_B_FLOATS = SM_KP * SM_LDB > SM_T * SM_LDA ? SM_KP * SM_LDB : SM_T * SM_LDA;
+constexpr int SM_STAGE_FLOATS = SM_A_FLOATS + SM_B_FLOATS;
+constexpr int SM_SMEM_BYTES = SM_STAGES * SM_STAGE_FLOATS * 4;
+static_assert(SM_SMEM_BYTES >= 8 * SM_T * SM_T * 4, "reduction buffer fits in the ring");
+
+// Copies rows [r0, r0 + 32) x K columns [k0, k0 + 128) of a K-contiguous matrix into a
+// [32][SM_LDA] tile (zero outside [0, rows) x [0, K)).
+template <bool VEC>
+__device__ __forceinline__ void small_load_kmajor(float* dst, const float* src, int64_t ld,
+                                                  int64_t r0, int64_t rows, int64_t k0, int64_t K,
+                                                  int tid) {
+  if (VEC) {
+#pragma unroll
+    for (int h = 0; h < (SM_T * SM_KP / 4) / NT; ++h) {
+      const int q = tid + h * NT;
+      const int r = q / (SM_KP / 4), c4 = q % (SM_KP / 4);
+      const int64_t gr = r0 + r, gk = k0 + c4 * 4;
+      const int bytes = gr < rows ? clamp_bytes(K - gk) : 0;
+      cp_async_16(smem_u32(dst + r * SM_LDA + c4 * 4), bytes ? src + gr * ld + gk : src, bytes);
+    }
+  } else {
+#pragma unroll 4
+    for (int h = 0; h < (SM_T * SM_KP) / NT; ++h) {
+      const int e = tid + h * NT;
+      const int r = e / SM_KP, k = e % SM_KP;
+      const int64_t gr = r0 + r, gk = k0 + k;
+      const bool ok = gr < rows && gk < K;
+      cp_async_4(smem_u32(dst + r * SM_LDA + k), ok ? src + gr * ld + gk : src, ok ? 4 : 0);
+    }
+  }
+}
+
+// Copies K rows [k0, k0 + 128) x columns [n0, n0 + 32) of an N-contiguous matrix into a
+// [128][SM_LDB] tile (zero outside [0, K) x [0, N)).
+template <bool VEC>
+__device__ __forceinline__ void small_load_nmajor(float* dst, const float* src, int64_t ld,
+                                                  int64_t k0, int64_t K, int64_t n0, int64_t N,
+                                                  int tid) {
+  if (VEC) {
+#pragma unroll
+    for (int h = 0; h < (SM_KP * SM_T / 4) / NT; ++h) {
+      const int q = tid + h * NT;
+      const int r = q / (SM_T / 4), c4 = q % (SM_T / 4);
+      const int64_t gk = k0 + r, gn = n0 + c4 * 4;
+      const int bytes = gk < K ? clamp_bytes(N - gn) : 0;
+      cp_async_16(smem_u32(dst + r * SM_LDB + c4 * 4), bytes ? src + gk * ld + gn : src, bytes);
+    }
+  } else {
+#pragma unroll 4
+    for (int h = 0; h < (SM_KP * SM_T) / NT; ++h) {
+      const int e = tid + h * NT;
+      const int r = e / SM_T, n = e % SM_T;
+      const int64_t gk = k0 + r, gn = n0 + n;
+      const bool ok = gk < K && gn < N;
+      cp_async_4(smem_u32(dst + r * SM_LDB + n), ok ? src + gk * ld + gn : src, ok ? 4 : 0);
+    }
+  }
+}
+
+// Grid: tiles32 * S CTAs; CTA j computes K chunk j % S (of S equal chunks, in 128-wide
+// pieces) of 32 x 32 tile j / S.  Lane l of warp w holds rows (l >> 2) + 8 r (r < 4) and
+// columns 8 (l & 3) + c (c < 8) for the K-steps [16 w, 16 w + 16) of every piece.
+template <bool TRANS_B, bool VEC>
+__global__ void __launch_bounds__(NT) sgemm_small_kernel(const SimtParams p) {
+  extern __shared__ __align__(16) float sm[];
+  __shared__ uint32_t s_is_last;
+  pdl_trigger();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = p.sk_splits;
+  const int64_t tile = blockIdx.x / S;
+  const int chunk = static_cast<int>(blockIdx.x % S);
+  const int64_t tiles_mn = p.tiles_m * p.tiles_n;
+  const int64_t b = tile / tiles_mn;
+  const int64_t t_in = tile - b * tiles_mn;
+  const int64_t m0 = (t_in / p.tiles_n) * SM_T, n0 = (t_in % p.tiles_n) * SM_T;
+  const float* A = p.A + b * p.strideA;
+  const float* B = p.B + b * p.strideB;
+  const int64_t KP_total = (p.K + SM_KP - 1) / SM_KP;
+  const int64_t pbeg = static_cast<int64_t>(chunk) * KP_total / S;
+  const int64_t pend = static_cast<int64_t>(chunk + 1) * KP_total / S;
+  const int npieces = static_cast<int>(pend - pbeg);
+
+  // The first piece's operands go to L2 while the previous grid of the stream drains: a
+  // prefetch returns nothing to the program, and L2 is the device's point of coherence, so
+  // loads issued after the wait still see every write of the previous grid.  One 128-byte
+  // line per thread for each of A and B (32 rows x 512 bytes, and 128 K rows x 128 bytes or
+  // 32 rows x 512 bytes for B^T).
+  if (npieces > 0) {
+    const int64_t k0 = pbeg * SM_KP;
+    const int r = tid >> 3, seg = (tid & 7) * 32;  // 32 rows x 8 lines of 32 floats
+    if (m0 + r < p.M && k0 + seg < p.K) prefetch_l2(A + (m0 + r) * p.lda + k0 + seg);
+    if (TRANS_B) {
+      if (n0 + r < p.N && k0 + seg < p.K) prefetch_l2(B + (n0 + r) * p.ldb + k0 + seg);
+    } else {
+      const int kr = tid >> 1, cs = (tid & 1) * 16;  // 128 K rows x 2 half-lines
+      if (k0 + kr < p.K && n0 + cs < p.N) prefetch_l2(B + (k0 + kr) * p.ldb + n0 + cs);
+    }
+  }
+  pdl_wait();
+
+  auto load_piece = [&](int piece, int stage) {
+    float* as = sm + stage * SM_STAGE_FLOATS;
+    float* bs = as + SM_A_FLOATS;
+    const int64_t k0 = (pbeg + piece) * SM_KP;
+    small_load_kmajor<VEC>(as, A, p.lda, m0, p.M, k0, p.K, tid);
+    if (TRANS_B)
+      small_load_kmajor<VEC>(bs, B, p.ldb, n0, p.N, k0, p.K, tid);
+    else
+      small_load_nmajor<VEC>(bs, B, p.ldb, k0, p.K, n0, p.N, tid);
+  };
+
+  const int lr = lane >> 2, lc = lane & 3;
+  float acc[4][8];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < 8; ++c) acc[r][c] = 0.f;
+
+  if (npieces > 0) load_piece(0, 0);
+  cp_async_commit();
+  for (int pc = 0; pc < npieces; ++pc) {
+    if (pc + 1 < npieces) load_piece(pc + 1, (pc + 1) & 1);
+    cp_async_commit();
+    cp_async_wait<1>();
+    __syncthreads();
+    const float* as = sm + (pc & 1) * SM_STAGE_FLOATS;
+    const float* bs = as + SM_A_FLOATS;
+#pragma unroll
+    for (int kg = 0; kg < 4; ++kg) {
+      const int kk = warp * 16 + kg * 4;
+      float4 a[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) a[r] = *reinterpret_cast<const float4*>(as + (lr + 8 * r) * SM_LDA + kk);
+      if (TRANS_B) {
+        float4 bt[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          bt[c] = *reinterpret_cast<const float4*>(bs + (lc * 8 + c) * SM_LDA + kk);
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4)
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int c = 0; c < 8; c += 2)
+              ffma2(acc[r][c], acc[r][c + 1], f4get(a[r], k4), f4get(bt[c], k4), f4get(bt[c + 1], k4));
+      } else {
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const float4 b0 = *reinterpret_cast<const float4*>(bs + (kk + k4) * SM_LDB + lc * 8);
+          const float4 b1 = *reinterpret_cast<const float4*>(bs + (kk + k4) * SM_LDB + lc * 8 + 4);
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const float av = f4get(a[r], k4);
+            ffma2(acc[r][0], acc[r][1], av, b0.x, b0.y);
+            ffma2(acc[r][2], acc[r][3], av, b0.z, b0.w);
+            ffma2(acc[r][4], acc[r][5], av, b1.x, b1.y);
+            ffma2(acc[r][6], acc[r][7], av, b1.z, b1.w);
+          }
+        }
+      }
+    }
+    __syncthreads();  // the stage is refilled by the next iteration's copies
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+
+  // The 8 warps' partial tiles, added in warp order; thread t then owns outputs 4t..4t+3
+  // (row 4t / 32, columns 4t % 32 ..).
+  float* red = sm;
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < 8; c += 4)
+      *reinterpret_cast<float4*>(red + warp * SM_T * SM_T + (lr + 8 * r) * SM_T + lc * 8 + c) =
+          make_float4(acc[r][c], acc[r][c + 1], acc[r][c + 2], acc[r][c + 3]);
+  __syncthreads();
+  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const float4 x = *reinterpret_cast<const float4*>(red + w * SM_T * SM_T + tid * 4);
+    v.x += x.x; v.y += x.y; v.z += x.z; v.w += x.w;
+  }
+  if (S > 1) {
+    float4* mine = reinterpret_cast<float4*>(p.ws) + (tile * S + chunk) * (SM_T * SM_T / 4) + tid;
+    __stcg(mine, v);
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t prev;
+      asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(prev) : "l"(&p.counters[tile]) : "memory");
+      const bool last = prev + 1u == static_cast<uint32_t>(S);
+      if (last) p.counters[tile] = 0u;  // ready for the next call
+      s_is_last = last ? 1u : 0u;
+    }
+    __syncthreads();
+    if (!s_is_last) return;
+    v = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int cc = 0; cc < S; ++cc) {
+      const float4 x = __ldcg(reinterpret_cast<const float4*>(p.ws) + (tile * S + cc) * (SM_T * SM_T / 4) + tid);
+      v.x += x.x; v.y += x.y; v.z += x.z; v.w += x.w;
+    }
+  }
+  const int64_t gm = m0 + (tid * 4) / SM_T, gn = n0 + (tid * 4) % SM_T;
+  if (gm >= p.M) return;
+  float* crow = p.C + b * p.strideC + gm * p.ldc;
+  const float alpha = p.alpha, beta = p.beta;
+  const float vv[4] = {v.x, v.y, v.z, v.w};
+  if (VEC && gn + 3 < p.N) {
+    float4* dst = reinterpret_cast<float4*>(crow + gn);
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (beta != 0.f) o = *dst;
+    *dst = make_float4(fmaf(alpha, vv[0], beta * o.x), fmaf(alpha, vv[1], beta * o.y),
+                       fmaf(alpha, vv[2], beta * o.z), fmaf(alpha, vv[3], beta * o.w));
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (gn + j < p.N)
+        crow[gn + j] = beta != 0.f ? fmaf(alpha, vv[j], beta * crow[gn + j]) : alpha * vv[j];
+  }
+}
+
+template <bool TRANS_B, bool VEC>
+cudaError_t launch_small_variant(const SimtParams& p, cudaStream_t s) {
+  auto kern = sgemm_small_kernel<TRANS_B, VEC>;
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t e = ensure_smem_attr(kern, SM_SMEM_BYTES, attr_done);
+  if (e != cudaSuccess) return e;
+  const int64_t grid = p.batch * p.tiles_m * p.tiles_n * p.sk_splits;
+  return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(NT), SM_SMEM_BYTES, s, p);
+}
+
 template <bool TRANS_B>
 int ctas_per_sm_tma() {
   static std::atomic<int> cached{0};
@@ -799,6 +1045,11 @@ int ctas_per_sm_tma() {
 int sgemm_simt_ctas_per_sm(bool trans_b, bool vec) {
   if (vec) return trans_b ? ctas_per_sm_tma<true>() : ctas_per_sm_tma<false>();
   return trans_b ? ctas_per_sm_variant<true, false>() : ctas_per_sm_variant<false, false>();
+}
+
+cudaError_t launch_sgemm_simt_small(const SimtParams& p, bool trans_b, bool vec, cudaStream_t s) {
+  if (trans_b) return vec ? launch_small_variant<true, true>(p, s) : launch_small_variant<true, false>(p, s);
+  return vec ? launch_small_variant<false, true>(p, s) : launch_small_variant<false, false>(p, s);
 }
 
 cudaError_t launch_sgemm_simt(const SimtParams& p, bool trans_b, bool vec, cudaStream_t s) {

@@ -172,14 +172,17 @@ def test_quant_traffic_model_reproduces_example_5_8():
     assert sep / MiB - w_out == g["input_separate_mib"] and fus / MiB - w_out == g["input_fused_mib"]
 
 
-def test_fp32_plan_splits_k_when_tiles_are_few():
-    # 256^3: 4 tiles for 2 x 152 resident CTAs -- K is cut into 8 chunks of 32 (one K tile);
-    # with a quarter of the slots or more filled, chunks keep at least 256 of K.
+def test_fp32_plan_small_and_streamk():
+    # 256^3: 4 tiles of 128 x 128 for 2 x 152 resident CTAs -- the small-tile kernel, 64
+    # tiles of 32 x 32, K = 256 in one chunk (two staged pieces of 128).
     p = dg.dg_plan_gemm(0, 256, 256, 256, num_sms=152)
-    assert (p["tiles"], p["splits"], p["tail_tiles"], p["grid"]) == (4, 8, 4, 32)
+    assert (p["tile_m"], p["tiles"], p["splits"], p["grid"], p["kblocks"]) == (32, 64, 1, 64, 2)
+    assert p["workspace_bytes"] == 0
+    # 200 x 136 x 1000: 35 small tiles, K cut in 2 chunks of at least 4 pieces.
     p = dg.dg_plan_gemm(0, 200, 136, 1000, num_sms=152)
-    assert p["splits"] == 16 and p["grid"] == 64                      # at most 16 chunks
-    assert dg.dg_plan_gemm(0, 7, 9, 5, num_sms=152)["splits"] == 1      # one K tile: no split
+    assert (p["tile_m"], p["tiles"], p["splits"], p["grid"]) == (32, 35, 2, 70)
+    assert p["workspace_bytes"] == 35 * 2 * 32 * 32 * 4 + 35 * 4
+    assert dg.dg_plan_gemm(0, 7, 9, 5, num_sms=152)["splits"] == 1      # one K piece: no split
     # 1000 x 3000 x 777: 192 tiles x 25 K tiles for 304 resident CTAs -- stream-K, 15.8 K
     # tiles per CTA (splits 0); 4096^3 keeps whole-tile waves and a split tail.
     p = dg.dg_plan_gemm(0, 1000, 3000, 777, num_sms=152)
@@ -194,8 +197,8 @@ def _cdiv(a, b):
 
 def test_plan_properties_on_random_shapes():
     # Invariants of the planner over seeded random shapes, recomputed here from the tile
-    # sizes: tile counts, grids, the FP32 tail split, the decode stream-K grid, CTA pairs and
-    # their widths, stream-K tails and workspace sizes.
+    # sizes: tile counts, grids, the FP32 small-tile, tail-split and stream-K schedules, the
+    # decode stream-K grid, CTA pairs and their widths, stream-K tails and workspace sizes.
     rng = np.random.default_rng(20261202)
     sms = 152
     for _ in range(1500):
@@ -203,66 +206,82 @@ def test_plan_properties_on_random_shapes():
         N = int(rng.choice([rng.integers(1, 300), rng.integers(1, 20000)]))
         K = int(rng.choice([rng.integers(1, 200), rng.integers(1, 9000)]))
         batch = int(rng.choice([1, 1, 1, rng.integers(2, 70)]))
-        # FP32
-        p = dg.dg_plan_gemm(0, M, N, K, batch=batch, num_sms=sms)
-        assert p["kernel"] == dg.DG_KERNEL_SIMT_F32
-        tiles = batch * _cdiv(M, 128) * _cdiv(N, 128)
-        assert p["tiles"] == tiles and p["kblocks"] == _cdiv(K, p["tile_k"])
-        G, KT = 2 * sms, p["kblocks"]
-        streamk = (tiles < G and tiles * KT >= 4 * G and 4 * tiles > G
-                   and _cdiv(tiles * KT, G) <= 7 * KT)
-        if streamk:
-            # Stream-K: tiles for between a quarter and one wave, at least 4 K tiles per
-            # resident CTA, ranges of at most 7 tiles' K (so at most 8 segments); one wave of
-            # CTAs over all tiles.
-            assert p["splits"] == 0 and p["grid"] == G and p["tail_tiles"] == tiles
-            assert p["workspace_bytes"] == 2 * G * 16 * 256 * 16 + tiles * 4
+        _check_f32_plan(M, N, K, batch, sms)
+        _check_bf16_fp8_plans(M, N, K, batch, sms)
+
+
+def _check_f32_plan(M, N, K, batch, sms):
+    p = dg.dg_plan_gemm(0, M, N, K, batch=batch, num_sms=sms)
+    assert p["kernel"] == dg.DG_KERNEL_SIMT_F32
+    tiles = batch * _cdiv(M, 128) * _cdiv(N, 128)
+    G = 2 * sms
+    if 4 * tiles <= G:
+        # Small-tile kernel: 32 x 32 tiles, K in 128-wide pieces, chunks of at least 4
+        # pieces, at most 16 chunks, at most as many chunk CTAs as are resident.
+        t32 = batch * _cdiv(M, 32) * _cdiv(N, 32)
+        pieces = _cdiv(K, 128)
+        S = max(1, min(G // t32, _cdiv(pieces, 4), 16))
+        assert (p["tile_m"], p["tile_n"], p["tile_k"]) == (32, 32, 128)
+        assert (p["tiles"], p["kblocks"], p["splits"], p["grid"]) == (t32, pieces, S, t32 * S)
+        assert p["workspace_bytes"] == (t32 * S * 4096 + t32 * 4 if S > 1 else 0)
+        return
+    KT = _cdiv(K, p["tile_k"])
+    assert p["tiles"] == tiles and p["kblocks"] == KT
+    if tiles < G and tiles * KT >= 4 * G and _cdiv(tiles * KT, G) <= 7 * KT:
+        # Stream-K: tiles for between a quarter and one wave, at least 4 K tiles per
+        # resident CTA, ranges of at most 7 tiles' K (so at most 8 segments); one wave of
+        # CTAs over all tiles.
+        assert p["splits"] == 0 and p["grid"] == G and p["tail_tiles"] == tiles
+        assert p["workspace_bytes"] == 2 * G * 16 * 256 * 16 + tiles * 4
+        return
+    assert p["splits"] >= 1 and 0 <= p["tail_tiles"] <= tiles
+    assert p["grid"] == tiles - p["tail_tiles"] + p["tail_tiles"] * p["splits"]
+    if p["splits"] > 1:
+        # Chunks of at least 256 of K (8 K tiles), at most 3 waves of chunk CTAs on the
+        # 2 x 152 resident slots.
+        assert p["tail_tiles"] > 0 and p["tail_tiles"] * p["splits"] <= 3 * G
+        assert p["splits"] <= p["kblocks"] // 8
+        assert p["workspace_bytes"] > 0
+    else:
+        assert p["tail_tiles"] == 0 and p["workspace_bytes"] == 0
+
+
+def _check_bf16_fp8_plans(M, N, K, batch, sms):
+    # BF16 and FP8 (FP8 is planned for one problem only)
+    for dtype in (1, 2) if batch == 1 else (1,):
+        q = dg.dg_plan_gemm(dtype, M, N, K, batch=batch, num_sms=sms)
+        if dtype == 1 and batch == 1 and M <= 32:
+            assert q["kernel"] == dg.DG_KERNEL_THIN_BF16
+            assert q["ntok"] == (16 if M <= 16 else 32)
+            units = _cdiv(N, 128) * _cdiv(K, 64)
+            assert q["tiles"] == _cdiv(N, 128) and q["grid"] == min(units, sms)
+            continue
+        tk = 128 if dtype == 2 else 64
+        assert q["tile_k"] == tk and q["kblocks"] == _cdiv(K, tk)
+        bn = q["tile_n"]
+        if q["kernel"] == dg.DG_KERNEL_TC2_BF16:
+            assert batch == 1 and _cdiv(M, 128) >= 2 and q["tile_m"] == 256
+            tm2 = _cdiv(_cdiv(M, 128), 2)
+            assert q["tiles"] == tm2 * _cdiv(N, bn)
+            assert q["grid"] % 2 == 0 and q["grid"] // 2 == min(q["tiles"], sms // 2)
+            if dtype == 2:
+                w256 = _cdiv(tm2 * _cdiv(N, 256), sms // 2) * 256
+                w224 = _cdiv(tm2 * _cdiv(N, 224), sms // 2) * 224
+                assert bn == (224 if w224 < w256 else 256)
+            else:
+                assert bn == 256
+            G = q["grid"] // 2
         else:
-            assert p["splits"] >= 1 and 0 <= p["tail_tiles"] <= tiles
-            assert p["grid"] == tiles - p["tail_tiles"] + p["tail_tiles"] * p["splits"]
-            if p["splits"] > 1:
-                # Chunks of at least 256 of K (8 K tiles), at most 3 waves of chunk CTAs on the
-                # 2 x 152 resident slots; when the tiles fill under a quarter of the slots,
-                # chunks go down to one K tile, at most 16.
-                few = 4 * tiles <= G
-                assert p["tail_tiles"] > 0 and p["tail_tiles"] * p["splits"] <= 3 * G
-                assert p["splits"] <= (min(16, p["kblocks"]) if few else p["kblocks"] // 8)
-                assert p["workspace_bytes"] > 0
-            else:
-                assert p["tail_tiles"] == 0 and p["workspace_bytes"] == 0
-        # BF16 and FP8 (FP8 is planned for one problem only)
-        for dtype in (1, 2) if batch == 1 else (1,):
-            q = dg.dg_plan_gemm(dtype, M, N, K, batch=batch, num_sms=sms)
-            if dtype == 1 and batch == 1 and M <= 32:
-                assert q["kernel"] == dg.DG_KERNEL_THIN_BF16
-                assert q["ntok"] == (16 if M <= 16 else 32)
-                units = _cdiv(N, 128) * _cdiv(K, 64)
-                assert q["tiles"] == _cdiv(N, 128) and q["grid"] == min(units, sms)
-                continue
-            tk = 128 if dtype == 2 else 64
-            assert q["tile_k"] == tk and q["kblocks"] == _cdiv(K, tk)
-            bn = q["tile_n"]
-            if q["kernel"] == dg.DG_KERNEL_TC2_BF16:
-                assert batch == 1 and _cdiv(M, 128) >= 2 and q["tile_m"] == 256
-                tm2 = _cdiv(_cdiv(M, 128), 2)
-                assert q["tiles"] == tm2 * _cdiv(N, bn)
-                assert q["grid"] % 2 == 0 and q["grid"] // 2 == min(q["tiles"], sms // 2)
-                if dtype == 2:
-                    w256 = _cdiv(tm2 * _cdiv(N, 256), sms // 2) * 256
-                    w224 = _cdiv(tm2 * _cdiv(N, 224), sms // 2) * 224
-                    assert bn == (224 if w224 < w256 else 256)
-                else:
-                    assert bn == 256
-                G = q["grid"] // 2
-            else:
-                assert q["kernel"] == dg.DG_KERNEL_TC_BF16 and q["tile_m"] == 128
-                assert q["tiles"] == batch * _cdiv(M, 128) * _cdiv(N, bn)
-                assert q["grid"] == min(q["tiles"], sms)
-                G = q["grid"]
-            if q["tail_tiles"]:
-                assert q["tiles"] > G and q["tail_tiles"] == q["tiles"] % G
-                assert q["kblocks"] >= 16 and (q["tiles"] // G) * q["kblocks"] >= 96
-                assert 1 <= q["splits"] <= min(4 * q["tail_tiles"], G)
-                assert q["workspace_bytes"] > 0
-            else:
-                assert q["splits"] == 1
+            assert q["kernel"] == dg.DG_KERNEL_TC_BF16 and q["tile_m"] == 128
+            assert q["tiles"] == batch * _cdiv(M, 128) * _cdiv(N, bn)
+            assert q["grid"] == min(q["tiles"], sms)
+            G = q["grid"]
+        if q["tail_tiles"]:
+            assert q["tiles"] > G and q["tail_tiles"] == q["tiles"] % G
+            assert q["kblocks"] >= 16 and (q["tiles"] // G) * q["kblocks"] >= 96
+            assert 1 <= q["splits"] <= min(4 * q["tail_tiles"], G)
+            assert q["workspace_bytes"] > 0
+        else:
+            assert q["splits"] == 1
+
+
