@@ -5,12 +5,17 @@
 //
 // One CTA computes one 128-row query tile of one head and streams the head's keys and values
 // through shared memory in blocks of 128 rows:
-//   warp 0     TMA producer: the Q tile once, then K_j and V_j into two 2-slot rings;
+//   warp 0     TMA producer of Q (once) and K_j into a 3-slot ring;
 //   warp 1     allocates TMEM and issues the MMAs: S_j = Q K_j^T into one of two TMEM score
 //              buffers, O += P_j V_j into the TMEM output accumulator;
 //   warps 2-5  softmax and epilogue, one query row per thread (the TMEM lane of that row):
 //              the running maximum m and sum l in registers, p = 2^(s * scale * log2 e - m)
-//              rounded to BF16 into shared memory as the A operand of the P V product.
+//              rounded to BF16 into TMEM as the A operand of the P V product;
+//   warp 6     TMA producer of V_j into a 3-slot ring.
+// K and V have producers of their own so that a K load waits only for the S product that
+// frees its slot: with one producer issuing K_j, V_j, K_j+1, ... in order, the next K load
+// queued behind a V load whose slot frees only after the softmax and P V of an earlier block,
+// and the S products (and with them the softmax) waited for K.
 // The recurrence is the pages' (m' = max(m, max s), r = e^(m - m'), l' = r l + sum p,
 // u' = r u + sum p v), with one change that leaves the result unchanged: the reference
 // point m is moved only when the block maximum exceeds it by more than 2^8 in the weights,
@@ -42,7 +47,9 @@ constexpr int kBQ = 128, kBKV = 128, kHD = 128;
 constexpr int kSoftWarps = 4;
 constexpr int kHalves = kSoftWarps / 4;       // key / column parts per row
 constexpr int kKeysPer = kBKV / kHalves;      // keys of a block per thread
-constexpr int kThreads = 64 + 32 * kSoftWarps;
+constexpr int kVWarp = 2 + kSoftWarps;          // the V producer
+constexpr int kThreads = 64 + 32 * kSoftWarps + 32;
+constexpr int kKStages = 3, kVStages = 3;        // K and V ring slots (32 KiB each)
 constexpr uint32_t kTile = 128 * kHD * 2;  // 128 rows x 128 BF16: two 64-column boxes, 32 KiB
 constexpr uint32_t kHalf = kTile / 2;      // one 128-row x 64-column box (128-byte rows)
 constexpr uint32_t kTmemCols = 512;        // S[0] at 0, S[1] at 128, O at 256, P[0..1] at 384
@@ -50,11 +57,11 @@ constexpr uint32_t kOCol = 256;
 constexpr uint32_t kPCol = 384;            // P in TMEM: 64 columns (128 BF16 pairs) per buffer
 constexpr float kMoveLog2 = 8.f;           // move m when the block raises it by > 8 (log2)
 
-// Shared memory: Q | K[2] | V[2] (32 KiB each, 1024-byte aligned) | control | l exchange.
+// Shared memory: Q | K[3] | V[3] (32 KiB each, 1024-byte aligned) | control | l exchange.
 struct AttnCtl {
   uint64_t qfull;
-  uint64_t kfull[2], kempty[2], vfull[2], vempty[2];
-  uint64_t sfull[2], pfull[2], odone[2];
+  uint64_t kfull[kKStages], kempty[kKStages], vfull[kVStages], vempty[kVStages];
+  uint64_t sfull[2], sfree[2], pfull[2], odone[2];
   uint64_t drain;
   uint32_t tmem_base;
   uint32_t abort;
@@ -62,8 +69,10 @@ struct AttnCtl {
   uint32_t epi_ok;   // the softmax warps' common verdict before the epilogue
 };
 static_assert(sizeof(AttnCtl) <= 256, "control block");
-// Q | K[2] | V[2] (32 KiB each) | control (256 B) | the halves' l exchange (1 KiB).
-constexpr uint32_t kSmemBytes = 1024 + 5 * kTile + 256 + 1024;
+// Q | K[3] | V[3] (32 KiB each) | control (256 B) | the halves' l exchange (1 KiB).
+constexpr uint32_t kRingTiles = 1 + kKStages + kVStages;
+constexpr uint32_t kSmemBytes = 1024 + kRingTiles * kTile + 256 + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -74,6 +83,71 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Three-input maximum (one instruction on sm_100 and later).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Two FP32 lanes in one 64-bit register (low lane first) and the packed FP32 operations on
+// them: each lane is rounded exactly as the scalar instruction would round it.
+__device__ __forceinline__ uint64_t f2_pack(uint32_t lo, uint32_t hi) {
+  return static_cast<uint64_t>(hi) << 32 | lo;
+}
+__device__ __forceinline__ float f2_lo(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float f2_hi(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// The maximum of a row's 128 scores of one block (TMEM words, FP32): 64 three-input maxima
+// over 8 independent chains.
+__device__ __forceinline__ float block_row_max(const uint32_t (&sv)[4][32]) {
+  float mx8[8];
+#pragma unroll
+  for (int t = 0; t < 8; ++t) mx8[t] = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+#pragma unroll
+    for (int k = 0; k < 32; k += 2)
+      mx8[(k >> 1) & 7] = max3f(mx8[(k >> 1) & 7], __uint_as_float(sv[c][k]), __uint_as_float(sv[c][k + 1]));
+  return max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+}
+
+// The weights p = 2^(s * cl + nb) of keys 32 c0 .. 32 (c0 + NC) - 1 of a row, two keys per
+// packed FMA, rounded to BF16 pairs into pw (32-key chunk c in pw[c / 2], words 16 (c % 2) ..);
+// returns their sum, kept in eight FP32 lanes (four packed partial sums) and added in a fixed
+// order, so every kernel that calls this gets the same bits for the same scores.
+template <int NC>
+__device__ __forceinline__ float block_weights(const uint32_t (&sv)[4][32], int c0, float cl, float nb,
+                                               uint32_t (&pw)[NC / 2][32]) {
+  const uint64_t cl2 = f2_pack(__float_as_uint(cl), __float_as_uint(cl));
+  const uint64_t nb2 = f2_pack(__float_as_uint(nb), __float_as_uint(nb));
+  uint64_t ls4[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) ls4[t] = 0;
+#pragma unroll
+  for (int c = 0; c < NC; ++c)
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const uint64_t x = f2_fma(f2_pack(sv[c0 + c][2 * k], sv[c0 + c][2 * k + 1]), cl2, nb2);
+      const float p0 = ex2(f2_lo(x));
+      const float p1 = ex2(f2_hi(x));
+      ls4[k & 3] = f2_add(ls4[k & 3], f2_pack(__float_as_uint(p0), __float_as_uint(p1)));
+      pw[c >> 1][(c & 1) * 16 + k] = pack2(p0, p1);
+    }
+  return ((f2_lo(ls4[0]) + f2_hi(ls4[0])) + (f2_lo(ls4[1]) + f2_hi(ls4[1]))) +
+         ((f2_lo(ls4[2]) + f2_hi(ls4[2])) + (f2_lo(ls4[3]) + f2_hi(ls4[3])));
 }
 
 // 32 lanes x 32 consecutive 32-bit TMEM columns from registers (thread i -> lane base+i).
@@ -142,9 +216,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle atoms need 1024-byte alignment
-  const uint32_t sQ = base, sK = base + kTile, sV = base + 3 * kTile;
-  AttnCtl* ctl = reinterpret_cast<AttnCtl*>(smem_raw + (base - raw) + 5 * kTile);
-  float* xl = reinterpret_cast<float*>(smem_raw + (base - raw) + 5 * kTile + 256);  // [2][128]
+  const uint32_t sQ = base, sK = base + kTile, sV = base + (1 + kKStages) * kTile;
+  AttnCtl* ctl = reinterpret_cast<AttnCtl*>(smem_raw + (base - raw) + kRingTiles * kTile);
+  float* xl = reinterpret_cast<float*>(smem_raw + (base - raw) + kRingTiles * kTile + 256);  // [2][128]
   volatile uint32_t* abort = &ctl->abort;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -183,13 +257,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&ctl->qfull), 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(smem_u32(&ctl->kfull[s]), 1);
       mbar_init(smem_u32(&ctl->kempty[s]), 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
       mbar_init(smem_u32(&ctl->vfull[s]), 1);
       mbar_init(smem_u32(&ctl->vempty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&ctl->sfull[s]), 1);
-      mbar_init(smem_u32(&ctl->pfull[s]), kSoftWarps);  // one arrival per softmax warp
+      mbar_init(smem_u32(&ctl->sfree[s]), kSoftWarps);  // one arrival per softmax warp
+      mbar_init(smem_u32(&ctl->pfull[s]), kSoftWarps);
       mbar_init(smem_u32(&ctl->odone[s]), 1);
     }
     mbar_init(smem_u32(&ctl->drain), 1);
@@ -213,41 +292,42 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait();
 
   const int32_t zb = static_cast<int32_t>(b);
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+  if (warp == 0 || warp == kVWarp) {
+    // ------------------------------------------------------------ TMA producers (Q, K | V)
     if (lane == 0) {
+      const bool isk = warp == 0;
+      const int stages = isk ? kKStages : kVStages;
+      const uint32_t ring = isk ? sK : sV;
+      const CUtensorMap* map = isk ? &tmK : &tmV;
+      uint64_t* full = isk ? ctl->kfull : ctl->vfull;
+      uint64_t* empty = isk ? ctl->kempty : ctl->vempty;
       const uint32_t qf = smem_u32(&ctl->qfull);
-      mbar_arrive_expect_tx(qf, kTile);
-      load_box(sQ, &tmQ, qf, 0, static_cast<int32_t>(q0), zb, rank3);
-      load_box(sQ + kHalf, &tmQ, qf, 64, static_cast<int32_t>(q0), zb, rank3);
-      int64_t issued = 0;  // blocks whose K and V loads were both issued
-      bool k_only = false; // the last block's K load was issued but not its V load
+      if (isk) {
+        mbar_arrive_expect_tx(qf, kTile);
+        load_box(sQ, &tmQ, qf, 0, static_cast<int32_t>(q0), zb, rank3);
+        load_box(sQ + kHalf, &tmQ, qf, 64, static_cast<int32_t>(q0), zb, rank3);
+      }
+      int64_t issued = 0;
+      uint32_t s = 0, ph = 0;  // ring slot and its phase parity for block j
       for (int64_t j = 0; j < nkv; ++j) {
-        const uint32_t s = j & 1, ph = (j >> 1) & 1;
+        if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u, abort, p.status, kDevTimeoutProducer)) break;
+        const uint32_t f = smem_u32(&full[s]);
         const int32_t y = static_cast<int32_t>((j0 + j) * kBKV);
-        if (!mbar_wait(smem_u32(&ctl->kempty[s]), ph ^ 1u, abort, p.status, kDevTimeoutProducer)) break;
-        const uint32_t kf = smem_u32(&ctl->kfull[s]);
-        mbar_arrive_expect_tx(kf, kTile);
-        load_box(sK + s * kTile, &tmK, kf, 0, y, zb, rank3);
-        load_box(sK + s * kTile + kHalf, &tmK, kf, 64, y, zb, rank3);
-        k_only = true;
-        if (!mbar_wait(smem_u32(&ctl->vempty[s]), ph ^ 1u, abort, p.status, kDevTimeoutProducer)) break;
-        const uint32_t vf = smem_u32(&ctl->vfull[s]);
-        mbar_arrive_expect_tx(vf, kTile);
-        load_box(sV + s * kTile, &tmV, vf, 0, y, zb, rank3);
-        load_box(sV + s * kTile + kHalf, &tmV, vf, 64, y, zb, rank3);
-        k_only = false;
+        mbar_arrive_expect_tx(f, kTile);
+        load_box(ring + s * kTile, map, f, 0, y, zb, rank3);
+        load_box(ring + s * kTile + kHalf, map, f, 64, y, zb, rank3);
         ++issued;
+        if (++s == static_cast<uint32_t>(stages)) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
       if (*abort) {
         // No copy may still be landing in shared memory when the CTA exits: wait for the
         // last loads issued into each slot (earlier ones were consumed before the reuse).
-        drain_wait(qf, 0, p.status);
-        const int64_t kl = issued + (k_only ? 1 : 0);
-        for (int64_t j = kl > 2 ? kl - 2 : 0; j < kl; ++j)
-          drain_wait(smem_u32(&ctl->kfull[j & 1]), (j >> 1) & 1, p.status);
-        for (int64_t j = issued > 2 ? issued - 2 : 0; j < issued; ++j)
-          drain_wait(smem_u32(&ctl->vfull[j & 1]), (j >> 1) & 1, p.status);
+        if (isk) drain_wait(qf, 0, p.status);
+        for (int64_t j = issued > stages ? issued - stages : 0; j < issued; ++j)
+          drain_wait(smem_u32(&full[j % stages]), static_cast<uint32_t>((j / stages) & 1), p.status);
       }
     }
   } else if (warp == 1) {
@@ -258,51 +338,81 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idO = idesc_bf16_f32(128, 128, false, true);
       bool ok = mbar_wait(smem_u32(&ctl->qfull), 0, abort, p.status, kDevTimeoutMma);
+      // Operand descriptors of the ring bases, advanced per MMA by the start-address field
+      // alone (16-byte units; every offset stays inside the 256 KiB the field spans), so each
+      // MMA costs the issuing thread a few integer additions: the issuing thread shares its
+      // SM sub-partition with a softmax warp, and its instruction count per MMA showed in the
+      // tensor pipe's rate (1001 -> 1048 TFLOPS on 64 heads x 2048).
+      const uint64_t dQ = sdesc_sw128(sQ, 16, 1024), dK = sdesc_sw128(sK, 16, 1024);
+      const uint64_t dV = sdesc_sw128(sV, kHalf, 1024);
+      // S products are issued in block order: ks / kph track the K ring slot of the next one.
+      uint32_t ks = 0, kph = 0;
       auto issue_s = [&](int64_t j) -> bool {
-        const uint32_t s = j & 1, ph = (j >> 1) & 1;
-        if (!mbar_wait(smem_u32(&ctl->kfull[s]), ph, abort, p.status, kDevTimeoutMma)) return false;
+        const uint32_t sb = j & 1;  // score buffer
+        if (!mbar_wait(smem_u32(&ctl->kfull[ks]), kph, abort, p.status, kDevTimeoutMma)) return false;
         tc_fence_after();
-        const uint32_t kb = sK + s * kTile;
+        const uint64_t dKs = dK + ks * (kTile >> 4);
 #pragma unroll
         for (int k = 0; k < kHD / 16; ++k) {
           // 16 columns of d per MMA: 32 bytes inside a 128-byte swizzle row, the second
           // 64 columns in the second box.
-          const uint32_t off = (k >> 2) * kHalf + (k & 3) * 32;
-          umma_bf16(tmem + s * 128, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
-                    idS, k > 0 ? 1u : 0u);
+          const uint32_t off = ((k >> 2) * kHalf + (k & 3) * 32) >> 4;
+          umma_bf16(tmem + sb * 128, dQ + off, dKs + off, idS, k > 0 ? 1u : 0u);
         }
-        umma_commit(smem_u32(&ctl->kempty[s]));
-        umma_commit(smem_u32(&ctl->sfull[s]));
+        umma_commit(smem_u32(&ctl->kempty[ks]));
+        umma_commit(smem_u32(&ctl->sfull[sb]));
+        if (++ks == kKStages) {
+          ks = 0;
+          kph ^= 1u;
+        }
         return true;
       };
+      // Per block j: S_j+2 goes into score buffer j % 2 as soon as the softmax has read S_j
+      // into registers, so it runs while the softmax of block j exponentiates; P_j V_j follows
+      // once the weights are in TMEM.  (Issuing S_j+2 only after P_j V_j queued every score
+      // product behind the softmax of the block two earlier.)
       if (ok) ok = issue_s(0);
       if (ok && nkv > 1) ok = issue_s(1);
+      uint32_t vs = 0, vph = 0;  // V ring slot of block j
       for (int64_t j = 0; ok && j < nkv; ++j) {
         const uint32_t s = j & 1, ph = (j >> 1) & 1;
+        if (j + 2 < nkv) {
+          if (!mbar_wait(smem_u32(&ctl->sfree[s]), ph, abort, p.status, kDevTimeoutMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (!issue_s(j + 2)) {
+            ok = false;
+            break;
+          }
+        }
         if (!mbar_wait(smem_u32(&ctl->pfull[s]), ph, abort, p.status, kDevTimeoutMma) ||
-            !mbar_wait(smem_u32(&ctl->vfull[s]), ph, abort, p.status, kDevTimeoutMma)) {
+            !mbar_wait(smem_u32(&ctl->vfull[vs]), vph, abort, p.status, kDevTimeoutMma)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t vb = sV + s * kTile;
+        const uint64_t dVs = dV + vs * (kTile >> 4);
 #pragma unroll
         for (int k = 0; k < kBKV / 16; ++k) {
-          // P: 16 keys = 32 bytes in the swizzle row (second box for keys 64..127).
-          // V: 16 key rows = 2 KiB; its two 64-column halves of d are one box apart (LBO).
-          const uint64_t bdesc = sdesc_sw128(vb + k * 2048, kHalf, 1024);
-          // 16 keys of P = 8 packed columns of the TMEM P buffer.
-          umma_bf16_ts(tmem + kOCol, tmem + kPCol + s * 64 + k * 8, bdesc, idO, (j > 0 || k > 0) ? 1u : 0u);
+          // V: 16 key rows = 2 KiB per MMA; its two 64-column halves of d are one box apart
+          // (LBO).  A = P: 16 keys = 8 packed columns of the TMEM P buffer.
+          umma_bf16_ts(tmem + kOCol, tmem + kPCol + s * 64 + k * 8, dVs + k * (2048 >> 4), idO,
+                       (j > 0 || k > 0) ? 1u : 0u);
         }
-        umma_commit(smem_u32(&ctl->vempty[s]));
+        umma_commit(smem_u32(&ctl->vempty[vs]));
         umma_commit(smem_u32(&ctl->odone[s]));
-        if (j + 2 < nkv) ok = issue_s(j + 2);
+        if (++vs == kVStages) {
+          vs = 0;
+          vph ^= 1u;
+        }
       }
       // Every MMA finished before TMEM is released.
       umma_commit(smem_u32(&ctl->drain));
       drain_wait(smem_u32(&ctl->drain), 0, p.status);
     }
-  } else {
+  } else if (warp < kVWarp) {
     // ------------------------------------------------------------ softmax + epilogue
     // One query row per thread (the TMEM lane of warp w % 4's quadrant).  With 8 warps, warps
     // w and w + 4 split each block's keys and the row's columns of O in halves; both read the
@@ -329,8 +439,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tl + s * 128 + c * 32, sv[c]);
       tmem_ld_wait();
+      // S_j is in registers: its buffer may take S_j+2.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->sfree[s]));
       const int64_t kv0 = (j0 + j) * kBKV;
-      if (kv0 + kBKV > p.Lkv || (CAUSAL && j0 + j == qt)) {
+      const bool masked = kv0 + kBKV > p.Lkv || (CAUSAL && j0 + j == qt);
+      if (masked) {
         // Keys at or past `lim` are not visible to this row: weight 0.
         const int64_t lim = CAUSAL ? (qrow + 1 < p.Lkv ? qrow + 1 : p.Lkv) : p.Lkv;
         const int64_t nv = lim - kv0;
@@ -341,16 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 32; ++k)
             if (c * 32 + k >= nvis) sv[c][k] = 0xFF800000u;  // -inf
       }
-      float mx8[8];
-#pragma unroll
-      for (int t = 0; t < 8; ++t) mx8[t] = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int k = 0; k < 32; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], __uint_as_float(sv[c][k]));
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      const float m_blk = mx * cl;  // the block's maximum in log2 units (scale > 0)
+      const float m_blk = block_row_max(sv) * cl;  // the block's maximum in log2 units (scale > 0)
       float r = 1.f;
       if (m_blk > m_run + kMoveLog2) {
         r = ex2(m_run - m_blk);  // 0 on the first block (m_run = -inf)
@@ -363,21 +469,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
         break;
       }
-      float ls8[8];
-#pragma unroll
-      for (int t = 0; t < 8; ++t) ls8[t] = 0.f;
       uint32_t pw[kKeysPer / 64][32];  // this thread's weights as packed BF16 pairs
-#pragma unroll
-      for (int c = 0; c < kKeysPer / 32; ++c)
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const int cc = half * (kKeysPer / 32) + c;  // 32-key chunk of the block
-          const float p0 = ex2(fmaf(__uint_as_float(sv[cc][2 * k]), cl, nb));
-          const float p1 = ex2(fmaf(__uint_as_float(sv[cc][2 * k + 1]), cl, nb));
-          ls8[k & 7] += p0 + p1;
-          pw[c >> 1][(c & 1) * 16 + k] = pack2(p0, p1);
-        }
-      const float lsum = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
+      const float lsum = block_weights<kKeysPer / 32>(sv, half * (kKeysPer / 32), cl, nb, pw);
       l_run = l_run * r + lsum;
 #pragma unroll
       for (int c = 0; c < kKeysPer / 64; ++c)
@@ -533,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_store_2d(&tmO, sQ + kHalf, 64, static_cast<int32_t>(q0));
       }
       bulk_commit();
-      bulk_wait<0>();
+      bulk_wait_read<0>();  // the CTA may retire once the store has read shared memory
     }
   }
 
@@ -754,7 +847,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tl + c * 32, sv[c]);
       tmem_ld_wait();
       const int64_t kv0 = j * kBKV;
-      if (kv0 + kBKV > p.Lkv) {
+      const bool masked = kv0 + kBKV > p.Lkv;
+      if (masked) {
         const int64_t nv = p.Lkv - kv0;
         const int nvis = nv > kBKV ? kBKV : static_cast<int>(nv);
 #pragma unroll
@@ -763,16 +857,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           for (int k = 0; k < 32; ++k)
             if (c * 32 + k >= nvis) sv[c][k] = 0xFF800000u;
       }
-      float mx8[8];
-#pragma unroll
-      for (int t = 0; t < 8; ++t) mx8[t] = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int k = 0; k < 32; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], __uint_as_float(sv[c][k]));
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      const float m_blk = mx * cl;
+      const float m_blk = block_row_max(sv) * cl;
       float r = 1.f;
       if (m_blk > m_run + kMoveLog2) {
         r = ex2(m_run - m_blk);
@@ -780,20 +865,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       }
       const bool rescale = j > 0 && __any_sync(0xffffffffu, r != 1.f);
       const float nb = (m_run == -INFINITY) ? 0.f : -m_run;
-      float ls8[8];
-#pragma unroll
-      for (int t = 0; t < 8; ++t) ls8[t] = 0.f;
       uint32_t pw[2][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const float p0 = ex2(fmaf(__uint_as_float(sv[c][2 * k]), cl, nb));
-          const float p1 = ex2(fmaf(__uint_as_float(sv[c][2 * k + 1]), cl, nb));
-          ls8[k & 7] += p0 + p1;
-          pw[c >> 1][(c & 1) * 16 + k] = pack2(p0, p1);
-        }
-      const float lsum = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
+      const float lsum = block_weights<4>(sv, 0, cl, nb, pw);
       l_run = l_run * r + lsum;
       // P over the first 64 columns of this tile's S (already read into registers).
       tmem_st_32x32b_x32(tl, pw[0]);
