@@ -63,6 +63,7 @@ struct AttnCtl {
   uint64_t kfull[kKStages], kempty[kKStages], vfull[kVStages], vempty[kVStages];
   uint64_t sfull[2], sfree[2], pfull[2], odone[2];
   uint64_t drain;
+  uint64_t mfull;  // split over keys: the other chunks' partials in shared memory
   uint32_t tmem_base;
   uint32_t abort;
   uint32_t is_last;  // split over keys: this CTA merges the tile's chunks
@@ -193,6 +194,14 @@ __device__ __forceinline__ void load_box(uint32_t dst, const CUtensorMap* m, uin
   else tma_load_2d(dst, m, bar, x, y);
 }
 
+// Global -> shared bulk copy (16-byte aligned addresses, size a multiple of 16), completing
+// on the mbarrier's transaction count.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint32_t* status) {
   uint32_t never = 0;
   return mbar_wait(bar, parity, &never, status, kDevTimeoutDrain);
@@ -229,22 +238,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   {
     int64_t id = blockIdx.x;
     if (p.chunk > 0) {
-      qt = 0;
-      b = 0;
-      nkv = 0;
-      for (int64_t t = p.q_tiles - 1; t >= 0; --t) {
-        const int64_t nk = CAUSAL ? t + 1 : p.kv_blocks;
-        const int64_t ch = (nk + p.chunk - 1) / p.chunk;
-        if (id < ch * p.batch) {
-          qt = t;
-          b = id % p.batch;
-          kc = id / p.batch;
-          nch = ch;
-          j0 = kc * p.chunk;
-          nkv = (nk - j0 < p.chunk ? nk - j0 : p.chunk);
+      // Tile t has ch(t) = ceil(nk(t) / chunk) chunks, numbered tile by tile from the top
+      // tile down, batch index fastest.  Non-causal: ch is the same for every tile.  Causal
+      // (nk = t + 1): ch(t) = k on the band of tiles (k - 1) * chunk .. k * chunk - 1, so the
+      // walk goes band by band (a few steps) instead of tile by tile.
+      const int64_t C = p.chunk, B = p.batch;
+      int64_t k = CAUSAL ? (p.q_tiles + C - 1) / C : (p.kv_blocks + C - 1) / C;
+      int64_t hi = p.q_tiles - 1;  // the band's highest tile
+      for (;;) {
+        const int64_t lo = CAUSAL ? (k - 1) * C : 0;
+        const int64_t n = (hi - lo + 1) * k * B;  // items of the band
+        if (id < n || k <= 1 || !CAUSAL) {
+          const int64_t u = id / (k * B), r = id - u * (k * B);
+          qt = hi - u;
+          b = r % B;
+          kc = r / B;
+          nch = k;
+          j0 = kc * C;
+          const int64_t nk = CAUSAL ? qt + 1 : p.kv_blocks;
+          nkv = nk - j0 < C ? nk - j0 : C;
           break;
         }
-        id -= ch * p.batch;
+        id -= n;
+        hi = lo - 1;
+        --k;
       }
     } else {
       qt = p.q_tiles - 1 - id / p.batch;
@@ -272,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&ctl->odone[s]), 1);
     }
     mbar_init(smem_u32(&ctl->drain), 1);
+    mbar_init(smem_u32(&ctl->mfull), 1);
     ctl->abort = 0;
     ctl->is_last = 1;
     fence_barrier_init();
@@ -579,39 +597,102 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       softmax_bar();
       if (ctl->is_last) {
-        // The tile's chunks are the items blockIdx.x + (k - kc) * batch, k < nch.
+        // The tile's chunks are the items blockIdx.x + (k - kc) * batch, k < nch; the sums run
+        // in chunk order.  With at most four chunks, the other chunks' u come into the idle K / V
+        // rings (3 x 64 KiB) by bulk copies and this chunk's own u is read from TMEM (the same
+        // FP32 values it published); more chunks read their partials from L2.
         const float* first = mine - kc * p.batch * kAttnPartFloats;
         auto part = [&](int64_t k) { return first + k * p.batch * kAttnPartFloats; };
+        constexpr uint32_t kPartBytes = 128 * 128 * 4;
+        const bool via_smem = nch <= 4;
+        const uint32_t mb = smem_u32(&ctl->mfull);
+        if (via_smem && threadIdx.x == 64) {
+          asm volatile("fence.proxy.async.global;" ::: "memory");  // the acquired partials, for the copy engine
+          mbar_arrive_expect_tx(mb, static_cast<uint32_t>(nch - 1) * kPartBytes);
+          for (int64_t k = 0, slot = 0; k < nch; ++k)
+            if (k != kc) bulk_g2s(sK + static_cast<uint32_t>(slot++) * kPartBytes, part(k), kPartBytes, mb);
+        }
         float ms = -INFINITY;
+#pragma unroll 4
         for (int64_t k = 0; k < nch; ++k) ms = fmaxf(ms, __ldcg(part(k) + 128 * 128 + row));
         float ls = 0.f;
+#pragma unroll 4
         for (int64_t k = 0; k < nch; ++k)
           ls += ex2(__ldcg(part(k) + 128 * 128 + row) - ms) * __ldcg(part(k) + 128 * 128 + 128 + row);
         const float inv = 1.f / ls;
+        bool mok = true;
+        if (via_smem) {
+          // The chunks' weights 2^(m_k - m*), k < 4, in registers (selected, not indexed).
+          const float w0 = ex2(__ldcg(part(0) + 128 * 128 + row) - ms);
+          const float w1 = ex2(__ldcg(part(1) + 128 * 128 + row) - ms);
+          const float w2 = nch > 2 ? ex2(__ldcg(part(2) + 128 * 128 + row) - ms) : 0.f;
+          const float w3 = nch > 3 ? ex2(__ldcg(part(3) + 128 * 128 + row) - ms) : 0.f;
+          mok = warp_wait(mb, 0, abort, p.status);
+          if (!mok && threadIdx.x == 64) drain_wait(mb, 0, p.status);
+          const float4* ring4 = reinterpret_cast<const float4*>(smem_raw + (sK - raw));
 #pragma unroll 1
-        for (int c = kCols * half; c < kCols * half + kCols; ++c) {
-          float f[32];
+          for (int c = kCols * half; mok && c < kCols * half + kCols; ++c) {
+            float f[32];
 #pragma unroll
-          for (int k = 0; k < 32; ++k) f[k] = 0.f;
-          for (int64_t k = 0; k < nch; ++k) {
-            const float* pk = part(k);
-            const float w = ex2(__ldcg(pk + 128 * 128 + row) - ms);
-            const float4* u4 = reinterpret_cast<const float4*>(pk) + c * 8 * 128 + row;
-            float4 v[8];
+            for (int k = 0; k < 32; ++k) f[k] = 0.f;
+            for (int k = 0; k < nch; ++k) {
+              const float w = k == 0 ? w0 : k == 1 ? w1 : k == 2 ? w2 : w3;
+              if (k == kc) {
+                uint32_t o[32];
+                tmem_ld_32x32b_x32(tl + kOCol + c * 32, o);
+                tmem_ld_wait();
 #pragma unroll
-            for (int g = 0; g < 8; ++g) v[g] = __ldcg(u4 + g * 128);
+                for (int q = 0; q < 32; ++q) f[q] = fmaf(w, __uint_as_float(o[q]), f[q]);
+              } else {
+                const float4* u4 = ring4 + (k < kc ? k : k - 1) * (kPartBytes / 16) + c * 8 * 128 + row;
 #pragma unroll
-            for (int g = 0; g < 8; ++g) {
-              f[4 * g] = fmaf(w, v[g].x, f[4 * g]);
-              f[4 * g + 1] = fmaf(w, v[g].y, f[4 * g + 1]);
-              f[4 * g + 2] = fmaf(w, v[g].z, f[4 * g + 2]);
-              f[4 * g + 3] = fmaf(w, v[g].w, f[4 * g + 3]);
+                for (int g = 0; g < 8; ++g) {
+                  const float4 v = u4[g * 128];
+                  f[4 * g] = fmaf(w, v.x, f[4 * g]);
+                  f[4 * g + 1] = fmaf(w, v.y, f[4 * g + 1]);
+                  f[4 * g + 2] = fmaf(w, v.z, f[4 * g + 2]);
+                  f[4 * g + 3] = fmaf(w, v.w, f[4 * g + 3]);
+                }
+              }
+            }
+#pragma unroll
+            for (int k = 0; k < 32; ++k) f[k] *= inv;
+            stage(c, f);
+          }
+        } else {
+#pragma unroll 1
+          for (int c2 = kCols * half; c2 < kCols * half + kCols; c2 += 2) {
+            float f[2][32];
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int k = 0; k < 32; ++k) f[h][k] = 0.f;
+            for (int64_t k = 0; k < nch; ++k) {
+              const float* pk = part(k);
+              const float w = ex2(__ldcg(pk + 128 * 128 + row) - ms);
+              const float4* u4 = reinterpret_cast<const float4*>(pk) + c2 * 8 * 128 + row;
+              float4 v[16];
+#pragma unroll
+              for (int g = 0; g < 16; ++g) v[g] = __ldcg(u4 + g * 128);
+#pragma unroll
+              for (int g = 0; g < 16; ++g) {
+                float* fh = f[g >> 3];
+                const int b4 = 4 * (g & 7);
+                fh[b4] = fmaf(w, v[g].x, fh[b4]);
+                fh[b4 + 1] = fmaf(w, v[g].y, fh[b4 + 1]);
+                fh[b4 + 2] = fmaf(w, v[g].z, fh[b4 + 2]);
+                fh[b4 + 3] = fmaf(w, v[g].w, fh[b4 + 3]);
+              }
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+              for (int k = 0; k < 32; ++k) f[h][k] *= inv;
+              stage(c2 + h, f[h]);
             }
           }
-#pragma unroll
-          for (int k = 0; k < 32; ++k) f[k] *= inv;
-          stage(c, f);
         }
+        if (!mok) *abort = 1;
         fence_proxy_async_smem();
       }
     }
