@@ -744,6 +744,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (FP8) fp8_scale(r, p, gm, tn * OUT_N + ch * 32);
             if (gm < p.M) store_row_chunk(p, cbase, tn * OUT_N + ch * 32, r);
           }
+          // The partials are scratch that nothing reads again before the next call rewrites
+          // them: drop their L2 lines so they are never written back to DRAM.  A warp drops
+          // the lines of its own 32 rows (4 x 128 bytes per column group) once all its lanes
+          // have read them.
+          __syncwarp();
+          for (int64_t cc = first; cc <= lastc; ++cc) {
+            const uint8_t* pbase = reinterpret_cast<const uint8_t*>(part_of(cc) - row + q * 32);
+#pragma unroll 4
+            for (int i = lane; i < (BN / 4) * 4; i += 32)
+              discard_l2(pbase + (static_cast<size_t>(i >> 2) * BM * 16) + (i & 3) * 128);
+          }
         }
         epi_bar();  // is_last is rewritten only after everyone read it
         continue;

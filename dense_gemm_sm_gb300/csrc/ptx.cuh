@@ -92,6 +92,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Drops the 128-byte L2 line at `line` (128-byte aligned) without writing it back: for
+// scratch data that is dead once read.
+__device__ __forceinline__ void discard_l2(const void* line) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(line) : "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
