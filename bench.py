@@ -102,7 +102,8 @@ class Workload:
             M, N, K = w["M"], w["N"], w["K"]
             return dict(kind="f32", w=w, batch=1, flops=2.0 * M * N * K,
                         algo_bytes=4.0 * (M * K + K * N + (2 if w["beta"] != 0 else 1) * M * N),
-                        bound="alu", unit="TFLOPS", kernel="sgemm_simt_kernel",
+                        bound="alu", unit="TFLOPS",
+                        kernel="sgemm_small_kernel" if name == "sgemm_256" else "sgemm_tma_kernel",
                         sources=["sgemm_simt.cu"] + COMMON_SOURCES,
                         desc=f"FP32 SGEMM M={M} N={N} K={K} lda={w['lda']} ldb={w['ldb']} "
                              f"ldc={w['ldc']} alpha={float(w['alpha'])} beta={float(w['beta'])}")

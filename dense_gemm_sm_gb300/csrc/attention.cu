@@ -232,8 +232,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Work item: query tiles in decreasing order (causal: the longest rows start first); with
-  // a split over keys, the tile's chunk `kc` of nch covers its key blocks j0 .. j0 + nkv - 1.
+  // Work item: causal, query tiles in decreasing order (the longest rows start first); not
+  // causal, head by head; with a split over keys, the tile's chunk `kc` of nch covers its
+  // key blocks j0 .. j0 + nkv - 1.
   int64_t qt, b, j0 = 0, kc = 0, nch = 1, nkv;
   {
     int64_t id = blockIdx.x;
@@ -263,10 +264,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         hi = lo - 1;
         --k;
       }
-    } else {
+    } else if (CAUSAL) {
       qt = p.q_tiles - 1 - id / p.batch;
       b = id % p.batch;
-      nkv = CAUSAL ? qt + 1 : p.kv_blocks;
+      nkv = qt + 1;
+    } else {
+      // Head by head, so that the CTAs running together share few heads' K and V, which then
+      // stay in L2 while all of the head's query tiles stream them.
+      b = id / p.q_tiles;
+      qt = id - b * p.q_tiles;
+      nkv = p.kv_blocks;
     }
   }
   const int64_t q0 = qt * kBQ;
