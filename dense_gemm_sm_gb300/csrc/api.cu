@@ -179,7 +179,10 @@ void plan_f32(int64_t M, int64_t N, int64_t K, int64_t batch, int64_t resident, 
   pl->tile_n = kSimtBN;
   pl->tile_k = kSimtBK;
   pl->stages = kSimtStages;
-  pl->group = kRasterGroup;
+  // Groups of 16 tile rows: on 4096^3 the DRAM traffic per call was 453 / 427 / 707 / 564 MB
+  // with groups of 8 / 16 / 32 / 4 rows (two 128 x 128 tiles per SM: about ten tile rows
+  // run together), the time the same.
+  pl->group = 2 * kRasterGroup;
   pl->tiles = batch * cdiv(M, kSimtBM) * cdiv(N, kSimtBN);
   pl->kblocks = cdiv(K, kSimtBK);
   pl->vec = 1;
@@ -412,7 +415,11 @@ dg_status f32_impl(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
   p.batch = batch;
   p.tiles_m = cdiv(M, kSimtBM);
   p.tiles_n = cdiv(N, kSimtBN);
-  p.group = kRasterGroup;
+  p.group = pl.group;
+  if (const char* e = std::getenv("DG_SIMT_GROUP")) {  // tuning override (sweeps)
+    const int g = std::atoi(e);
+    if (g >= 1 && g <= 4096) p.group = g;
+  }
   p.dp_tiles = dp;
   p.sk_tiles = sk;
   p.sk_splits = splits;

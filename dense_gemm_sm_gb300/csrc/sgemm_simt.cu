@@ -186,6 +186,16 @@ __device__ __forceinline__ void simt_finish(const SimtParams& p, float (&acc)[8]
         }
       }
     }
+    // The partials are scratch that nothing reads again before the next call rewrites them:
+    // drop their L2 lines so they are never written back.  A warp drops the lines holding
+    // its own 32 float4 of each of the 16 groups (4 x 128 bytes) once its lanes have read them.
+    __syncwarp();
+    for (int cc = 0; cc < S; ++cc) {
+      const uint8_t* pb = reinterpret_cast<const uint8_t*>(reinterpret_cast<const float4*>(p.ws) +
+                                                           ((sk_tile * S + cc) * 16) * NT + warp * 32);
+#pragma unroll
+      for (int i = lane; i < 16 * 4; i += 32) discard_l2(pb + static_cast<size_t>(i >> 2) * NT * 16 + (i & 3) * 128);
+    }
     if (tid == 0) p.counters[sk_tile] = 0u;  // ready for the next call
   }
 
@@ -539,6 +549,18 @@ __device__ __forceinline__ void sk_segment_finish(const SimtParams& p, float (&a
         acc[q >> 1][4 * (q & 1) + 2] += part[q8].z;
         acc[q >> 1][4 * (q & 1) + 3] += part[q8].w;
       }
+    }
+  }
+  // The partials are dead scratch now: drop their L2 lines (see simt_finish).
+  {
+    const int warp = tid >> 5, lane = tid & 31;
+    __syncwarp();
+    for (int64_t cc = first; cc <= last; ++cc) {
+      const int sl = sk_start<int64_t>(cc, U, G) >= sg.tile * KT ? 0 : 1;
+      const uint8_t* pb = reinterpret_cast<const uint8_t*>(reinterpret_cast<const float4*>(p.ws) +
+                                                           ((cc * 2 + sl) * 16) * NT + warp * 32);
+#pragma unroll
+      for (int i = lane; i < 16 * 4; i += 32) discard_l2(pb + static_cast<size_t>(i >> 2) * NT * 16 + (i & 3) * 128);
     }
   }
   simt_finish<TRANS_B, true>(p, acc, sg.x_b, sg.x_m, sg.x_n, sg.tile, -1, s_is_last);
