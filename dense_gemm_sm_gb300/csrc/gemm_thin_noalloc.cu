@@ -40,22 +40,43 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNaScratchBytes
 
 std::mutex g_na_mu;
 unsigned char* g_na_addr[kNaMaxDevices] = {};
+CUcontext g_na_ctx[kNaMaxDevices] = {};  // the context the cached address belongs to
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<CtxGetCurrentFn>(nullptr);
+    return reinterpret_cast<CtxGetCurrentFn>(p);
+  }();
+  return fn;
+}
 
 // Device address of the scratch array on `dev` (the current device).  In host code the
-// array's name is only a host-side stand-in, so the address is taken once per device with
-// cudaGetSymbolAddress and cached.  The array starts zeroed (module load), and the kernel
-// leaves every arrival counter at zero when it finishes, so calls need no memset; the first
-// call on a device still zeroes the counters on its stream once, and a call that gave up on
-// a bounded wait is cleaned up by dg_device_status (noalloc_reset_counters below).
+// array's name is only a host-side stand-in, so the address is taken with
+// cudaGetSymbolAddress and cached per device together with the current context: a new
+// context (after cudaDeviceReset, say) loads the module again at a new address, so the
+// address is looked up again when the context differs.  The array starts zeroed (module
+// load), and the kernel leaves every arrival counter at zero when it finishes, so calls need
+// no memset; the first call in a context still zeroes the counters on its stream once, and a
+// call that gave up on a bounded wait is cleaned up by dg_device_status
+// (noalloc_reset_counters below).
 cudaError_t scratch_address(int dev, cudaStream_t s, unsigned char** out) {
+  CUcontext ctx = nullptr;
+  CtxGetCurrentFn get = ctx_get_current();
+  if (!get || get(&ctx) != CUDA_SUCCESS) return cudaErrorInitializationError;
   std::lock_guard<std::mutex> lock(g_na_mu);
-  if (!g_na_addr[dev]) {
+  if (!g_na_addr[dev] || g_na_ctx[dev] != ctx) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
     e = cudaMemsetAsync(static_cast<unsigned char*>(p) + kNaPartialBytes, 0, kNaCounterBytes, s);
     if (e != cudaSuccess) return e;
     g_na_addr[dev] = static_cast<unsigned char*>(p);
+    g_na_ctx[dev] = ctx;
   }
   *out = g_na_addr[dev];
   return cudaSuccess;

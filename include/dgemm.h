@@ -122,11 +122,12 @@ dg_status gemm_bf16_strided_batched(int64_t M, int64_t N, int64_t K, float alpha
  *   - Arguments, layout and result are those of gemm_bf16 (op(B) = B), restricted to
  *     M <= 16 and N <= 1,048,576; larger sizes return DG_ERR_UNSUPPORTED and enqueue
  *     nothing.  Alignment rules as gemm_bf16 (DG_ERR_MISALIGNED).
- *   - Calls no cudaMalloc, cudaFree or other allocating routine.  The first call on a
- *     device does that device's set-up: it looks up the array's device address
+ *   - Calls no cudaMalloc, cudaFree or other allocating routine.  The first call in a
+ *     device's context does that context's set-up: it looks up the array's device address
  *     (cudaGetSymbolAddress) and zeroes the arrival counters once (cudaMemsetAsync on
  *     `stream`); make that first call before any stream capture.  The address is cached
- *     for the life of the process and does not survive cudaDeviceReset on that device.
+ *     with the context it belongs to; a call in another context (after cudaDeviceReset,
+ *     say) does the set-up again.
  *   - Every call shares the one array and leaves its contents behind.  The kernel leaves
  *     every arrival counter at zero when it finishes, so later calls enqueue only the
  *     kernel; after a bounded wait gave up (dg_device_status returns DG_ERR_TIMEOUT) that
