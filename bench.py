@@ -46,18 +46,21 @@ SM_MAX_MHZ_NOMINAL = 2070.0      # only if MEASURED_PEAKS.json gives no maximum 
 # kernel's sources (kernel file, planner, headers) matches the one it was taken with.
 COMMON_SOURCES = ["api.cu", "dg_internal.h", "ptx.cuh", "tile_sched.h"]
 MEASURED_TRAFFIC = {
-    "sgemm_4096": {"bytes_per_launch": 464_847_872, "source_hash": "a93b4b847359fd31"},
-    "sgemm_ragged": {"bytes_per_launch": 26_462_464, "source_hash": "a93b4b847359fd31"},
-    "ffn_bf16": {"bytes_per_launch": 163_321_088, "source_hash": "3198cecd1ee343c5"},
-    "ffn_gate_up": {"bytes_per_launch": 234_397_184, "source_hash": "3198cecd1ee343c5"},
-    "bf16_4096": {"bytes_per_launch": 147_519_488, "source_hash": "3198cecd1ee343c5"},
-    "qk_batched": {"bytes_per_launch": 1_078_651_904, "source_hash": "3198cecd1ee343c5"},
-    "decode_m1": {"bytes_per_launch": 105_342_208, "source_hash": "36ed44c05924eb42"},
-    "decode_m4": {"bytes_per_launch": 105_141_248, "source_hash": "36ed44c05924eb42"},
-    "decode_m16": {"bytes_per_launch": 105_492_736, "source_hash": "36ed44c05924eb42"},
-    "attn_batched": {"bytes_per_launch": 267_400_448, "source_hash": "49821aa59b33e504"},
-    "fp8_ffn": {"bytes_per_launch": 57_830_912, "source_hash": "910aedba867a0f09"},
-    "decode_chain_m1": {"bytes_per_launch": 408_459_520, "source_hash": "6056eb10f7537d26"},
+    "sgemm_4096": {"bytes_per_launch": 388_554_752, "source_hash": "e0c17bedb5bd0641"},
+    "sgemm_ragged": {"bytes_per_launch": 24_652_800, "source_hash": "e0c17bedb5bd0641"},
+    "sgemm_256": {"bytes_per_launch": 554_496, "source_hash": "e0c17bedb5bd0641"},
+    "ffn_bf16": {"bytes_per_launch": 154_208_000, "source_hash": "e7a1d6aa9905ba81"},
+    "ffn_gate_up": {"bytes_per_launch": 233_758_976, "source_hash": "e7a1d6aa9905ba81"},
+    "bf16_4096": {"bytes_per_launch": 134_060_288, "source_hash": "e7a1d6aa9905ba81"},
+    "qk_batched": {"bytes_per_launch": 1_078_743_040, "source_hash": "e7a1d6aa9905ba81"},
+    "decode_m1": {"bytes_per_launch": 105_198_336, "source_hash": "242151324e3e1c84"},
+    "decode_m4": {"bytes_per_launch": 105_306_624, "source_hash": "242151324e3e1c84"},
+    "decode_m16": {"bytes_per_launch": 105_571_840, "source_hash": "242151324e3e1c84"},
+    "decode_chain_m1": {"bytes_per_launch": 408_524_544, "source_hash": "90edeb0e96c056db"},
+    "attn_batched": {"bytes_per_launch": 115_854_080, "source_hash": "be88d91f52fd7d16"},
+    "attn_causal_8k": {"bytes_per_launch": 6_360_320, "source_hash": "be88d91f52fd7d16"},
+    "fp8_ffn": {"bytes_per_launch": 57_952_768, "source_hash": "54946ecf6cdcc20e"},
+    "fp8_quant_gemm": {"bytes_per_launch": 23_177_728, "source_hash": "54946ecf6cdcc20e", "quantiser_bytes_per_launch": 12_605_696},
 }
 
 
@@ -321,14 +324,21 @@ class Workload:
             unit = "GB/s"
             note = f"HBM copy bandwidth of {peaks['source']} peaks"
         traffic = None
+        other = None
         t = MEASURED_TRAFFIC.get(self.name)
         if t and t["source_hash"] == kernel_source_hash(self.sources):
             traffic = t["bytes_per_launch"]
-        return {"bound": "tensor" if self.bound == "tensor8" else self.bound,
-                "achieved": round(achieved, 3), "peak": round(peak, 1),
-                "unit": unit, "frac": round(achieved / peak, 4), "traffic": traffic,
-                "kernel": self.kernel, "algorithmic": {"flops": self.flops, "bytes": self.algo_bytes},
-                "peak_note": note}
+            if "quantiser_bytes_per_launch" in t:
+                # the step's other kernel (the per-row quantiser before the FP8 GEMM)
+                other = {"kernel": "quantize_rows_kernel", "traffic": t["quantiser_bytes_per_launch"]}
+        out = {"bound": "tensor" if self.bound == "tensor8" else self.bound,
+               "achieved": round(achieved, 3), "peak": round(peak, 1),
+               "unit": unit, "frac": round(achieved / peak, 4), "traffic": traffic,
+               "kernel": self.kernel, "algorithmic": {"flops": self.flops, "bytes": self.algo_bytes},
+               "peak_note": note}
+        if other is not None:
+            out["other_kernel"] = other
+        return out
 
 
 # --------------------------------------------------------------------------- clocks
