@@ -559,6 +559,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       constexpr uint32_t idesc = FP8 ? idesc_e4m3_f32(PAIR ? 2 * BM : BM, BN, false, !B_KMAJOR)
                                      : idesc_bf16_f32(PAIR ? 2 * BM : BM, BN, false, !B_KMAJOR);
       uint32_t it = 0, lt = 0;
+      uint32_t s = 0, ph = 0;  // ring stage of block `it` and its phase parity
+      // Operand descriptors of the ring bases, advanced by the start-address field alone
+      // (16-byte units; every offset stays inside the 256 KiB the field spans), so an MMA costs
+      // the issuing thread a few integer additions.
+      const uint64_t dA = sdesc_sw128(a_ring, 16, 1024);
+      const uint64_t dB = B_KMAJOR ? sdesc_sw128(b_ring, 16, 1024) : sdesc_sw128(b_ring, 8192, 1024);
       bool ok = true;
       TcWalk walk(p, cid, ncl);
       TcItem item;
@@ -573,7 +579,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_after();
         const uint32_t d = tmem_base + acc * BN;
         for (int kb = item.kbeg; kb < item.kend; ++kb) {
-          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
           // Pair: full[s] counts the bytes of both CTAs' stage s (acquire at cluster scope).
           if (!(PAIR ? mbar_wait_cluster(smem_u32(&ctl->full[s]), ph, abort, p.status, kDevTimeoutMma)
                      : mbar_wait(smem_u32(&ctl->full[s]), ph, abort, p.status, kDevTimeoutMma))) {
@@ -581,16 +586,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = a_ring + s * A_BYTES, b0 = b_ring + s * Cfg::B_BYTES;
+          const uint64_t dAs = dA + ((s * A_BYTES) >> 4), dBs = dB + ((s * Cfg::B_BYTES) >> 4);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             // A (K-major, 128B swizzle): K step of 16 elements = 32 bytes inside the atom.
-            const uint64_t adesc = sdesc_sw128(a0 + k * 32, 16, 1024);
+            const uint64_t adesc = dAs + ((k * 32) >> 4);
             // B: K-major like A, or N-major: 64-column atoms 8 KiB apart (LBO), 8-row
             // groups 1 KiB apart (SBO), K step of 16 rows = 2 KiB.  For the pair the same
             // offsets describe each CTA's share of A and B.
-            const uint64_t bdesc = B_KMAJOR ? sdesc_sw128(b0 + k * 32, 16, 1024)
-                                            : sdesc_sw128(b0 + k * 2048, 8192, 1024);
+            const uint64_t bdesc = dBs + ((B_KMAJOR ? k * 32 : k * 2048) >> 4);
             const uint32_t accum = (kb > item.kbeg || k > 0) ? 1u : 0u;
             if (FP8) {
               if (PAIR) umma2_f8(d, adesc, bdesc, idesc, accum);
@@ -605,6 +609,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             else umma_commit(smem_u32(&ctl->empty[s]));
           }
           ++it;
+          if (++s == static_cast<uint32_t>(STAGES)) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
         if (!ok) break;
         if (PAIR) umma2_commit_both(smem_u32(&ctl->tfull[acc]));
