@@ -296,7 +296,11 @@ void plan_bf16(int64_t M, int64_t N, int64_t K, int64_t batch, int sms, dg_plan*
         pl->tile_n = bn;
       }
     }
-    pl->stages = 6;
+    // BF16 pairs stage two 128-byte K atoms (128 elements) in 3 stages, FP8 pairs one atom
+    // (128 elements) in 6 (gemm_tc.cu, TcCfg).
+    pl->stages = fp8 ? 6 : 3;
+    if (!fp8) pl->tile_k *= 2;
+    pl->kblocks = cdiv(K, pl->tile_k);
     pl->group = kRasterGroup / 2;  // in 256-row tile rows: the same 8 rows of 128
     pl->tiles = cdiv(cdiv(M, kTcBM), 2) * cdiv(N, bn);
     const int64_t clusters = pl->tiles < sms / 2 ? pl->tiles : sms / 2;
@@ -312,8 +316,9 @@ void plan_bf16(int64_t M, int64_t N, int64_t K, int64_t batch, int sms, dg_plan*
   // most 4 CTAs.  tail_tiles = the stream-K tiles, splits = the CTAs sharing them.
   pl->splits = 1;
   pl->tail_tiles = 0;
-  if (pl->tiles > G && pl->tiles % G != 0 && pl->kblocks >= 16 &&
-      (pl->tiles / G) * pl->kblocks >= 96) {
+  // The thresholds count 128-byte K atoms (a pair's stage holds two).
+  const int64_t katoms = pl->kblocks * (pair && !fp8 ? 2 : 1);
+  if (pl->tiles > G && pl->tiles % G != 0 && katoms >= 16 && (pl->tiles / G) * katoms >= 96) {
     pl->tail_tiles = pl->tiles % G;
     const int64_t c4 = 4 * pl->tail_tiles;
     pl->splits = static_cast<int32_t>(c4 < G ? c4 : G);

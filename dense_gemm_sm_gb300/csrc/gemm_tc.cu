@@ -46,17 +46,28 @@ constexpr int NUM_THREADS = 192;
 
 // PAIR: a CTA pair (cluster of 2) computes a 256 x BN tile with tcgen05.mma.cta_group::2;
 // each CTA holds its 128 rows of A and BN / 2 columns of B, so a stage is half as large.
-template <int BN, bool B_KMAJOR, bool PAIR = false>
+// A stage holds KA K atoms of 128 bytes per row (64 BF16 or 128 FP8 elements each): BF16 pairs
+// take two (8 MMAs per stage), the rest one.  Every stage costs the MMA issuer a barrier wait,
+// a fence and a commit that the tensor pipe does not hide: measured without operand loads, the
+// FFN's stage took ~240 cycles beyond its 4 MMAs in BF16, added in full when the stage's MMAs
+// were doubled; two atoms per stage pay it half as often (4096^3 1707 -> 1741 TFLOPS, gate/up
+// 1633 -> 1662, FFN equal).  FP8 pairs keep one atom and six stages: with three stages of two
+// atoms the FFN shape lost 2% (2537 -> 2480 TFLOPS).
+template <int BN, bool B_KMAJOR, bool PAIR = false, bool FP8 = false>
 struct TcCfg {
   static constexpr int BNC = PAIR ? BN / 2 : BN;  // B columns held by this CTA
-  // N-major B arrives as 64-column boxes (8 KiB each), K-major B as one BNC-row box.
+  static constexpr int KA = PAIR && !FP8 ? 2 : 1;  // K atoms per stage
+  static constexpr uint32_t A_STAGE = KA * A_BYTES;
+  // N-major B arrives as 64-column boxes (8 KiB per atom each), K-major B as one BNC-row box
+  // per atom.
   static constexpr int NBOX = (BNC + 63) / 64;
-  static constexpr uint32_t B_BYTES = NBOX * 8192;  // stage footprint
-  static constexpr uint32_t B_LOAD_BYTES = B_KMAJOR ? BNC * BK * 2 : NBOX * 8192;  // expect_tx
-  static constexpr int STAGES = PAIR ? 6 : (BN >= 192 ? 4 : 6);
+  static constexpr uint32_t B_ATOM = NBOX * 8192;   // one atom's footprint
+  static constexpr uint32_t B_BYTES = KA * B_ATOM;  // stage footprint
+  static constexpr uint32_t B_LOAD_BYTES = KA * (B_KMAJOR ? BNC * BK * 2 : NBOX * 8192);  // expect_tx
+  static constexpr int STAGES = PAIR ? (KA == 2 ? 3 : 6) : (BN >= 192 ? 4 : 6);
   // Two accumulators of BN columns; the allocation is a power of two.
   static constexpr uint32_t TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
-  static constexpr uint32_t RING_BYTES = STAGES * (A_BYTES + B_BYTES);
+  static constexpr uint32_t RING_BYTES = STAGES * (A_STAGE + B_BYTES);
   // Epilogue staging for TMA stores: 4 warps x 2 buffers x (32 rows x 128 bytes).
   static constexpr uint32_t STAGE_OUT_BYTES = 4 * 2 * 4096;
   static constexpr uint32_t BAR_BYTES = 256;
@@ -398,19 +409,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC,
                    const TcParams p, const int fault) {
-  using Cfg = TcCfg<BN, B_KMAJOR, PAIR>;
+  using Cfg = TcCfg<BN, B_KMAJOR, PAIR, FP8>;
   static_assert(!PAIR || ((BN == 256 || (BN == 224 && FP8)) && !RANK3),
                 "pair tiles are 256 x 256 (FP8 also 256 x 224), one problem");
   static_assert(!DUAL || (BN == 256 && !B_KMAJOR && !RANK3), "gate/up: 2 x 128 columns, N-major");
   static_assert(!FP8 || (B_KMAJOR && !RANK3 && !DUAL), "FP8: one problem, K-major B");
-  constexpr int BK_ELEMS = FP8 ? 128 : BK;  // K elements per stage (128 bytes per row)
+  constexpr int ATOM_K = FP8 ? 128 : BK;           // K elements per 128-byte atom row
+  constexpr int KA = Cfg::KA;
+  constexpr int BK_ELEMS = KA * ATOM_K;            // K elements per stage
   constexpr int OUT_N = DUAL ? BN / 2 : BN;  // output columns per tile
   constexpr int STAGES = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t ring = (raw + 1023u) & ~1023u;            // 1024-byte aligned swizzle atoms
   const uint32_t a_ring = ring;
-  const uint32_t b_ring = ring + STAGES * A_BYTES;
+  const uint32_t b_ring = ring + STAGES * Cfg::A_STAGE;
   const uint32_t out_stage = ring + Cfg::RING_BYTES;  // 1024-byte aligned
   SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem_raw + (ring - raw) + Cfg::RING_BYTES +
                                             Cfg::STAGE_OUT_BYTES);
@@ -488,26 +501,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           const int32_t kx = kb * BK_ELEMS;
-          const uint32_t adst = a_ring + s * A_BYTES, bdst = b_ring + s * Cfg::B_BYTES;
+          const uint32_t adst = a_ring + s * Cfg::A_STAGE, bdst = b_ring + s * Cfg::B_BYTES;
           if (PAIR) {
             // Both CTAs' loads of stage s count on rank 0's full[s]; rank 0 posts the bytes
             // of both (a load may land before the post: the count is signed within a phase).
+            // A and K-major B: one box per atom, the atoms B_ATOM / 16 KiB apart; N-major B:
+            // 64-column boxes KA atoms deep (KA * 64 rows of K), chunks KA * 8 KiB apart.
             const uint32_t fb = cluster_addr(smem_u32(&ctl->full[s]), 0u);
-            if (rank == 0) mbar_arrive_expect_tx(smem_u32(&ctl->full[s]), 2 * (A_BYTES + Cfg::B_LOAD_BYTES));
-            tma_load_2d_pair(adst, &tmA, fb, kx, ym);
+            if (rank == 0) mbar_arrive_expect_tx(smem_u32(&ctl->full[s]), 2 * (Cfg::A_STAGE + Cfg::B_LOAD_BYTES));
+#pragma unroll
+            for (int a = 0; a < KA; ++a) tma_load_2d_pair(adst + a * A_BYTES, &tmA, fb, kx + a * ATOM_K, ym);
             if (B_KMAJOR) {
-              tma_load_2d_pair(bdst, &tmB, fb, kx, xn);
+#pragma unroll
+              for (int a = 0; a < KA; ++a) tma_load_2d_pair(bdst + a * Cfg::B_ATOM, &tmB, fb, kx + a * ATOM_K, xn);
             } else if (B3D) {
               tma_load_3d_pair(bdst, mb1, fb, 0, kx, xn / 64);
             } else {
 #pragma unroll
-              for (int j = 0; j < Cfg::NBOX; ++j) tma_load_2d_pair(bdst + j * 8192u, mb1, fb, xn + 64 * j, kx);
+              for (int j = 0; j < Cfg::NBOX; ++j) tma_load_2d_pair(bdst + j * (KA * 8192u), mb1, fb, xn + 64 * j, kx);
             }
             ++it;
             continue;
           }
           const uint32_t fb = smem_u32(&ctl->full[s]);
-          mbar_arrive_expect_tx(fb, A_BYTES + Cfg::B_LOAD_BYTES);
+          mbar_arrive_expect_tx(fb, Cfg::A_STAGE + Cfg::B_LOAD_BYTES);
           if (RANK3) tma_load_3d(adst, &tmA, fb, kx, ym, zb);
           else tma_load_2d(adst, &tmA, fb, kx, ym);
           if (B_KMAJOR) {
@@ -564,7 +581,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // (16-byte units; every offset stays inside the 256 KiB the field spans), so an MMA costs
       // the issuing thread a few integer additions.
       const uint64_t dA = sdesc_sw128(a_ring, 16, 1024);
-      const uint64_t dB = B_KMAJOR ? sdesc_sw128(b_ring, 16, 1024) : sdesc_sw128(b_ring, 8192, 1024);
+      const uint64_t dB = B_KMAJOR ? sdesc_sw128(b_ring, 16, 1024) : sdesc_sw128(b_ring, KA * 8192, 1024);
       bool ok = true;
       TcWalk walk(p, cid, ncl);
       TcItem item;
@@ -586,15 +603,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t dAs = dA + ((s * A_BYTES) >> 4), dBs = dB + ((s * Cfg::B_BYTES) >> 4);
+          const uint64_t dAs = dA + ((s * Cfg::A_STAGE) >> 4), dBs = dB + ((s * Cfg::B_BYTES) >> 4);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            // A (K-major, 128B swizzle): K step of 16 elements = 32 bytes inside the atom.
-            const uint64_t adesc = dAs + ((k * 32) >> 4);
-            // B: K-major like A, or N-major: 64-column atoms 8 KiB apart (LBO), 8-row
-            // groups 1 KiB apart (SBO), K step of 16 rows = 2 KiB.  For the pair the same
-            // offsets describe each CTA's share of A and B.
-            const uint64_t bdesc = dBs + ((B_KMAJOR ? k * 32 : k * 2048) >> 4);
+          for (int k = 0; k < KA * (BK / 16); ++k) {
+            const int a = k / (BK / 16), kk = k % (BK / 16);  // atom, MMA inside the atom
+            // A (K-major, 128B swizzle): atoms 16 KiB apart; K step of one MMA = 32 bytes
+            // inside the atom (16 BF16 or 32 FP8 elements).
+            const uint64_t adesc = dAs + ((a * A_BYTES + kk * 32) >> 4);
+            // B: K-major like A (atoms B_ATOM apart), or N-major: 64-column chunks KA * 8 KiB
+            // apart (LBO), 8-row groups 1 KiB apart (SBO), K step of 16 rows = 2 KiB through
+            // the KA atoms' rows.  For the pair the same offsets describe each CTA's share.
+            const uint64_t bdesc = dBs + ((B_KMAJOR ? a * Cfg::B_ATOM + kk * 32 : k * 2048) >> 4);
             const uint32_t accum = (kb > item.kbeg || k > 0) ? 1u : 0u;
             if (FP8) {
               if (PAIR) umma2_f8(d, adesc, bdesc, idesc, accum);
@@ -964,7 +983,7 @@ cudaError_t launch_tc_variant(const CUtensorMap& ma, const CUtensorMap& mb, cons
                               const CUtensorMap& mc, const TcParams& p, int num_ctas,
                               cudaStream_t s) {
   auto kern = gemm_tc_kernel<BN, B_KMAJOR, RANK3, B3D, PAIR, DUAL, FP8>;
-  constexpr uint32_t smem = TcCfg<BN, B_KMAJOR, PAIR>::SMEM_BYTES;
+  constexpr uint32_t smem = TcCfg<BN, B_KMAJOR, PAIR, FP8>::SMEM_BYTES;
   static_assert(smem <= 232448, "shared memory per CTA");
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = ensure_smem_attr(kern, smem, attr_done);
@@ -1014,6 +1033,9 @@ cudaError_t launch_gemm_tc(const TcParams& p, int bn, const void* A, int64_t lda
   // reaches past a row) and the tile width is whole chunks.
   const bool b3d = !fp8 && !b_kmajor && batch <= 1 && p.N % 64 == 0 && bn % 64 == 0 &&
                    p.N >= (dual ? bn / 2 : bn);
+  // BF16 pairs stage two K atoms: N-major B boxes are 2 * BK rows of K deep (A and K-major B
+  // take one box per atom).
+  const uint32_t bk_rows = pair && !fp8 ? 2 * BK : BK;
   bool ok_b;
   if (fp8)
     ok_b = make_tile_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, p.K, p.N, ldb, 1, 0, 128,
@@ -1022,18 +1044,18 @@ cudaError_t launch_gemm_tc(const TcParams& p, int bn, const void* A, int64_t lda
     ok_b = make_bf16_map(&mb, B, p.K, p.N, ldb, batch, strideB, BK, bnc);
   else if (b3d)
     ok_b = make_tile_map(&mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, 64, p.K, ldb,
-                         static_cast<uint64_t>(p.N / 64), 64, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B,
+                         static_cast<uint64_t>(p.N / 64), 64, 64, bk_rows, CU_TENSOR_MAP_SWIZZLE_128B,
                          static_cast<uint32_t>(bnc / 64));
   else
-    ok_b = make_bf16_map(&mb, B, p.N, p.K, ldb, batch, strideB, 64, BK);
+    ok_b = make_bf16_map(&mb, B, p.N, p.K, ldb, batch, strideB, 64, bk_rows);
   if (!ok_b) return cudaErrorInvalidValue;
   mb2 = mb;
   if (dual) {
     const bool ok_b2 =
         b3d ? make_tile_map(&mb2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B2, 64, p.K, ldb2,
-                            static_cast<uint64_t>(p.N / 64), 64, 64, BK,
+                            static_cast<uint64_t>(p.N / 64), 64, 64, bk_rows,
                             CU_TENSOR_MAP_SWIZZLE_128B, static_cast<uint32_t>(bnc / 64))
-            : make_bf16_map(&mb2, B2, p.N, p.K, ldb2, 1, 0, 64, BK);
+            : make_bf16_map(&mb2, B2, p.N, p.K, ldb2, 1, 0, 64, bk_rows);
     if (!ok_b2) return cudaErrorInvalidValue;
   }
   CUtensorMap mc;

@@ -69,7 +69,8 @@ def test_plan_fp8_pair_width():
     # FFN shape: 4 x 48 tiles of 256 = 3 waves of 76 pairs (768) vs 4 x 55 of 224 (672).
     ffn = dg.dg_plan_gemm(2, 1024, 12288, 4096, num_sms=152)
     assert ffn["kernel"] == dg.DG_KERNEL_TC2_BF16 and ffn["tile_n"] == 224 and ffn["tiles"] == 220
-    assert ffn["tile_k"] == 128 and ffn["kblocks"] == 32 and ffn["tail_tiles"] == 0
+    # FP8 pairs stage one 128-byte K atom (BF16 pairs two).
+    assert ffn["tile_k"] == 128 and ffn["kblocks"] == 32 and ffn["tail_tiles"] == 0 and ffn["stages"] == 6
     # Example 5-8 GEMM: 16 x 6 tiles (2 waves, 512) vs 16 x 7 (2 waves, 448).
     assert dg.dg_plan_gemm(2, 4096, 1536, 4096, num_sms=152)["tile_n"] == 224
     # 2 x 35 tiles of 256 fit one wave; 2 x 40 of 224 would need two.
@@ -256,8 +257,11 @@ def _check_bf16_fp8_plans(M, N, K, batch, sms):
             units = _cdiv(N, 128) * _cdiv(K, 64)
             assert q["tiles"] == _cdiv(N, 128) and q["grid"] == min(units, sms)
             continue
-        tk = 128 if dtype == 2 else 64
+        pair = q["kernel"] == dg.DG_KERNEL_TC2_BF16
+        ka = 2 if pair and dtype == 1 else 1  # 128-byte K atoms per stage
+        tk = (128 if dtype == 2 else 64) * ka
         assert q["tile_k"] == tk and q["kblocks"] == _cdiv(K, tk)
+        assert q["stages"] == ((3 if ka == 2 else 6) if pair else (4 if q["tile_n"] >= 192 else 6))
         bn = q["tile_n"]
         if q["kernel"] == dg.DG_KERNEL_TC2_BF16:
             assert batch == 1 and _cdiv(M, 128) >= 2 and q["tile_m"] == 256
@@ -277,8 +281,9 @@ def _check_bf16_fp8_plans(M, N, K, batch, sms):
             assert q["grid"] == min(q["tiles"], sms)
             G = q["grid"]
         if q["tail_tiles"]:
+            # thresholds in 128-byte K atoms
             assert q["tiles"] > G and q["tail_tiles"] == q["tiles"] % G
-            assert q["kblocks"] >= 16 and (q["tiles"] // G) * q["kblocks"] >= 96
+            assert q["kblocks"] * ka >= 16 and (q["tiles"] // G) * q["kblocks"] * ka >= 96
             assert 1 <= q["splits"] <= min(4 * q["tail_tiles"], G)
             assert q["workspace_bytes"] > 0
         else:
