@@ -46,21 +46,21 @@ SM_MAX_MHZ_NOMINAL = 2070.0      # only if MEASURED_PEAKS.json gives no maximum 
 # kernel's sources (kernel file, planner, headers) matches the one it was taken with.
 COMMON_SOURCES = ["api.cu", "dg_internal.h", "ptx.cuh", "tile_sched.h"]
 MEASURED_TRAFFIC = {
-    "sgemm_4096": {"bytes_per_launch": 388_554_752, "source_hash": "e0c17bedb5bd0641"},
-    "sgemm_ragged": {"bytes_per_launch": 24_652_800, "source_hash": "e0c17bedb5bd0641"},
-    "sgemm_256": {"bytes_per_launch": 554_496, "source_hash": "e0c17bedb5bd0641"},
-    "ffn_bf16": {"bytes_per_launch": 154_208_000, "source_hash": "e7a1d6aa9905ba81"},
-    "ffn_gate_up": {"bytes_per_launch": 233_758_976, "source_hash": "e7a1d6aa9905ba81"},
-    "bf16_4096": {"bytes_per_launch": 134_060_288, "source_hash": "e7a1d6aa9905ba81"},
-    "qk_batched": {"bytes_per_launch": 1_078_743_040, "source_hash": "e7a1d6aa9905ba81"},
-    "decode_m1": {"bytes_per_launch": 105_198_336, "source_hash": "242151324e3e1c84"},
-    "decode_m4": {"bytes_per_launch": 105_306_624, "source_hash": "242151324e3e1c84"},
-    "decode_m16": {"bytes_per_launch": 105_571_840, "source_hash": "242151324e3e1c84"},
-    "decode_chain_m1": {"bytes_per_launch": 408_524_544, "source_hash": "90edeb0e96c056db"},
-    "attn_batched": {"bytes_per_launch": 115_854_080, "source_hash": "be88d91f52fd7d16"},
-    "attn_causal_8k": {"bytes_per_launch": 6_360_320, "source_hash": "be88d91f52fd7d16"},
-    "fp8_ffn": {"bytes_per_launch": 57_952_768, "source_hash": "54946ecf6cdcc20e"},
-    "fp8_quant_gemm": {"bytes_per_launch": 23_177_728, "source_hash": "54946ecf6cdcc20e", "quantiser_bytes_per_launch": 12_605_696},
+    "sgemm_4096": {"bytes_per_launch": 388_868_608, "source_hash": "e90c5c171ec77a81"},
+    "sgemm_ragged": {"bytes_per_launch": 24_665_344, "source_hash": "e90c5c171ec77a81"},
+    "sgemm_256": {"bytes_per_launch": 554_240, "source_hash": "e90c5c171ec77a81"},
+    "ffn_bf16": {"bytes_per_launch": 150_730_752, "source_hash": "b49d157f5b547065"},
+    "ffn_gate_up": {"bytes_per_launch": 232_507_904, "source_hash": "b49d157f5b547065"},
+    "bf16_4096": {"bytes_per_launch": 131_843_328, "source_hash": "b49d157f5b547065"},
+    "qk_batched": {"bytes_per_launch": 1_078_787_584, "source_hash": "b49d157f5b547065"},
+    "decode_m1": {"bytes_per_launch": 104_879_616, "source_hash": "fcbaba222da94a3d"},
+    "decode_m4": {"bytes_per_launch": 105_319_424, "source_hash": "fcbaba222da94a3d"},
+    "decode_m16": {"bytes_per_launch": 105_675_520, "source_hash": "fcbaba222da94a3d"},
+    "decode_chain_m1": {"bytes_per_launch": 408_517_376, "source_hash": "2e8a06e855c12dd8"},
+    "attn_batched": {"bytes_per_launch": 116_075_008, "source_hash": "5c5fab7452fd54ff"},
+    "attn_causal_8k": {"bytes_per_launch": 6_360_064, "source_hash": "5c5fab7452fd54ff"},
+    "fp8_ffn": {"bytes_per_launch": 57_798_912, "source_hash": "2d2f1dc164bf18bc"},
+    "fp8_quant_gemm": {"bytes_per_launch": 23_177_472, "source_hash": "2d2f1dc164bf18bc", "quantiser_bytes_per_launch": 12_605_696},
 }
 
 
